@@ -1,0 +1,282 @@
+/*
+ * oasis.h -- C ABI of the GB300 look-ahead sparse decode step (OasisKV).
+ *
+ * The step, per layer and per decode step t ([R] = "Pith review of OasisKV:
+ * Scaling In-Decode KV Cache Beyond HBM with Lookahead Sparse Prefetching",
+ * section "What carries the argument"; [V] = the pith.science verdict record
+ * of arXiv 2608.08097, field "key_machinery"):
+ *   a1  one shared paged-attention pass serves the normal query q and the
+ *       speculative draft query qd of every request over the head-wise
+ *       resident set of K blocks (B = 16 tokens each, GQA);
+ *   a2  the draft query scores every logical block from per-block
+ *       coordinate-wise min/max key summaries held in HBM with the upper bound
+ *       sum_j sum_i max(qd_ji * min_i, qd_ji * max_i) (j over the KV head's
+ *       query heads);
+ *   a3  a head-wise top-K ranking of all logical blocks;
+ *   a4  capped eviction: each admitted non-resident block is paired with the
+ *       least-recently-selected resident block, at most
+ *       C = floor(fetch_ratio * K) admissions per (request, KV head) per step
+ *       ([S] = "OasisKV: Scaling In-Decode KV Cache Beyond HBM with Lookahead
+ *       Sparse Prefetching" (agihunt.info summary), fetch-cap ablation);
+ *   a5  the admitted blocks are gathered from pinned host memory into HBM on a
+ *       side stream, overlapped with other work, and are used from step t+1
+ *       on ([R] abstract: "staged in HBMs before being used in the next decode
+ *       step").
+ *
+ * Conventions
+ *   - Every call returns an oasis_status.  No call aborts, prints or exits.
+ *   - Device work is asynchronous on the caller's cudaStream_t (passed as
+ *     void*, NULL = legacy default stream).  oasis_sync() waits for all work
+ *     of the context and reports deferred device-side errors.
+ *   - Ownership: every buffer is allocated by the caller and lent to the
+ *     library for the life of the context; the library never frees it.  The
+ *     library itself allocates only CUDA streams and events.  oasis_query_sizes
+ *     reports every buffer size.
+ *   - Shapes: R requests, Hq query heads, Hkv KV heads (G = Hq/Hkv <= 4), head
+ *     dim d = 128, block size B = 16, K resident blocks per (request, KV head),
+ *     NBmax logical blocks of capacity per (request, KV head), C admissions per
+ *     step, U = K + C pool units per (request, KV head).  Query head j reads KV
+ *     head j / G.  One "unit" is the keys and values of one block of one KV
+ *     head: [2][B][d] bf16 = 8 KiB.
+ *   - Double-buffered state.  Step t reads table (t & 1) of res_ids / phys and
+ *     ctx_len; its admission writes table ((t + 1) & 1).  Consecutive steps of
+ *     one layer must therefore use consecutive t.  After step t the logical
+ *     resident set is res_ids[(t + 1) & 1] and slot s holds pool unit
+ *     phys[(t + 1) & 1][s].
+ *   - Not thread-safe: one host thread drives a context at a time.
+ *
+ * Layouts (row-major, innermost last; "dev" = device memory, "pinned" =
+ * page-locked host memory that the device can map):
+ *   kv_pool    dev    [R][Hkv][U][2][B][d]      bf16   resident units + C spares
+ *   summaries  dev    [R][Hkv][NBmax][2][d]     bf16   [0] = min row, [1] = max row
+ *   host_kv    pinned [R][Hkv][NBmax][2][B][d]  bf16   full KV store ([0]=K,[1]=V)
+ *   res_ids    dev    [2][R][Hkv][K]            int32  logical block per slot, -1 empty
+ *   stamps     dev    [R][Hkv][K]               int32  step of last selection, -1 never
+ *   phys       dev    [2][R][Hkv][U]            int32  pool unit per slot; [K..U) spares
+ *   ctx_len    dev    [2][R]                    int32  tokens per request
+ *   q, q_draft dev    [R][Hq][d]                bf16
+ *   out        dev    [R][Hq][d]                bf16, or fp32 if cfg.out_fp32
+ *   topk_ids   dev    [R][Hkv][K]               int32  rank order, -1 padded
+ *   topk_scores dev   [R][Hkv][K]               fp32   (nullable)
+ *   admit_ids, admit_slots, evict_ids  dev [R][Hkv][C] int32 (-1 padded)
+ *   n_admit    dev    [R][Hkv]                  int32
+ */
+#ifndef OASIS_H
+#define OASIS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define OASIS_API __attribute__((visibility("default")))
+#else
+#define OASIS_API
+#endif
+
+typedef enum {
+  OASIS_OK = 0,
+  OASIS_EINVAL = -1,   /* bad argument: null pointer, size, alignment, range */
+  OASIS_ENOMEM = -2,   /* a host-side resource (stream/event/mapping) failed */
+  OASIS_ECUDA = -3,    /* a CUDA runtime call failed; see oasis_last_error */
+  OASIS_ETIMEOUT = -4, /* a bounded wait ran out (device or host side) */
+  OASIS_ESTATE = -5,   /* call out of order (e.g. step before load) */
+  OASIS_EDEVICE = -6   /* a kernel reported bad data (see oasis_sync) */
+} oasis_status;
+
+/* Device error word bits, reported by oasis_sync() as OASIS_EDEVICE. */
+#define OASIS_DEVERR_BAD_BLOCK_ID 0x1u /* a block id >= NBmax or past context */
+#define OASIS_DEVERR_TIMEOUT 0x2u      /* a kernel's bounded barrier wait expired */
+#define OASIS_DEVERR_BAD_UNIT 0x4u     /* a pool unit index >= U */
+
+typedef struct {
+  int32_t num_layers;
+  int32_t num_requests;  /* R */
+  int32_t max_blocks;    /* NBmax */
+  int32_t num_q_heads;   /* Hq */
+  int32_t num_kv_heads;  /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 4 */
+  int32_t head_dim;      /* d; must be 128 */
+  int32_t block_size;    /* B; must be 16 */
+  int32_t topk;          /* K; 1..256 and K <= max_blocks */
+  float fetch_ratio;     /* C = floor(fetch_ratio * K), 0 <= fetch_ratio <= 1 */
+  float softmax_scale;   /* 0 -> 1/sqrt(d) */
+  int32_t out_fp32;      /* attention outputs in fp32 (1) or bf16 (0) */
+  int32_t device;        /* CUDA device ordinal */
+} oasis_config;
+
+typedef struct {
+  size_t kv_pool_bytes;   /* per layer */
+  size_t summaries_bytes; /* per layer */
+  size_t host_kv_bytes;   /* per layer (pinned host) */
+  size_t res_ids_bytes;   /* per layer, both tables */
+  size_t stamps_bytes;    /* per layer */
+  size_t phys_bytes;      /* per layer, both tables */
+  size_t ctx_len_bytes;   /* once */
+  size_t workspace_bytes; /* once, device, 256-byte aligned */
+  int32_t fetch_cap;      /* C */
+  int32_t units_per_head; /* U = K + C */
+} oasis_sizes;
+
+typedef struct {
+  /* Arrays of num_layers pointers (the arrays themselves are copied at
+   * oasis_init).  kv_pool, summaries and host_kv must be 16-byte aligned. */
+  void* const* kv_pool;
+  void* const* summaries;
+  void* const* host_kv; /* pinned host pointers (cudaHostAlloc / registered) */
+  int32_t* const* res_ids;
+  int32_t* const* stamps;
+  int32_t* const* phys;
+  int32_t* ctx_len;     /* [2][R] */
+  void* workspace;      /* workspace_bytes of device memory */
+} oasis_buffers;
+
+typedef struct oasis_ctx oasis_ctx;
+
+/* Sizes of every caller-owned buffer for cfg.  Pure host computation (needs
+ * no GPU).  EINVAL on an unsupported configuration. */
+OASIS_API int oasis_query_sizes(const oasis_config* cfg, oasis_sizes* out);
+
+/* Validate cfg and bufs, map the host stores, build the TMA descriptors and
+ * create the side stream and events.  Buffers are not initialised: call
+ * oasis_build_summaries and oasis_load_resident per layer before its first
+ * step. */
+OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
+                         oasis_ctx** out);
+
+/* Wait for the context's work and release its streams and events (not the
+ * caller's buffers).  NULL is accepted. */
+OASIS_API int oasis_destroy(oasis_ctx* ctx);
+
+/* Message for the last failed call on ctx (never NULL). */
+OASIS_API const char* oasis_last_error(const oasis_ctx* ctx);
+
+/* Wait for all work of the context (both streams) and return OASIS_EDEVICE if
+ * a kernel raised a device error bit since the last oasis_sync (the bits are
+ * then cleared; *device_bits receives them when non-NULL). */
+OASIS_API int oasis_sync(oasis_ctx* ctx, uint32_t* device_bits);
+
+/* Support (a0): per-block min/max key summaries of `layer` over the tokens
+ * below ctx_len[table] ([R] "coordinate-wise min/max per block, in the style
+ * of Quest").  Reads the pinned host store through its device mapping. */
+OASIS_API int oasis_build_summaries(oasis_ctx* ctx, int layer, int table,
+                                    void* stream);
+
+/* Support: take res_ids[first_step & 1] (written by the caller; ids distinct
+ * per (r, h), -1 = empty) as the resident set at the start of step
+ * first_step, set phys[first_step & 1] to the identity (slot s -> unit s,
+ * spares K..U-1), set every stamp to -1 and copy the resident blocks from the
+ * host store into the pool. */
+OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step,
+                                  void* stream);
+
+/* a1: look-ahead attention ([R], [V]: "one shared attention kernel processes
+ * the normal token and the draft token over the same resident sparse KV
+ * set").  For every request r and query head j, separately for q and q_draft:
+ * softmax(x . k / scale) . v over the valid tokens of the occupied slots of
+ * KV head j / G in table (step & 1).  A block's valid tokens are those below
+ * ctx_len[step & 1][r]; a head with no valid token outputs zeros. */
+OASIS_API int oasis_lookahead_attn(oasis_ctx* ctx, int layer, int step,
+                                   const void* q, const void* q_draft,
+                                   void* out, void* out_draft, void* stream);
+
+/* a2 + a3: summary scan and head-wise top-K ([R]: the draft query "scans
+ * compressed key summaries ... produces a head-wise top-K ranking of all
+ * logical blocks without restoring any keys").  For every (r, h) and every
+ * logical block b < ceil(ctx_len[step & 1][r] / B):
+ *   s[b] = sum_{j in group(h)} sum_i max(qd_ji * min_bi, qd_ji * max_bi)
+ * then topk_ids = the first min(K, NB_r) blocks by (s desc, b asc), -1
+ * padded; topk_scores (nullable) the matching s (fp32) or -inf. */
+OASIS_API int oasis_score_topk(oasis_ctx* ctx, int layer, int step,
+                               const void* q_draft, int32_t* topk_ids,
+                               float* topk_scores, void* stream);
+
+/* a4: capped least-recently-selected eviction ([R]: "a capped-eviction
+ * policy pairs each admitted nonresident block with a least-recently-selected
+ * resident block"), per (r, h), from table (step & 1) into table
+ * ((step + 1) & 1):
+ *   (i)   stamp = step for every slot whose block is in topk_ids;
+ *   (ii)  M = blocks of topk_ids not resident, in rank order;
+ *   (iii) E = slots whose block is not in topk_ids, ordered empty first, then
+ *         by (stamp, block id, slot) ascending;
+ *   (iv)  n = min(|M|, C);
+ *   (v)   for i < n: evict_ids[i] = block of E[i]; slot E[i] takes M[i] with
+ *         stamp = step; admit_ids[i] = M[i], admit_slots[i] = E[i]; the
+ *         admitted block is assigned the spare pool unit phys[K + i] and the
+ *         evicted unit becomes that spare.
+ * topk_ids must hold distinct ids.  Output lists are -1 padded to C. */
+OASIS_API int oasis_admit_evict(oasis_ctx* ctx, int layer, int step,
+                                const int32_t* topk_ids, int32_t* admit_ids,
+                                int32_t* admit_slots, int32_t* evict_ids,
+                                int32_t* n_admit, void* stream);
+
+/* a5: prefetch gather ([V]: the "gather kernel" reading pinned CPU memory
+ * through the CUDA UVA mapping).  For every (r, h) and i < n_admit: copy host
+ * unit (r, h, admit_ids[i]) into pool unit phys[(step + 1) & 1][admit_slots[i]]
+ * (byte copy of keys and values).  Those units are spares of table (step & 1),
+ * so the copy may run while step `step`'s attention reads that table. */
+OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step,
+                             const int32_t* admit_ids,
+                             const int32_t* admit_slots,
+                             const int32_t* n_admit, void* stream);
+
+/* a1..a5 as one layer-step (a6, [R] "layer-local synchronization").  On
+ * `stream`: wait for this layer's previous side work, then a1.  On the
+ * context's high-priority side stream, concurrently: a2+a3, a4, a5 into the
+ * context's workspace lists.  Returns at once; the next oasis_step (or
+ * oasis_join) of the same layer orders after the side work.  Inputs must
+ * stay valid until then. */
+OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
+                         const void* q_draft, void* out, void* out_draft,
+                         void* stream);
+
+/* Make `stream` wait for this layer's outstanding side work (event wait, no
+ * host block). */
+OASIS_API int oasis_join(oasis_ctx* ctx, int layer, void* stream);
+
+/* oasis_step with host buffers: q/q_draft are copied from (pinned) host
+ * memory into the workspace, the step runs, and out/out_draft are copied back
+ * to host memory, all on `stream`.  Host buffers must stay valid until the
+ * stream reaches the copies. */
+OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step,
+                              const void* q_host, const void* q_draft_host,
+                              void* out_host, void* out_draft_host,
+                              void* stream);
+
+/* Pointers to the context's per-layer workspace lists written by oasis_step
+ * (topk_ids, topk_scores, admit_ids, admit_slots, evict_ids, n_admit; any
+ * may be NULL). */
+OASIS_API int oasis_step_lists(oasis_ctx* ctx, int layer, int32_t** topk_ids,
+                               float** topk_scores, int32_t** admit_ids,
+                               int32_t** admit_slots, int32_t** evict_ids,
+                               int32_t** n_admit);
+
+/* Support (a0, growing contexts): append one token per request to `layer`.
+ * k_new, v_new: dev [R][Hkv][d] bf16.  The token goes to position
+ * p = ctx_len[step & 1][r]: written into the host store, folded into the
+ * tail block's summary (a new block starts at min = max = key), and written
+ * into the resident copy if block p / B is resident in table
+ * ((step + 1) & 1).  Runs after the layer's side work of step `step`. */
+OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step,
+                                 const void* k_new, const void* v_new,
+                                 void* stream);
+
+/* ctx_len[(step + 1) & 1][r] = ctx_len[step & 1][r] + grow for every r. */
+OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
+                                    void* stream);
+
+/* Kernel timing: when enabled, oasis_step records CUDA events around each of
+ * its kernels on the stream that launches it. */
+OASIS_API int oasis_profile_enable(oasis_ctx* ctx, int enable);
+
+/* Sum of kernel durations (ms) and launch counts since the last read, in the
+ * order attention, score_topk, admit_evict, prefetch.  Synchronises. */
+OASIS_API int oasis_profile_read(oasis_ctx* ctx, double* ms_sum4,
+                                 int64_t* count4);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

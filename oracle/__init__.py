@@ -1,0 +1,206 @@
+"""CPU oracle for OasisKV's per-layer look-ahead sparse decode step.
+
+TEST INFRASTRUCTURE ONLY.  The oracle is a plain, sequential C++ restatement
+of the method (``oasis_oracle.cpp``, fp64 sums, one rounding) plus this thin
+ctypes wrapper.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference arm may import it.  It shares no code with
+the CUDA library and never reads a value produced by it: its inputs come from
+the seeded workload generators and its own earlier results.
+
+Arrays are numpy: bf16 data as ``uint16`` bit patterns, ids/stamps as
+``int32``, scores and attention outputs as ``float32``.  Layouts follow
+``oasis_oracle.h``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oasis_oracle.cpp")
+_LIB_PATH = os.path.join(_HERE, "liboasis_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``liboasis_oracle.so`` (g++, no CUDA)."""
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < max(
+                os.path.getmtime(_SRC),
+                os.path.getmtime(os.path.join(_HERE, "oasis_oracle.h")))):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call([
+            "g++", "-O2", "-std=c++17", "-shared", "-fPIC", "-o", tmp, _SRC
+        ])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        sig = {
+            "orc_summary_build": [P, P, I, I, I, I, I, P],
+            "orc_attention_rh": [P, P, P, P, P, I, I, I, I, I, I, I, D, I, I, P],
+            "orc_score_rh": [P, P, P, I, I, I, I, I, I, I, I, P],
+            "orc_topk_rh": [P, I, I, P],
+            "orc_admit_evict_rh": [P, P, P, I, I, I, P, P, P, P],
+            "orc_step_rh": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, D,
+                            I, I, P, P, P, P, P, P, P],
+            "orc_append_token": [P, P, P, P, P, I, I, I, I, I, I],
+        }
+        for name, args in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray, dtype) -> ctypes.c_void_p:
+    if a.dtype != np.dtype(dtype):
+        raise TypeError(f"expected {np.dtype(dtype)}, got {a.dtype}")
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("array must be C-contiguous")
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _ok(rc: int, name: str) -> None:
+    if rc != 0:
+        raise ValueError(f"oracle {name} rejected its arguments")
+
+
+def num_blocks(ctx: int, B: int) -> int:
+    return 0 if ctx <= 0 else (ctx + B - 1) // B
+
+
+def summary_build(host_kv: np.ndarray, ctx_len: np.ndarray) -> np.ndarray:
+    """Per-block min/max key summaries, ``[R][Hkv][NBmax][2][d]`` uint16."""
+    R, Hkv, NBmax, _, B, d = host_kv.shape
+    summ = np.zeros((R, Hkv, NBmax, 2, d), dtype=np.uint16)
+    _ok(_load().orc_summary_build(_p(host_kv, np.uint16), _p(ctx_len, np.int32),
+                                  R, Hkv, NBmax, B, d, _p(summ, np.uint16)),
+        "summary_build")
+    return summ
+
+
+def attention_rh(host_kv, ctx_len, res, q, qd, r, h, scale=None):
+    """Attention outputs ``[2][G][d]`` float32 of one (r, h)."""
+    R, Hkv, NBmax, _, B, d = host_kv.shape
+    Hq = q.shape[1]
+    K = res.shape[-1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.empty((2, Hq // Hkv, d), dtype=np.float32)
+    _ok(_load().orc_attention_rh(
+        _p(host_kv, np.uint16), _p(ctx_len, np.int32), _p(res, np.int32),
+        _p(q, np.uint16), _p(qd, np.uint16), R, Hq, Hkv, NBmax, B, d, K,
+        float(scale), r, h, _p(out, np.float32)), "attention_rh")
+    return out
+
+
+def score_rh(summ, ctx_len, qd, r, h, B):
+    """Summary scores ``[NBmax]`` float32 of one (r, h) (-inf past the context)."""
+    R, Hkv, NBmax, _, d = summ.shape
+    Hq = qd.shape[1]
+    s = np.empty(NBmax, dtype=np.float32)
+    _ok(_load().orc_score_rh(_p(summ, np.uint16), _p(ctx_len, np.int32),
+                             _p(qd, np.uint16), R, Hq, Hkv, NBmax, d, B, r, h,
+                             _p(s, np.float32)), "score_rh")
+    return s
+
+
+def topk_rh(scores: np.ndarray, nb: int, K: int) -> np.ndarray:
+    """Block ids in rank order (score desc, id asc), ``[K]`` int32, -1 padded."""
+    scores = np.ascontiguousarray(scores, dtype=np.float32)
+    out = np.empty(K, dtype=np.int32)
+    _ok(_load().orc_topk_rh(_p(scores, np.float32), nb, K, _p(out, np.int32)),
+        "topk_rh")
+    return out
+
+
+def admit_evict_rh(res_row, stamp_row, topk, C, step):
+    """Capped LRS eviction of one (r, h); updates ``res_row``/``stamp_row`` in
+    place and returns ``(admit_ids, admit_slots, evict_ids, n_admit)``."""
+    K = res_row.shape[0]
+    a = np.empty(max(C, 1), dtype=np.int32)
+    s = np.empty(max(C, 1), dtype=np.int32)
+    e = np.empty(max(C, 1), dtype=np.int32)
+    n = np.zeros(1, dtype=np.int32)
+    topk = np.ascontiguousarray(topk, dtype=np.int32)
+    _ok(_load().orc_admit_evict_rh(_p(res_row, np.int32), _p(stamp_row, np.int32),
+                                   _p(topk, np.int32), K, C, step, _p(a, np.int32),
+                                   _p(s, np.int32), _p(e, np.int32),
+                                   _p(n, np.int32)), "admit_evict_rh")
+    return a[:C], s[:C], e[:C], int(n[0])
+
+
+def append_token(host_kv, summ, ctx_len, k_new, v_new, r):
+    """Write one token (``[Hkv][d]`` keys and values) at position ctx_len[r]
+    and fold its key into the tail summary; ctx_len is not changed."""
+    R, Hkv, NBmax, _, B, d = host_kv.shape
+    _ok(_load().orc_append_token(_p(host_kv, np.uint16), _p(summ, np.uint16),
+                                 _p(ctx_len, np.int32), _p(k_new, np.uint16),
+                                 _p(v_new, np.uint16), R, Hkv, NBmax, B, d, r),
+        "append_token")
+
+
+class LayerOracle:
+    """Oracle state of one layer restricted to a set of (r, h) pairs.
+
+    The pairs are independent in every stage of the step, so a sample of them
+    can be followed at full problem size.  ``res``/``stamp`` hold the whole
+    ``[R][Hkv][K]`` tables but only the tracked pairs are advanced.
+    """
+
+    def __init__(self, host_kv, summ, ctx_len, res0, K, C, pairs, scale=None):
+        self.host_kv, self.summ, self.ctx_len = host_kv, summ, ctx_len
+        self.R, self.Hkv, self.NBmax, _, self.B, self.d = host_kv.shape
+        self.K, self.C = K, C
+        self.res = np.array(res0, dtype=np.int32, copy=True)
+        self.stamp = np.full_like(self.res, -1)
+        self.pairs = [tuple(int(x) for x in p) for p in pairs]
+        self.scale = 1.0 / np.sqrt(self.d) if scale is None else scale
+        self._scores = np.empty(self.NBmax, dtype=np.float32)
+
+    def step(self, q, qd, t, topk_override=None):
+        """Run one layer-step for every tracked pair.
+
+        ``topk_override`` maps (r, h) -> a top-K list to use for the eviction
+        in place of the oracle's own (used to hold both sides in lockstep when
+        an id inside the tie window differs).  Returns a dict keyed by (r, h)
+        with attn [2][G][d], scores, topk, admit_ids, admit_slots, evict_ids,
+        n_admit.
+        """
+        L = _load()
+        Hq = q.shape[1]
+        out = {}
+        for (r, h) in self.pairs:
+            attn = np.empty((2, Hq // self.Hkv, self.d), dtype=np.float32)
+            scores = np.empty(self.NBmax, dtype=np.float32)
+            _ok(L.orc_attention_rh(_p(self.host_kv, np.uint16),
+                                   _p(self.ctx_len, np.int32), _p(self.res, np.int32),
+                                   _p(q, np.uint16), _p(qd, np.uint16), self.R, Hq,
+                                   self.Hkv, self.NBmax, self.B, self.d, self.K,
+                                   float(self.scale), r, h, _p(attn, np.float32)),
+                "attention_rh")
+            _ok(L.orc_score_rh(_p(self.summ, np.uint16), _p(self.ctx_len, np.int32),
+                               _p(qd, np.uint16), self.R, Hq, self.Hkv, self.NBmax,
+                               self.d, self.B, r, h, _p(scores, np.float32)),
+                "score_rh")
+            nb = min(num_blocks(int(self.ctx_len[r]), self.B), self.NBmax)
+            topk = topk_rh(scores, nb, self.K)
+            used = topk
+            if topk_override is not None and (r, h) in topk_override:
+                used = np.ascontiguousarray(topk_override[(r, h)], dtype=np.int32)
+            a, s, e, n = admit_evict_rh(self.res[r, h], self.stamp[r, h], used,
+                                        self.C, t)
+            out[(r, h)] = dict(attn=attn, scores=scores, topk=topk, admit_ids=a,
+                               admit_slots=s, evict_ids=e, n_admit=n)
+        return out

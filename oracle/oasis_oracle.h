@@ -1,0 +1,107 @@
+/*
+ * oasis_oracle.h -- plain, slow, sequential CPU restatement of OasisKV's
+ * per-layer look-ahead sparse decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this code: only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline / reference arm use it.  It shares no code,
+ * header, constant or helper with the CUDA library (include/oasis.h).
+ *
+ * Sources (page titles and sections):
+ *   [R]  "Pith review of OasisKV: Scaling In-Decode KV Cache Beyond HBM with
+ *         Lookahead Sparse Prefetching" (pith.science), section "What carries
+ *         the argument"; "Assumptions & free parameters"; the abstract.
+ *   [S]  "OasisKV: Scaling In-Decode KV Cache Beyond HBM with Lookahead Sparse
+ *         Prefetching" (agihunt.info summary), the fetch-cap ablation paragraph.
+ *   [V]  pith.science verdict record for arXiv 2608.08097, field
+ *         "key_machinery".
+ *
+ * Arithmetic: bf16 inputs are held as raw uint16 bit patterns and widened to
+ * double by a 16-bit shift; every sum is taken in double and rounded once.
+ *
+ * Layouts (row-major, innermost last):
+ *   host_kv [R][Hkv][NBmax][2][B][d]  bf16   (index 0 = keys, 1 = values)
+ *   summ    [R][Hkv][NBmax][2][d]     bf16   (index 0 = min row, 1 = max row)
+ *   q, qd   [R][Hq][d]                bf16   (normal and draft queries)
+ *   res     [R][Hkv][K]               int32  (logical block id per slot, -1 = empty)
+ *   stamp   [R][Hkv][K]               int32  (step of last selection, -1 = never)
+ *   topk    [R][Hkv][K]               int32  (block ids in rank order, -1 pad)
+ * Query head j reads KV head j / (Hq / Hkv).
+ *
+ * Every function returns 0 on success and -1 on an argument error.
+ *
+ * Parity pins: every function below is pinned by tests under tests/ against
+ * closed forms, brute force or library routines (see test_oracle_pins.py).
+ */
+#ifndef OASIS_ORACLE_H
+#define OASIS_ORACLE_H
+#include <stdint.h>
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Per-block coordinate-wise min/max of the keys over the block's valid tokens
+ * ([R] "compressed key summaries (coordinate-wise min/max per block, in the
+ * style of Quest)").  Blocks b < ceil(ctx_len[r]/B) are written; others are
+ * left untouched. */
+int orc_summary_build(const uint16_t* host_kv, const int32_t* ctx_len, int R,
+                      int Hkv, int NBmax, int B, int d, uint16_t* summ);
+
+/* Sparse attention of one (request r, KV head h) over its resident blocks,
+ * for the normal query and the draft query of each of the G query heads of
+ * the group ([R] "one shared attention kernel processes the normal token and
+ * the draft token over the same resident sparse KV set").
+ * out[2][G][d] (fp32): out[0] for q, out[1] for the draft query. */
+int orc_attention_rh(const uint16_t* host_kv, const int32_t* ctx_len,
+                     const int32_t* res, const uint16_t* q, const uint16_t* qd,
+                     int R, int Hq, int Hkv, int NBmax, int B, int d, int K,
+                     double scale, int r, int h, float* out);
+
+/* Summary score of every logical block b < ceil(ctx_len[r]/B) for one
+ * (r, h): s[b] = sum over the group's query heads j and dims i of
+ * max(qd[j][i]*min[b][i], qd[j][i]*max[b][i])  ([R] the draft query "scans
+ * compressed key summaries").  scores[NBmax] (fp32, one rounding of a double
+ * sum); entries b >= NB_r are set to -inf. */
+int orc_score_rh(const uint16_t* summ, const int32_t* ctx_len,
+                 const uint16_t* qd, int R, int Hq, int Hkv, int NBmax, int d,
+                 int B, int r, int h, float* scores);
+
+/* Head-wise top-K of one (r, h): the first min(K, NB) block ids ordered by
+ * (score descending, id ascending); the rest of topk[K] is -1
+ * ([R] "a head-wise top-K ranking of all logical blocks"). */
+int orc_topk_rh(const float* scores, int NB, int K, int32_t* topk);
+
+/* Capped eviction for one (r, h) at step t ([R] "a capped-eviction policy
+ * pairs each admitted nonresident block with a least-recently-selected
+ * resident block"; [S] fetch cap).  Updates res[K] and stamp[K] in place and
+ * writes admit_ids/admit_slots/evict_ids[C] (-1 padded) and *n_admit. */
+int orc_admit_evict_rh(int32_t* res, int32_t* stamp, const int32_t* topk,
+                       int K, int C, int step, int32_t* admit_ids,
+                       int32_t* admit_slots, int32_t* evict_ids,
+                       int32_t* n_admit);
+
+/* One whole layer-step for one (r, h): attention (on the resident set as it
+ * stands at the start of the step) -> summary score -> top-K -> capped
+ * eviction.  The prefetch needs no work on this logical view: the oracle
+ * reads block contents straight from the host store.  scores_scratch needs
+ * NBmax floats.  Outputs as in the functions above. */
+int orc_step_rh(const uint16_t* host_kv, const uint16_t* summ,
+                const int32_t* ctx_len, int32_t* res, int32_t* stamp,
+                const uint16_t* q, const uint16_t* qd, int R, int Hq, int Hkv,
+                int NBmax, int B, int d, int K, int C, int step, double scale,
+                int r, int h, float* attn_out, float* scores_scratch,
+                int32_t* topk, int32_t* admit_ids, int32_t* admit_slots,
+                int32_t* evict_ids, int32_t* n_admit);
+
+/* Append one decoded token to request r of one layer: write k_new/v_new
+ * ([Hkv][d] each) at position pos = ctx_len[r] into the host store and fold
+ * the key into the tail block's summary (a fresh block starts as min = max =
+ * key).  ctx_len itself is not changed.  Requires pos < NBmax*B. */
+int orc_append_token(uint16_t* host_kv, uint16_t* summ, const int32_t* ctx_len,
+                     const uint16_t* k_new, const uint16_t* v_new, int R,
+                     int Hkv, int NBmax, int B, int d, int r);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
