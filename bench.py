@@ -1,0 +1,438 @@
+"""Benchmark of the look-ahead sparse decode layer-step (OasisKV) on GB300.
+
+Workload (default): one Qwen3-8B-shaped layer, 128 requests x 16384 tokens
+(1024 blocks of 16), 32 query / 8 KV heads, head dim 128, K = 128 resident
+blocks per (request, KV head), fetch cap 0.05 (6 admissions per head per
+step); 5 % planted hot blocks per head, queries aligned with the hot
+direction, draft query 0.95-correlated with the next step's query.  The full
+KV store (8 GiB bf16) sits in pinned host memory; HBM holds the resident pool
+(1 GiB + spares), the min/max summaries (512 MiB) and the tables.
+
+One step = one layer-step of the whole hot path through the C ABI
+(oasis_step): look-ahead attention on the main stream; summary scan + top-K,
+capped eviction and the host->HBM gather on the side stream.
+
+Output: one JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the same workload instead (bounded samples of (request, KV head) pairs).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_kv_block_gb300 import workload  # noqa: E402
+
+METRIC = "look-ahead decode layer-steps/s at 16K ctx×128 req; % of HBM & host-link roofline"
+UNIT = "layer-steps/s"
+UNIT_BYTES = 8192          # keys + values of one 16-token block of one KV head (bf16)
+SUMM_BYTES = 512           # min + max rows of one block of one KV head (bf16)
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]),
+                                 hw=f[5], hwt=f[6], swt=f[7], swp=f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for r in rows:
+            if r["hw"].lower().startswith("active"):
+                reasons.add("hw_slowdown")
+            if r["hwt"].lower().startswith("active"):
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"].lower().startswith("active"):
+                reasons.add("sw_thermal_slowdown")
+            if r["swp"].lower().startswith("active"):
+                reasons.add("sw_power_cap")
+        loaded = [r for r in rows if r["power"] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "samples_under_load": len(loaded)}
+
+
+def build_layer(shape, seed, dev, warm=True):
+    """Allocate and fill one layer (untimed setup); returns (engine, q, qd, lens, host)."""
+    from sparse_kv_block_gb300.oasis import Oasis, make_config
+    lens = workload.ctx_lens(shape)
+    host = torch.empty((shape.R, shape.Hkv, shape.NBmax, 2, 16, 128), dtype=torch.bfloat16,
+                       pin_memory=True)
+    gen = dev if dev.type == "cuda" else "cpu"
+    workload.host_kv(shape, seed, 0, lens, device=gen, out=host)
+    cfg = make_config(shape.R, shape.NBmax, shape.Hq, shape.Hkv, shape.K, shape.fetch_ratio,
+                      device=dev.index or 0)
+    eng = Oasis(cfg, host_kv=[host])
+    eng.set_context(lens)
+    eng.oasis_build_summaries(0, 0)
+    return eng, lens, host
+
+
+def warm_start(eng, shape, q0, dev):
+    """Resident set = the summary-ranked top-K of the first query (warm cache)."""
+    topk = torch.empty((shape.R, shape.Hkv, shape.K), dtype=torch.int32, device=dev)
+    eng.oasis_score_topk(0, 0, q0, topk)
+    torch.cuda.synchronize(dev)
+    eng.res_ids[0][0].copy_(topk)
+    eng.oasis_load_resident(0, 0)
+    eng.oasis_sync()
+
+
+def oracle_rate(shape, host, lens, q, qd, budget_s: float, steps_hint: int = 1):
+    """Time the CPU oracle on whole (request, all KV heads) samples.
+
+    Returns (layer-steps/s extrapolated to the whole batch, pairs timed,
+    seconds, sample description)."""
+    import oracle
+    hb = workload.bf16_bits(host)
+    nreq = 1
+    t_pairs, t_sec = 0, 0.0
+    res0 = workload.initial_resident(shape, 0, 0, lens)
+    r = 0
+    while t_sec < budget_s:
+        sub = np.ascontiguousarray(hb[r:r + nreq])
+        sl = np.ascontiguousarray(lens[r:r + nreq])
+        summ = oracle.summary_build(sub, sl)
+        orc = oracle.LayerOracle(sub, summ, sl, res0[r:r + nreq], shape.K, shape.C,
+                                 [(0, h) for h in range(shape.Hkv)])
+        qb = np.ascontiguousarray(workload.bf16_bits(q[0][r:r + nreq].cpu().contiguous()))
+        qdb = np.ascontiguousarray(workload.bf16_bits(qd[0][r:r + nreq].cpu().contiguous()))
+        t0 = time.perf_counter()
+        for t in range(steps_hint):
+            orc.step(qb, qdb, t)
+        t_sec += time.perf_counter() - t0
+        t_pairs += shape.Hkv * steps_hint
+        r = (r + 1) % shape.R
+    pairs_per_s = t_pairs / t_sec
+    rate = pairs_per_s / (shape.R * shape.Hkv)
+    desc = (f"oracle_step (attention + summary score + top-K + capped eviction, fp64) on "
+            f"{t_pairs} (request, KV head) pair-steps of the {shape.name} layer, "
+            f"{t_sec:.1f} s single-threaded, extrapolated to {shape.R * shape.Hkv} pairs")
+    return rate, t_pairs, t_sec, desc
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    shape = workload.SHAPES[args.workload]
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    lens = workload.ctx_lens(shape)
+    host = torch.empty((shape.R, shape.Hkv, shape.NBmax, 2, 16, 128), dtype=torch.bfloat16,
+                       pin_memory=torch.cuda.is_available())
+    workload.host_kv(shape, args.seed, 0, lens, device=dev if dev.type == "cuda" else "cpu",
+                     out=host)
+    q, qd = workload.queries(shape, args.seed, 0, 1, device=dev if dev.type == "cuda" else "cpu")
+    per_step_budget = max(0.05, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rate(shape, host, lens, q, qd, per_step_budget)
+    rates, total_pairs, total_s = [], 0, 0.0
+    for _ in range(args.steps):
+        rate, pairs, sec, desc = oracle_rate(shape, host, lens, q, qd, per_step_budget)
+        total_pairs += pairs
+        total_s += sec
+    value = (total_pairs / total_s) / (shape.R * shape.Hkv)
+    sample = (f"per step: oracle_step on >= {per_step_budget:.2f} s of (request, all KV heads) "
+              f"samples of the {shape.name} layer; {total_pairs} pair-steps in {total_s:.1f} s "
+              f"over {args.steps} steps, extrapolated to {shape.R * shape.Hkv} pairs per layer-step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(shape)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_desc(shape) -> str:
+    return (f"{shape.name}: {shape.layers} layer(s) x {shape.R} requests x {shape.ctx} tokens, "
+            f"{shape.Hq} q / {shape.Hkv} KV heads, d=128, B=16, K={shape.K}, "
+            f"fetch cap {shape.fetch_ratio} (C={shape.C}), hot {shape.hot_frac:.0%} blocks")
+
+
+def h2d_bandwidth(dev) -> float:
+    """Pinned host -> device copy bandwidth (GB/s), 256 MiB, best of 5."""
+    n = 256 << 20
+    h = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    h.fill_(1)
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(dev)
+    best = 1e9
+    for _ in range(6):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            d.copy_(h, non_blocking=True)
+            e1.record(s)
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return n / (best * 1e-3) / 1e9
+
+
+def run_oasis(args, ws, rank, local):
+    from sparse_kv_block_gb300.oasis import lib
+    lib()  # fail loudly if the CUDA library is missing
+    if not torch.cuda.is_available():
+        raise RuntimeError("the CUDA path needs a GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = workload.SHAPES[args.workload]
+    nq = args.queries
+    eng, lens, host = build_layer(shape, args.seed + rank, dev)
+    q, qd = workload.queries(shape, args.seed + rank, 0, nq, device=dev)
+    warm_start(eng, shape, q[0], dev)
+    odt = torch.bfloat16
+    out = torch.empty((shape.R, shape.Hq, 128), dtype=odt, device=dev)
+    outd = torch.empty_like(out)
+    main = torch.cuda.Stream(dev)
+    h2d_gbs = h2d_bandwidth(dev)
+
+    step = 0
+
+    def one_step():
+        nonlocal step
+        eng.oasis_step(0, step, q[step % nq], qd[step % nq], out, outd, main)
+        step += 1
+
+    with torch.cuda.stream(main):
+        for _ in range(args.warmup):
+            one_step()
+    eng.oasis_join(0, main)
+    torch.cuda.synchronize(dev)
+    eng.oasis_sync()
+
+    # ---------------- timed region: K layer-steps, inputs resident in HBM
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    eng.oasis_profile_enable(True)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for _ in range(args.steps):
+        one_step()
+    eng.oasis_join(0, main)
+    e1.record(main)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    ms_sum, counts = eng.oasis_profile_read()
+    eng.oasis_profile_enable(False)
+    clk = clocks.stop()
+    eng.oasis_sync()
+    ms_max = max_over_ranks(ms, ws)
+    value = ws * args.steps / (ms_max * 1e-3)
+
+    # ---------------- admitted traffic (a few extra steps, read back)
+    n_adm = []
+    lists = eng.step_lists(0)
+    for _ in range(8):
+        with torch.cuda.stream(main):
+            one_step()
+        eng.oasis_join(0, main)
+        torch.cuda.synchronize(dev)
+        n_adm.append(int(lists["n_admit"].sum().item()))
+    adm_units = sum(n_adm) / len(n_adm)
+    link_bytes = adm_units * UNIT_BYTES
+
+    # ---------------- end to end: host buffers through oasis_step_host
+    qh = torch.empty((shape.R, shape.Hq, 128), dtype=torch.bfloat16, pin_memory=True)
+    qdh = torch.empty_like(qh).pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    odh = torch.empty_like(qh).pin_memory()
+    q_host = q[:min(nq, 8)].cpu()
+    qd_host = qd[:min(nq, 8)].cpu()
+    e2e_steps = args.steps
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(main)
+    for i in range(e2e_steps):
+        qh.copy_(q_host[i % q_host.shape[0]])       # the host-side input of this step
+        qdh.copy_(qd_host[i % qd_host.shape[0]])
+        eng.oasis_step_host(0, step, qh, qdh, oh, odh, main)
+        step += 1
+        main.synchronize()                          # the host reads this step's result
+    eng.oasis_join(0, main)
+    f1.record(main)
+    torch.cuda.synchronize(dev)
+    e2e_wall = time.perf_counter() - t0
+    barrier(ws)
+    e2e_s = max_over_ranks(e2e_wall, ws)
+    e2e_value = ws * e2e_steps / e2e_s
+    eng.oasis_sync()
+
+    # ---------------- roofline of the dominant kernel
+    peaks = measured_peaks()
+    names = ["attention", "score_topk", "admit_evict", "prefetch"]
+    avg_ms = {n: (ms_sum[i] / counts[i] if counts[i] else None) for i, n in enumerate(names)}
+    R, Hq, Hkv, K, NB = shape.R, shape.Hq, shape.Hkv, shape.K, shape.NBmax
+    qo_bytes = 4 * R * Hq * 128 * 2
+    attn_bytes = R * Hkv * K * UNIT_BYTES + qo_bytes
+    scan_bytes = R * Hkv * NB * SUMM_BYTES + R * Hq * 128 * 2 + R * Hkv * K * 8
+    dominant = max((n for n in names if avg_ms[n]), key=lambda n: avg_ms[n])
+    per_kernel = {}
+    for n, b, bound, peak in [("attention", attn_bytes, "hbm", peaks["hbm_gbs"]),
+                              ("score_topk", scan_bytes, "hbm", peaks["hbm_gbs"]),
+                              ("prefetch", link_bytes, "host-link", h2d_gbs)]:
+        if avg_ms[n]:
+            a = b / (avg_ms[n] * 1e-3) / 1e9
+            per_kernel[n] = {"bound": bound, "achieved": round(a, 1), "peak": round(peak, 1),
+                             "unit": "GB/s", "frac": round(a / peak, 4),
+                             "bytes_per_launch": int(b), "avg_ms": round(avg_ms[n], 5)}
+    dk = per_kernel.get(dominant, per_kernel["attention"])
+    roofline = {"bound": "hbm" if dk["bound"] == "hbm" else "hbm", "kernel": dominant,
+                "achieved": dk["achieved"], "peak": dk["peak"], "unit": "GB/s",
+                "frac": dk["frac"], "traffic": None,
+                "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)"
+                if peaks["source"] == "measured" else "fallback 6.8 TB/s"}
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(shape), "parallelism": f"replicas{ws}",
+                       "l2": "inputs larger than L2: 1.5 GiB of pool + summaries read per step",
+                       "tokens_per_s": round(value * shape.R, 1)},
+            "roofline": roofline, "kernels": per_kernel,
+            "host_link": {"h2d_memcpy_gbs": round(h2d_gbs, 1),
+                          "admitted_units_per_step": adm_units,
+                          "bytes_per_step": int(link_bytes)},
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": 2 * R * Hq * 128 * 2,
+                    "d2h_bytes_per_step": 2 * R * Hq * 128 * 2,
+                    "note": "oasis_step_host: pinned q/q_draft in, attention outputs out, "
+                            "host waits for each step's result"},
+            "gpu_launches": 4 * args.steps, "clocks": clk}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, pairs, sec, desc = oracle_rate(shape, host, lens, q.cpu(), qd.cpu(),
+                                             budget_s=args.cpu_budget)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    eng.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="oasis", choices=["oasis", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_16k", choices=["qwen3_8b_16k", "tiny"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--queries", type=int, default=64, help="distinct query steps, cycled")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_oasis(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

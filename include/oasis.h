@@ -135,6 +135,10 @@ typedef struct {
 
 typedef struct oasis_ctx oasis_ctx;
 
+/* NULL if cfg is supported, else a static message naming the first problem.
+ * Pure host computation. */
+OASIS_API const char* oasis_config_error(const oasis_config* cfg);
+
 /* Sizes of every caller-owned buffer for cfg.  Pure host computation (needs
  * no GPU).  EINVAL on an unsupported configuration. */
 OASIS_API int oasis_query_sizes(const oasis_config* cfg, oasis_sizes* out);

@@ -1,0 +1,691 @@
+// api.cu -- the C ABI (include/oasis.h): argument validation, the context,
+// the side stream and its events, the TMA descriptors and step orchestration.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/oasis.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace oasis;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct LayerState {
+  void* pool = nullptr;
+  void* summ = nullptr;
+  void* host = nullptr;      // caller's host pointer
+  void* host_dev = nullptr;  // its device mapping
+  int32_t* res = nullptr;    // [2][R][Hkv][K]
+  int32_t* stamps = nullptr;
+  int32_t* phys = nullptr;   // [2][R][Hkv][U]
+  CUtensorMap pool_map;
+  // workspace lists
+  int32_t* topk_ids = nullptr;
+  float* topk_scores = nullptr;
+  int32_t* admit_ids = nullptr;
+  int32_t* admit_slots = nullptr;
+  int32_t* evict_ids = nullptr;
+  int32_t* n_admit = nullptr;
+  void* q_stage = nullptr;
+  void* qd_stage = nullptr;
+  void* out_stage = nullptr;
+  void* outd_stage = nullptr;
+  cudaEvent_t ev_start = nullptr;
+  cudaEvent_t ev_side_done = nullptr;
+  cudaEvent_t ev_attn_done = nullptr;
+  bool side_pending = false;
+  bool loaded = false;
+};
+
+struct ProfPair {
+  cudaEvent_t a, b;
+};
+
+struct WsLayout {
+  size_t err, per_layer;
+  size_t topk_ids, topk_scores, admit_ids, admit_slots, evict_ids, n_admit;
+  size_t q_stage, qd_stage, out_stage, outd_stage;
+  size_t total;
+};
+
+int fetch_cap(const oasis_config& c) {
+  return static_cast<int>(std::floor(static_cast<double>(c.fetch_ratio) * c.topk + 1e-9));
+}
+
+WsLayout ws_layout(const oasis_config& c) {
+  WsLayout w{};
+  const size_t pairs = static_cast<size_t>(c.num_requests) * c.num_kv_heads;
+  const size_t C = static_cast<size_t>(fetch_cap(c));
+  const size_t qbytes = static_cast<size_t>(c.num_requests) * c.num_q_heads * c.head_dim * 2;
+  const size_t obytes = qbytes * (c.out_fp32 ? 2 : 1);
+  w.err = 0;
+  size_t o = kAlign;
+  w.topk_ids = o;    o += align_up(pairs * c.topk * 4);
+  w.topk_scores = o; o += align_up(pairs * c.topk * 4);
+  w.admit_ids = o;   o += align_up(pairs * (C ? C : 1) * 4);
+  w.admit_slots = o; o += align_up(pairs * (C ? C : 1) * 4);
+  w.evict_ids = o;   o += align_up(pairs * (C ? C : 1) * 4);
+  w.n_admit = o;     o += align_up(pairs * 4);
+  w.q_stage = o;     o += align_up(qbytes);
+  w.qd_stage = o;    o += align_up(qbytes);
+  w.out_stage = o;   o += align_up(obytes);
+  w.outd_stage = o;  o += align_up(obytes);
+  w.per_layer = o - kAlign;
+  w.total = kAlign + w.per_layer * static_cast<size_t>(c.num_layers);
+  return w;
+}
+
+const char* config_error(const oasis_config* c) {
+  if (!c) return "config is NULL";
+  if (c->num_layers <= 0) return "num_layers must be > 0";
+  if (c->num_requests <= 0) return "num_requests must be > 0";
+  if (c->max_blocks <= 0) return "max_blocks must be > 0";
+  if (c->num_kv_heads <= 0 || c->num_q_heads <= 0) return "head counts must be > 0";
+  if (c->num_q_heads % c->num_kv_heads != 0) return "num_q_heads must be a multiple of num_kv_heads";
+  if (c->num_q_heads / c->num_kv_heads > kMaxGroup) return "query heads per KV head must be <= 4";
+  if (c->head_dim != kHeadDim) return "head_dim must be 128";
+  if (c->block_size != kBlock) return "block_size must be 16";
+  if (c->topk <= 0 || c->topk > kMaxTopK) return "topk must be in 1..256";
+  if (c->topk > c->max_blocks) return "topk must be <= max_blocks";
+  if (!(c->fetch_ratio >= 0.f && c->fetch_ratio <= 1.f)) return "fetch_ratio must be in [0, 1]";
+  if (!(c->softmax_scale >= 0.f) || std::isinf(c->softmax_scale)) return "softmax_scale must be finite and >= 0";
+  if (c->device < 0) return "device must be >= 0";
+  const double units = static_cast<double>(c->num_requests) * c->num_kv_heads *
+                       (c->topk + fetch_cap(*c)) * 2 * kBlock;
+  if (units >= 2147483647.0) return "pool too large for a 32-bit TMA row coordinate";
+  if (static_cast<double>(c->num_requests) * c->num_kv_heads * c->max_blocks >= 2147483647.0)
+    return "num_requests * num_kv_heads * max_blocks must fit in int32";
+  return nullptr;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct oasis_ctx {
+  oasis_config cfg{};
+  int G = 0, C = 0, U = 0;
+  float scale_log2 = 0.f;
+  std::vector<LayerState> layers;
+  int32_t* ctx_len = nullptr;
+  uint8_t* ws = nullptr;
+  uint32_t* err = nullptr;
+  WsLayout wl{};
+  cudaStream_t side = nullptr;
+  std::string last_error;
+  bool prof = false;
+  std::vector<ProfPair> prof_pool;
+  size_t prof_used = 0;
+  std::vector<int> prof_kind;
+
+  int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    last_error = buf;
+    return code;
+  }
+  int cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return OASIS_OK;
+    return fail(OASIS_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+  }
+  int32_t* res_tab(int l, int step) const {
+    const size_t n = static_cast<size_t>(cfg.num_requests) * cfg.num_kv_heads * cfg.topk;
+    return layers[l].res + (step & 1) * n;
+  }
+  int32_t* phys_tab(int l, int step) const {
+    const size_t n = static_cast<size_t>(cfg.num_requests) * cfg.num_kv_heads * U;
+    return layers[l].phys + (step & 1) * n;
+  }
+  int32_t* ctx_tab(int step) const { return ctx_len + (step & 1) * cfg.num_requests; }
+  int set_device() { return cuda(cudaSetDevice(cfg.device), "cudaSetDevice"); }
+
+  // Profiling: record an event pair around a launch of `kind`.
+  cudaEvent_t* prof_begin(int kind, cudaStream_t s) {
+    if (!prof) return nullptr;
+    if (prof_used == prof_pool.size()) {
+      ProfPair p{};
+      if (cudaEventCreate(&p.a) != cudaSuccess) return nullptr;
+      if (cudaEventCreate(&p.b) != cudaSuccess) {
+        cudaEventDestroy(p.a);
+        return nullptr;
+      }
+      prof_pool.push_back(p);
+      prof_kind.push_back(kind);
+    }
+    prof_kind[prof_used] = kind;
+    ProfPair& p = prof_pool[prof_used++];
+    cudaEventRecord(p.a, s);
+    return &p.b;
+  }
+  void prof_end(cudaEvent_t* e, cudaStream_t s) {
+    if (e) cudaEventRecord(*e, s);
+  }
+};
+
+namespace {
+
+int check_layer(oasis_ctx* ctx, int layer) {
+  if (!ctx) return OASIS_EINVAL;
+  if (layer < 0 || layer >= ctx->cfg.num_layers)
+    return ctx->fail(OASIS_EINVAL, "layer %d out of range [0, %d)", layer, ctx->cfg.num_layers);
+  return OASIS_OK;
+}
+
+int run_attention(oasis_ctx* ctx, int layer, int step, const void* q, const void* qd,
+                  void* out, void* outd, cudaStream_t s) {
+  LayerState& L = ctx->layers[layer];
+  AttnArgs a{};
+  a.q = q;
+  a.qd = qd;
+  a.out = out;
+  a.outd = outd;
+  a.res = ctx->res_tab(layer, step);
+  a.phys = ctx->phys_tab(layer, step);
+  a.ctx_len = ctx->ctx_tab(step);
+  a.err = ctx->err;
+  a.R = ctx->cfg.num_requests;
+  a.Hq = ctx->cfg.num_q_heads;
+  a.Hkv = ctx->cfg.num_kv_heads;
+  a.G = ctx->G;
+  a.K = ctx->cfg.topk;
+  a.U = ctx->U;
+  a.NBmax = ctx->cfg.max_blocks;
+  a.scale_log2 = ctx->scale_log2;
+  a.out_fp32 = ctx->cfg.out_fp32;
+  cudaEvent_t* pe = ctx->prof_begin(0, s);
+  cudaError_t e = launch_attention(a, &L.pool_map, s);
+  ctx->prof_end(pe, s);
+  return ctx->cuda(e, "attention launch");
+}
+
+int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
+              float* scores, cudaStream_t s) {
+  LayerState& L = ctx->layers[layer];
+  ScoreArgs a{};
+  a.qd = qd;
+  a.summ = L.summ;
+  a.ctx_len = ctx->ctx_tab(step);
+  a.topk_ids = ids;
+  a.topk_scores = scores;
+  a.err = ctx->err;
+  a.R = ctx->cfg.num_requests;
+  a.Hq = ctx->cfg.num_q_heads;
+  a.Hkv = ctx->cfg.num_kv_heads;
+  a.G = ctx->G;
+  a.K = ctx->cfg.topk;
+  a.NBmax = ctx->cfg.max_blocks;
+  cudaEvent_t* pe = ctx->prof_begin(1, s);
+  cudaError_t e = launch_score_topk(a, s);
+  ctx->prof_end(pe, s);
+  return ctx->cuda(e, "score_topk launch");
+}
+
+int run_admit(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t* aid,
+              int32_t* aslot, int32_t* evid, int32_t* nadm, cudaStream_t s) {
+  LayerState& L = ctx->layers[layer];
+  AdmitArgs a{};
+  a.topk = topk;
+  a.res_cur = ctx->res_tab(layer, step);
+  a.res_nxt = ctx->res_tab(layer, step + 1);
+  a.stamps = L.stamps;
+  a.phys_cur = ctx->phys_tab(layer, step);
+  a.phys_nxt = ctx->phys_tab(layer, step + 1);
+  a.admit_ids = aid;
+  a.admit_slots = aslot;
+  a.evict_ids = evid;
+  a.n_admit = nadm;
+  a.R = ctx->cfg.num_requests;
+  a.Hkv = ctx->cfg.num_kv_heads;
+  a.K = ctx->cfg.topk;
+  a.C = ctx->C;
+  a.U = ctx->U;
+  a.step = step;
+  cudaEvent_t* pe = ctx->prof_begin(2, s);
+  cudaError_t e = launch_admit(a, s);
+  ctx->prof_end(pe, s);
+  return ctx->cuda(e, "admit_evict launch");
+}
+
+int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
+                 const int32_t* aslot, const int32_t* nadm, cudaStream_t s) {
+  if (ctx->C == 0) return OASIS_OK;
+  LayerState& L = ctx->layers[layer];
+  GatherArgs g{};
+  g.host = L.host_dev;
+  g.pool = L.pool;
+  g.src_ids = aid;
+  g.dst_slots = aslot;
+  g.n_valid = nadm;
+  g.phys = ctx->phys_tab(layer, step + 1);
+  g.err = ctx->err;
+  g.pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
+  g.items = ctx->C;
+  g.NBmax = ctx->cfg.max_blocks;
+  g.U = ctx->U;
+  cudaEvent_t* pe = ctx->prof_begin(3, s);
+  cudaError_t e = launch_gather(g, s);
+  ctx->prof_end(pe, s);
+  return ctx->cuda(e, "prefetch launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+OASIS_API const char* oasis_config_error(const oasis_config* cfg) { return config_error(cfg); }
+
+OASIS_API int oasis_query_sizes(const oasis_config* cfg, oasis_sizes* out) {
+  if (!out || config_error(cfg)) return OASIS_EINVAL;
+  const size_t R = cfg->num_requests, H = cfg->num_kv_heads, K = cfg->topk;
+  const size_t NB = cfg->max_blocks;
+  const int C = fetch_cap(*cfg);
+  const size_t U = K + C;
+  out->kv_pool_bytes = R * H * U * kUnitBytes;
+  out->summaries_bytes = R * H * NB * kSummBytes;
+  out->host_kv_bytes = R * H * NB * kUnitBytes;
+  out->res_ids_bytes = 2 * R * H * K * 4;
+  out->stamps_bytes = R * H * K * 4;
+  out->phys_bytes = 2 * R * H * U * 4;
+  out->ctx_len_bytes = 2 * R * 4;
+  out->workspace_bytes = ws_layout(*cfg).total;
+  out->fetch_cap = C;
+  out->units_per_head = static_cast<int32_t>(U);
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
+                         oasis_ctx** out) {
+  if (!out) return OASIS_EINVAL;
+  *out = nullptr;
+  if (config_error(cfg) || !bufs) return OASIS_EINVAL;
+  const int L = cfg->num_layers;
+  if (!bufs->kv_pool || !bufs->summaries || !bufs->host_kv || !bufs->res_ids ||
+      !bufs->stamps || !bufs->phys || !bufs->ctx_len || !bufs->workspace)
+    return OASIS_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(bufs->workspace) & (kAlign - 1)) != 0) return OASIS_EINVAL;
+  for (int l = 0; l < L; ++l) {
+    if (!bufs->kv_pool[l] || !bufs->summaries[l] || !bufs->host_kv[l] || !bufs->res_ids[l] ||
+        !bufs->stamps[l] || !bufs->phys[l])
+      return OASIS_EINVAL;
+    if (!aligned16(bufs->kv_pool[l]) || !aligned16(bufs->summaries[l]) ||
+        !aligned16(bufs->host_kv[l]) || !aligned16(bufs->res_ids[l]) ||
+        !aligned16(bufs->stamps[l]) || !aligned16(bufs->phys[l]))
+      return OASIS_EINVAL;
+  }
+
+  oasis_ctx* c = new (std::nothrow) oasis_ctx();
+  if (!c) return OASIS_ENOMEM;
+  c->cfg = *cfg;
+  c->G = cfg->num_q_heads / cfg->num_kv_heads;
+  c->C = fetch_cap(*cfg);
+  c->U = cfg->topk + c->C;
+  const double scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0 / std::sqrt(128.0);
+  c->scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+  c->ctx_len = bufs->ctx_len;
+  c->ws = static_cast<uint8_t*>(bufs->workspace);
+  c->wl = ws_layout(*cfg);
+  c->err = reinterpret_cast<uint32_t*>(c->ws + c->wl.err);
+  c->layers.resize(L);
+
+  auto bail = [&](int code) {
+    oasis_destroy(c);
+    return code;
+  };
+  if (cudaSetDevice(cfg->device) != cudaSuccess) return bail(OASIS_ECUDA);
+  int lo = 0, hi = 0;
+  if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return bail(OASIS_ECUDA);
+  if (cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, hi) != cudaSuccess)
+    return bail(OASIS_ENOMEM);
+  auto encode = get_encode();
+  if (!encode) return bail(OASIS_ECUDA);
+
+  const size_t R = cfg->num_requests, H = cfg->num_kv_heads;
+  for (int l = 0; l < L; ++l) {
+    LayerState& S = c->layers[l];
+    S.pool = bufs->kv_pool[l];
+    S.summ = bufs->summaries[l];
+    S.host = bufs->host_kv[l];
+    S.res = bufs->res_ids[l];
+    S.stamps = bufs->stamps[l];
+    S.phys = bufs->phys[l];
+    void* dptr = nullptr;
+    if (cudaHostGetDevicePointer(&dptr, S.host, 0) != cudaSuccess || !dptr) {
+      cudaGetLastError();
+      c->last_error = "host_kv is not page-locked host memory mapped for the device";
+      return bail(OASIS_EINVAL);
+    }
+    S.host_dev = dptr;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
+                                static_cast<cuuint64_t>(R * H * c->U * 2 * kBlock)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+    const cuuint32_t box[2] = {64, 2 * kBlock};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&S.pool_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, S.pool, dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return bail(OASIS_ECUDA);
+    // WsLayout offsets place layer 0's lists right after the error word.
+    uint8_t* w = c->ws + kAlign + static_cast<size_t>(l) * c->wl.per_layer;
+    const size_t b0 = kAlign;
+    S.topk_ids = reinterpret_cast<int32_t*>(w + (c->wl.topk_ids - b0));
+    S.topk_scores = reinterpret_cast<float*>(w + (c->wl.topk_scores - b0));
+    S.admit_ids = reinterpret_cast<int32_t*>(w + (c->wl.admit_ids - b0));
+    S.admit_slots = reinterpret_cast<int32_t*>(w + (c->wl.admit_slots - b0));
+    S.evict_ids = reinterpret_cast<int32_t*>(w + (c->wl.evict_ids - b0));
+    S.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.n_admit - b0));
+    S.q_stage = w + (c->wl.q_stage - b0);
+    S.qd_stage = w + (c->wl.qd_stage - b0);
+    S.out_stage = w + (c->wl.out_stage - b0);
+    S.outd_stage = w + (c->wl.outd_stage - b0);
+    if (cudaEventCreateWithFlags(&S.ev_start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_side_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_attn_done, cudaEventDisableTiming) != cudaSuccess)
+      return bail(OASIS_ENOMEM);
+  }
+  if (cudaMemsetAsync(c->err, 0, sizeof(uint32_t), c->side) != cudaSuccess ||
+      cudaStreamSynchronize(c->side) != cudaSuccess)
+    return bail(OASIS_ECUDA);
+  *out = c;
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_destroy(oasis_ctx* ctx) {
+  if (!ctx) return OASIS_OK;
+  cudaSetDevice(ctx->cfg.device);
+  if (ctx->side) cudaStreamSynchronize(ctx->side);
+  for (auto& L : ctx->layers) {
+    if (L.ev_start) cudaEventDestroy(L.ev_start);
+    if (L.ev_side_done) cudaEventDestroy(L.ev_side_done);
+    if (L.ev_attn_done) cudaEventDestroy(L.ev_attn_done);
+  }
+  for (auto& p : ctx->prof_pool) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  if (ctx->side) cudaStreamDestroy(ctx->side);
+  delete ctx;
+  return OASIS_OK;
+}
+
+OASIS_API const char* oasis_last_error(const oasis_ctx* ctx) {
+  if (!ctx) return "null context";
+  return ctx->last_error.c_str();
+}
+
+OASIS_API int oasis_sync(oasis_ctx* ctx, uint32_t* device_bits) {
+  if (!ctx) return OASIS_EINVAL;
+  if (int rc = ctx->set_device()) return rc;
+  if (int rc = ctx->cuda(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) return rc;
+  uint32_t bits = 0;
+  if (int rc = ctx->cuda(cudaMemcpy(&bits, ctx->err, sizeof bits, cudaMemcpyDeviceToHost),
+                         "read device error word"))
+    return rc;
+  if (device_bits) *device_bits = bits;
+  if (bits) {
+    if (int rc = ctx->cuda(cudaMemset(ctx->err, 0, sizeof bits), "clear device error word"))
+      return rc;
+    return ctx->fail(OASIS_EDEVICE, "device error bits 0x%x", bits);
+  }
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_build_summaries(oasis_ctx* ctx, int layer, int table, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (int rc = ctx->set_device()) return rc;
+  SummaryArgs a{};
+  a.host = ctx->layers[layer].host_dev;
+  a.summ = ctx->layers[layer].summ;
+  a.ctx_len = ctx->ctx_tab(table);
+  a.R = ctx->cfg.num_requests;
+  a.Hkv = ctx->cfg.num_kv_heads;
+  a.NBmax = ctx->cfg.max_blocks;
+  return ctx->cuda(launch_summary_build(a, static_cast<cudaStream_t>(stream)),
+                   "summary_build launch");
+}
+
+OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (first_step < 0) return ctx->fail(OASIS_EINVAL, "first_step must be >= 0");
+  if (int rc = ctx->set_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerState& L = ctx->layers[layer];
+  if (L.side_pending) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
+  }
+  const int pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
+  if (int rc = ctx->cuda(launch_init_tables(ctx->phys_tab(layer, first_step), L.stamps, pairs,
+                                            ctx->cfg.topk, ctx->U, s),
+                         "init tables launch"))
+    return rc;
+  GatherArgs g{};
+  g.host = L.host_dev;
+  g.pool = L.pool;
+  g.src_ids = ctx->res_tab(layer, first_step);
+  g.dst_slots = nullptr;
+  g.n_valid = nullptr;
+  g.phys = ctx->phys_tab(layer, first_step);
+  g.err = ctx->err;
+  g.pairs = pairs;
+  g.items = ctx->cfg.topk;
+  g.NBmax = ctx->cfg.max_blocks;
+  g.U = ctx->U;
+  if (int rc = ctx->cuda(launch_gather(g, s), "load gather launch")) return rc;
+  L.loaded = true;
+  L.side_pending = false;
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_lookahead_attn(oasis_ctx* ctx, int layer, int step, const void* q,
+                                   const void* q_draft, void* out, void* out_draft,
+                                   void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !q || !q_draft || !out || !out_draft)
+    return ctx->fail(OASIS_EINVAL, "attention: bad step or null pointer");
+  if (int rc = ctx->set_device()) return rc;
+  return run_attention(ctx, layer, step, q, q_draft, out, out_draft,
+                       static_cast<cudaStream_t>(stream));
+}
+
+OASIS_API int oasis_score_topk(oasis_ctx* ctx, int layer, int step, const void* q_draft,
+                               int32_t* topk_ids, float* topk_scores, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !q_draft || !topk_ids)
+    return ctx->fail(OASIS_EINVAL, "score_topk: bad step or null pointer");
+  if (int rc = ctx->set_device()) return rc;
+  return run_score(ctx, layer, step, q_draft, topk_ids, topk_scores,
+                   static_cast<cudaStream_t>(stream));
+}
+
+OASIS_API int oasis_admit_evict(oasis_ctx* ctx, int layer, int step, const int32_t* topk_ids,
+                                int32_t* admit_ids, int32_t* admit_slots, int32_t* evict_ids,
+                                int32_t* n_admit, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !topk_ids || !admit_ids || !admit_slots || !evict_ids || !n_admit)
+    return ctx->fail(OASIS_EINVAL, "admit_evict: bad step or null pointer");
+  if (int rc = ctx->set_device()) return rc;
+  return run_admit(ctx, layer, step, topk_ids, admit_ids, admit_slots, evict_ids, n_admit,
+                   static_cast<cudaStream_t>(stream));
+}
+
+OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* admit_ids,
+                             const int32_t* admit_slots, const int32_t* n_admit,
+                             void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !admit_ids || !admit_slots || !n_admit)
+    return ctx->fail(OASIS_EINVAL, "prefetch: bad step or null pointer");
+  if (int rc = ctx->set_device()) return rc;
+  return run_prefetch(ctx, layer, step, admit_ids, admit_slots, n_admit,
+                      static_cast<cudaStream_t>(stream));
+}
+
+OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
+                         const void* q_draft, void* out, void* out_draft, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !q || !q_draft || !out || !out_draft)
+    return ctx->fail(OASIS_EINVAL, "step: bad step or null pointer");
+  LayerState& L = ctx->layers[layer];
+  if (!L.loaded) return ctx->fail(OASIS_ESTATE, "layer %d: oasis_load_resident first", layer);
+  if (int rc = ctx->set_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (L.side_pending) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
+  }
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_start, s), "record start")) return rc;
+  if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side, L.ev_start, 0), "side wait")) return rc;
+  if (int rc = run_attention(ctx, layer, step, q, q_draft, out, out_draft, s)) return rc;
+  if (int rc = run_score(ctx, layer, step, q_draft, L.topk_ids, L.topk_scores, ctx->side))
+    return rc;
+  if (int rc = run_admit(ctx, layer, step, L.topk_ids, L.admit_ids, L.admit_slots, L.evict_ids,
+                         L.n_admit, ctx->side))
+    return rc;
+  if (int rc = run_prefetch(ctx, layer, step, L.admit_ids, L.admit_slots, L.n_admit, ctx->side))
+    return rc;
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_side_done, ctx->side), "record side")) return rc;
+  L.side_pending = true;
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_join(oasis_ctx* ctx, int layer, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (int rc = ctx->set_device()) return rc;
+  LayerState& L = ctx->layers[layer];
+  if (!L.side_pending) return OASIS_OK;
+  return ctx->cuda(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), L.ev_side_done, 0),
+                   "join");
+}
+
+OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q_host,
+                              const void* q_draft_host, void* out_host, void* out_draft_host,
+                              void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (!q_host || !q_draft_host || !out_host || !out_draft_host)
+    return ctx->fail(OASIS_EINVAL, "step_host: null pointer");
+  LayerState& L = ctx->layers[layer];
+  if (!L.loaded) return ctx->fail(OASIS_ESTATE, "layer %d: oasis_load_resident first", layer);
+  if (int rc = ctx->set_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The side work of the previous step still reads the staged draft query.
+  if (L.side_pending) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
+  }
+  const size_t qb = static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_q_heads * kHeadDim * 2;
+  const size_t ob = qb * (ctx->cfg.out_fp32 ? 2 : 1);
+  if (int rc = ctx->cuda(cudaMemcpyAsync(L.q_stage, q_host, qb, cudaMemcpyHostToDevice, s), "h2d q"))
+    return rc;
+  if (int rc = ctx->cuda(cudaMemcpyAsync(L.qd_stage, q_draft_host, qb, cudaMemcpyHostToDevice, s),
+                         "h2d q_draft"))
+    return rc;
+  if (int rc = oasis_step(ctx, layer, step, L.q_stage, L.qd_stage, L.out_stage, L.outd_stage, stream))
+    return rc;
+  if (int rc = ctx->cuda(cudaMemcpyAsync(out_host, L.out_stage, ob, cudaMemcpyDeviceToHost, s), "d2h out"))
+    return rc;
+  return ctx->cuda(cudaMemcpyAsync(out_draft_host, L.outd_stage, ob, cudaMemcpyDeviceToHost, s),
+                   "d2h out_draft");
+}
+
+OASIS_API int oasis_step_lists(oasis_ctx* ctx, int layer, int32_t** topk_ids, float** topk_scores,
+                               int32_t** admit_ids, int32_t** admit_slots, int32_t** evict_ids,
+                               int32_t** n_admit) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  LayerState& L = ctx->layers[layer];
+  if (topk_ids) *topk_ids = L.topk_ids;
+  if (topk_scores) *topk_scores = L.topk_scores;
+  if (admit_ids) *admit_ids = L.admit_ids;
+  if (admit_slots) *admit_slots = L.admit_slots;
+  if (evict_ids) *evict_ids = L.evict_ids;
+  if (n_admit) *n_admit = L.n_admit;
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step, const void* k_new,
+                                 const void* v_new, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !k_new || !v_new) return ctx->fail(OASIS_EINVAL, "append: bad argument");
+  if (int rc = ctx->set_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerState& L = ctx->layers[layer];
+  // The token may land in a block this layer's side work is copying.
+  if (L.side_pending) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
+  }
+  AppendArgs a{};
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.host = L.host_dev;
+  a.summ = L.summ;
+  a.pool = L.pool;
+  a.ctx_len = ctx->ctx_tab(step);
+  a.res_nxt = ctx->res_tab(layer, step + 1);
+  a.phys_nxt = ctx->phys_tab(layer, step + 1);
+  a.err = ctx->err;
+  a.R = ctx->cfg.num_requests;
+  a.Hkv = ctx->cfg.num_kv_heads;
+  a.NBmax = ctx->cfg.max_blocks;
+  a.K = ctx->cfg.topk;
+  a.U = ctx->U;
+  return ctx->cuda(launch_append(a, s), "append launch");
+}
+
+OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow, void* stream) {
+  if (!ctx) return OASIS_EINVAL;
+  if (step < 0 || grow < 0) return ctx->fail(OASIS_EINVAL, "advance: bad argument");
+  if (int rc = ctx->set_device()) return rc;
+  return ctx->cuda(launch_advance(ctx->ctx_tab(step), ctx->ctx_tab(step + 1),
+                                  ctx->cfg.num_requests, grow, static_cast<cudaStream_t>(stream)),
+                   "advance launch");
+}
+
+OASIS_API int oasis_profile_enable(oasis_ctx* ctx, int enable) {
+  if (!ctx) return OASIS_EINVAL;
+  ctx->prof = enable != 0;
+  ctx->prof_used = 0;
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_profile_read(oasis_ctx* ctx, double* ms_sum4, int64_t* count4) {
+  if (!ctx || !ms_sum4 || !count4) return OASIS_EINVAL;
+  if (int rc = ctx->set_device()) return rc;
+  if (int rc = ctx->cuda(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) return rc;
+  for (int k = 0; k < 4; ++k) {
+    ms_sum4[k] = 0.0;
+    count4[k] = 0;
+  }
+  for (size_t i = 0; i < ctx->prof_used; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, ctx->prof_pool[i].a, ctx->prof_pool[i].b) == cudaSuccess) {
+      ms_sum4[ctx->prof_kind[i]] += ms;
+      count4[ctx->prof_kind[i]] += 1;
+    }
+  }
+  ctx->prof_used = 0;
+  return OASIS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,316 @@
+// attn.cu -- look-ahead attention (step a1).
+//
+// One shared pass serves the normal and the draft query of every query head
+// of a KV head over that head's resident blocks ("Pith review of OasisKV",
+// section "What carries the argument": one shared attention kernel processes
+// the normal token and the draft token over the same resident sparse KV set).
+//
+// GB300 mapping.  One CTA per (request, KV head); four warps, each streaming
+// its own share of the resident units through a private two-deep ring of
+// 8 KiB shared-memory stages filled by TMA tensor copies (128-byte swizzle,
+// so ldmatrix reads are bank-conflict free).  The contraction per 16-token
+// unit is tiny (16 tokens x 8 query vectors x 128 dims), so it runs on
+// mma.sync m16n8k16 with the tokens as M and the 2 x G <= 8 query vectors as
+// N: S^T = K_unit * Q^T, online softmax over tokens, then O^T += V^T * P^T
+// with P^T moved into the B-operand layout by movmatrix.  The kernel is
+// bound by HBM reads of the resident units (8 KiB per unit).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace oasis {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 2;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStageBytes = kUnitBytes;            // 8 KiB: [half][32 rows][128 B]
+constexpr int kRingBytes = kWarps * kStages * kStageBytes;
+constexpr int kBarOffset = kRingBytes;
+constexpr int kListOffset = kBarOffset + 256;
+constexpr int kCountOffset = kListOffset + kMaxTopK * 8;
+constexpr int kSmemBytes = kCountOffset + 16 + 1024;  // + alignment slack
+
+struct UnitRef {
+  int unit;   // global pool unit index (pair * U + phys slot unit)
+  int valid;  // valid tokens, 1..16
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t s = smem_u32(p);
+  return p + ((1024u - (s & 1023u)) & 1023u);
+}
+
+// Byte offset of (row, 16-byte chunk) inside one 64-column half of a stage,
+// as written by a TMA copy with 128-byte swizzle into a 1024-aligned buffer.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kThreads)
+    attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap pool_map) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOffset);
+  UnitRef* list = reinterpret_cast<UnitRef*>(base + kListOffset);
+  int* count_s = reinterpret_cast<int*>(base + kCountOffset);
+
+  const int pair = blockIdx.x;
+  const int r = pair / a.Hkv;
+  const int h = pair - r * a.Hkv;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ctx = a.ctx_len[r];
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kWarps * kStages; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+    prefetch_tensormap(&pool_map);
+  }
+  if (warp == 0) {
+    // Compact the occupied slots (in slot order) into the unit list.
+    const int32_t* res = a.res + static_cast<size_t>(pair) * a.K;
+    const int32_t* phys = a.phys + static_cast<size_t>(pair) * a.U;
+    int n = 0;
+    for (int c = 0; c < a.K; c += 32) {
+      const int s = c + lane;
+      bool ok = false;
+      int unit = 0, valid = 0;
+      if (s < a.K) {
+        const int id = res[s];
+        if (id >= 0) {
+          valid = min(kBlock, ctx - id * kBlock);
+          unit = phys[s];
+          if (id >= a.NBmax || valid <= 0) {
+            raise_error(a.err, kErrBadBlock);
+          } else if (unit < 0 || unit >= a.U) {
+            raise_error(a.err, kErrBadUnit);
+          } else {
+            ok = true;
+          }
+        }
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, ok);
+      if (ok) {
+        UnitRef u;
+        u.unit = pair * a.U + unit;
+        u.valid = valid;
+        list[n + __popc(bal & ((1u << lane) - 1u))] = u;
+      }
+      n += __popc(bal);
+    }
+    if (lane == 0) *count_s = n;
+  }
+
+  // B fragments of Q^T (d x 8 query vectors): column n = which * 4 + gi,
+  // which 0 = normal query, 1 = draft query; gi = query head within the group.
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  uint32_t qf[8][2];
+  {
+    const int which = g >> 2, gi = g & 3;
+    if (gi < a.G) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(
+          static_cast<const __nv_bfloat16*>(which ? a.qd : a.q) +
+          (static_cast<size_t>(r) * a.Hq + h * a.G + gi) * kHeadDim);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qf[kk][0] = __ldg(src + 8 * kk + t);
+        qf[kk][1] = __ldg(src + 8 * kk + 4 + t);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) qf[kk][0] = qf[kk][1] = 0u;
+    }
+  }
+  __syncthreads();
+
+  const int n_units = *count_s;
+  const int my_count = n_units > warp ? (n_units - warp + kWarps - 1) / kWarps : 0;
+  uint8_t* my_ring = base + warp * kStages * kStageBytes;
+  uint64_t* my_bars = bars + warp * kStages;
+
+  auto issue = [&](int k) {
+    const int st = k % kStages;
+    const int y = list[warp + k * kWarps].unit * (2 * kBlock);
+    uint8_t* dst = my_ring + st * kStageBytes;
+    mbar_arrive_expect_tx(&my_bars[st], kStageBytes);
+    tma_load_2d(dst, &pool_map, 0, y, &my_bars[st]);
+    tma_load_2d(dst + kStageBytes / 2, &pool_map, 64, y, &my_bars[st]);
+  };
+  if (lane == 0) {
+    for (int k = 0; k < kStages && k < my_count; ++k) issue(k);
+  }
+
+  // Per-lane ldmatrix row/chunk constants.
+  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;  // K rows (tokens)
+  const int kch = lane >> 4;
+  const int vrow = kBlock + (lane & 7) + ((lane >> 4) & 1) * 8;  // V rows
+  const int vch = (lane >> 3) & 1;
+
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const float sc = a.scale_log2;
+
+  int k = 0;
+  bool failed = false;
+  for (; k < my_count; ++k) {
+    const int st = k % kStages;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&my_bars[st], (k / kStages) & 1));
+    if (!ok) {
+      failed = true;
+      break;
+    }
+    const int valid = list[warp + k * kWarps].valid;
+    uint8_t* stage = my_ring + st * kStageBytes;
+    const uint32_t sb = smem_u32(stage);
+
+    // S^T (16 tokens x 8 queries) = K_unit (16 x 128) * Q^T (128 x 8)
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const int half = kk >> 2;
+      const int chunk = (kk & 3) * 2 + kch;
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(sb + half * (kStageBytes / 2) + swz(krow, chunk), a0, a1, a2, a3);
+      mma_bf16_16816(s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+    }
+
+    // Online softmax over tokens (rows g, g+8) per query column (2t, 2t+1).
+    float x0 = s[0] * sc, x1 = s[1] * sc, x2 = s[2] * sc, x3 = s[3] * sc;
+    if (g >= valid) x0 = x1 = -INFINITY;
+    if (g + 8 >= valid) x2 = x3 = -INFINITY;
+    float t0 = fmaxf(x0, x2), t1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+      t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+    }
+    const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+    l0 = l0 * al0 + p0 + p2;
+    l1 = l1 * al1 + p1 + p3;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+    const uint32_t b0 = movmatrix_t(pack_bf16x2(p0, p1));
+    const uint32_t b1 = movmatrix_t(pack_bf16x2(p2, p3));
+
+    if (valid < kBlock) {
+      // Zero the value rows past the context so that 0 * garbage stays 0.
+      const int nchunks = (kBlock - valid) * 16;
+      for (int j = lane; j < nchunks; j += 32) {
+        const int row = kBlock + valid + (j >> 4);
+        const int half = (j >> 3) & 1;
+        *reinterpret_cast<uint4*>(stage + half * (kStageBytes / 2) + row * 128 +
+                                  ((j & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+    }
+
+    // O^T (128 dims x 8 queries) += V^T (128 x 16 tokens) * P^T (16 x 8)
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int half = mt >> 2;
+      const int chunk = (mt & 3) * 2 + vch;
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(sb + half * (kStageBytes / 2) + swz(vrow, chunk), a0, a1, a2, a3);
+      mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+    }
+    __syncwarp();
+    if (lane == 0 && k + kStages < my_count) issue(k + kStages);
+  }
+  if (failed) {
+    if (lane == 0) raise_error(a.err, kErrTimeout);
+    // Drain this warp's copies still in flight before the ring is reused.
+    for (int kk = k; kk < my_count && kk < k + kStages; ++kk)
+      (void)mbar_wait(&my_bars[kk % kStages], (kk / kStages) & 1);
+  }
+
+  // Row sums: reduce over the 8 lanes that share t.
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+
+  __syncthreads();  // every ring slot has been consumed: reuse as merge space
+  float* mo = reinterpret_cast<float*>(base);           // [kWarps][8][128]
+  float* mm = mo + kWarps * 8 * kHeadDim;               // [kWarps][8]
+  float* ml = mm + kWarps * 8;                          // [kWarps][8]
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int d0 = mt * 16 + g;
+    mo[(warp * 8 + 2 * t) * kHeadDim + d0] = o[mt][0];
+    mo[(warp * 8 + 2 * t + 1) * kHeadDim + d0] = o[mt][1];
+    mo[(warp * 8 + 2 * t) * kHeadDim + d0 + 8] = o[mt][2];
+    mo[(warp * 8 + 2 * t + 1) * kHeadDim + d0 + 8] = o[mt][3];
+  }
+  if (g == 0) {
+    mm[warp * 8 + 2 * t] = m0;
+    mm[warp * 8 + 2 * t + 1] = m1;
+    ml[warp * 8 + 2 * t] = l0;
+    ml[warp * 8 + 2 * t + 1] = l1;
+  }
+  __syncthreads();
+
+  for (int e = threadIdx.x; e < 8 * kHeadDim; e += kThreads) {
+    const int n = e >> 7;
+    const int dd = e & (kHeadDim - 1);
+    const int which = n >> 2, gi = n & 3;
+    if (gi >= a.G) continue;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, mm[w * 8 + n]);
+    float acc = 0.f, den = 0.f;
+    if (mx > -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = exp2f(mm[w * 8 + n] - mx);
+        acc += f * mo[(w * 8 + n) * kHeadDim + dd];
+        den += f * ml[w * 8 + n];
+      }
+    }
+    const float v = den > 0.f ? acc / den : 0.f;
+    const size_t idx = (static_cast<size_t>(r) * a.Hq + h * a.G + gi) * kHeadDim + dd;
+    void* dst = which ? a.outd : a.out;
+    if (a.out_fp32)
+      static_cast<float*>(dst)[idx] = v;
+    else
+      static_cast<__nv_bfloat16*>(dst)[idx] = __float2bfloat16_rn(v);
+  }
+}
+
+}  // namespace
+
+size_t attention_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
+                             cudaStream_t s) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int grid = a.R * a.Hkv;
+  if (grid == 0) return cudaSuccess;
+  attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, *pool_map);
+  return cudaGetLastError();
+}
+
+}  // namespace oasis

@@ -1,0 +1,98 @@
+// kernels.h -- host-side launchers of the look-ahead sparse decode kernels.
+// Plain C++ structs, no torch types; used by the C ABI in api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace oasis {
+
+struct AttnArgs {
+  const void* q;         // [R][Hq][d] bf16
+  const void* qd;        // [R][Hq][d] bf16
+  void* out;             // [R][Hq][d] bf16 or fp32
+  void* outd;            // [R][Hq][d] bf16 or fp32
+  const int32_t* res;    // [R][Hkv][K]  table of this step
+  const int32_t* phys;   // [R][Hkv][U]  table of this step
+  const int32_t* ctx_len;  // [R]        table of this step
+  uint32_t* err;
+  int R, Hq, Hkv, G, K, U, NBmax;
+  float scale_log2;      // softmax scale * log2(e)
+  int out_fp32;
+};
+
+struct ScoreArgs {
+  const void* qd;        // [R][Hq][d] bf16
+  const void* summ;      // [R][Hkv][NBmax][2][d] bf16
+  const int32_t* ctx_len;  // [R]
+  int32_t* topk_ids;     // [R][Hkv][K]
+  float* topk_scores;    // [R][Hkv][K] or null
+  uint32_t* err;
+  int R, Hq, Hkv, G, K, NBmax;
+};
+
+struct AdmitArgs {
+  const int32_t* topk;       // [R][Hkv][K]
+  const int32_t* res_cur;    // [R][Hkv][K]
+  int32_t* res_nxt;          // [R][Hkv][K]
+  int32_t* stamps;           // [R][Hkv][K]
+  const int32_t* phys_cur;   // [R][Hkv][U]
+  int32_t* phys_nxt;         // [R][Hkv][U]
+  int32_t* admit_ids;        // [R][Hkv][C]
+  int32_t* admit_slots;      // [R][Hkv][C]
+  int32_t* evict_ids;        // [R][Hkv][C]
+  int32_t* n_admit;          // [R][Hkv]
+  int R, Hkv, K, C, U, step;
+};
+
+// Copies 8 KiB units host -> pool.  Item i of pair p = (r, h) reads block
+// src_ids[p*items + i] (skipped if < 0 or i >= n_valid[p]) and writes pool
+// unit phys[p*U + slot], slot = dst_slots ? dst_slots[p*items + i] : i.
+struct GatherArgs {
+  const void* host;          // device alias of the pinned store
+  void* pool;
+  const int32_t* src_ids;
+  const int32_t* dst_slots;  // may be null
+  const int32_t* n_valid;    // may be null
+  const int32_t* phys;
+  uint32_t* err;
+  int pairs, items, NBmax, U;
+};
+
+struct SummaryArgs {
+  const void* host;          // device alias of the pinned store
+  void* summ;
+  const int32_t* ctx_len;
+  int R, Hkv, NBmax;
+};
+
+struct AppendArgs {
+  const void* k_new;         // [R][Hkv][d]
+  const void* v_new;
+  void* host;                // device alias of the pinned store
+  void* summ;
+  void* pool;
+  const int32_t* ctx_len;    // the step's table
+  const int32_t* res_nxt;
+  const int32_t* phys_nxt;
+  uint32_t* err;
+  int R, Hkv, NBmax, K, U;
+};
+
+cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
+                             cudaStream_t s);
+cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_admit(const AdmitArgs& a, cudaStream_t s);
+cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+cudaError_t launch_init_tables(int32_t* phys, int32_t* stamps, int pairs,
+                               int K, int U, cudaStream_t s);
+cudaError_t launch_summary_build(const SummaryArgs& a, cudaStream_t s);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_advance(const int32_t* cur, int32_t* nxt, int R, int grow,
+                           cudaStream_t s);
+
+size_t attention_smem_bytes();
+size_t score_topk_smem_bytes(int K);
+
+}  // namespace oasis

@@ -1,0 +1,325 @@
+// score_topk.cu -- summary scan and head-wise top-K (steps a2 + a3).
+//
+// The draft query scores every logical block of its request from the
+// per-block min/max key summaries and the blocks are ranked head-wise
+// ("Pith review of OasisKV", section "What carries the argument": the draft
+// query scans compressed key summaries, coordinate-wise min/max per block in
+// the style of Quest, and produces a head-wise top-K ranking of all logical
+// blocks without restoring any keys).
+//
+// Score of block b for KV head h (group = the G query heads of h):
+//   s[b] = sum_j sum_i max(qd_ji * mn_bi, qd_ji * mx_bi).
+// Because mn <= mx, max(x*mn, x*mx) = max(x,0)*mx + min(x,0)*mn, so the sum
+// over the group folds into one dot product of length 2d with the weights
+// W+ = sum_j max(qd_j, 0) (on the max row) and W- = sum_j min(qd_j, 0) (on
+// the min row).  Each block then costs 256 multiply-adds on 512 bytes: the
+// scan is a pure HBM stream.
+//
+// GB300 mapping.  One CTA per (request, KV head): a producer warp streams the
+// request's contiguous summary rows through a 3-deep ring of 16 KiB stages
+// with 1-D bulk copies; eight consumer warps each score 4 blocks per stage
+// (one 16-byte load per lane per block, transposed shuffle reduction), keep
+// a running top-KP list in registers (bitonic sort of each filled buffer of
+// KP keys, then a bitonic merge), and finally merge their lists in a tree.
+// Keys are 64-bit: order-preserving score bits above the complemented block
+// id, so ties break to the lower id and all keys are distinct.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace oasis {
+namespace {
+
+constexpr int kCW = 8;                       // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;     // + one producer warp
+constexpr int kChunk = 32;                   // blocks per stage
+constexpr int kChunkBytes = kChunk * kSummBytes;  // 16 KiB
+constexpr int kStages = 3;
+
+template <int KPL>
+struct Layout {
+  static constexpr int KP = 32 * KPL;
+  static constexpr int ring = 0;
+  static constexpr int bars = kStages * kChunkBytes;
+  static constexpr int keys = bars + 64;     // [kCW][KP] uint64
+  static constexpr int total = keys + kCW * KP * 8 + 128;
+};
+
+// One compare-exchange stage over E = 32*KPL keys (key e = i*32 + lane in
+// x[i]); partner e ^ j; the block of `size` keys holding e is ordered
+// descending when ((e & size) == 0) == desc.
+template <int KPL>
+__device__ __forceinline__ void bitonic_stage(uint64_t (&x)[KPL], int size,
+                                              int j, bool desc) {
+  const int lane = threadIdx.x & 31;
+  if (j >= 32) {
+    const int jr = j >> 5;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      if ((i & jr) == 0) {
+        const int p = i | jr;
+        const int e = i * 32 + lane;
+        const bool d = ((e & size) == 0) == desc;
+        const uint64_t lo = x[i], hi = x[p];
+        const bool sw = d ? (lo < hi) : (lo > hi);
+        x[i] = sw ? hi : lo;
+        x[p] = sw ? lo : hi;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int e = i * 32 + lane;
+      const uint64_t y = __shfl_xor_sync(0xffffffffu, x[i], j);
+      const bool lower = (lane & j) == 0;
+      const bool d = ((e & size) == 0) == desc;
+      const bool take_max = (lower == d);
+      x[i] = take_max ? (x[i] > y ? x[i] : y) : (x[i] < y ? x[i] : y);
+    }
+  }
+}
+
+template <int KPL>
+__device__ __forceinline__ void bitonic_sort(uint64_t (&x)[KPL], bool desc) {
+  constexpr int E = 32 * KPL;
+#pragma unroll
+  for (int size = 2; size <= E; size <<= 1) {
+#pragma unroll
+    for (int j = size >> 1; j > 0; j >>= 1) bitonic_stage<KPL>(x, size, j, desc);
+  }
+}
+
+// a (descending) <- top E of a U b, descending; b must be ascending.
+template <int KPL>
+__device__ __forceinline__ void merge_top(uint64_t (&a)[KPL],
+                                          const uint64_t (&b)[KPL]) {
+  constexpr int E = 32 * KPL;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) a[i] = a[i] > b[i] ? a[i] : b[i];
+#pragma unroll
+  for (int j = E >> 1; j > 0; j >>= 1) bitonic_stage<KPL>(a, E, j, true);
+}
+
+template <int KPL>
+__global__ void __launch_bounds__(kThreads)
+    score_topk_kernel(const ScoreArgs a) {
+  using L = Layout<KPL>;
+  constexpr int KP = L::KP;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem + L::ring;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);
+  uint64_t* empty = full + kStages;
+  uint64_t* keybuf = reinterpret_cast<uint64_t*>(smem + L::keys);
+
+  const int pair = blockIdx.x;
+  const int r = pair / a.Hkv;
+  const int h = pair - r * a.Hkv;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ctx = a.ctx_len[r];
+  int nb = ctx > 0 ? (ctx + kBlock - 1) / kBlock : 0;
+  if (nb > a.NBmax) {
+    if (threadIdx.x == 0) raise_error(a.err, kErrBadBlock);
+    nb = a.NBmax;
+  }
+  const int nchunks = (nb + kChunk - 1) / kChunk;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kCW);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  uint64_t top[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) top[i] = 0ull;
+
+  if (warp == kCW) {
+    // ---------------- producer: stream this (r, h)'s summary rows
+    if (lane == 0) {
+      const uint8_t* src = static_cast<const uint8_t*>(a.summ) +
+                           static_cast<size_t>(pair) * a.NBmax * kSummBytes;
+      int c = 0;
+      bool ok = true;
+      for (; c < nchunks && ok; ++c) {
+        const int st = c % kStages;
+        if (c >= kStages) ok = mbar_wait(&empty[st], ((c / kStages) - 1) & 1);
+        if (!ok) break;
+        const int nblk = min(kChunk, nb - c * kChunk);
+        const uint32_t bytes = static_cast<uint32_t>(nblk) * kSummBytes;
+        mbar_arrive_expect_tx(&full[st], bytes);
+        bulk_g2s(ring + st * kChunkBytes,
+                 src + static_cast<size_t>(c) * kChunkBytes, bytes, &full[st]);
+      }
+      if (!ok) raise_error(a.err, kErrTimeout);
+      // Drain: the latest phase issued on each stage must have landed before
+      // the CTA may exit (a no-op on the normal path).
+      for (int cc = max(0, c - kStages); cc < c; ++cc)
+        (void)mbar_wait(&full[cc % kStages], (cc / kStages) & 1);
+    }
+  } else {
+    // ---------------- consumers: score, then keep a running top-KP
+    // Lane weights: lanes 0-15 cover the min row, 16-31 the max row, 8 dims each.
+    const int row = lane >> 4;
+    const int d0 = (lane & 15) * 8;
+    float w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0.f;
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.qd) +
+                              (static_cast<size_t>(r) * a.Hq + h * a.G) * kHeadDim + d0;
+    for (int gi = 0; gi < a.G; ++gi) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qg + gi * kHeadDim));
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = bf16lo(wd[i]), hi = bf16hi(wd[i]);
+        w[2 * i] += row ? fmaxf(lo, 0.f) : fminf(lo, 0.f);
+        w[2 * i + 1] += row ? fmaxf(hi, 0.f) : fminf(hi, 0.f);
+      }
+    }
+    uint64_t* mybuf = keybuf + warp * KP;
+    int cnt = 0;
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c % kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (c / kStages) & 1));
+      if (!ok) break;
+      const int nblk = min(kChunk, nb - c * kChunk);
+      const uint8_t* stage = ring + st * kChunkBytes;
+      float v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = warp * 4 + q;
+        float acc = 0.f;
+        if (j < nblk) {
+          const uint4 u = *reinterpret_cast<const uint4*>(stage + j * kSummBytes + lane * 16);
+          acc = w[0] * bf16lo(u.x);
+          acc = fmaf(w[1], bf16hi(u.x), acc);
+          acc = fmaf(w[2], bf16lo(u.y), acc);
+          acc = fmaf(w[3], bf16hi(u.y), acc);
+          acc = fmaf(w[4], bf16lo(u.z), acc);
+          acc = fmaf(w[5], bf16hi(u.z), acc);
+          acc = fmaf(w[6], bf16lo(u.w), acc);
+          acc = fmaf(w[7], bf16hi(u.w), acc);
+        }
+        v[q] = acc;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      // Transposed reduction of 4 values over 32 lanes: 6 shuffles.
+      const bool b4 = lane & 16, b3 = lane & 8;
+      float k0 = b4 ? v[2] : v[0], k1 = b4 ? v[3] : v[1];
+      const float s0 = b4 ? v[0] : v[2], s1 = b4 ? v[1] : v[3];
+      k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+      k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+      float x = b3 ? k1 : k0;
+      x += __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
+      x += __shfl_xor_sync(0xffffffffu, x, 4);
+      x += __shfl_xor_sync(0xffffffffu, x, 2);
+      x += __shfl_xor_sync(0xffffffffu, x, 1);
+      // lane 8q' holds block warp*4 + q' with q' = (lane>>4)*2 + ((lane>>3)&1)
+      const int q = ((lane >> 4) << 1) | ((lane >> 3) & 1);
+      const int nv = max(0, min(4, nblk - warp * 4));
+      if ((lane & 7) == 0 && q < nv) {
+        const uint32_t b = static_cast<uint32_t>(c * kChunk + warp * 4 + q);
+        mybuf[cnt + q] = (static_cast<uint64_t>(float_key(x)) << 32) | (~b);
+      }
+      cnt += nv;
+      if (cnt == KP) {
+        __syncwarp();
+        uint64_t nk[KPL];
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) nk[i] = mybuf[i * 32 + lane];
+        __syncwarp();
+        bitonic_sort<KPL>(nk, false);
+        merge_top<KPL>(top, nk);
+        cnt = 0;
+      }
+    }
+    if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
+    if (cnt > 0) {
+      __syncwarp();
+      uint64_t nk[KPL];
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) {
+        const int e = i * 32 + lane;
+        nk[i] = e < cnt ? mybuf[e] : 0ull;
+      }
+      __syncwarp();
+      bitonic_sort<KPL>(nk, false);
+      merge_top<KPL>(top, nk);
+    }
+  }
+
+  // ---------------- tree merge of the consumer warps' lists
+#pragma unroll 1
+  for (int sz = 1; sz < kCW; sz <<= 1) {
+    __syncthreads();
+    if (warp < kCW && (warp % (2 * sz)) == sz) {
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) keybuf[warp * KP + i * 32 + lane] = top[i];
+    }
+    __syncthreads();
+    if (warp < kCW && (warp % (2 * sz)) == 0) {
+      const uint64_t* p = keybuf + (warp + sz) * KP;
+      uint64_t nk[KPL];
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) nk[i] = p[KP - 1 - (i * 32 + lane)];
+      merge_top<KPL>(top, nk);
+    }
+  }
+
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int e = i * 32 + lane;
+      if (e < a.K) {
+        const uint64_t key = top[i];
+        const int id = key == 0ull ? -1 : static_cast<int>(~static_cast<uint32_t>(key));
+        a.topk_ids[static_cast<size_t>(pair) * a.K + e] = id;
+        if (a.topk_scores)
+          a.topk_scores[static_cast<size_t>(pair) * a.K + e] =
+              key == 0ull ? -INFINITY : key_float(static_cast<uint32_t>(key >> 32));
+      }
+    }
+  }
+}
+
+template <int KPL>
+cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(score_topk_kernel<KPL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Layout<KPL>::total);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int grid = a.R * a.Hkv;
+  if (grid == 0) return cudaSuccess;
+  score_topk_kernel<KPL><<<grid, kThreads, Layout<KPL>::total, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t score_topk_smem_bytes(int K) {
+  if (K <= 32) return Layout<1>::total;
+  if (K <= 64) return Layout<2>::total;
+  if (K <= 128) return Layout<4>::total;
+  return Layout<8>::total;
+}
+
+cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s) {
+  if (a.K <= 32) return launch_kpl<1>(a, s);
+  if (a.K <= 64) return launch_kpl<2>(a, s);
+  if (a.K <= 128) return launch_kpl<4>(a, s);
+  return launch_kpl<8>(a, s);
+}
+
+}  // namespace oasis

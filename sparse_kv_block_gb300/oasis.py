@@ -1,0 +1,302 @@
+"""ctypes binding of the C ABI in ``include/oasis.h`` (``liboasis.so``).
+
+Every function here marshals arguments and calls the library; all device
+work runs in the library's CUDA kernels.  PyTorch is used only to allocate
+device / pinned memory and to name streams.  If the library is missing the
+import fails loudly: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_double, c_float, c_int, c_int32, c_int64, c_size_t, c_uint32, c_void_p
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liboasis.so")
+
+OASIS_OK, OASIS_EINVAL, OASIS_ENOMEM, OASIS_ECUDA = 0, -1, -2, -3
+OASIS_ETIMEOUT, OASIS_ESTATE, OASIS_EDEVICE = -4, -5, -6
+STATUS_NAMES = {0: "OK", -1: "EINVAL", -2: "ENOMEM", -3: "ECUDA", -4: "ETIMEOUT",
+                -5: "ESTATE", -6: "EDEVICE"}
+
+
+class oasis_config(ctypes.Structure):
+    _fields_ = [("num_layers", c_int32), ("num_requests", c_int32), ("max_blocks", c_int32),
+                ("num_q_heads", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
+                ("block_size", c_int32), ("topk", c_int32), ("fetch_ratio", c_float),
+                ("softmax_scale", c_float), ("out_fp32", c_int32), ("device", c_int32)]
+
+
+class oasis_sizes(ctypes.Structure):
+    _fields_ = [("kv_pool_bytes", c_size_t), ("summaries_bytes", c_size_t),
+                ("host_kv_bytes", c_size_t), ("res_ids_bytes", c_size_t),
+                ("stamps_bytes", c_size_t), ("phys_bytes", c_size_t),
+                ("ctx_len_bytes", c_size_t), ("workspace_bytes", c_size_t),
+                ("fetch_cap", c_int32), ("units_per_head", c_int32)]
+
+
+class oasis_buffers(ctypes.Structure):
+    _fields_ = [("kv_pool", POINTER(c_void_p)), ("summaries", POINTER(c_void_p)),
+                ("host_kv", POINTER(c_void_p)), ("res_ids", POINTER(c_void_p)),
+                ("stamps", POINTER(c_void_p)), ("phys", POINTER(c_void_p)),
+                ("ctx_len", c_void_p), ("workspace", c_void_p)]
+
+
+class OasisError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+# Declared exports: name -> (restype, argtypes).  Tests check this list against
+# include/oasis.h.
+_P = c_void_p
+EXPORTS = {
+    "oasis_config_error": (c_char_p, [POINTER(oasis_config)]),
+    "oasis_query_sizes": (c_int, [POINTER(oasis_config), POINTER(oasis_sizes)]),
+    "oasis_init": (c_int, [POINTER(oasis_config), POINTER(oasis_buffers), POINTER(c_void_p)]),
+    "oasis_destroy": (c_int, [_P]),
+    "oasis_last_error": (c_char_p, [_P]),
+    "oasis_sync": (c_int, [_P, POINTER(c_uint32)]),
+    "oasis_build_summaries": (c_int, [_P, c_int, c_int, _P]),
+    "oasis_load_resident": (c_int, [_P, c_int, c_int, _P]),
+    "oasis_lookahead_attn": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
+    "oasis_score_topk": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
+    "oasis_admit_evict": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P, _P]),
+    "oasis_prefetch": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
+    "oasis_step": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
+    "oasis_join": (c_int, [_P, c_int, _P]),
+    "oasis_step_host": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
+    "oasis_step_lists": (c_int, [_P, c_int, POINTER(c_void_p), POINTER(c_void_p),
+                                 POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
+                                 POINTER(c_void_p)]),
+    "oasis_append_token": (c_int, [_P, c_int, c_int, _P, _P, _P]),
+    "oasis_advance_context": (c_int, [_P, c_int, c_int, _P]),
+    "oasis_profile_enable": (c_int, [_P, c_int]),
+    "oasis_profile_read": (c_int, [_P, POINTER(c_double), POINTER(c_int64)]),
+}
+
+_lib = None
+
+
+def lib():
+    """Load liboasis.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        import torch.cuda  # noqa: F401  (loads the CUDA runtime the library links)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in EXPORTS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def make_config(R, NBmax, Hq, Hkv, K, fetch_ratio, layers=1, softmax_scale=0.0,
+                out_fp32=False, device=0, d=128, B=16) -> oasis_config:
+    return oasis_config(layers, R, NBmax, Hq, Hkv, d, B, K, fetch_ratio, softmax_scale,
+                        1 if out_fp32 else 0, device)
+
+
+def oasis_config_error(cfg: oasis_config) -> Optional[str]:
+    m = lib().oasis_config_error(ctypes.byref(cfg))
+    return None if m is None else m.decode()
+
+
+def oasis_query_sizes(cfg: oasis_config) -> oasis_sizes:
+    out = oasis_sizes()
+    rc = lib().oasis_query_sizes(ctypes.byref(cfg), ctypes.byref(out))
+    if rc != OASIS_OK:
+        raise OasisError(rc, oasis_config_error(cfg) or "query_sizes failed")
+    return out
+
+
+class Oasis:
+    """A library context plus the caller-owned buffers it was given.
+
+    Buffers are allocated with torch (device memory and pinned host memory
+    for the KV store unless ``host_kv`` tensors are passed in) and kept alive
+    here.  Methods map one-to-one onto the C ABI calls.
+    """
+
+    def __init__(self, cfg: oasis_config, host_kv: Optional[Sequence[torch.Tensor]] = None):
+        self.cfg = cfg
+        self.sizes = oasis_query_sizes(cfg)
+        L, R, Hkv = cfg.num_layers, cfg.num_requests, cfg.num_kv_heads
+        K, U, NB = cfg.topk, self.sizes.units_per_head, cfg.max_blocks
+        self.C, self.U = self.sizes.fetch_cap, U
+        dev = torch.device("cuda", cfg.device)
+        self.device = dev
+        if host_kv is None:
+            host_kv = [torch.zeros((R, Hkv, NB, 2, 16, 128), dtype=torch.bfloat16,
+                                   pin_memory=True) for _ in range(L)]
+        if len(host_kv) != L:
+            raise ValueError("need one host store per layer")
+        for t in host_kv:
+            if t.numel() * t.element_size() != self.sizes.host_kv_bytes or not t.is_pinned():
+                raise ValueError("host_kv must be pinned and of host_kv_bytes")
+        self.host_kv = list(host_kv)
+        self.kv_pool = [torch.zeros((R, Hkv, U, 2, 16, 128), dtype=torch.bfloat16, device=dev)
+                        for _ in range(L)]
+        self.summaries = [torch.zeros((R, Hkv, NB, 2, 128), dtype=torch.bfloat16, device=dev)
+                          for _ in range(L)]
+        self.res_ids = [torch.full((2, R, Hkv, K), -1, dtype=torch.int32, device=dev)
+                        for _ in range(L)]
+        self.stamps = [torch.full((R, Hkv, K), -1, dtype=torch.int32, device=dev)
+                       for _ in range(L)]
+        self.phys = [torch.zeros((2, R, Hkv, U), dtype=torch.int32, device=dev) for _ in range(L)]
+        self.ctx_len = torch.zeros((2, R), dtype=torch.int32, device=dev)
+        self.workspace = torch.zeros(self.sizes.workspace_bytes, dtype=torch.uint8, device=dev)
+
+        def arr(ts):
+            a = (c_void_p * L)(*[t.data_ptr() for t in ts])
+            return a
+        self._arrs = [arr(self.kv_pool), arr(self.summaries), arr(self.host_kv),
+                      arr(self.res_ids), arr(self.stamps), arr(self.phys)]
+        bufs = oasis_buffers(*[ctypes.cast(a, POINTER(c_void_p)) for a in self._arrs],
+                             self.ctx_len.data_ptr(), self.workspace.data_ptr())
+        handle = c_void_p()
+        torch.cuda.synchronize(dev)
+        rc = lib().oasis_init(ctypes.byref(cfg), ctypes.byref(bufs), ctypes.byref(handle))
+        if rc != OASIS_OK:
+            raise OasisError(rc, oasis_config_error(cfg) or "oasis_init failed "
+                             "(buffers not pinned/mapped, or CUDA error)")
+        self.ctx = handle.value
+
+    # ------------------------------------------------------------------ util
+    def _check(self, rc: int) -> None:
+        if rc != OASIS_OK:
+            raise OasisError(rc, lib().oasis_last_error(self.ctx).decode())
+
+    def close(self) -> None:
+        if getattr(self, "ctx", None):
+            lib().oasis_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ------------------------------------------------------------ C ABI calls
+    def oasis_sync(self) -> int:
+        bits = c_uint32(0)
+        rc = lib().oasis_sync(self.ctx, ctypes.byref(bits))
+        if rc not in (OASIS_OK, OASIS_EDEVICE):
+            self._check(rc)
+        if rc == OASIS_EDEVICE:
+            raise OasisError(rc, f"device error bits 0x{bits.value:x}")
+        return bits.value
+
+    def oasis_build_summaries(self, layer: int, table: int = 0, stream=None) -> None:
+        self._check(lib().oasis_build_summaries(self.ctx, layer, table, _stream(stream)))
+
+    def oasis_load_resident(self, layer: int, first_step: int = 0, stream=None) -> None:
+        self._check(lib().oasis_load_resident(self.ctx, layer, first_step, _stream(stream)))
+
+    def oasis_lookahead_attn(self, layer, step, q, qd, out, outd, stream=None) -> None:
+        self._check(lib().oasis_lookahead_attn(self.ctx, layer, step, _ptr(q), _ptr(qd),
+                                               _ptr(out), _ptr(outd), _stream(stream)))
+
+    def oasis_score_topk(self, layer, step, qd, topk_ids, topk_scores=None, stream=None) -> None:
+        self._check(lib().oasis_score_topk(self.ctx, layer, step, _ptr(qd), _ptr(topk_ids),
+                                           _ptr(topk_scores), _stream(stream)))
+
+    def oasis_admit_evict(self, layer, step, topk_ids, admit_ids, admit_slots, evict_ids,
+                          n_admit, stream=None) -> None:
+        self._check(lib().oasis_admit_evict(self.ctx, layer, step, _ptr(topk_ids),
+                                            _ptr(admit_ids), _ptr(admit_slots),
+                                            _ptr(evict_ids), _ptr(n_admit), _stream(stream)))
+
+    def oasis_prefetch(self, layer, step, admit_ids, admit_slots, n_admit, stream=None) -> None:
+        self._check(lib().oasis_prefetch(self.ctx, layer, step, _ptr(admit_ids),
+                                         _ptr(admit_slots), _ptr(n_admit), _stream(stream)))
+
+    def oasis_step(self, layer, step, q, qd, out, outd, stream=None) -> None:
+        self._check(lib().oasis_step(self.ctx, layer, step, _ptr(q), _ptr(qd), _ptr(out),
+                                     _ptr(outd), _stream(stream)))
+
+    def oasis_join(self, layer, stream=None) -> None:
+        self._check(lib().oasis_join(self.ctx, layer, _stream(stream)))
+
+    def oasis_step_host(self, layer, step, q_host, qd_host, out_host, outd_host,
+                        stream=None) -> None:
+        self._check(lib().oasis_step_host(self.ctx, layer, step, _ptr(q_host), _ptr(qd_host),
+                                          _ptr(out_host), _ptr(outd_host), _stream(stream)))
+
+    def oasis_step_lists(self, layer: int) -> dict:
+        ps = [c_void_p() for _ in range(6)]
+        self._check(lib().oasis_step_lists(self.ctx, layer, *[ctypes.byref(p) for p in ps]))
+        return dict(zip(["topk_ids", "topk_scores", "admit_ids", "admit_slots", "evict_ids",
+                         "n_admit"], [p.value for p in ps]))
+
+    def oasis_append_token(self, layer, step, k_new, v_new, stream=None) -> None:
+        self._check(lib().oasis_append_token(self.ctx, layer, step, _ptr(k_new), _ptr(v_new),
+                                             _stream(stream)))
+
+    def oasis_advance_context(self, step, grow=1, stream=None) -> None:
+        self._check(lib().oasis_advance_context(self.ctx, step, grow, _stream(stream)))
+
+    def oasis_profile_enable(self, enable: bool = True) -> None:
+        self._check(lib().oasis_profile_enable(self.ctx, 1 if enable else 0))
+
+    def oasis_profile_read(self) -> tuple:
+        ms = (c_double * 4)()
+        cnt = (c_int64 * 4)()
+        self._check(lib().oasis_profile_read(self.ctx, ms, cnt))
+        return list(ms), list(cnt)
+
+    # ------------------------------------------------------- tensor views
+    def step_lists(self, layer: int) -> dict:
+        """The workspace lists of `layer` as torch tensors (views, no copy)."""
+        p = self.oasis_step_lists(layer)
+        R, Hkv, K, C = self.cfg.num_requests, self.cfg.num_kv_heads, self.cfg.topk, self.C
+        out = {}
+        for name, shape, dt in [("topk_ids", (R, Hkv, K), torch.int32),
+                                ("topk_scores", (R, Hkv, K), torch.float32),
+                                ("admit_ids", (R, Hkv, max(C, 1)), torch.int32),
+                                ("admit_slots", (R, Hkv, max(C, 1)), torch.int32),
+                                ("evict_ids", (R, Hkv, max(C, 1)), torch.int32),
+                                ("n_admit", (R, Hkv), torch.int32)]:
+            n = 1
+            for s in shape:
+                n *= s
+            off = p[name] - self.workspace.data_ptr()
+            es = torch.tensor([], dtype=dt).element_size()
+            out[name] = self.workspace[off:off + n * es].view(dt).view(shape)
+        return out
+
+    def set_context(self, lens) -> None:
+        """Set both ctx_len tables (plain host-to-device copy)."""
+        t = torch.as_tensor(lens, dtype=torch.int32)
+        self.ctx_len.copy_(t.view(1, -1).expand(2, -1))
+
+    def set_resident(self, layer: int, res, first_step: int = 0) -> None:
+        """Write the caller's resident table for `first_step` (host-to-device copy)."""
+        self.res_ids[layer][first_step & 1].copy_(torch.as_tensor(res, dtype=torch.int32))

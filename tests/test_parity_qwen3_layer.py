@@ -1,0 +1,91 @@
+"""GPU parity at the full Qwen3-8B-shaped layer (128 requests x 16384 tokens,
+32 q / 8 KV heads, K = 128, cap 0.05; 8 GiB pinned KV store), in the kernels'
+benchmark launch configuration, on sampled (request, KV head) pairs that the
+oracle follows one by one, plus properties checked on every pair."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_kv_block_gb300 import workload
+from tests import _harness as H
+
+pytestmark = pytest.mark.gpu
+
+SHAPE = workload.SHAPES["qwen3_8b_16k"]
+SAMPLE = [(0, 0), (0, 7), (5, 2), (31, 4), (64, 1), (77, 6), (100, 3), (127, 0), (127, 7)]
+
+
+@pytest.fixture(scope="module")
+def layer():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    L = H.make_layer(SHAPE, seed=0, steps=6, gen_device="cuda", pairs=SAMPLE)
+    yield L
+    L.eng.close()
+
+
+def test_summaries_sampled(layer):
+    H.check_summaries(layer, SAMPLE)
+
+
+def test_staged_lockstep_and_properties(layer):
+    dev = torch.device("cuda", 0)
+    L = layer
+    for t in range(3):
+        H.run_staged_step(L, t, dev, check_pool_every=False)
+        nxt = (t + 1) & 1
+        H.check_pool(L, nxt, SAMPLE)
+        # properties on every pair
+        res = L.eng.res_ids[0][nxt]
+        srt, _ = torch.sort(res, dim=-1)
+        assert (srt[..., 1:] != srt[..., :-1]).all(), "duplicate resident id"
+        assert int((res >= 0).sum()) == SHAPE.R * SHAPE.Hkv * SHAPE.K
+        phys = L.eng.phys[0][nxt]
+        ps, _ = torch.sort(phys, dim=-1)
+        assert torch.equal(ps, torch.arange(L.eng.U, device=dev, dtype=torch.int32).expand_as(ps))
+        # every resident unit in the pool equals its host block (all pairs)
+        host = L.host
+        for r0 in range(0, SHAPE.R, 16):
+            r1 = r0 + 16
+            ids = res[r0:r1].long().cpu()
+            want = torch.stack([host[r][torch.arange(SHAPE.Hkv)[:, None], ids[r - r0]]
+                                for r in range(r0, r1)])
+            units = phys[r0:r1, :, :SHAPE.K].long()
+            pool = L.eng.kv_pool[0][r0:r1]
+            got = pool[torch.arange(16, device=dev)[:, None, None],
+                       torch.arange(SHAPE.Hkv, device=dev)[None, :, None], units]
+            assert torch.equal(got.view(torch.int16).cpu(), want.view(torch.int16))
+
+
+def test_fused_steps_sampled(layer):
+    # oasis_step (main + side stream) continues from the lockstep state; a
+    # sampled pair leaves the check if its list differs inside the tie window.
+    dev = torch.device("cuda", 0)
+    L = layer
+    eng = L.eng
+    out = torch.empty((SHAPE.R, SHAPE.Hq, 128), dtype=torch.bfloat16, device=dev)
+    outd = torch.empty_like(out)
+    live = list(SAMPLE)
+    for t in range(3, 6):
+        eng.oasis_step(0, t, L.q[t].to(dev), L.qd[t].to(dev), out, outd)
+        eng.oasis_join(0)
+        eng.oasis_sync()
+        L.orc.pairs = live
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        H.check_attention([out.float().cpu().numpy(), outd.float().cpu().numpy()], ref, SHAPE.G)
+        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0).items()}
+        res_n = eng.res_ids[0][(t + 1) & 1].cpu().numpy()
+        keep = []
+        for (r, h), v in ref.items():
+            assert H.topk_agrees(lists["topk_ids"][r, h], v["topk"], v["scores"], SHAPE.K)
+            if not np.array_equal(lists["topk_ids"][r, h], v["topk"]):
+                continue
+            assert lists["n_admit"][r, h] == v["n_admit"]
+            assert (lists["admit_ids"][r, h, :SHAPE.C] == v["admit_ids"]).all()
+            assert (res_n[r, h] == L.orc.res[r, h]).all()
+            keep.append((r, h))
+        live = keep
+        assert len(live) >= len(SAMPLE) - 2
+        H.check_pool(L, (t + 1) & 1, live)
