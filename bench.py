@@ -203,7 +203,7 @@ def oracle_rate(shape, host, lens, q, qd, budget_s: float, steps_hint: int = 1):
 def run_reference(args, ws, rank):
     if rank != 0:
         return
-    shape = workload.SHAPES[args.workload]
+    shape = get_shape(args)
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
     lens = workload.ctx_lens(shape)
     host = torch.empty((shape.R, shape.Hkv, shape.NBmax, 2, 16, 128), dtype=torch.bfloat16,
@@ -233,6 +233,14 @@ def run_reference(args, ws, rank):
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def get_shape(args):
+    import dataclasses
+    shape = workload.SHAPES[args.workload]
+    if args.requests:
+        shape = dataclasses.replace(shape, R=args.requests, name=f"{shape.name}_r{args.requests}")
+    return shape
 
 
 def workload_desc(shape) -> str:
@@ -268,7 +276,7 @@ def run_oasis(args, ws, rank, local):
         raise RuntimeError("the CUDA path needs a GPU")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    shape = workload.SHAPES[args.workload]
+    shape = get_shape(args)
     nq = args.queries
     eng, lens, host = build_layer(shape, args.seed + rank, dev)
     q, qd = workload.queries(shape, args.seed + rank, 0, nq, device=dev)
@@ -310,7 +318,7 @@ def run_oasis(args, ws, rank, local):
     torch.cuda.synchronize(dev)
     barrier(ws)
     ms = e0.elapsed_time(e1)
-    ms_sum, counts = eng.oasis_profile_read()
+    ms_sum, counts, off_sum = eng.oasis_profile_read()
     eng.oasis_profile_enable(False)
     clk = clocks.stop()
     eng.oasis_sync()
@@ -362,6 +370,7 @@ def run_oasis(args, ws, rank, local):
     peaks = measured_peaks()
     names = ["attention", "score_topk", "admit_evict", "prefetch"]
     avg_ms = {n: (ms_sum[i] / counts[i] if counts[i] else None) for i, n in enumerate(names)}
+    avg_start = {n: (off_sum[i] / counts[i] if counts[i] else None) for i, n in enumerate(names)}
     R, Hq, Hkv, K, NB = shape.R, shape.Hq, shape.Hkv, shape.K, shape.NBmax
     qo_bytes = 4 * R * Hq * 128 * 2
     attn_bytes = R * Hkv * K * UNIT_BYTES + qo_bytes
@@ -375,7 +384,8 @@ def run_oasis(args, ws, rank, local):
             a = b / (avg_ms[n] * 1e-3) / 1e9
             per_kernel[n] = {"bound": bound, "achieved": round(a, 1), "peak": round(peak, 1),
                              "unit": "GB/s", "frac": round(a / peak, 4),
-                             "bytes_per_launch": int(b), "avg_ms": round(avg_ms[n], 5)}
+                             "bytes_per_launch": int(b), "avg_ms": round(avg_ms[n], 5),
+                             "avg_start_ms": round(avg_start[n], 5)}
     dk = per_kernel.get(dominant, per_kernel["attention"])
     roofline = {"bound": "hbm" if dk["bound"] == "hbm" else "hbm", "kernel": dominant,
                 "achieved": dk["achieved"], "peak": dk["peak"], "unit": "GB/s",
@@ -421,6 +431,8 @@ def main():
     ap.add_argument("--queries", type=int, default=64, help="distinct query steps, cycled")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="override the request count (small cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -276,9 +276,11 @@ OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
 OASIS_API int oasis_profile_enable(oasis_ctx* ctx, int enable);
 
 /* Sum of kernel durations (ms) and launch counts since the last read, in the
- * order attention, score_topk, admit_evict, prefetch.  Synchronises. */
+ * order attention, score_topk, admit_evict, prefetch; start_ms_sum4
+ * (nullable) receives the summed start offsets of those launches from the
+ * start of their oasis_step.  Synchronises. */
 OASIS_API int oasis_profile_read(oasis_ctx* ctx, double* ms_sum4,
-                                 int64_t* count4);
+                                 int64_t* count4, double* start_ms_sum4);
 
 #ifdef __cplusplus
 }

@@ -49,6 +49,8 @@ struct LayerState {
 
 struct ProfPair {
   cudaEvent_t a, b;
+  int kind;
+  int start;  // index of the step-start event this launch belongs to
 };
 
 struct WsLayout {
@@ -139,7 +141,8 @@ struct oasis_ctx {
   bool prof = false;
   std::vector<ProfPair> prof_pool;
   size_t prof_used = 0;
-  std::vector<int> prof_kind;
+  std::vector<cudaEvent_t> prof_starts;
+  size_t prof_starts_used = 0;
 
   int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -165,7 +168,17 @@ struct oasis_ctx {
   int32_t* ctx_tab(int step) const { return ctx_len + (step & 1) * cfg.num_requests; }
   int set_device() { return cuda(cudaSetDevice(cfg.device), "cudaSetDevice"); }
 
-  // Profiling: record an event pair around a launch of `kind`.
+  // Profiling: a timing event at the start of each step, and an event pair
+  // around each launch of `kind` (0 attention, 1 score_topk, 2 admit, 3 gather).
+  void prof_step_start(cudaStream_t s) {
+    if (!prof) return;
+    if (prof_starts_used == prof_starts.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return;
+      prof_starts.push_back(e);
+    }
+    cudaEventRecord(prof_starts[prof_starts_used++], s);
+  }
   cudaEvent_t* prof_begin(int kind, cudaStream_t s) {
     if (!prof) return nullptr;
     if (prof_used == prof_pool.size()) {
@@ -176,10 +189,10 @@ struct oasis_ctx {
         return nullptr;
       }
       prof_pool.push_back(p);
-      prof_kind.push_back(kind);
     }
-    prof_kind[prof_used] = kind;
     ProfPair& p = prof_pool[prof_used++];
+    p.kind = kind;
+    p.start = static_cast<int>(prof_starts_used) - 1;
     cudaEventRecord(p.a, s);
     return &p.b;
   }
@@ -429,6 +442,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
     cudaEventDestroy(p.a);
     cudaEventDestroy(p.b);
   }
+  for (auto& e : ctx->prof_starts) cudaEventDestroy(e);
   if (ctx->side) cudaStreamDestroy(ctx->side);
   delete ctx;
   return OASIS_OK;
@@ -558,6 +572,7 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
     if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
   }
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_start, s), "record start")) return rc;
+  ctx->prof_step_start(s);
   if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side, L.ev_start, 0), "side wait")) return rc;
   if (int rc = run_attention(ctx, layer, step, q, q_draft, out, out_draft, s)) return rc;
   if (int rc = run_score(ctx, layer, step, q_draft, L.topk_ids, L.topk_scores, ctx->side))
@@ -666,25 +681,34 @@ OASIS_API int oasis_profile_enable(oasis_ctx* ctx, int enable) {
   if (!ctx) return OASIS_EINVAL;
   ctx->prof = enable != 0;
   ctx->prof_used = 0;
+  ctx->prof_starts_used = 0;
   return OASIS_OK;
 }
 
-OASIS_API int oasis_profile_read(oasis_ctx* ctx, double* ms_sum4, int64_t* count4) {
+OASIS_API int oasis_profile_read(oasis_ctx* ctx, double* ms_sum4, int64_t* count4,
+                                 double* start_ms_sum4) {
   if (!ctx || !ms_sum4 || !count4) return OASIS_EINVAL;
   if (int rc = ctx->set_device()) return rc;
   if (int rc = ctx->cuda(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) return rc;
   for (int k = 0; k < 4; ++k) {
     ms_sum4[k] = 0.0;
     count4[k] = 0;
+    if (start_ms_sum4) start_ms_sum4[k] = 0.0;
   }
   for (size_t i = 0; i < ctx->prof_used; ++i) {
+    const ProfPair& p = ctx->prof_pool[i];
     float ms = 0.f;
-    if (cudaEventElapsedTime(&ms, ctx->prof_pool[i].a, ctx->prof_pool[i].b) == cudaSuccess) {
-      ms_sum4[ctx->prof_kind[i]] += ms;
-      count4[ctx->prof_kind[i]] += 1;
+    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+      ms_sum4[p.kind] += ms;
+      count4[p.kind] += 1;
+      float off = 0.f;
+      if (start_ms_sum4 && p.start >= 0 &&
+          cudaEventElapsedTime(&off, ctx->prof_starts[p.start], p.a) == cudaSuccess)
+        start_ms_sum4[p.kind] += off;
     }
   }
   ctx->prof_used = 0;
+  ctx->prof_starts_used = 0;
   return OASIS_OK;
 }
 

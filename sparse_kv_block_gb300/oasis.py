@@ -76,7 +76,7 @@ EXPORTS = {
     "oasis_append_token": (c_int, [_P, c_int, c_int, _P, _P, _P]),
     "oasis_advance_context": (c_int, [_P, c_int, c_int, _P]),
     "oasis_profile_enable": (c_int, [_P, c_int]),
-    "oasis_profile_read": (c_int, [_P, POINTER(c_double), POINTER(c_int64)]),
+    "oasis_profile_read": (c_int, [_P, POINTER(c_double), POINTER(c_int64), POINTER(c_double)]),
 }
 
 _lib = None
@@ -267,10 +267,12 @@ class Oasis:
         self._check(lib().oasis_profile_enable(self.ctx, 1 if enable else 0))
 
     def oasis_profile_read(self) -> tuple:
+        """(summed ms, launch counts, summed start offsets in ms) per kernel kind."""
         ms = (c_double * 4)()
         cnt = (c_int64 * 4)()
-        self._check(lib().oasis_profile_read(self.ctx, ms, cnt))
-        return list(ms), list(cnt)
+        off = (c_double * 4)()
+        self._check(lib().oasis_profile_read(self.ctx, ms, cnt, off))
+        return list(ms), list(cnt), list(off)
 
     # ------------------------------------------------------- tensor views
     def step_lists(self, layer: int) -> dict:
