@@ -369,8 +369,11 @@ def run_oasis(args, ws, rank, local):
     # ---------------- roofline of the dominant kernel
     peaks = measured_peaks()
     names = ["attention", "score_topk", "admit_evict", "prefetch"]
-    avg_ms = {n: (ms_sum[i] / counts[i] if counts[i] else None) for i, n in enumerate(names)}
+    # Per step: summed durations of each kind's launches (several request
+    # groups per step for the side work), and the mean start offset.
+    avg_ms = {n: (ms_sum[i] / args.steps if counts[i] else None) for i, n in enumerate(names)}
     avg_start = {n: (off_sum[i] / counts[i] if counts[i] else None) for i, n in enumerate(names)}
+    launches = {n: counts[i] / args.steps for i, n in enumerate(names)}
     R, Hq, Hkv, K, NB = shape.R, shape.Hq, shape.Hkv, shape.K, shape.NBmax
     qo_bytes = 4 * R * Hq * 128 * 2
     attn_bytes = R * Hkv * K * UNIT_BYTES + qo_bytes
@@ -384,7 +387,8 @@ def run_oasis(args, ws, rank, local):
             a = b / (avg_ms[n] * 1e-3) / 1e9
             per_kernel[n] = {"bound": bound, "achieved": round(a, 1), "peak": round(peak, 1),
                              "unit": "GB/s", "frac": round(a / peak, 4),
-                             "bytes_per_launch": int(b), "avg_ms": round(avg_ms[n], 5),
+                             "bytes_per_step": int(b), "ms_per_step": round(avg_ms[n], 5),
+                             "launches_per_step": launches[n],
                              "avg_start_ms": round(avg_start[n], 5)}
     dk = per_kernel.get(dominant, per_kernel["attention"])
     roofline = {"bound": "hbm" if dk["bound"] == "hbm" else "hbm", "kernel": dominant,
@@ -409,7 +413,7 @@ def run_oasis(args, ws, rank, local):
                     "d2h_bytes_per_step": 2 * R * Hq * 128 * 2,
                     "note": "oasis_step_host: pinned q/q_draft in, attention outputs out, "
                             "host waits for each step's result"},
-            "gpu_launches": 4 * args.steps, "clocks": clk}
+            "gpu_launches": int(sum(counts)), "clocks": clk}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, pairs, sec, desc = oracle_rate(shape, host, lens, q.cpu(), qd.cpu(),
                                              budget_s=args.cpu_budget)

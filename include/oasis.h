@@ -95,7 +95,7 @@ typedef enum {
 typedef struct {
   int32_t num_layers;
   int32_t num_requests;  /* R */
-  int32_t max_blocks;    /* NBmax */
+  int32_t max_blocks;    /* NBmax, <= 131072 */
   int32_t num_q_heads;   /* Hq */
   int32_t num_kv_heads;  /* Hkv; Hq % Hkv == 0 and Hq / Hkv <= 4 */
   int32_t head_dim;      /* d; must be 128 */
@@ -105,6 +105,8 @@ typedef struct {
   float softmax_scale;   /* 0 -> 1/sqrt(d) */
   int32_t out_fp32;      /* attention outputs in fp32 (1) or bf16 (0) */
   int32_t device;        /* CUDA device ordinal */
+  int32_t side_groups;   /* request groups oasis_step pipelines its side work
+                            in (0 = one per 256 (request, KV head) pairs, <= 8) */
 } oasis_config;
 
 typedef struct {

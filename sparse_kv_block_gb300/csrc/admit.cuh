@@ -1,0 +1,148 @@
+// admit.cuh -- capped least-recently-selected eviction of one
+// (request, KV head) by one warp (step a4), shared by the stand-alone admit
+// kernel and the tail of the fused score + top-K + admit kernel.
+//
+// "Pith review of OasisKV", section "What carries the argument": a
+// capped-eviction policy pairs each admitted nonresident block with a
+// least-recently-selected resident block so per-step traffic is bounded.
+// Reading of the pages: (i) stamp re-selected residents with the step;
+// (ii) missing top-K blocks in rank order; (iii) eviction candidates = slots
+// whose block is not selected, empty first, then (stamp, block id, slot)
+// ascending; (iv) at most C admissions; (v) the i-th missing block replaces
+// the i-th candidate.  The admitted block takes spare pool unit K+i and the
+// evicted unit becomes that spare, so the gather never writes a unit that
+// the current table still references.
+//
+// Membership is tested with two NBmax-bit bitmaps in shared memory; the
+// eviction order is a bitonic sort of 64-bit keys
+//   [63] occupied | [62:32] stamp+1 | [31:8] block id+1 | [7:0] slot
+// (selected slots get the all-ones key and sort last).
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sortnet.cuh"
+
+namespace oasis {
+
+struct AdmitWarpSmem {
+  int topk[kMaxTopK];
+  int res[kMaxTopK];
+  int stamp[kMaxTopK];
+  int phys[2 * kMaxTopK];
+  int missing[kMaxTopK];
+  int evslot[kMaxTopK];
+  unsigned char in_t[kMaxTopK];
+};
+
+__host__ __device__ inline int bitmap_words(int nb) { return (nb + 31) >> 5; }
+
+// Shared bytes one warp needs: the struct plus two bitmaps, 16-byte rounded.
+__host__ __device__ inline size_t admit_warp_smem_bytes(int NBmax) {
+  return (sizeof(AdmitWarpSmem) + 2 * 4 * static_cast<size_t>(bitmap_words(NBmax)) + 15) &
+         ~static_cast<size_t>(15);
+}
+
+// Precondition: S.topk[0..K) holds this pair's top-K list (rank order, -1
+// padded) and the warp has synchronised.  bm points at 2*bitmap_words(NBmax)
+// words of this warp's shared memory.
+template <int KPL>
+__device__ void admit_warp(const AdmitArgs& a, int pair, AdmitWarpSmem& S, uint32_t* bm) {
+  const int lane = threadIdx.x & 31;
+  const int K = a.K, C = a.C, U = a.U, NB = a.NBmax;
+  const int nw = bitmap_words(NB);
+  uint32_t* bmT = bm;
+  uint32_t* bmR = bm + nw;
+  const size_t ok = static_cast<size_t>(pair) * K;
+  const size_t ou = static_cast<size_t>(pair) * U;
+
+  for (int s = lane; s < K; s += 32) {
+    S.res[s] = a.res_cur[ok + s];
+    S.stamp[s] = a.stamps[ok + s];
+  }
+  for (int u = lane; u < U; u += 32) S.phys[u] = a.phys_cur[ou + u];
+  for (int w = lane; w < 2 * nw; w += 32) bm[w] = 0u;
+  __syncwarp();
+  for (int s = lane; s < K; s += 32) {
+    const int b = S.topk[s];
+    if (b >= 0 && b < NB) atomicOr(&bmT[b >> 5], 1u << (b & 31));
+    const int id = S.res[s];
+    if (id >= 0 && id < NB) atomicOr(&bmR[id >> 5], 1u << (id & 31));
+  }
+  __syncwarp();
+
+  // (i) re-selected residents take the step as their stamp.
+  for (int s = lane; s < K; s += 32) {
+    const int id = S.res[s];
+    const bool f = id >= 0 && id < NB && ((bmT[id >> 5] >> (id & 31)) & 1u);
+    S.in_t[s] = f;
+    if (f) S.stamp[s] = a.step;
+  }
+  // (ii) missing blocks in rank order.
+  int n_missing = 0;
+  for (int c = 0; c < K; c += 32) {
+    const int i = c + lane;
+    const int b = i < K ? S.topk[i] : -1;
+    const bool m = b >= 0 && b < NB && !((bmR[b >> 5] >> (b & 31)) & 1u);
+    const unsigned bal = __ballot_sync(0xffffffffu, m);
+    if (m) S.missing[n_missing + __popc(bal & ((1u << lane) - 1u))] = b;
+    n_missing += __popc(bal);
+  }
+  const int n = min(n_missing, C);
+  __syncwarp();
+
+  // (iii) eviction order.
+  uint64_t key[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int s = i * 32 + lane;
+    if (s < K && !S.in_t[s]) {
+      const uint64_t occ = S.res[s] >= 0 ? 1ull : 0ull;
+      key[i] = (occ << 63) | (static_cast<uint64_t>(static_cast<uint32_t>(S.stamp[s] + 1)) << 32) |
+               (static_cast<uint64_t>(static_cast<uint32_t>(S.res[s] + 1) & 0xffffffu) << 8) |
+               static_cast<uint64_t>(s);
+    } else {
+      key[i] = ~0ull;
+    }
+  }
+  bitonic_sort<KPL>(key, false);
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int e = i * 32 + lane;
+    if (e < n) S.evslot[e] = static_cast<int>(key[i] & 0xffu);
+  }
+  __syncwarp();
+
+  // (iv, v) outputs and the next tables.
+  for (int i = lane; i < C; i += 32) {
+    const size_t oc = static_cast<size_t>(pair) * C + i;
+    if (i < n) {
+      const int s = S.evslot[i];
+      a.admit_ids[oc] = S.missing[i];
+      a.admit_slots[oc] = s;
+      a.evict_ids[oc] = S.res[s];
+    } else {
+      a.admit_ids[oc] = -1;
+      a.admit_slots[oc] = -1;
+      a.evict_ids[oc] = -1;
+    }
+  }
+  if (lane == 0) a.n_admit[pair] = n;
+  __syncwarp();
+  for (int i = lane; i < n; i += 32) {
+    const int s = S.evslot[i];
+    const int unit_old = S.phys[s];
+    S.res[s] = S.missing[i];
+    S.stamp[s] = a.step;
+    S.phys[s] = S.phys[K + i];
+    S.phys[K + i] = unit_old;
+  }
+  __syncwarp();
+  for (int s = lane; s < K; s += 32) {
+    a.res_nxt[ok + s] = S.res[s];
+    a.stamps[ok + s] = S.stamp[s];
+  }
+  for (int u = lane; u < U; u += 32) a.phys_nxt[ou + u] = S.phys[u];
+}
+
+}  // namespace oasis

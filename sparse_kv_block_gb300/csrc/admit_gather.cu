@@ -1,5 +1,6 @@
 // admit_gather.cu -- capped eviction (a4), prefetch gather (a5) and the
 // support kernels: table initialisation, summary build and token append.
+#include "admit.cuh"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -7,125 +8,37 @@ namespace oasis {
 namespace {
 
 // ------------------------------------------------------------------ a4
-// Capped least-recently-selected eviction, one warp per (request, KV head)
-// ("Pith review of OasisKV", section "What carries the argument": a
-// capped-eviction policy pairs each admitted nonresident block with a
-// least-recently-selected resident block so per-step traffic is bounded).
-// Reading of the pages: (i) stamp re-selected residents with the step;
-// (ii) missing top-K blocks in rank order; (iii) candidates = unselected
-// slots, empty first, then (stamp, block id, slot) ascending; (iv) at most C;
-// (v) pair the i-th missing block with the i-th candidate.  The admitted
-// block takes spare pool unit K+i; the evicted unit becomes that spare, so
-// the copy never touches a unit the current table still references.
+// Stand-alone capped eviction: one warp per (request, KV head), the list
+// read from global memory (the fused score kernel runs the same admit_warp
+// on its own top-K list).
 constexpr int kAdmitWarps = 4;
 
-struct AdmitSmem {
-  int topk[kMaxTopK];
-  int res[kMaxTopK];
-  int stamp[kMaxTopK];
-  int phys[2 * kMaxTopK];
-  unsigned char in_t[kMaxTopK];
-  unsigned char is_res[kMaxTopK];
-  int missing[kMaxTopK];
-  int evslot[kMaxTopK];
-};
-
+template <int KPL>
 __global__ void __launch_bounds__(kAdmitWarps * 32) admit_kernel(const AdmitArgs a) {
-  __shared__ AdmitSmem sm_all[kAdmitWarps];
+  extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * kAdmitWarps + warp;
-  if (pair >= a.R * a.Hkv) return;  // warp-uniform; no block barrier follows
-  AdmitSmem& S = sm_all[warp];
-  const int K = a.K, C = a.C, U = a.U;
-  const size_t ok_ = static_cast<size_t>(pair) * K;
-  const size_t ou = static_cast<size_t>(pair) * U;
-
-  for (int s = lane; s < K; s += 32) {
-    S.topk[s] = a.topk[ok_ + s];
-    S.res[s] = a.res_cur[ok_ + s];
-    S.stamp[s] = a.stamps[ok_ + s];
-  }
-  for (int u = lane; u < U; u += 32) S.phys[u] = a.phys_cur[ou + u];
+  const int local = blockIdx.x * kAdmitWarps + warp;
+  if (local >= a.pairs) return;  // warp-uniform; no block barrier follows
+  const int pair = a.pair0 + local;
+  uint8_t* mine = smem + warp * admit_warp_smem_bytes(a.NBmax);
+  AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(mine);
+  for (int s = lane; s < a.K; s += 32) S.topk[s] = a.topk[static_cast<size_t>(pair) * a.K + s];
   __syncwarp();
+  admit_warp<KPL>(a, pair, S, reinterpret_cast<uint32_t*>(mine + sizeof(AdmitWarpSmem)));
+}
 
-  // Membership both ways (K x K compares; K <= 256).
-  for (int s = lane; s < K; s += 32) {
-    const int id = S.res[s];
-    bool f = false;
-    if (id >= 0)
-      for (int i = 0; i < K; ++i) f |= (S.topk[i] == id);
-    S.in_t[s] = f;
-    if (f) S.stamp[s] = a.step;
-    const int b = S.topk[s];
-    bool rr = false;
-    if (b >= 0)
-      for (int i = 0; i < K; ++i) rr |= (S.res[i] == b);
-    S.is_res[s] = rr;
+template <int KPL>
+cudaError_t launch_admit_kpl(const AdmitArgs& a, cudaStream_t s) {
+  const size_t smem = kAdmitWarps * admit_warp_smem_bytes(a.NBmax);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(admit_kernel<KPL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
   }
-  __syncwarp();
-
-  // (ii) missing blocks in rank order (ballot compaction).
-  int n_missing = 0;
-  for (int c = 0; c < K; c += 32) {
-    const int i = c + lane;
-    const bool m = i < K && S.topk[i] >= 0 && !S.is_res[i];
-    const unsigned bal = __ballot_sync(0xffffffffu, m);
-    if (m) S.missing[n_missing + __popc(bal & ((1u << lane) - 1u))] = S.topk[i];
-    n_missing += __popc(bal);
-  }
-  const int n = min(n_missing, C);
-
-  // (iii) rank of each eviction candidate under (nonempty, stamp, id, slot).
-  for (int s = lane; s < K; s += 32) {
-    if (S.in_t[s]) continue;
-    const int ne = S.res[s] >= 0, st = S.stamp[s], id = S.res[s];
-    int rank = 0;
-    for (int s2 = 0; s2 < K; ++s2) {
-      if (S.in_t[s2] || s2 == s) continue;
-      const int ne2 = S.res[s2] >= 0, st2 = S.stamp[s2], id2 = S.res[s2];
-      const bool less = ne2 != ne ? ne2 < ne
-                                  : st2 != st ? st2 < st : id2 != id ? id2 < id : s2 < s;
-      rank += less;
-    }
-    if (rank < n) S.evslot[rank] = s;
-  }
-  __syncwarp();
-
-  // (v) outputs and the next tables.
-  for (int i = lane; i < C; i += 32) {
-    const size_t oc = static_cast<size_t>(pair) * C + i;
-    if (i < n) {
-      const int s = S.evslot[i];
-      a.admit_ids[oc] = S.missing[i];
-      a.admit_slots[oc] = s;
-      a.evict_ids[oc] = S.res[s];
-    } else {
-      a.admit_ids[oc] = -1;
-      a.admit_slots[oc] = -1;
-      a.evict_ids[oc] = -1;
-    }
-  }
-  if (lane == 0) a.n_admit[pair] = n;
-  __syncwarp();
-  // Each admission i: slot E[i] takes block M[i] and spare unit K+i; the
-  // evicted unit moves to spare position K+i.  Lanes own distinct i, and the
-  // evicted slots are distinct, so the updates do not collide.
-  for (int i = lane; i < n; i += 32) {
-    const int s = S.evslot[i];
-    const int unit_old = S.phys[s];
-    const int unit_new = S.phys[K + i];
-    S.res[s] = S.missing[i];
-    S.stamp[s] = a.step;
-    S.phys[s] = unit_new;
-    S.phys[K + i] = unit_old;
-  }
-  __syncwarp();
-  for (int s = lane; s < K; s += 32) {
-    a.res_nxt[ok_ + s] = S.res[s];
-    a.stamps[ok_ + s] = S.stamp[s];
-  }
-  for (int u = lane; u < U; u += 32) a.phys_nxt[ou + u] = S.phys[u];
+  admit_kernel<KPL><<<(a.pairs + kAdmitWarps - 1) / kAdmitWarps, kAdmitWarps * 32, smem, s>>>(a);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ a5
@@ -139,10 +52,12 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
   const int lane = threadIdx.x & 31;
   const long long nwarps = static_cast<long long>(gridDim.x) * (kGatherThreads / 32);
   const long long total = static_cast<long long>(a.pairs) * a.items;
-  for (long long it = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); it < total;
-       it += nwarps) {
-    const int pair = static_cast<int>(it / a.items);
-    const int i = static_cast<int>(it - static_cast<long long>(pair) * a.items);
+  for (long long lt = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); lt < total;
+       lt += nwarps) {
+    const int local = static_cast<int>(lt / a.items);
+    const int i = static_cast<int>(lt - static_cast<long long>(local) * a.items);
+    const int pair = a.pair0 + local;
+    const long long it = static_cast<long long>(pair) * a.items + i;
     if (a.n_valid && i >= a.n_valid[pair]) continue;
     const int id = a.src_ids[it];
     if (id < 0) continue;
@@ -317,10 +232,11 @@ int sm_count() {
 }  // namespace
 
 cudaError_t launch_admit(const AdmitArgs& a, cudaStream_t s) {
-  const int pairs = a.R * a.Hkv;
-  if (pairs == 0) return cudaSuccess;
-  admit_kernel<<<(pairs + kAdmitWarps - 1) / kAdmitWarps, kAdmitWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  if (a.pairs <= 0) return cudaSuccess;
+  if (a.K <= 32) return launch_admit_kpl<1>(a, s);
+  if (a.K <= 64) return launch_admit_kpl<2>(a, s);
+  if (a.K <= 128) return launch_admit_kpl<4>(a, s);
+  return launch_admit_kpl<8>(a, s);
 }
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {

@@ -43,6 +43,7 @@ struct LayerState {
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_side_done = nullptr;
   cudaEvent_t ev_attn_done = nullptr;
+  std::vector<cudaEvent_t> ev_group;  // one per side-work request group
   bool side_pending = false;
   bool loaded = false;
 };
@@ -102,6 +103,8 @@ const char* config_error(const oasis_config* c) {
   if (!(c->fetch_ratio >= 0.f && c->fetch_ratio <= 1.f)) return "fetch_ratio must be in [0, 1]";
   if (!(c->softmax_scale >= 0.f) || std::isinf(c->softmax_scale)) return "softmax_scale must be finite and >= 0";
   if (c->device < 0) return "device must be >= 0";
+  if (c->max_blocks > kMaxBlocksPerHead) return "max_blocks must be <= 131072";
+  if (c->side_groups < 0 || c->side_groups > 64) return "side_groups must be in 0..64";
   const double units = static_cast<double>(c->num_requests) * c->num_kv_heads *
                        (c->topk + fetch_cap(*c)) * 2 * kBlock;
   if (units >= 2147483647.0) return "pool too large for a 32-bit TMA row coordinate";
@@ -130,13 +133,15 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct oasis_ctx {
   oasis_config cfg{};
   int G = 0, C = 0, U = 0;
+  int groups = 1;  // request groups the side work is pipelined in
   float scale_log2 = 0.f;
   std::vector<LayerState> layers;
   int32_t* ctx_len = nullptr;
   uint8_t* ws = nullptr;
   uint32_t* err = nullptr;
   WsLayout wl{};
-  cudaStream_t side = nullptr;
+  cudaStream_t side = nullptr;   // scan + top-K + admission
+  cudaStream_t side2 = nullptr;  // host -> HBM gathers
   std::string last_error;
   bool prof = false;
   std::vector<ProfPair> prof_pool;
@@ -237,8 +242,36 @@ int run_attention(oasis_ctx* ctx, int layer, int step, const void* q, const void
   return ctx->cuda(e, "attention launch");
 }
 
+AdmitArgs admit_args(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t* aid,
+                     int32_t* aslot, int32_t* evid, int32_t* nadm) {
+  AdmitArgs a{};
+  a.topk = topk;
+  a.res_cur = ctx->res_tab(layer, step);
+  a.res_nxt = ctx->res_tab(layer, step + 1);
+  a.stamps = ctx->layers[layer].stamps;
+  a.phys_cur = ctx->phys_tab(layer, step);
+  a.phys_nxt = ctx->phys_tab(layer, step + 1);
+  a.admit_ids = aid;
+  a.admit_slots = aslot;
+  a.evict_ids = evid;
+  a.n_admit = nadm;
+  a.R = ctx->cfg.num_requests;
+  a.Hkv = ctx->cfg.num_kv_heads;
+  a.K = ctx->cfg.topk;
+  a.C = ctx->C;
+  a.U = ctx->U;
+  a.NBmax = ctx->cfg.max_blocks;
+  a.step = step;
+  a.pair0 = 0;
+  a.pairs = a.R * a.Hkv;
+  return a;
+}
+
+// Scan + top-K of pairs [pair0, pair0 + pairs); with `fused` also their
+// capped eviction into the layer's workspace lists.
 int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
-              float* scores, cudaStream_t s) {
+              float* scores, cudaStream_t s, int pair0 = 0, int pairs = -1,
+              bool fused = false) {
   LayerState& L = ctx->layers[layer];
   ScoreArgs a{};
   a.qd = qd;
@@ -253,6 +286,12 @@ int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
   a.G = ctx->G;
   a.K = ctx->cfg.topk;
   a.NBmax = ctx->cfg.max_blocks;
+  a.pair0 = pair0;
+  a.pairs = pairs < 0 ? a.R * a.Hkv : pairs;
+  a.fuse_admit = fused ? 1 : 0;
+  if (fused)
+    a.admit = admit_args(ctx, layer, step, nullptr, L.admit_ids, L.admit_slots, L.evict_ids,
+                         L.n_admit);
   cudaEvent_t* pe = ctx->prof_begin(1, s);
   cudaError_t e = launch_score_topk(a, s);
   ctx->prof_end(pe, s);
@@ -261,24 +300,7 @@ int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
 
 int run_admit(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t* aid,
               int32_t* aslot, int32_t* evid, int32_t* nadm, cudaStream_t s) {
-  LayerState& L = ctx->layers[layer];
-  AdmitArgs a{};
-  a.topk = topk;
-  a.res_cur = ctx->res_tab(layer, step);
-  a.res_nxt = ctx->res_tab(layer, step + 1);
-  a.stamps = L.stamps;
-  a.phys_cur = ctx->phys_tab(layer, step);
-  a.phys_nxt = ctx->phys_tab(layer, step + 1);
-  a.admit_ids = aid;
-  a.admit_slots = aslot;
-  a.evict_ids = evid;
-  a.n_admit = nadm;
-  a.R = ctx->cfg.num_requests;
-  a.Hkv = ctx->cfg.num_kv_heads;
-  a.K = ctx->cfg.topk;
-  a.C = ctx->C;
-  a.U = ctx->U;
-  a.step = step;
+  AdmitArgs a = admit_args(ctx, layer, step, topk, aid, aslot, evid, nadm);
   cudaEvent_t* pe = ctx->prof_begin(2, s);
   cudaError_t e = launch_admit(a, s);
   ctx->prof_end(pe, s);
@@ -286,7 +308,8 @@ int run_admit(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t*
 }
 
 int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
-                 const int32_t* aslot, const int32_t* nadm, cudaStream_t s) {
+                 const int32_t* aslot, const int32_t* nadm, cudaStream_t s, int pair0 = 0,
+                 int pairs = -1) {
   if (ctx->C == 0) return OASIS_OK;
   LayerState& L = ctx->layers[layer];
   GatherArgs g{};
@@ -297,7 +320,8 @@ int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
   g.n_valid = nadm;
   g.phys = ctx->phys_tab(layer, step + 1);
   g.err = ctx->err;
-  g.pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
+  g.pair0 = pair0;
+  g.pairs = pairs < 0 ? ctx->cfg.num_requests * ctx->cfg.num_kv_heads : pairs;
   g.items = ctx->C;
   g.NBmax = ctx->cfg.max_blocks;
   g.U = ctx->U;
@@ -373,8 +397,16 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
   if (cudaSetDevice(cfg->device) != cudaSuccess) return bail(OASIS_ECUDA);
   int lo = 0, hi = 0;
   if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return bail(OASIS_ECUDA);
-  if (cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, hi) != cudaSuccess)
+  if (cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, hi) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&c->side2, cudaStreamNonBlocking, hi) != cudaSuccess)
     return bail(OASIS_ENOMEM);
+  {
+    const int pairs = cfg->num_requests * cfg->num_kv_heads;
+    c->groups = cfg->side_groups > 0 ? cfg->side_groups : (pairs + 255) / 256;
+    if (c->groups > 8 && cfg->side_groups == 0) c->groups = 8;
+    if (c->groups > pairs) c->groups = pairs;
+    if (c->groups < 1) c->groups = 1;
+  }
   auto encode = get_encode();
   if (!encode) return bail(OASIS_ECUDA);
 
@@ -421,6 +453,10 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
         cudaEventCreateWithFlags(&S.ev_side_done, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_attn_done, cudaEventDisableTiming) != cudaSuccess)
       return bail(OASIS_ENOMEM);
+    S.ev_group.assign(c->groups, nullptr);
+    for (auto& e : S.ev_group)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+        return bail(OASIS_ENOMEM);
   }
   if (cudaMemsetAsync(c->err, 0, sizeof(uint32_t), c->side) != cudaSuccess ||
       cudaStreamSynchronize(c->side) != cudaSuccess)
@@ -433,7 +469,10 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (!ctx) return OASIS_OK;
   cudaSetDevice(ctx->cfg.device);
   if (ctx->side) cudaStreamSynchronize(ctx->side);
+  if (ctx->side2) cudaStreamSynchronize(ctx->side2);
   for (auto& L : ctx->layers) {
+    for (auto& e : L.ev_group)
+      if (e) cudaEventDestroy(e);
     if (L.ev_start) cudaEventDestroy(L.ev_start);
     if (L.ev_side_done) cudaEventDestroy(L.ev_side_done);
     if (L.ev_attn_done) cudaEventDestroy(L.ev_attn_done);
@@ -444,6 +483,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   }
   for (auto& e : ctx->prof_starts) cudaEventDestroy(e);
   if (ctx->side) cudaStreamDestroy(ctx->side);
+  if (ctx->side2) cudaStreamDestroy(ctx->side2);
   delete ctx;
   return OASIS_OK;
 }
@@ -506,6 +546,7 @@ OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step, voi
   g.n_valid = nullptr;
   g.phys = ctx->phys_tab(layer, first_step);
   g.err = ctx->err;
+  g.pair0 = 0;
   g.pairs = pairs;
   g.items = ctx->cfg.topk;
   g.NBmax = ctx->cfg.max_blocks;
@@ -541,7 +582,8 @@ OASIS_API int oasis_admit_evict(oasis_ctx* ctx, int layer, int step, const int32
                                 int32_t* admit_ids, int32_t* admit_slots, int32_t* evict_ids,
                                 int32_t* n_admit, void* stream) {
   if (int rc = check_layer(ctx, layer)) return rc;
-  if (step < 0 || !topk_ids || !admit_ids || !admit_slots || !evict_ids || !n_admit)
+  if (step < 0 || step > (1 << 30) || !topk_ids || !admit_ids || !admit_slots || !evict_ids ||
+      !n_admit)
     return ctx->fail(OASIS_EINVAL, "admit_evict: bad step or null pointer");
   if (int rc = ctx->set_device()) return rc;
   return run_admit(ctx, layer, step, topk_ids, admit_ids, admit_slots, evict_ids, n_admit,
@@ -562,7 +604,7 @@ OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t*
 OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
                          const void* q_draft, void* out, void* out_draft, void* stream) {
   if (int rc = check_layer(ctx, layer)) return rc;
-  if (step < 0 || !q || !q_draft || !out || !out_draft)
+  if (step < 0 || step > (1 << 30) || !q || !q_draft || !out || !out_draft)
     return ctx->fail(OASIS_EINVAL, "step: bad step or null pointer");
   LayerState& L = ctx->layers[layer];
   if (!L.loaded) return ctx->fail(OASIS_ESTATE, "layer %d: oasis_load_resident first", layer);
@@ -574,15 +616,35 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_start, s), "record start")) return rc;
   ctx->prof_step_start(s);
   if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side, L.ev_start, 0), "side wait")) return rc;
+  if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_start, 0), "side2 wait")) return rc;
+  // Side work first so that its CTAs are queued ahead of the attention grid.
+  // Request group g: scan + top-K + admission on `side`, then its gather on
+  // `side2` as soon as the group's admissions exist, so the host link starts
+  // early and stays busy while later groups are scanned.
+  const int pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
+  for (int g = 0; g < ctx->groups; ++g) {
+    const int p0 = static_cast<int>(static_cast<long long>(pairs) * g / ctx->groups);
+    const int p1 = static_cast<int>(static_cast<long long>(pairs) * (g + 1) / ctx->groups);
+    if (int rc = run_score(ctx, layer, step, q_draft, L.topk_ids, L.topk_scores, ctx->side, p0,
+                           p1 - p0, true))
+      return rc;
+    if (ctx->C > 0) {
+      if (int rc = ctx->cuda(cudaEventRecord(L.ev_group[g], ctx->side), "record group"))
+        return rc;
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[g], 0), "group wait"))
+        return rc;
+      if (int rc = run_prefetch(ctx, layer, step, L.admit_ids, L.admit_slots, L.n_admit,
+                                ctx->side2, p0, p1 - p0))
+        return rc;
+    }
+  }
+  if (ctx->C == 0) {
+    if (int rc = ctx->cuda(cudaEventRecord(L.ev_group[0], ctx->side), "record group")) return rc;
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[0], 0), "group wait"))
+      return rc;
+  }
   if (int rc = run_attention(ctx, layer, step, q, q_draft, out, out_draft, s)) return rc;
-  if (int rc = run_score(ctx, layer, step, q_draft, L.topk_ids, L.topk_scores, ctx->side))
-    return rc;
-  if (int rc = run_admit(ctx, layer, step, L.topk_ids, L.admit_ids, L.admit_slots, L.evict_ids,
-                         L.n_admit, ctx->side))
-    return rc;
-  if (int rc = run_prefetch(ctx, layer, step, L.admit_ids, L.admit_slots, L.n_admit, ctx->side))
-    return rc;
-  if (int rc = ctx->cuda(cudaEventRecord(L.ev_side_done, ctx->side), "record side")) return rc;
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_side_done, ctx->side2), "record side")) return rc;
   L.side_pending = true;
   return OASIS_OK;
 }

@@ -22,16 +22,8 @@ struct AttnArgs {
   int out_fp32;
 };
 
-struct ScoreArgs {
-  const void* qd;        // [R][Hq][d] bf16
-  const void* summ;      // [R][Hkv][NBmax][2][d] bf16
-  const int32_t* ctx_len;  // [R]
-  int32_t* topk_ids;     // [R][Hkv][K]
-  float* topk_scores;    // [R][Hkv][K] or null
-  uint32_t* err;
-  int R, Hq, Hkv, G, K, NBmax;
-};
-
+// Pairs (request, KV head) are flattened as pair = r * Hkv + h; a launch
+// covers pairs [pair0, pair0 + pairs).
 struct AdmitArgs {
   const int32_t* topk;       // [R][Hkv][K]
   const int32_t* res_cur;    // [R][Hkv][K]
@@ -43,7 +35,21 @@ struct AdmitArgs {
   int32_t* admit_slots;      // [R][Hkv][C]
   int32_t* evict_ids;        // [R][Hkv][C]
   int32_t* n_admit;          // [R][Hkv]
-  int R, Hkv, K, C, U, step;
+  int R, Hkv, K, C, U, NBmax, step;
+  int pair0, pairs;
+};
+
+struct ScoreArgs {
+  const void* qd;        // [R][Hq][d] bf16
+  const void* summ;      // [R][Hkv][NBmax][2][d] bf16
+  const int32_t* ctx_len;  // [R]
+  int32_t* topk_ids;     // [R][Hkv][K]
+  float* topk_scores;    // [R][Hkv][K] or null
+  uint32_t* err;
+  int R, Hq, Hkv, G, K, NBmax;
+  int pair0, pairs;
+  int fuse_admit;        // run the capped eviction of each pair in the tail
+  AdmitArgs admit;       // used when fuse_admit (its topk field is ignored)
 };
 
 // Copies 8 KiB units host -> pool.  Item i of pair p = (r, h) reads block
@@ -57,7 +63,7 @@ struct GatherArgs {
   const int32_t* n_valid;    // may be null
   const int32_t* phys;
   uint32_t* err;
-  int pairs, items, NBmax, U;
+  int pair0, pairs, items, NBmax, U;
 };
 
 struct SummaryArgs {
@@ -94,5 +100,8 @@ cudaError_t launch_advance(const int32_t* cur, int32_t* nxt, int R, int grow,
 
 size_t attention_smem_bytes();
 size_t score_topk_smem_bytes(int K);
+
+// Largest NBmax the fused score + admit kernel can hold in shared memory.
+constexpr int kMaxBlocksPerHead = 131072;
 
 }  // namespace oasis

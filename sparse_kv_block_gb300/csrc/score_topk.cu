@@ -23,8 +23,10 @@
 // KP keys, then a bitonic merge), and finally merge their lists in a tree.
 // Keys are 64-bit: order-preserving score bits above the complemented block
 // id, so ties break to the lower id and all keys are distinct.
+#include "admit.cuh"
 #include "common.cuh"
 #include "kernels.h"
+#include "sortnet.cuh"
 
 namespace oasis {
 namespace {
@@ -44,60 +46,9 @@ struct Layout {
   static constexpr int total = keys + kCW * KP * 8 + 128;
 };
 
-// One compare-exchange stage over E = 32*KPL keys (key e = i*32 + lane in
-// x[i]); partner e ^ j; the block of `size` keys holding e is ordered
-// descending when ((e & size) == 0) == desc.
-template <int KPL>
-__device__ __forceinline__ void bitonic_stage(uint64_t (&x)[KPL], int size,
-                                              int j, bool desc) {
-  const int lane = threadIdx.x & 31;
-  if (j >= 32) {
-    const int jr = j >> 5;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      if ((i & jr) == 0) {
-        const int p = i | jr;
-        const int e = i * 32 + lane;
-        const bool d = ((e & size) == 0) == desc;
-        const uint64_t lo = x[i], hi = x[p];
-        const bool sw = d ? (lo < hi) : (lo > hi);
-        x[i] = sw ? hi : lo;
-        x[p] = sw ? lo : hi;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      const int e = i * 32 + lane;
-      const uint64_t y = __shfl_xor_sync(0xffffffffu, x[i], j);
-      const bool lower = (lane & j) == 0;
-      const bool d = ((e & size) == 0) == desc;
-      const bool take_max = (lower == d);
-      x[i] = take_max ? (x[i] > y ? x[i] : y) : (x[i] < y ? x[i] : y);
-    }
-  }
-}
-
-template <int KPL>
-__device__ __forceinline__ void bitonic_sort(uint64_t (&x)[KPL], bool desc) {
-  constexpr int E = 32 * KPL;
-#pragma unroll
-  for (int size = 2; size <= E; size <<= 1) {
-#pragma unroll
-    for (int j = size >> 1; j > 0; j >>= 1) bitonic_stage<KPL>(x, size, j, desc);
-  }
-}
-
-// a (descending) <- top E of a U b, descending; b must be ascending.
-template <int KPL>
-__device__ __forceinline__ void merge_top(uint64_t (&a)[KPL],
-                                          const uint64_t (&b)[KPL]) {
-  constexpr int E = 32 * KPL;
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) a[i] = a[i] > b[i] ? a[i] : b[i];
-#pragma unroll
-  for (int j = E >> 1; j > 0; j >>= 1) bitonic_stage<KPL>(a, E, j, true);
-}
+static_assert(kStages * kChunkBytes >=
+                  sizeof(AdmitWarpSmem) + 2 * 4 * (kMaxBlocksPerHead / 32),
+              "the fused admit reuses the ring");
 
 template <int KPL>
 __global__ void __launch_bounds__(kThreads)
@@ -110,7 +61,7 @@ __global__ void __launch_bounds__(kThreads)
   uint64_t* empty = full + kStages;
   uint64_t* keybuf = reinterpret_cast<uint64_t*>(smem + L::keys);
 
-  const int pair = blockIdx.x;
+  const int pair = a.pair0 + blockIdx.x;
   const int r = pair / a.Hkv;
   const int h = pair - r * a.Hkv;
   const int warp = threadIdx.x >> 5;
@@ -159,6 +110,7 @@ __global__ void __launch_bounds__(kThreads)
       for (int cc = max(0, c - kStages); cc < c; ++cc)
         (void)mbar_wait(&full[cc % kStages], (cc / kStages) & 1);
     }
+    __syncwarp();
   } else {
     // ---------------- consumers: score, then keep a running top-KP
     // Lane weights: lanes 0-15 cover the min row, 16-31 the max row, 8 dims each.
@@ -272,6 +224,8 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   if (warp == 0) {
+    // The ring is idle now (every bulk copy has landed and been consumed).
+    AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(ring);
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
       const int e = i * 32 + lane;
@@ -282,7 +236,13 @@ __global__ void __launch_bounds__(kThreads)
         if (a.topk_scores)
           a.topk_scores[static_cast<size_t>(pair) * a.K + e] =
               key == 0ull ? -INFINITY : key_float(static_cast<uint32_t>(key >> 32));
+        S.topk[e] = id;
       }
+    }
+    if (a.fuse_admit) {
+      __syncwarp();
+      admit_warp<KPL>(a.admit, pair, S,
+                      reinterpret_cast<uint32_t*>(ring + sizeof(AdmitWarpSmem)));
     }
   }
 }
@@ -300,9 +260,8 @@ cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int grid = a.R * a.Hkv;
-  if (grid == 0) return cudaSuccess;
-  score_topk_kernel<KPL><<<grid, kThreads, Layout<KPL>::total, s>>>(a);
+  if (a.pairs <= 0) return cudaSuccess;
+  score_topk_kernel<KPL><<<a.pairs, kThreads, Layout<KPL>::total, s>>>(a);
   return cudaGetLastError();
 }
 

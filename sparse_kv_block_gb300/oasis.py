@@ -27,7 +27,8 @@ class oasis_config(ctypes.Structure):
     _fields_ = [("num_layers", c_int32), ("num_requests", c_int32), ("max_blocks", c_int32),
                 ("num_q_heads", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
                 ("block_size", c_int32), ("topk", c_int32), ("fetch_ratio", c_float),
-                ("softmax_scale", c_float), ("out_fp32", c_int32), ("device", c_int32)]
+                ("softmax_scale", c_float), ("out_fp32", c_int32), ("device", c_int32),
+                ("side_groups", c_int32)]
 
 
 class oasis_sizes(ctypes.Structure):
@@ -118,9 +119,9 @@ def _stream(s) -> Optional[int]:
 
 
 def make_config(R, NBmax, Hq, Hkv, K, fetch_ratio, layers=1, softmax_scale=0.0,
-                out_fp32=False, device=0, d=128, B=16) -> oasis_config:
+                out_fp32=False, device=0, d=128, B=16, side_groups=0) -> oasis_config:
     return oasis_config(layers, R, NBmax, Hq, Hkv, d, B, K, fetch_ratio, softmax_scale,
-                        1 if out_fp32 else 0, device)
+                        1 if out_fp32 else 0, device, side_groups)
 
 
 def oasis_config_error(cfg: oasis_config) -> Optional[str]:

@@ -71,9 +71,13 @@ def test_small_groups_and_many_requests(dev):
     L.eng.close()
 
 
-def test_fused_step_matches_oracle(dev):
-    L = H.make_layer(TINY, seed=5, steps=6, out_fp32=True)
-    sh, eng = L.shape, L.eng
+@pytest.mark.parametrize("groups,R", [(0, 2), (3, 5), (10, 5)])
+def test_fused_step_matches_oracle(dev, groups, R):
+    # oasis_step: fused scan + top-K + admission per request group on one side
+    # stream, gathers per group on another; uneven and one-pair groups too.
+    sh = dataclasses.replace(TINY, R=R)
+    L = H.make_layer(sh, seed=5, steps=6, out_fp32=True, side_groups=groups)
+    eng = L.eng
     out = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
     outd = torch.empty_like(out)
     for t in range(6):
