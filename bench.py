@@ -141,7 +141,7 @@ class ClockSampler:
                 "samples_under_load": len(loaded)}
 
 
-def build_layer(shape, seed, dev, warm=True):
+def build_layer(shape, seed, dev, side_groups=0, schedule=0):
     """Allocate and fill one layer (untimed setup); returns (engine, q, qd, lens, host)."""
     from sparse_kv_block_gb300.oasis import Oasis, make_config
     lens = workload.ctx_lens(shape)
@@ -150,7 +150,7 @@ def build_layer(shape, seed, dev, warm=True):
     gen = dev if dev.type == "cuda" else "cpu"
     workload.host_kv(shape, seed, 0, lens, device=gen, out=host)
     cfg = make_config(shape.R, shape.NBmax, shape.Hq, shape.Hkv, shape.K, shape.fetch_ratio,
-                      device=dev.index or 0)
+                      device=dev.index or 0, side_groups=side_groups, schedule=schedule)
     eng = Oasis(cfg, host_kv=[host])
     eng.set_context(lens)
     eng.oasis_build_summaries(0, 0)
@@ -278,7 +278,7 @@ def run_oasis(args, ws, rank, local):
     torch.cuda.set_device(dev)
     shape = get_shape(args)
     nq = args.queries
-    eng, lens, host = build_layer(shape, args.seed + rank, dev)
+    eng, lens, host = build_layer(shape, args.seed + rank, dev, args.side_groups, args.schedule)
     q, qd = workload.queries(shape, args.seed + rank, 0, nq, device=dev)
     warm_start(eng, shape, q[0], dev)
     odt = torch.bfloat16
@@ -424,17 +424,220 @@ def run_oasis(args, ws, rank, local):
     eng.close()
 
 
+def run_oasis_layers(args, ws, rank, local):
+    """Multi-layer decode loop: every step runs oasis_step for each layer in
+    order on one main stream; each layer's side work overlaps the next
+    layers.  Host stores are shared by layers l and l + M when the host
+    cannot pin one per layer (M = --host-stores); every layer keeps its own
+    summaries, resident pool and tables."""
+    from sparse_kv_block_gb300.oasis import Oasis, lib, make_config
+    lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = get_shape(args)
+    L, nq = shape.layers, min(args.queries, 16)
+    M = max(1, min(L, args.host_stores))
+    lens = workload.ctx_lens(shape)
+    stores = []
+    for m in range(M):
+        h = torch.empty((shape.R, shape.Hkv, shape.NBmax, 2, 16, 128), dtype=torch.bfloat16,
+                        pin_memory=True)
+        workload.host_kv(shape, args.seed + rank, m, lens, device=dev, out=h)
+        stores.append(h)
+    cfg = make_config(shape.R, shape.NBmax, shape.Hq, shape.Hkv, shape.K, shape.fetch_ratio,
+                      layers=L, device=local, side_groups=args.side_groups,
+                      schedule=args.schedule)
+    eng = Oasis(cfg, host_kv=[stores[l % M] for l in range(L)])
+    eng.set_context(lens)
+    qs, qds = [], []
+    for l in range(L):
+        q, qd = workload.queries(shape, args.seed + rank, l, nq, device=dev)
+        qs.append(q)
+        qds.append(qd)
+        eng.oasis_build_summaries(l, 0)
+        topk = torch.empty((shape.R, shape.Hkv, shape.K), dtype=torch.int32, device=dev)
+        eng.oasis_score_topk(l, 0, q[0], topk)
+        torch.cuda.synchronize(dev)
+        eng.res_ids[l][0].copy_(topk)
+        eng.oasis_load_resident(l, 0)
+    eng.oasis_sync()
+    outs = [torch.empty((shape.R, shape.Hq, 128), dtype=torch.bfloat16, device=dev)
+            for _ in range(2)]
+    main = torch.cuda.Stream(dev)
+    h2d_gbs = h2d_bandwidth(dev)
+    step = 0
+
+    def one_step():
+        nonlocal step
+        for l in range(L):
+            eng.oasis_step(l, step, qs[l][step % nq], qds[l][step % nq], outs[0], outs[1], main)
+        step += 1
+
+    for _ in range(args.warmup):
+        one_step()
+    for l in range(L):
+        eng.oasis_join(l, main)
+    torch.cuda.synchronize(dev)
+    eng.oasis_sync()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    eng.oasis_profile_enable(True)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for _ in range(args.steps):
+        one_step()
+    for l in range(L):
+        eng.oasis_join(l, main)
+    e1.record(main)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    ms_sum, counts, off_sum = eng.oasis_profile_read()
+    eng.oasis_profile_enable(False)
+    clk = clocks.stop()
+    eng.oasis_sync()
+    ms_max = max_over_ranks(ms, ws)
+    value = ws * args.steps * L / (ms_max * 1e-3)
+    adm = 0
+    for l in range(L):
+        adm += int(eng.step_lists(l)["n_admit"].sum().item())
+    link_bytes = adm / L * UNIT_BYTES
+    peaks = measured_peaks()
+    R, Hq, Hkv, K, NB = shape.R, shape.Hq, shape.Hkv, shape.K, shape.NBmax
+    names = ["attention", "score_topk", "admit_evict", "prefetch"]
+    per = {}
+    for i, n in enumerate(names):
+        if counts[i]:
+            per[n] = {"ms_per_layer_step": round(ms_sum[i] / (args.steps * L), 5),
+                      "launches_per_layer_step": counts[i] / (args.steps * L)}
+    attn_bytes = R * Hkv * K * UNIT_BYTES + 4 * R * Hq * 128 * 2
+    scan_bytes = R * Hkv * NB * SUMM_BYTES
+    a_ms = ms_sum[0] / counts[0]
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(shape), "host_stores": M,
+                       "note": f"layers l and l+{M} share one pinned host store",
+                       "tokens_per_s": round(value * R / L, 1),
+                       "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "kernel": "attention",
+                         "achieved": round(attn_bytes / (a_ms * 1e-3) / 1e9, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(attn_bytes / (a_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                         "traffic": None},
+            "hbm_bytes_per_layer_step": attn_bytes + scan_bytes,
+            "hbm_achieved_gbs_whole_step": round((attn_bytes + scan_bytes) * value / 1e9, 1),
+            "host_link": {"h2d_memcpy_gbs": round(h2d_gbs, 1),
+                          "bytes_per_layer_step": int(link_bytes),
+                          "achieved_gbs_whole_step": round(link_bytes * value / 1e9, 1)},
+            "kernels": per, "gpu_launches": int(sum(counts)), "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    eng.close()
+
+
+def run_cap_sweep(args, ws, rank, local):
+    """Fetch-cap sweep on the single-layer shape: for each cap, layer-steps/s,
+    host-to-device bytes per step, and the top-K agreement between the draft
+    query's selection at step t and the next step's true query (both ranked
+    by the summary score through oasis_score_topk)."""
+    import dataclasses
+    from sparse_kv_block_gb300.oasis import Oasis, lib, make_config
+    lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    base = get_shape(args)
+    lens = workload.ctx_lens(base)
+    host = torch.empty((base.R, base.Hkv, base.NBmax, 2, 16, 128), dtype=torch.bfloat16,
+                       pin_memory=True)
+    workload.host_kv(base, args.seed, 0, lens, device=dev, out=host)
+    nq = args.queries
+    q, qd = workload.queries(base, args.seed, 0, nq + 1, device=dev)
+    main = torch.cuda.Stream(dev)
+    results = []
+    for cap in (0.01, 0.05, 0.25, 1.0):
+        shape = dataclasses.replace(base, fetch_ratio=cap)
+        cfg = make_config(shape.R, shape.NBmax, shape.Hq, shape.Hkv, shape.K, cap,
+                          device=local, side_groups=args.side_groups, schedule=args.schedule)
+        eng = Oasis(cfg, host_kv=[host])
+        eng.set_context(lens)
+        eng.oasis_build_summaries(0, 0)
+        warm_start(eng, shape, q[0], dev)
+        out = torch.empty((shape.R, shape.Hq, 128), dtype=torch.bfloat16, device=dev)
+        outd = torch.empty_like(out)
+        lists = eng.step_lists(0)
+        true_topk = torch.empty((shape.R, shape.Hkv, shape.K), dtype=torch.int32, device=dev)
+        P, NB, K = shape.R * shape.Hkv, shape.NBmax, shape.K
+        agree, adm = [], []
+        step = 0
+        for _ in range(args.warmup):
+            eng.oasis_step(0, step, q[step % nq], qd[step % nq], out, outd, main)
+            step += 1
+        eng.oasis_join(0, main)
+        torch.cuda.synchronize(dev)
+        for _ in range(8):      # agreement and admissions, read back per step
+            t = step % nq
+            eng.oasis_step(0, step, q[t], qd[t], out, outd, main)
+            eng.oasis_join(0, main)
+            eng.oasis_score_topk(0, step, q[t + 1], true_topk, None, main)
+            torch.cuda.synchronize(dev)
+            a = torch.zeros((P, NB + 1), device=dev)
+            b = torch.zeros((P, NB + 1), device=dev)
+            a.scatter_(1, lists["topk_ids"].view(P, K).long() + 1, 1.0)
+            b.scatter_(1, true_topk.view(P, K).long() + 1, 1.0)
+            agree.append(float(((a * b)[:, 1:].sum(1) / K).mean()))
+            adm.append(int(lists["n_admit"].sum()))
+            step += 1
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for _ in range(args.steps):
+            eng.oasis_step(0, step, q[step % nq], qd[step % nq], out, outd, main)
+            step += 1
+        eng.oasis_join(0, main)
+        e1.record(main)
+        torch.cuda.synchronize(dev)
+        eng.oasis_sync()
+        ms = e0.elapsed_time(e1) / args.steps
+        results.append({"fetch_ratio": cap, "C": shape.C,
+                        "layer_steps_per_s": round(1e3 / ms, 1),
+                        "ms_per_step": round(ms, 4),
+                        "h2d_GB_per_layer_step": round(sum(adm) / len(adm) * UNIT_BYTES / 1e9, 5),
+                        "admitted_units_per_step": sum(adm) / len(adm),
+                        "topk_agreement_draft_vs_next": round(sum(agree) / len(agree), 5)})
+        eng.close()
+        del eng
+        torch.cuda.empty_cache()
+    if rank == 0:
+        print(json.dumps({"cap_sweep": results, "workload": workload_desc(base),
+                          "steps": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="oasis", choices=["oasis", "reference"])
-    ap.add_argument("--workload", default="qwen3_8b_16k", choices=["qwen3_8b_16k", "tiny"])
+    ap.add_argument("--workload", default="qwen3_8b_16k",
+                    choices=["qwen3_8b_16k", "tiny", "qwen3_8b_36l"])
+    ap.add_argument("--cap-sweep", action="store_true",
+                    help="fetch-cap sweep (0.01, 0.05, 0.25, 1.0) on the single-layer shape")
+    ap.add_argument("--host-stores", type=int, default=12,
+                    help="distinct pinned host stores of a multi-layer workload")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--queries", type=int, default=64, help="distinct query steps, cycled")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--side-groups", type=int, default=0,
+                    help="request groups of the side work (0 = library default)")
+    ap.add_argument("--schedule", type=int, default=0, help="0 scan first, 1 concurrent")
     ap.add_argument("--requests", type=int, default=0,
                     help="override the request count (small cases for profiling)")
     args = ap.parse_args()
@@ -443,6 +646,10 @@ def main():
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.cap_sweep:
+        run_cap_sweep(args, ws, rank, local)
+    elif workload.SHAPES[args.workload].layers > 1:
+        run_oasis_layers(args, ws, rank, local)
     else:
         run_oasis(args, ws, rank, local)
     if ws > 1:

@@ -107,7 +107,15 @@ typedef struct {
   int32_t device;        /* CUDA device ordinal */
   int32_t side_groups;   /* request groups oasis_step pipelines its side work
                             in (0 = one per 256 (request, KV head) pairs, <= 8) */
+  int32_t schedule;      /* OASIS_SCHEDULE_*: how oasis_step orders a1 */
 } oasis_config;
+
+/* oasis_step schedules.  SCAN_FIRST: the attention of a step starts when the
+ * step's scans are done, so the scans run alone and the host-link gathers
+ * start early and overlap the attention.  CONCURRENT: the attention starts at
+ * once, sharing HBM with the scans.  Results are identical. */
+#define OASIS_SCHEDULE_SCAN_FIRST 0
+#define OASIS_SCHEDULE_CONCURRENT 1
 
 typedef struct {
   size_t kv_pool_bytes;   /* per layer */

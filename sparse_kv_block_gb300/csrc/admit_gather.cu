@@ -45,8 +45,12 @@ cudaError_t launch_admit_kpl(const AdmitArgs& a, cudaStream_t s) {
 // Gather of 8 KiB units from the pinned host store (read through its device
 // mapping over the host link) into pool units, one warp per unit; every lane
 // issues all 16 of its 16-byte loads before storing, so each warp keeps a
-// whole unit in flight.
-constexpr int kGatherThreads = 256;
+// whole unit in flight.  The grid is kept small (at most kGatherCtas CTAs of
+// 4 warps, ~3 MiB in flight, several times the link's bandwidth-latency
+// product) so that it leaves the registers and warp slots of almost every
+// SM to the attention and scan kernels it runs beside.
+constexpr int kGatherThreads = 128;
+constexpr int kGatherCtas = 96;
 
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs a) {
   const int lane = threadIdx.x & 31;
@@ -244,8 +248,7 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
   if (total == 0) return cudaSuccess;
   const long long warps_needed = total;
   long long grid = (warps_needed + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
-  const long long cap = 2LL * sm_count();
-  if (grid > cap) grid = cap;
+  if (grid > kGatherCtas) grid = kGatherCtas;
   gather_kernel<<<static_cast<int>(grid), kGatherThreads, 0, s>>>(a);
   return cudaGetLastError();
 }

@@ -42,7 +42,7 @@ struct LayerState {
   void* outd_stage = nullptr;
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_side_done = nullptr;
-  cudaEvent_t ev_attn_done = nullptr;
+  cudaEvent_t ev_scan_done = nullptr;
   std::vector<cudaEvent_t> ev_group;  // one per side-work request group
   bool side_pending = false;
   bool loaded = false;
@@ -105,6 +105,8 @@ const char* config_error(const oasis_config* c) {
   if (c->device < 0) return "device must be >= 0";
   if (c->max_blocks > kMaxBlocksPerHead) return "max_blocks must be <= 131072";
   if (c->side_groups < 0 || c->side_groups > 64) return "side_groups must be in 0..64";
+  if (c->schedule != OASIS_SCHEDULE_SCAN_FIRST && c->schedule != OASIS_SCHEDULE_CONCURRENT)
+    return "schedule must be OASIS_SCHEDULE_SCAN_FIRST or OASIS_SCHEDULE_CONCURRENT";
   const double units = static_cast<double>(c->num_requests) * c->num_kv_heads *
                        (c->topk + fetch_cap(*c)) * 2 * kBlock;
   if (units >= 2147483647.0) return "pool too large for a 32-bit TMA row coordinate";
@@ -451,7 +453,7 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
     S.outd_stage = w + (c->wl.outd_stage - b0);
     if (cudaEventCreateWithFlags(&S.ev_start, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_side_done, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&S.ev_attn_done, cudaEventDisableTiming) != cudaSuccess)
+        cudaEventCreateWithFlags(&S.ev_scan_done, cudaEventDisableTiming) != cudaSuccess)
       return bail(OASIS_ENOMEM);
     S.ev_group.assign(c->groups, nullptr);
     for (auto& e : S.ev_group)
@@ -475,7 +477,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
       if (e) cudaEventDestroy(e);
     if (L.ev_start) cudaEventDestroy(L.ev_start);
     if (L.ev_side_done) cudaEventDestroy(L.ev_side_done);
-    if (L.ev_attn_done) cudaEventDestroy(L.ev_attn_done);
+    if (L.ev_scan_done) cudaEventDestroy(L.ev_scan_done);
   }
   for (auto& p : ctx->prof_pool) {
     cudaEventDestroy(p.a);
@@ -642,6 +644,13 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
     if (int rc = ctx->cuda(cudaEventRecord(L.ev_group[0], ctx->side), "record group")) return rc;
     if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[0], 0), "group wait"))
       return rc;
+  }
+  if (ctx->cfg.schedule == OASIS_SCHEDULE_SCAN_FIRST) {
+    // The scan gets the whole HBM bandwidth and the SMs first, so the
+    // gathers (host-link bound) start as early as possible; the attention
+    // then overlaps the gathers, which write only spare units.
+    if (int rc = ctx->cuda(cudaEventRecord(L.ev_scan_done, ctx->side), "record scan")) return rc;
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_scan_done, 0), "wait scan")) return rc;
   }
   if (int rc = run_attention(ctx, layer, step, q, q_draft, out, out_draft, s)) return rc;
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_side_done, ctx->side2), "record side")) return rc;

@@ -28,7 +28,10 @@ class oasis_config(ctypes.Structure):
                 ("num_q_heads", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
                 ("block_size", c_int32), ("topk", c_int32), ("fetch_ratio", c_float),
                 ("softmax_scale", c_float), ("out_fp32", c_int32), ("device", c_int32),
-                ("side_groups", c_int32)]
+                ("side_groups", c_int32), ("schedule", c_int32)]
+
+
+SCHEDULE_SCAN_FIRST, SCHEDULE_CONCURRENT = 0, 1
 
 
 class oasis_sizes(ctypes.Structure):
@@ -119,9 +122,10 @@ def _stream(s) -> Optional[int]:
 
 
 def make_config(R, NBmax, Hq, Hkv, K, fetch_ratio, layers=1, softmax_scale=0.0,
-                out_fp32=False, device=0, d=128, B=16, side_groups=0) -> oasis_config:
+                out_fp32=False, device=0, d=128, B=16, side_groups=0,
+                schedule=0) -> oasis_config:
     return oasis_config(layers, R, NBmax, Hq, Hkv, d, B, K, fetch_ratio, softmax_scale,
-                        1 if out_fp32 else 0, device, side_groups)
+                        1 if out_fp32 else 0, device, side_groups, schedule)
 
 
 def oasis_config_error(cfg: oasis_config) -> Optional[str]:

@@ -41,7 +41,8 @@ class Layer:
 
 
 def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_fp32=False,
-               gen_device="cpu", pairs=None, res0=None, side_groups=0) -> Layer:
+               gen_device="cpu", pairs=None, res0=None, side_groups=0,
+               schedule=0) -> Layer:
     if K is not None or fetch_ratio is not None:
         shape = dataclasses.replace(shape, K=K if K is not None else shape.K,
                                     fetch_ratio=shape.fetch_ratio if fetch_ratio is None else fetch_ratio)
@@ -54,7 +55,7 @@ def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_
     if res0 is None:
         res0 = workload.initial_resident(shape, seed, 0, lens)
     cfg = make_config(shape.R, shape.NBmax, shape.Hq, shape.Hkv, shape.K, shape.fetch_ratio,
-                      out_fp32=out_fp32, side_groups=side_groups)
+                      out_fp32=out_fp32, side_groups=side_groups, schedule=schedule)
     eng = Oasis(cfg, host_kv=[host])
     eng.set_context(lens)
     eng.set_resident(0, res0, 0)

@@ -71,12 +71,13 @@ def test_small_groups_and_many_requests(dev):
     L.eng.close()
 
 
-@pytest.mark.parametrize("groups,R", [(0, 2), (3, 5), (10, 5)])
-def test_fused_step_matches_oracle(dev, groups, R):
+@pytest.mark.parametrize("groups,R,schedule", [(0, 2, 0), (3, 5, 0), (10, 5, 0), (3, 5, 1)])
+def test_fused_step_matches_oracle(dev, groups, R, schedule):
     # oasis_step: fused scan + top-K + admission per request group on one side
-    # stream, gathers per group on another; uneven and one-pair groups too.
+    # stream, gathers per group on another; uneven and one-pair groups too;
+    # both schedules.
     sh = dataclasses.replace(TINY, R=R)
-    L = H.make_layer(sh, seed=5, steps=6, out_fp32=True, side_groups=groups)
+    L = H.make_layer(sh, seed=5, steps=6, out_fp32=True, side_groups=groups, schedule=schedule)
     eng = L.eng
     out = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
     outd = torch.empty_like(out)
