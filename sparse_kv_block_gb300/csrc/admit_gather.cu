@@ -1,5 +1,7 @@
 // admit_gather.cu -- capped eviction (a4), prefetch gather (a5) and the
 // support kernels: table initialisation, summary build and token append.
+#include <cstdlib>
+
 #include "admit.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -45,12 +47,14 @@ cudaError_t launch_admit_kpl(const AdmitArgs& a, cudaStream_t s) {
 // Gather of 8 KiB units from the pinned host store (read through its device
 // mapping over the host link) into pool units, one warp per unit; every lane
 // issues all 16 of its 16-byte loads before storing, so each warp keeps a
-// whole unit in flight.  The grid is kept small (at most kGatherCtas CTAs of
-// 4 warps, ~3 MiB in flight, several times the link's bandwidth-latency
-// product) so that it leaves the registers and warp slots of almost every
-// SM to the attention and scan kernels it runs beside.
+// whole unit in flight.  The grid is kept small: at most kGatherCtas CTAs of
+// 4 warps, 2 MiB of host reads in flight.  Measured on GB300 (pinned H2D
+// ~210 GB/s): 16 / 32 / 64 / 96 CTAs move 131 / 174 / 199 / 206 GB/s, while a
+// concurrent HBM-streaming kernel slows by 1 / 9 / 35 / 48 %: the host reads
+// in flight compete with HBM traffic in the memory system, so the grid stops
+// where the link is nearly saturated.
 constexpr int kGatherThreads = 128;
-constexpr int kGatherCtas = 96;
+constexpr int kGatherCtas = 64;
 
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs a) {
   const int lane = threadIdx.x & 31;
@@ -248,7 +252,13 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
   if (total == 0) return cudaSuccess;
   const long long warps_needed = total;
   long long grid = (warps_needed + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
-  if (grid > kGatherCtas) grid = kGatherCtas;
+  static const int cap = [] {
+    // Tuning override of the gather's CTA count (units in flight / 4).
+    const char* e = std::getenv("OASIS_GATHER_CTAS");
+    const int v = e ? std::atoi(e) : 0;
+    return v > 0 ? v : kGatherCtas;
+  }();
+  if (grid > cap) grid = cap;
   gather_kernel<<<static_cast<int>(grid), kGatherThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
