@@ -541,6 +541,75 @@ def run_oasis_layers(args, ws, rank, local):
     eng.close()
 
 
+def run_kernels_alone(args, ws, rank, local):
+    """Each stage of the step timed alone (CUDA events on its stream, after
+    warm-up) on the single-layer workload, through the stage-level C ABI
+    calls; reports achieved GB/s against the HBM / host-link peaks."""
+    from sparse_kv_block_gb300.oasis import lib
+    lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = get_shape(args)
+    eng, lens, host = build_layer(shape, args.seed, dev)
+    q, qd = workload.queries(shape, args.seed, 0, 4, device=dev)
+    warm_start(eng, shape, q[0], dev)
+    R, Hq, Hkv, K, C, NB = shape.R, shape.Hq, shape.Hkv, shape.K, shape.C, shape.NBmax
+    out = torch.empty((R, Hq, 128), dtype=torch.bfloat16, device=dev)
+    outd = torch.empty_like(out)
+    topk = torch.empty((R, Hkv, K), dtype=torch.int32, device=dev)
+    sc = torch.empty((R, Hkv, K), dtype=torch.float32, device=dev)
+    aid = torch.empty((R, Hkv, max(C, 1)), dtype=torch.int32, device=dev)
+    asl, evi = torch.empty_like(aid), torch.empty_like(aid)
+    nad = torch.empty((R, Hkv), dtype=torch.int32, device=dev)
+    st = torch.cuda.Stream(dev)
+    n = max(5, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(n):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    res = {}
+    res["attention_ms"] = timed(lambda: eng.oasis_lookahead_attn(0, 0, q[1], qd[1], out, outd, st))
+    res["score_topk_ms"] = timed(lambda: eng.oasis_score_topk(0, 0, qd[1], topk, sc, st))
+    eng.oasis_score_topk(0, 0, qd[1], topk, sc, st)
+    torch.cuda.synchronize(dev)
+    res["admit_evict_ms"] = timed(lambda: eng.oasis_admit_evict(0, 0, topk, aid, asl, evi, nad, st))
+    eng.oasis_admit_evict(0, 0, topk, aid, asl, evi, nad, st)
+    torch.cuda.synchronize(dev)
+    units = int(nad.sum())
+    res["prefetch_ms"] = timed(lambda: eng.oasis_prefetch(0, 0, aid, asl, nad, st))
+    eng.oasis_sync()
+    peaks = measured_peaks()
+    h2d = h2d_bandwidth(dev)
+    attn_b = R * Hkv * K * UNIT_BYTES + 4 * R * Hq * 128 * 2
+    scan_b = R * Hkv * NB * SUMM_BYTES + R * Hq * 128 * 2
+    gb = lambda b, ms: b / (ms * 1e-3) / 1e9
+    line = {"mode": "kernels-alone", "workload": workload_desc(shape), "iters": n,
+            "attention": {"ms": round(res["attention_ms"], 5), "bytes": attn_b,
+                          "GBs": round(gb(attn_b, res["attention_ms"]), 1),
+                          "frac_hbm": round(gb(attn_b, res["attention_ms"]) / peaks["hbm_gbs"], 4)},
+            "score_topk": {"ms": round(res["score_topk_ms"], 5), "bytes": scan_b,
+                           "GBs": round(gb(scan_b, res["score_topk_ms"]), 1),
+                           "frac_hbm": round(gb(scan_b, res["score_topk_ms"]) / peaks["hbm_gbs"], 4)},
+            "admit_evict": {"ms": round(res["admit_evict_ms"], 5)},
+            "prefetch": {"ms": round(res["prefetch_ms"], 5), "units": units,
+                         "GBs": round(gb(units * UNIT_BYTES, res["prefetch_ms"]), 1),
+                         "frac_h2d_memcpy": round(gb(units * UNIT_BYTES, res["prefetch_ms"]) / h2d, 4)},
+            "hbm_peak_gbs": peaks["hbm_gbs"], "h2d_memcpy_gbs": round(h2d, 1)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    eng.close()
+
+
 def run_cap_sweep(args, ws, rank, local):
     """Fetch-cap sweep on the single-layer shape: for each cap, layer-steps/s,
     host-to-device bytes per step, and the top-K agreement between the draft
@@ -627,6 +696,8 @@ def main():
     ap.add_argument("--impl", default="oasis", choices=["oasis", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_16k",
                     choices=["qwen3_8b_16k", "tiny", "qwen3_8b_36l"])
+    ap.add_argument("--kernels-alone", action="store_true",
+                    help="time each stage alone on the single-layer workload")
     ap.add_argument("--cap-sweep", action="store_true",
                     help="fetch-cap sweep (0.01, 0.05, 0.25, 1.0) on the single-layer shape")
     ap.add_argument("--host-stores", type=int, default=12,
@@ -648,6 +719,8 @@ def main():
         run_reference(args, ws, rank)
     elif args.cap_sweep:
         run_cap_sweep(args, ws, rank, local)
+    elif args.kernels_alone:
+        run_kernels_alone(args, ws, rank, local)
     elif workload.SHAPES[args.workload].layers > 1:
         run_oasis_layers(args, ws, rank, local)
     else:

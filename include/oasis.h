@@ -236,12 +236,17 @@ OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step,
                              const int32_t* admit_slots,
                              const int32_t* n_admit, void* stream);
 
-/* a1..a5 as one layer-step (a6, [R] "layer-local synchronization").  On
- * `stream`: wait for this layer's previous side work, then a1.  On the
- * context's high-priority side stream, concurrently: a2+a3, a4, a5 into the
- * context's workspace lists.  Returns at once; the next oasis_step (or
- * oasis_join) of the same layer orders after the side work.  Inputs must
- * stay valid until then. */
+/* a1..a5 as one layer-step (a6, [R] "layer-local synchronization").
+ * q_draft is first copied (on `stream`) into a per-layer staging buffer.
+ * Side work, on the context's two high-priority side streams, ordered after
+ * everything already on `stream` (so after this layer's previous attention):
+ * a2+a3 fused with a4 per request group, each group's a5 gather as soon as
+ * its admissions exist; results go to the context's workspace lists.  On
+ * `stream`: wait for this layer's previous side work (its admissions must be
+ * in the pool), with OASIS_SCHEDULE_SCAN_FIRST also for this step's scans,
+ * then a1.  Returns at once; q and q_draft may be reused once `stream`
+ * passes the call.  The next oasis_step of the layer (or oasis_join) orders
+ * the side work before its attention. */
 OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
                          const void* q_draft, void* out, void* out_draft,
                          void* stream);

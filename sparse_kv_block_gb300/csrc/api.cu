@@ -40,6 +40,7 @@ struct LayerState {
   void* qd_stage = nullptr;
   void* out_stage = nullptr;
   void* outd_stage = nullptr;
+  void* qd_ring[2] = {nullptr, nullptr};  // staged draft queries, by step parity
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_side_done = nullptr;
   cudaEvent_t ev_scan_done = nullptr;
@@ -57,7 +58,7 @@ struct ProfPair {
 struct WsLayout {
   size_t err, per_layer;
   size_t topk_ids, topk_scores, admit_ids, admit_slots, evict_ids, n_admit;
-  size_t q_stage, qd_stage, out_stage, outd_stage;
+  size_t q_stage, qd_stage, out_stage, outd_stage, qd_ring0, qd_ring1;
   size_t total;
 };
 
@@ -83,6 +84,8 @@ WsLayout ws_layout(const oasis_config& c) {
   w.qd_stage = o;    o += align_up(qbytes);
   w.out_stage = o;   o += align_up(obytes);
   w.outd_stage = o;  o += align_up(obytes);
+  w.qd_ring0 = o;    o += align_up(qbytes);
+  w.qd_ring1 = o;    o += align_up(qbytes);
   w.per_layer = o - kAlign;
   w.total = kAlign + w.per_layer * static_cast<size_t>(c.num_layers);
   return w;
@@ -451,6 +454,8 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
     S.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.n_admit - b0));
     S.q_stage = w + (c->wl.q_stage - b0);
     S.qd_stage = w + (c->wl.qd_stage - b0);
+    S.qd_ring[0] = w + (c->wl.qd_ring0 - b0);
+    S.qd_ring[1] = w + (c->wl.qd_ring1 - b0);
     S.out_stage = w + (c->wl.out_stage - b0);
     S.outd_stage = w + (c->wl.outd_stage - b0);
     if (cudaEventCreateWithFlags(&S.ev_start, cudaEventDisableTiming) != cudaSuccess ||
@@ -614,22 +619,34 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
   if (!L.loaded) return ctx->fail(OASIS_ESTATE, "layer %d: oasis_load_resident first", layer);
   if (int rc = ctx->set_device()) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (L.side_pending) {
-    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
-  }
+  // The side work reads the draft query from a per-layer double buffer, so
+  // the caller may reuse its buffer as soon as `stream` passes this call.
+  void* qd_copy = L.qd_ring[step & 1];
+  const size_t qbytes =
+      static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_q_heads * kHeadDim * 2;
+  if (int rc = ctx->cuda(cudaMemcpyAsync(qd_copy, q_draft, qbytes, cudaMemcpyDeviceToDevice, s),
+                         "stage q_draft"))
+    return rc;
+  // Start of this step's side work: everything earlier on `stream`, which
+  // includes the previous step's attention of this layer.  That is all the
+  // scan and the admission need (the admission rewrites the table the
+  // previous attention read, and its gathers write units that attention
+  // read), so the scan may overlap the previous step's gathers.
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_start, s), "record start")) return rc;
   ctx->prof_step_start(s);
   if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side, L.ev_start, 0), "side wait")) return rc;
   if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_start, 0), "side2 wait")) return rc;
-  // Side work first so that its CTAs are queued ahead of the attention grid.
+  // This step's attention needs the previous step's admissions in the pool.
+  if (L.side_pending) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
+  }
   // Request group g: scan + top-K + admission on `side`, then its gather on
-  // `side2` as soon as the group's admissions exist, so the host link starts
-  // early and stays busy while later groups are scanned.
+  // `side2` as soon as the group's admissions exist.
   const int pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
   for (int g = 0; g < ctx->groups; ++g) {
     const int p0 = static_cast<int>(static_cast<long long>(pairs) * g / ctx->groups);
     const int p1 = static_cast<int>(static_cast<long long>(pairs) * (g + 1) / ctx->groups);
-    if (int rc = run_score(ctx, layer, step, q_draft, L.topk_ids, L.topk_scores, ctx->side, p0,
+    if (int rc = run_score(ctx, layer, step, qd_copy, L.topk_ids, L.topk_scores, ctx->side, p0,
                            p1 - p0, true))
       return rc;
     if (ctx->C > 0) {
