@@ -390,12 +390,23 @@ def run_oasis(args, ws, rank, local):
                              "bytes_per_step": int(b), "ms_per_step": round(avg_ms[n], 5),
                              "launches_per_step": launches[n],
                              "avg_start_ms": round(avg_start[n], 5)}
+    hbm_src = ("measured hbm_gbs (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+               else "fallback 6.8 TB/s")
+    for n, k in per_kernel.items():
+        k["peak_source"] = (hbm_src if k["bound"] == "hbm" else
+                            "pinned cudaMemcpyAsync H2D, 256 MiB, measured in this run")
+    # DRAM bytes per attention launch: ncu dram__bytes_read+write on the
+    # 32-request case (269.26 + 0.13 MB) scaled by the 4x units of this
+    # workload; see profiles/dram_traffic_qwen3_8b_16k.md.
+    if shape.name == "qwen3_8b_16k" and "attention" in per_kernel:
+        per_kernel["attention"]["traffic"] = int(4 * (269.256192e6 + 0.12646e6))
+    # The dominant kernel is the longest per step; the attention (the largest
+    # HBM reader) is also reported on its own below.
     dk = per_kernel.get(dominant, per_kernel["attention"])
-    roofline = {"bound": "hbm" if dk["bound"] == "hbm" else "hbm", "kernel": dominant,
+    roofline = {"bound": dk["bound"], "kernel": dominant,
                 "achieved": dk["achieved"], "peak": dk["peak"], "unit": "GB/s",
-                "frac": dk["frac"], "traffic": None,
-                "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)"
-                if peaks["source"] == "measured" else "fallback 6.8 TB/s"}
+                "frac": dk["frac"], "traffic": dk.get("traffic"),
+                "peak_source": dk["peak_source"]}
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
@@ -404,7 +415,8 @@ def run_oasis(args, ws, rank, local):
             "config": {"workload": workload_desc(shape), "parallelism": f"replicas{ws}",
                        "l2": "inputs larger than L2: 1.5 GiB of pool + summaries read per step",
                        "tokens_per_s": round(value * shape.R, 1)},
-            "roofline": roofline, "kernels": per_kernel,
+            "roofline": roofline, "roofline_hbm": per_kernel.get("attention"),
+            "kernels": per_kernel,
             "host_link": {"h2d_memcpy_gbs": round(h2d_gbs, 1),
                           "admitted_units_per_step": adm_units,
                           "bytes_per_step": int(link_bytes)},
