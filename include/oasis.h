@@ -264,13 +264,14 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step,
                               void* out_host, void* out_draft_host,
                               void* stream);
 
-/* Pointers to the context's per-layer workspace lists written by oasis_step
+/* Pointers to the workspace lists that oasis_step(layer, step) writes
  * (topk_ids, topk_scores, admit_ids, admit_slots, evict_ids, n_admit; any
- * may be NULL). */
-OASIS_API int oasis_step_lists(oasis_ctx* ctx, int layer, int32_t** topk_ids,
-                               float** topk_scores, int32_t** admit_ids,
-                               int32_t** admit_slots, int32_t** evict_ids,
-                               int32_t** n_admit);
+ * may be NULL).  The lists are double-buffered by step parity: those of step
+ * t stay valid until oasis_step(layer, t + 2) is issued. */
+OASIS_API int oasis_step_lists(oasis_ctx* ctx, int layer, int step,
+                               int32_t** topk_ids, float** topk_scores,
+                               int32_t** admit_ids, int32_t** admit_slots,
+                               int32_t** evict_ids, int32_t** n_admit);
 
 /* Support (a0, growing contexts): append one token per request to `layer`.
  * k_new, v_new: dev [R][Hkv][d] bf16.  The token goes to position

@@ -29,13 +29,17 @@ struct LayerState {
   int32_t* stamps = nullptr;
   int32_t* phys = nullptr;   // [2][R][Hkv][U]
   CUtensorMap pool_map;
-  // workspace lists
-  int32_t* topk_ids = nullptr;
-  float* topk_scores = nullptr;
-  int32_t* admit_ids = nullptr;
-  int32_t* admit_slots = nullptr;
-  int32_t* evict_ids = nullptr;
-  int32_t* n_admit = nullptr;
+  // Workspace lists of oasis_step, double-buffered by step parity: the
+  // gathers of step t read lists[t & 1] while the admission of step t + 1
+  // may already write lists[(t + 1) & 1].
+  struct Lists {
+    int32_t* topk_ids = nullptr;
+    float* topk_scores = nullptr;
+    int32_t* admit_ids = nullptr;
+    int32_t* admit_slots = nullptr;
+    int32_t* evict_ids = nullptr;
+    int32_t* n_admit = nullptr;
+  } lists[2];
   void* q_stage = nullptr;
   void* qd_stage = nullptr;
   void* out_stage = nullptr;
@@ -74,12 +78,13 @@ WsLayout ws_layout(const oasis_config& c) {
   const size_t obytes = qbytes * (c.out_fp32 ? 2 : 1);
   w.err = 0;
   size_t o = kAlign;
-  w.topk_ids = o;    o += align_up(pairs * c.topk * 4);
-  w.topk_scores = o; o += align_up(pairs * c.topk * 4);
-  w.admit_ids = o;   o += align_up(pairs * (C ? C : 1) * 4);
-  w.admit_slots = o; o += align_up(pairs * (C ? C : 1) * 4);
-  w.evict_ids = o;   o += align_up(pairs * (C ? C : 1) * 4);
-  w.n_admit = o;     o += align_up(pairs * 4);
+  // each list twice (step parity 0 and 1), the copies adjacent
+  w.topk_ids = o;    o += 2 * align_up(pairs * c.topk * 4);
+  w.topk_scores = o; o += 2 * align_up(pairs * c.topk * 4);
+  w.admit_ids = o;   o += 2 * align_up(pairs * (C ? C : 1) * 4);
+  w.admit_slots = o; o += 2 * align_up(pairs * (C ? C : 1) * 4);
+  w.evict_ids = o;   o += 2 * align_up(pairs * (C ? C : 1) * 4);
+  w.n_admit = o;     o += 2 * align_up(pairs * 4);
   w.q_stage = o;     o += align_up(qbytes);
   w.qd_stage = o;    o += align_up(qbytes);
   w.out_stage = o;   o += align_up(obytes);
@@ -295,8 +300,9 @@ int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
   a.pairs = pairs < 0 ? a.R * a.Hkv : pairs;
   a.fuse_admit = fused ? 1 : 0;
   if (fused)
-    a.admit = admit_args(ctx, layer, step, nullptr, L.admit_ids, L.admit_slots, L.evict_ids,
-                         L.n_admit);
+    a.admit = admit_args(ctx, layer, step, nullptr, L.lists[step & 1].admit_ids,
+                         L.lists[step & 1].admit_slots, L.lists[step & 1].evict_ids,
+                         L.lists[step & 1].n_admit);
   cudaEvent_t* pe = ctx->prof_begin(1, s);
   cudaError_t e = launch_score_topk(a, s);
   ctx->prof_end(pe, s);
@@ -446,12 +452,21 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
     // WsLayout offsets place layer 0's lists right after the error word.
     uint8_t* w = c->ws + kAlign + static_cast<size_t>(l) * c->wl.per_layer;
     const size_t b0 = kAlign;
-    S.topk_ids = reinterpret_cast<int32_t*>(w + (c->wl.topk_ids - b0));
-    S.topk_scores = reinterpret_cast<float*>(w + (c->wl.topk_scores - b0));
-    S.admit_ids = reinterpret_cast<int32_t*>(w + (c->wl.admit_ids - b0));
-    S.admit_slots = reinterpret_cast<int32_t*>(w + (c->wl.admit_slots - b0));
-    S.evict_ids = reinterpret_cast<int32_t*>(w + (c->wl.evict_ids - b0));
-    S.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.n_admit - b0));
+    {
+      const size_t pairs = R * H;
+      const size_t tk = align_up(pairs * cfg->topk * 4);
+      const size_t ad = align_up(pairs * (c->C ? c->C : 1) * 4);
+      const size_t na = align_up(pairs * 4);
+      for (int p = 0; p < 2; ++p) {
+        auto& Lp = S.lists[p];
+        Lp.topk_ids = reinterpret_cast<int32_t*>(w + (c->wl.topk_ids - b0) + p * tk);
+        Lp.topk_scores = reinterpret_cast<float*>(w + (c->wl.topk_scores - b0) + p * tk);
+        Lp.admit_ids = reinterpret_cast<int32_t*>(w + (c->wl.admit_ids - b0) + p * ad);
+        Lp.admit_slots = reinterpret_cast<int32_t*>(w + (c->wl.admit_slots - b0) + p * ad);
+        Lp.evict_ids = reinterpret_cast<int32_t*>(w + (c->wl.evict_ids - b0) + p * ad);
+        Lp.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.n_admit - b0) + p * na);
+      }
+    }
     S.q_stage = w + (c->wl.q_stage - b0);
     S.qd_stage = w + (c->wl.qd_stage - b0);
     S.qd_ring[0] = w + (c->wl.qd_ring0 - b0);
@@ -646,7 +661,8 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
   for (int g = 0; g < ctx->groups; ++g) {
     const int p0 = static_cast<int>(static_cast<long long>(pairs) * g / ctx->groups);
     const int p1 = static_cast<int>(static_cast<long long>(pairs) * (g + 1) / ctx->groups);
-    if (int rc = run_score(ctx, layer, step, qd_copy, L.topk_ids, L.topk_scores, ctx->side, p0,
+    const LayerState::Lists& Ls = L.lists[step & 1];
+    if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side, p0,
                            p1 - p0, true))
       return rc;
     if (ctx->C > 0) {
@@ -654,7 +670,7 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
         return rc;
       if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[g], 0), "group wait"))
         return rc;
-      if (int rc = run_prefetch(ctx, layer, step, L.admit_ids, L.admit_slots, L.n_admit,
+      if (int rc = run_prefetch(ctx, layer, step, Ls.admit_ids, Ls.admit_slots, Ls.n_admit,
                                 ctx->side2, p0, p1 - p0))
         return rc;
     }
@@ -715,17 +731,19 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
                    "d2h out_draft");
 }
 
-OASIS_API int oasis_step_lists(oasis_ctx* ctx, int layer, int32_t** topk_ids, float** topk_scores,
-                               int32_t** admit_ids, int32_t** admit_slots, int32_t** evict_ids,
-                               int32_t** n_admit) {
+OASIS_API int oasis_step_lists(oasis_ctx* ctx, int layer, int step, int32_t** topk_ids,
+                               float** topk_scores, int32_t** admit_ids, int32_t** admit_slots,
+                               int32_t** evict_ids, int32_t** n_admit) {
   if (int rc = check_layer(ctx, layer)) return rc;
   LayerState& L = ctx->layers[layer];
-  if (topk_ids) *topk_ids = L.topk_ids;
-  if (topk_scores) *topk_scores = L.topk_scores;
-  if (admit_ids) *admit_ids = L.admit_ids;
-  if (admit_slots) *admit_slots = L.admit_slots;
-  if (evict_ids) *evict_ids = L.evict_ids;
-  if (n_admit) *n_admit = L.n_admit;
+  if (step < 0) return ctx->fail(OASIS_EINVAL, "step_lists: bad step");
+  const LayerState::Lists& Ls = L.lists[step & 1];
+  if (topk_ids) *topk_ids = Ls.topk_ids;
+  if (topk_scores) *topk_scores = Ls.topk_scores;
+  if (admit_ids) *admit_ids = Ls.admit_ids;
+  if (admit_slots) *admit_slots = Ls.admit_slots;
+  if (evict_ids) *evict_ids = Ls.evict_ids;
+  if (n_admit) *n_admit = Ls.n_admit;
   return OASIS_OK;
 }
 

@@ -23,6 +23,8 @@
 // KP keys, then a bitonic merge), and finally merge their lists in a tree.
 // Keys are 64-bit: order-preserving score bits above the complemented block
 // id, so ties break to the lower id and all keys are distinct.
+#include <cstdlib>
+
 #include "admit.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -35,25 +37,25 @@ constexpr int kCW = 8;                       // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;     // + one producer warp
 constexpr int kChunk = 32;                   // blocks per stage
 constexpr int kChunkBytes = kChunk * kSummBytes;  // 16 KiB
-constexpr int kStages = 3;
+constexpr int kAdmitScratch = sizeof(AdmitWarpSmem) + 2 * 4 * (kMaxBlocksPerHead / 32);
 
-template <int KPL>
+// Shared memory: the ring of ST stages (reused by the fused admission once
+// every stage has been consumed, so at least kAdmitScratch bytes), the
+// stage barriers, and the per-warp key buffers.
+template <int KPL, int ST>
 struct Layout {
   static constexpr int KP = 32 * KPL;
   static constexpr int ring = 0;
-  static constexpr int bars = kStages * kChunkBytes;
+  static constexpr int bars =
+      ((ST * kChunkBytes > kAdmitScratch ? ST * kChunkBytes : kAdmitScratch) + 127) / 128 * 128;
   static constexpr int keys = bars + 64;     // [kCW][KP] uint64
   static constexpr int total = keys + kCW * KP * 8 + 128;
 };
 
-static_assert(kStages * kChunkBytes >=
-                  sizeof(AdmitWarpSmem) + 2 * 4 * (kMaxBlocksPerHead / 32),
-              "the fused admit reuses the ring");
-
-template <int KPL>
+template <int KPL, int kStages>
 __global__ void __launch_bounds__(kThreads)
     score_topk_kernel(const ScoreArgs a) {
-  using L = Layout<KPL>;
+  using L = Layout<KPL, kStages>;
   constexpr int KP = L::KP;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem + L::ring;
@@ -247,31 +249,46 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int KPL>
-cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
+template <int KPL, int ST>
+cudaError_t launch_kpl_st(const ScoreArgs& a, cudaStream_t s) {
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(score_topk_kernel<KPL>,
+    e = cudaFuncSetAttribute(score_topk_kernel<KPL, ST>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<KPL>::total);
+                             Layout<KPL, ST>::total);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   if (a.pairs <= 0) return cudaSuccess;
-  score_topk_kernel<KPL><<<a.pairs, kThreads, Layout<KPL>::total, s>>>(a);
+  score_topk_kernel<KPL, ST><<<a.pairs, kThreads, Layout<KPL, ST>::total, s>>>(a);
   return cudaGetLastError();
+}
+
+// Ring depth: 3 stages by default; OASIS_SCAN_STAGES=2 (tuning override)
+// halves the ring so that more CTAs fit per SM.
+int scan_stages() {
+  static const int st = [] {
+    const char* e = std::getenv("OASIS_SCAN_STAGES");
+    return (e && std::atoi(e) == 2) ? 2 : 3;
+  }();
+  return st;
+}
+
+template <int KPL>
+cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
+  return scan_stages() == 2 ? launch_kpl_st<KPL, 2>(a, s) : launch_kpl_st<KPL, 3>(a, s);
 }
 
 }  // namespace
 
 size_t score_topk_smem_bytes(int K) {
-  if (K <= 32) return Layout<1>::total;
-  if (K <= 64) return Layout<2>::total;
-  if (K <= 128) return Layout<4>::total;
-  return Layout<8>::total;
+  if (K <= 32) return Layout<1, 3>::total;
+  if (K <= 64) return Layout<2, 3>::total;
+  if (K <= 128) return Layout<4, 3>::total;
+  return Layout<8, 3>::total;
 }
 
 cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s) {

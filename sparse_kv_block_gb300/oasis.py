@@ -74,7 +74,7 @@ EXPORTS = {
     "oasis_step": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
     "oasis_join": (c_int, [_P, c_int, _P]),
     "oasis_step_host": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
-    "oasis_step_lists": (c_int, [_P, c_int, POINTER(c_void_p), POINTER(c_void_p),
+    "oasis_step_lists": (c_int, [_P, c_int, c_int, POINTER(c_void_p), POINTER(c_void_p),
                                  POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
                                  POINTER(c_void_p)]),
     "oasis_append_token": (c_int, [_P, c_int, c_int, _P, _P, _P]),
@@ -255,9 +255,10 @@ class Oasis:
         self._check(lib().oasis_step_host(self.ctx, layer, step, _ptr(q_host), _ptr(qd_host),
                                           _ptr(out_host), _ptr(outd_host), _stream(stream)))
 
-    def oasis_step_lists(self, layer: int) -> dict:
+    def oasis_step_lists(self, layer: int, step: int) -> dict:
         ps = [c_void_p() for _ in range(6)]
-        self._check(lib().oasis_step_lists(self.ctx, layer, *[ctypes.byref(p) for p in ps]))
+        self._check(lib().oasis_step_lists(self.ctx, layer, step,
+                                           *[ctypes.byref(p) for p in ps]))
         return dict(zip(["topk_ids", "topk_scores", "admit_ids", "admit_slots", "evict_ids",
                          "n_admit"], [p.value for p in ps]))
 
@@ -280,9 +281,10 @@ class Oasis:
         return list(ms), list(cnt), list(off)
 
     # ------------------------------------------------------- tensor views
-    def step_lists(self, layer: int) -> dict:
-        """The workspace lists of `layer` as torch tensors (views, no copy)."""
-        p = self.oasis_step_lists(layer)
+    def step_lists(self, layer: int, step: int) -> dict:
+        """The workspace lists of oasis_step(layer, step) as torch tensors
+        (views, no copy; valid until step + 2 is issued)."""
+        p = self.oasis_step_lists(layer, step)
         R, Hkv, K, C = self.cfg.num_requests, self.cfg.num_kv_heads, self.cfg.topk, self.C
         out = {}
         for name, shape, dt in [("topk_ids", (R, Hkv, K), torch.int32),

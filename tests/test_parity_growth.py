@@ -49,7 +49,7 @@ def test_append_and_advance_match_oracle(dev, ctx0, steps):
             oracle.append_token(hb_orc, summ_orc, lens, kb[r], vb[r], r)
         lens += 1
         H.check_attention([out.cpu().numpy(), outd.cpu().numpy()], ref, sh.G)
-        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0).items()}
+        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
         for (r, h), v in ref.items():
             assert np.array_equal(lists["topk_ids"][r, h], v["topk"])
             assert (lists["admit_ids"][r, h, :sh.C] == v["admit_ids"]).all()

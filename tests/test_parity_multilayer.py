@@ -67,7 +67,7 @@ def test_three_layers_interleaved(dev, schedule):
         for l in range(nl):
             ref = orcs[l].step(workload.bf16_bits(qs[l][t]), workload.bf16_bits(qds[l][t]), t)
             H.check_attention([outs[l].cpu().numpy(), outds[l].cpu().numpy()], ref, sh.G)
-            lists = {k: v.cpu().numpy() for k, v in eng.step_lists(l).items()}
+            lists = {k: v.cpu().numpy() for k, v in eng.step_lists(l, t).items()}
             for (r, h), v in ref.items():
                 assert np.array_equal(lists["topk_ids"][r, h], v["topk"])
                 assert (lists["admit_ids"][r, h, :sh.C] == v["admit_ids"]).all()

@@ -75,7 +75,7 @@ def test_fused_steps_sampled(layer):
         L.orc.pairs = live
         ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
         H.check_attention([out.float().cpu().numpy(), outd.float().cpu().numpy()], ref, SHAPE.G)
-        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0).items()}
+        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
         res_n = eng.res_ids[0][(t + 1) & 1].cpu().numpy()
         keep = []
         for (r, h), v in ref.items():
@@ -89,3 +89,40 @@ def test_fused_steps_sampled(layer):
         live = keep
         assert len(live) >= len(SAMPLE) - 2
         H.check_pool(L, (t + 1) & 1, live)
+
+
+def test_back_to_back_steps_cap_025():
+    # Full size, cap 0.25 (32 admissions per head: gathers 4x longer than at
+    # 0.05), four steps issued back to back with no host synchronisation.
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    dev = torch.device("cuda", 0)
+    L = H.make_layer(SHAPE, seed=3, steps=5, fetch_ratio=0.25, gen_device="cuda", pairs=SAMPLE)
+    eng = L.eng
+    outs = [torch.empty((SHAPE.R, SHAPE.Hq, 128), dtype=torch.bfloat16, device=dev)
+            for _ in range(8)]
+    qg, qdg = L.q.to(dev), L.qd.to(dev)
+    for t in range(4):
+        eng.oasis_step(0, t, qg[t], qdg[t], outs[2 * t], outs[2 * t + 1])
+    eng.oasis_join(0)
+    eng.oasis_sync()
+    live = list(SAMPLE)
+    for t in range(4):
+        L.orc.pairs = live
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        H.check_attention([outs[2 * t].float().cpu().numpy(), outs[2 * t + 1].float().cpu().numpy()],
+                          ref, SHAPE.G)
+        if t >= 2:
+            lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
+            keep = []
+            for (r, h), v in ref.items():
+                assert H.topk_agrees(lists["topk_ids"][r, h], v["topk"], v["scores"], SHAPE.K)
+                if np.array_equal(lists["topk_ids"][r, h], v["topk"]):
+                    assert lists["n_admit"][r, h] == v["n_admit"]
+                    keep.append((r, h))
+            live = keep
+    res_n = eng.res_ids[0][0].cpu().numpy()
+    for (r, h) in live:
+        assert (res_n[r, h] == L.orc.res[r, h]).all()
+    H.check_pool(L, 0, live)
+    eng.close()

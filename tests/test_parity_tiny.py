@@ -88,7 +88,7 @@ def test_fused_step_matches_oracle(dev, groups, R, schedule):
         eng.oasis_sync()
         ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
         H.check_attention([out.cpu().numpy(), outd.cpu().numpy()], ref, sh.G)
-        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0).items()}
+        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
         for (r, h), v in ref.items():
             # a different list inside the tie window would end the lockstep run
             assert np.array_equal(lists["topk_ids"][r, h], v["topk"]), "tie window hit"
@@ -137,3 +137,32 @@ def test_device_error_word_on_bad_block_id(dev):
     assert "0x1" in str(ei.value)
     assert L.eng.oasis_sync() == 0      # bits were cleared
     L.eng.close()
+
+
+@pytest.mark.parametrize("ratio,groups,schedule", [(1.0, 3, 0), (0.25, 0, 1), (1.0, 1, 1)])
+def test_back_to_back_steps_without_host_sync(dev, ratio, groups, schedule):
+    # Steps issued back to back: step t+1's scan and admission may run while
+    # step t's gathers are still copying, so the step lists must be per step.
+    sh = dataclasses.replace(TINY, R=5)
+    L = H.make_layer(sh, seed=8, steps=8, fetch_ratio=ratio, out_fp32=True,
+                     side_groups=groups, schedule=schedule)
+    eng, sh = L.eng, L.shape
+    outs = [torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev) for _ in range(16)]
+    qg, qdg = L.q.to(dev), L.qd.to(dev)
+    for t in range(8):
+        eng.oasis_step(0, t, qg[t], qdg[t], outs[2 * t], outs[2 * t + 1])
+    eng.oasis_join(0)
+    eng.oasis_sync()
+    for t in range(8):
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        H.check_attention([outs[2 * t].cpu().numpy(), outs[2 * t + 1].cpu().numpy()], ref, sh.G)
+        if t >= 6:   # the lists of the last two steps are still in place
+            lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
+            for (r, h), v in ref.items():
+                assert np.array_equal(lists["topk_ids"][r, h], v["topk"])
+                assert lists["n_admit"][r, h] == v["n_admit"]
+                assert (lists["admit_slots"][r, h, :sh.C] == v["admit_slots"]).all()
+    assert (eng.res_ids[0][8 & 1].cpu().numpy() == L.orc.res).all()
+    assert (eng.stamps[0].cpu().numpy() == L.orc.stamp).all()
+    H.check_pool(L, 8 & 1)
+    eng.close()
