@@ -610,9 +610,14 @@ def run_kernels_alone(args, ws, rank, local):
     torch.cuda.synchronize(dev)
     units = int(nad.sum())
     res["prefetch_ms"] = timed(lambda: eng.oasis_prefetch(0, 0, aid, asl, nad, st))
+    # Dense anchor: the whole KV of the context in HBM, attention over all of it.
+    kv_dense = host.to(dev)
+    res["dense_ms"] = timed(lambda: eng.oasis_dense_attn(kv_dense, 0, q[1], qd[1], out, outd, st))
+    del kv_dense
     eng.oasis_sync()
     peaks = measured_peaks()
     h2d = h2d_bandwidth(dev)
+    dense_b = R * Hkv * NB * UNIT_BYTES + 4 * R * Hq * 128 * 2
     attn_b = R * Hkv * K * UNIT_BYTES + 4 * R * Hq * 128 * 2
     scan_b = R * Hkv * NB * SUMM_BYTES + R * Hq * 128 * 2
     gb = lambda b, ms: b / (ms * 1e-3) / 1e9
@@ -627,6 +632,10 @@ def run_kernels_alone(args, ws, rank, local):
             "prefetch": {"ms": round(res["prefetch_ms"], 5), "units": units,
                          "GBs": round(gb(units * UNIT_BYTES, res["prefetch_ms"]), 1),
                          "frac_h2d_memcpy": round(gb(units * UNIT_BYTES, res["prefetch_ms"]) / h2d, 4)},
+            "dense_attention": {"ms": round(res["dense_ms"], 5), "bytes": dense_b,
+                                "GBs": round(gb(dense_b, res["dense_ms"]), 1),
+                                "frac_hbm": round(gb(dense_b, res["dense_ms"]) / peaks["hbm_gbs"], 4),
+                                "layer_steps_per_s": round(1e3 / res["dense_ms"], 1)},
             "hbm_peak_gbs": peaks["hbm_gbs"], "h2d_memcpy_gbs": round(h2d, 1)}
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -196,6 +196,16 @@ OASIS_API int oasis_lookahead_attn(oasis_ctx* ctx, int layer, int step,
                                    const void* q, const void* q_draft,
                                    void* out, void* out_draft, void* stream);
 
+/* Dense anchor: full-context decode attention with the whole KV cache in HBM,
+ * the dense baseline the pages compare against ([S] throughput table: dense
+ * vLLM).  Same outputs as oasis_lookahead_attn, but over every block
+ * b < ceil(ctx_len[table][r] / B) of the caller's dense cache
+ * kv_dense [R][Hkv][NBmax][2][B][d] bf16 (device memory, 16-byte aligned;
+ * the same layout as the host store).  Uses no resident table. */
+OASIS_API int oasis_dense_attn(oasis_ctx* ctx, const void* kv_dense, int table,
+                               const void* q, const void* q_draft, void* out,
+                               void* out_draft, void* stream);
+
 /* a2 + a3: summary scan and head-wise top-K ([R]: the draft query "scans
  * compressed key summaries ... produces a head-wise top-K ranking of all
  * logical blocks without restoring any keys").  For every (r, h) and every

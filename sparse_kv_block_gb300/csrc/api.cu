@@ -592,6 +592,48 @@ OASIS_API int oasis_lookahead_attn(oasis_ctx* ctx, int layer, int step, const vo
                        static_cast<cudaStream_t>(stream));
 }
 
+OASIS_API int oasis_dense_attn(oasis_ctx* ctx, const void* kv_dense, int table, const void* q,
+                               const void* q_draft, void* out, void* out_draft,
+                               void* stream) {
+  if (!ctx) return OASIS_EINVAL;
+  if (table < 0 || !kv_dense || !q || !q_draft || !out || !out_draft)
+    return ctx->fail(OASIS_EINVAL, "dense_attn: bad table or null pointer");
+  if (!aligned16(kv_dense)) return ctx->fail(OASIS_EINVAL, "dense_attn: kv_dense not 16-byte aligned");
+  const double rows = static_cast<double>(ctx->cfg.num_requests) * ctx->cfg.num_kv_heads *
+                      ctx->cfg.max_blocks * 2 * kBlock;
+  if (rows >= 2147483647.0)
+    return ctx->fail(OASIS_EINVAL, "dense_attn: cache too large for a 32-bit TMA row coordinate");
+  if (int rc = ctx->set_device()) return rc;
+  auto encode = get_encode();
+  if (!encode) return ctx->fail(OASIS_ECUDA, "cuTensorMapEncodeTiled unavailable");
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+  const cuuint32_t box[2] = {64, 2 * kBlock};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv_dense), dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return ctx->fail(OASIS_ECUDA, "dense_attn: tensor map encode failed");
+  AttnArgs a{};
+  a.q = q;
+  a.qd = q_draft;
+  a.out = out;
+  a.outd = out_draft;
+  a.ctx_len = ctx->ctx_tab(table);
+  a.err = ctx->err;
+  a.R = ctx->cfg.num_requests;
+  a.Hq = ctx->cfg.num_q_heads;
+  a.Hkv = ctx->cfg.num_kv_heads;
+  a.G = ctx->G;
+  a.NBmax = ctx->cfg.max_blocks;
+  a.scale_log2 = ctx->scale_log2;
+  a.out_fp32 = ctx->cfg.out_fp32;
+  a.dense = 1;
+  return ctx->cuda(launch_attention(a, &map, static_cast<cudaStream_t>(stream)),
+                   "dense attention launch");
+}
+
 OASIS_API int oasis_score_topk(oasis_ctx* ctx, int layer, int step, const void* q_draft,
                                int32_t* topk_ids, float* topk_scores, void* stream) {
   if (int rc = check_layer(ctx, layer)) return rc;

@@ -66,7 +66,16 @@ __global__ void __launch_bounds__(kThreads)
     fence_barrier_init();
     prefetch_tensormap(&pool_map);
   }
-  if (warp == 0) {
+  if (a.dense) {
+    if (threadIdx.x == 0) {
+      int nb = ctx > 0 ? (ctx + kBlock - 1) / kBlock : 0;
+      if (nb > a.NBmax) {
+        raise_error(a.err, kErrBadBlock);
+        nb = a.NBmax;
+      }
+      *count_s = nb;
+    }
+  } else if (warp == 0) {
     // Compact the occupied slots (in slot order) into the unit list.
     const int32_t* res = a.res + static_cast<size_t>(pair) * a.K;
     const int32_t* phys = a.phys + static_cast<size_t>(pair) * a.U;
@@ -129,9 +138,19 @@ __global__ void __launch_bounds__(kThreads)
   uint8_t* my_ring = base + warp * kStages * kStageBytes;
   uint64_t* my_bars = bars + warp * kStages;
 
+  // The k-th unit of this warp: a pool unit from the compacted list, or in
+  // dense mode block `idx` of the pair's dense cache row.
+  auto unit_row = [&](int k) {
+    const int idx = warp + k * kWarps;
+    return a.dense ? pair * a.NBmax + idx : list[idx].unit;
+  };
+  auto unit_valid = [&](int k) {
+    const int idx = warp + k * kWarps;
+    return a.dense ? min(kBlock, ctx - idx * kBlock) : list[idx].valid;
+  };
   auto issue = [&](int k) {
     const int st = k % kStages;
-    const int y = list[warp + k * kWarps].unit * (2 * kBlock);
+    const int y = unit_row(k) * (2 * kBlock);
     uint8_t* dst = my_ring + st * kStageBytes;
     mbar_arrive_expect_tx(&my_bars[st], kStageBytes);
     tma_load_2d(dst, &pool_map, 0, y, &my_bars[st]);
@@ -162,7 +181,7 @@ __global__ void __launch_bounds__(kThreads)
       failed = true;
       break;
     }
-    const int valid = list[warp + k * kWarps].valid;
+    const int valid = unit_valid(k);
     uint8_t* stage = my_ring + st * kStageBytes;
     const uint32_t sb = smem_u32(stage);
 

@@ -20,6 +20,9 @@ struct AttnArgs {
   int R, Hq, Hkv, G, K, U, NBmax;
   float scale_log2;      // softmax scale * log2(e)
   int out_fp32;
+  // dense = 1: no resident table; every block b < ceil(ctx_len / B) of a pair
+  // is read from unit pair * NBmax + b of a dense [R][Hkv][NBmax] cache.
+  int dense;
 };
 
 // Pairs (request, KV head) are flattened as pair = r * Hkv + h; a launch

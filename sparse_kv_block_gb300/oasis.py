@@ -68,6 +68,7 @@ EXPORTS = {
     "oasis_build_summaries": (c_int, [_P, c_int, c_int, _P]),
     "oasis_load_resident": (c_int, [_P, c_int, c_int, _P]),
     "oasis_lookahead_attn": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
+    "oasis_dense_attn": (c_int, [_P, _P, c_int, _P, _P, _P, _P, _P]),
     "oasis_score_topk": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
     "oasis_admit_evict": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P, _P]),
     "oasis_prefetch": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
@@ -228,6 +229,10 @@ class Oasis:
     def oasis_lookahead_attn(self, layer, step, q, qd, out, outd, stream=None) -> None:
         self._check(lib().oasis_lookahead_attn(self.ctx, layer, step, _ptr(q), _ptr(qd),
                                                _ptr(out), _ptr(outd), _stream(stream)))
+
+    def oasis_dense_attn(self, kv_dense, table, q, qd, out, outd, stream=None) -> None:
+        self._check(lib().oasis_dense_attn(self.ctx, _ptr(kv_dense), table, _ptr(q), _ptr(qd),
+                                           _ptr(out), _ptr(outd), _stream(stream)))
 
     def oasis_score_topk(self, layer, step, qd, topk_ids, topk_scores=None, stream=None) -> None:
         self._check(lib().oasis_score_topk(self.ctx, layer, step, _ptr(qd), _ptr(topk_ids),
