@@ -642,6 +642,71 @@ def run_kernels_alone(args, ws, rank, local):
     eng.close()
 
 
+def run_miss_stall(args, ws, rank, local):
+    """The "stall" branch of a miss, against the look-ahead step ("drop").
+
+    Stall: every step ranks blocks with the step's own normal query, admits
+    up to C missing blocks, gathers them and only then runs the attention,
+    all on one stream (the fetch sits on the critical path).  Look-ahead:
+    oasis_step, where the draft query's selection is fetched beside the
+    attention for the next step.  Both through the C ABI, same workload."""
+    from sparse_kv_block_gb300.oasis import lib
+    lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = get_shape(args)
+    R, Hq, Hkv, K, C = shape.R, shape.Hq, shape.Hkv, shape.K, shape.C
+    nq = min(args.queries, 16)
+    results = {}
+    for mode in ("stall", "lookahead"):
+        eng, lens, host = build_layer(shape, args.seed, dev, args.side_groups, args.schedule)
+        q, qd = workload.queries(shape, args.seed, 0, nq, device=dev)
+        warm_start(eng, shape, q[0], dev)
+        out = torch.empty((R, Hq, 128), dtype=torch.bfloat16, device=dev)
+        outd = torch.empty_like(out)
+        topk = torch.empty((R, Hkv, K), dtype=torch.int32, device=dev)
+        aid = torch.empty((R, Hkv, max(C, 1)), dtype=torch.int32, device=dev)
+        asl, evi = torch.empty_like(aid), torch.empty_like(aid)
+        nad = torch.empty((R, Hkv), dtype=torch.int32, device=dev)
+        st = torch.cuda.Stream(dev)
+        step = 0
+
+        def one():
+            nonlocal step
+            t = step % nq
+            if mode == "stall":
+                # admission of step s writes table s+1, which this attention reads
+                eng.oasis_score_topk(0, step, q[t], topk, None, st)
+                eng.oasis_admit_evict(0, step, topk, aid, asl, evi, nad, st)
+                eng.oasis_prefetch(0, step, aid, asl, nad, st)
+                eng.oasis_lookahead_attn(0, step + 1, q[t], qd[t], out, outd, st)
+            else:
+                eng.oasis_step(0, step, q[t], qd[t], out, outd, st)
+            step += 1
+
+        for _ in range(args.warmup):
+            one()
+        eng.oasis_join(0, st)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(args.steps):
+            one()
+        eng.oasis_join(0, st)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        eng.oasis_sync()
+        ms = e0.elapsed_time(e1) / args.steps
+        results[mode] = {"ms_per_step": round(ms, 4), "layer_steps_per_s": round(1e3 / ms, 1)}
+        eng.close()
+        del eng, host
+        torch.cuda.empty_cache()
+    if rank == 0:
+        print(json.dumps({"mode": "miss-stall vs look-ahead", "workload": workload_desc(shape),
+                          "steps": args.steps, **results}), flush=True)
+
+
 def run_cap_sweep(args, ws, rank, local):
     """Fetch-cap sweep on the single-layer shape: for each cap, layer-steps/s,
     host-to-device bytes per step, and the top-K agreement between the draft
@@ -728,6 +793,8 @@ def main():
     ap.add_argument("--impl", default="oasis", choices=["oasis", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_16k",
                     choices=["qwen3_8b_16k", "tiny", "qwen3_8b_36l"])
+    ap.add_argument("--miss-stall", action="store_true",
+                    help="fetch on the critical path (stall) against the look-ahead step")
     ap.add_argument("--kernels-alone", action="store_true",
                     help="time each stage alone on the single-layer workload")
     ap.add_argument("--cap-sweep", action="store_true",
@@ -740,7 +807,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--side-groups", type=int, default=0,
                     help="request groups of the side work (0 = library default)")
-    ap.add_argument("--schedule", type=int, default=0, help="0 scan first, 1 concurrent")
+    ap.add_argument("--schedule", type=int, default=0,
+                    help="0 scan first, 1 concurrent, 2 the pages' three background streams")
     ap.add_argument("--requests", type=int, default=0,
                     help="override the request count (small cases for profiling)")
     args = ap.parse_args()
@@ -753,6 +821,8 @@ def main():
         run_cap_sweep(args, ws, rank, local)
     elif args.kernels_alone:
         run_kernels_alone(args, ws, rank, local)
+    elif args.miss_stall:
+        run_miss_stall(args, ws, rank, local)
     elif workload.SHAPES[args.workload].layers > 1:
         run_oasis_layers(args, ws, rank, local)
     else:

@@ -113,9 +113,14 @@ typedef struct {
 /* oasis_step schedules.  SCAN_FIRST: the attention of a step starts when the
  * step's scans are done, so the scans run alone and the host-link gathers
  * start early and overlap the attention.  CONCURRENT: the attention starts at
- * once, sharing HBM with the scans.  Results are identical. */
+ * once, sharing HBM with the scans.  THREE_STREAMS: the pipeline as the pages
+ * describe it ([R] "three background CUDA streams per layer -- top-K
+ * prediction, KV selection, and KV transfer"): a stand-alone scan + top-K, a
+ * stand-alone admission and the gathers on three streams, the attention
+ * starting at once.  Results are identical. */
 #define OASIS_SCHEDULE_SCAN_FIRST 0
 #define OASIS_SCHEDULE_CONCURRENT 1
+#define OASIS_SCHEDULE_THREE_STREAMS 2
 
 typedef struct {
   size_t kv_pool_bytes;   /* per layer */

@@ -49,6 +49,7 @@ struct LayerState {
   cudaEvent_t ev_side_done = nullptr;
   cudaEvent_t ev_scan_done = nullptr;
   std::vector<cudaEvent_t> ev_group;  // one per side-work request group
+  std::vector<cudaEvent_t> ev_group2; // admissions done (three-stream schedule)
   bool side_pending = false;
   bool loaded = false;
 };
@@ -113,8 +114,9 @@ const char* config_error(const oasis_config* c) {
   if (c->device < 0) return "device must be >= 0";
   if (c->max_blocks > kMaxBlocksPerHead) return "max_blocks must be <= 131072";
   if (c->side_groups < 0 || c->side_groups > 64) return "side_groups must be in 0..64";
-  if (c->schedule != OASIS_SCHEDULE_SCAN_FIRST && c->schedule != OASIS_SCHEDULE_CONCURRENT)
-    return "schedule must be OASIS_SCHEDULE_SCAN_FIRST or OASIS_SCHEDULE_CONCURRENT";
+  if (c->schedule != OASIS_SCHEDULE_SCAN_FIRST && c->schedule != OASIS_SCHEDULE_CONCURRENT &&
+      c->schedule != OASIS_SCHEDULE_THREE_STREAMS)
+    return "schedule must be one of OASIS_SCHEDULE_*";
   const double units = static_cast<double>(c->num_requests) * c->num_kv_heads *
                        (c->topk + fetch_cap(*c)) * 2 * kBlock;
   if (units >= 2147483647.0) return "pool too large for a 32-bit TMA row coordinate";
@@ -152,6 +154,7 @@ struct oasis_ctx {
   WsLayout wl{};
   cudaStream_t side = nullptr;   // scan + top-K + admission
   cudaStream_t side2 = nullptr;  // host -> HBM gathers
+  cudaStream_t side3 = nullptr;  // admissions (three-stream schedule only)
   std::string last_error;
   bool prof = false;
   std::vector<ProfPair> prof_pool;
@@ -310,8 +313,11 @@ int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
 }
 
 int run_admit(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t* aid,
-              int32_t* aslot, int32_t* evid, int32_t* nadm, cudaStream_t s) {
+              int32_t* aslot, int32_t* evid, int32_t* nadm, cudaStream_t s, int pair0 = 0,
+              int pairs = -1) {
   AdmitArgs a = admit_args(ctx, layer, step, topk, aid, aslot, evid, nadm);
+  a.pair0 = pair0;
+  if (pairs >= 0) a.pairs = pairs;
   cudaEvent_t* pe = ctx->prof_begin(2, s);
   cudaError_t e = launch_admit(a, s);
   ctx->prof_end(pe, s);
@@ -409,7 +415,8 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
   int lo = 0, hi = 0;
   if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return bail(OASIS_ECUDA);
   if (cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, hi) != cudaSuccess ||
-      cudaStreamCreateWithPriority(&c->side2, cudaStreamNonBlocking, hi) != cudaSuccess)
+      cudaStreamCreateWithPriority(&c->side2, cudaStreamNonBlocking, hi) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&c->side3, cudaStreamNonBlocking, hi) != cudaSuccess)
     return bail(OASIS_ENOMEM);
   {
     const int pairs = cfg->num_requests * cfg->num_kv_heads;
@@ -478,7 +485,11 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
         cudaEventCreateWithFlags(&S.ev_scan_done, cudaEventDisableTiming) != cudaSuccess)
       return bail(OASIS_ENOMEM);
     S.ev_group.assign(c->groups, nullptr);
+    S.ev_group2.assign(c->groups, nullptr);
     for (auto& e : S.ev_group)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+        return bail(OASIS_ENOMEM);
+    for (auto& e : S.ev_group2)
       if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
         return bail(OASIS_ENOMEM);
   }
@@ -494,8 +505,11 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   cudaSetDevice(ctx->cfg.device);
   if (ctx->side) cudaStreamSynchronize(ctx->side);
   if (ctx->side2) cudaStreamSynchronize(ctx->side2);
+  if (ctx->side3) cudaStreamSynchronize(ctx->side3);
   for (auto& L : ctx->layers) {
     for (auto& e : L.ev_group)
+      if (e) cudaEventDestroy(e);
+    for (auto& e : L.ev_group2)
       if (e) cudaEventDestroy(e);
     if (L.ev_start) cudaEventDestroy(L.ev_start);
     if (L.ev_side_done) cudaEventDestroy(L.ev_side_done);
@@ -508,6 +522,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   for (auto& e : ctx->prof_starts) cudaEventDestroy(e);
   if (ctx->side) cudaStreamDestroy(ctx->side);
   if (ctx->side2) cudaStreamDestroy(ctx->side2);
+  if (ctx->side3) cudaStreamDestroy(ctx->side3);
   delete ctx;
   return OASIS_OK;
 }
@@ -704,6 +719,30 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
     const int p0 = static_cast<int>(static_cast<long long>(pairs) * g / ctx->groups);
     const int p1 = static_cast<int>(static_cast<long long>(pairs) * (g + 1) / ctx->groups);
     const LayerState::Lists& Ls = L.lists[step & 1];
+    if (ctx->cfg.schedule == OASIS_SCHEDULE_THREE_STREAMS) {
+      // The pages' pipeline: top-K prediction, KV selection and KV transfer
+      // on three streams, each stage of a group ordered by an event.
+      if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side,
+                             p0, p1 - p0, false))
+        return rc;
+      if (int rc = ctx->cuda(cudaEventRecord(L.ev_group2[g], ctx->side), "record top-k"))
+        return rc;
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side3, L.ev_group2[g], 0), "wait top-k"))
+        return rc;
+      if (int rc = run_admit(ctx, layer, step, Ls.topk_ids, Ls.admit_ids, Ls.admit_slots,
+                             Ls.evict_ids, Ls.n_admit, ctx->side3, p0, p1 - p0))
+        return rc;
+      if (int rc = ctx->cuda(cudaEventRecord(L.ev_group[g], ctx->side3), "record group"))
+        return rc;
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[g], 0), "group wait"))
+        return rc;
+      if (ctx->C > 0) {
+        if (int rc = run_prefetch(ctx, layer, step, Ls.admit_ids, Ls.admit_slots, Ls.n_admit,
+                                  ctx->side2, p0, p1 - p0))
+          return rc;
+      }
+      continue;
+    }
     if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side, p0,
                            p1 - p0, true))
       return rc;

@@ -31,7 +31,7 @@ class oasis_config(ctypes.Structure):
                 ("side_groups", c_int32), ("schedule", c_int32)]
 
 
-SCHEDULE_SCAN_FIRST, SCHEDULE_CONCURRENT = 0, 1
+SCHEDULE_SCAN_FIRST, SCHEDULE_CONCURRENT, SCHEDULE_THREE_STREAMS = 0, 1, 2
 
 
 class oasis_sizes(ctypes.Structure):
