@@ -163,6 +163,24 @@ __device__ __forceinline__ float bf16hi(uint32_t w) {
   return __uint_as_float(w & 0xffff0000u);
 }
 
+// Packed fp32 pairs (Blackwell fma.rn.f32x2: two fp32 multiply-adds per
+// instruction on a 64-bit register pair, low half first).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2sum(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // Order-preserving map float -> uint32 (larger float, larger key).
 __device__ __forceinline__ uint32_t float_key(float f) {
   if (f == 0.0f) f = 0.0f;  // -0 and +0 rank equal

@@ -16,11 +16,12 @@
 // scan is a pure HBM stream.
 //
 // GB300 mapping.  One CTA per (request, KV head): a producer warp streams the
-// request's contiguous summary rows through a 3-deep ring of 16 KiB stages
+// request's contiguous summary rows through a 2-deep ring of 16 KiB stages
 // with 1-D bulk copies; eight consumer warps each score 4 blocks per stage
-// (one 16-byte load per lane per block, transposed shuffle reduction), keep
-// a running top-KP list in registers (bitonic sort of each filled buffer of
-// KP keys, then a bitonic merge), and finally merge their lists in a tree.
+// (one 16-byte load per lane per block, packed fp32x2 multiply-adds,
+// transposed shuffle reduction), keep a running top-KP list in registers
+// (bitonic sort of each filled buffer of KP keys, then a bitonic merge), and
+// finally merge their lists in a tree.
 // Keys are 64-bit: order-preserving score bits above the complemented block
 // id, so ties break to the lower id and all keys are distinct.
 #include <cstdlib>
@@ -133,8 +134,13 @@ __global__ void __launch_bounds__(kThreads)
         w[2 * i + 1] += row ? fmaxf(hi, 0.f) : fminf(hi, 0.f);
       }
     }
+    // Weights as fp32 pairs for the packed fp32x2 multiply-add.
+    uint64_t w2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w2[i] = f2pack(w[2 * i], w[2 * i + 1]);
     uint64_t* mybuf = keybuf + warp * KP;
     int cnt = 0;
+    bool have_top = false;  // false while `top` still holds only empty keys
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
       const int st = c % kStages;
@@ -149,14 +155,12 @@ __global__ void __launch_bounds__(kThreads)
         float acc = 0.f;
         if (j < nblk) {
           const uint4 u = *reinterpret_cast<const uint4*>(stage + j * kSummBytes + lane * 16);
-          acc = w[0] * bf16lo(u.x);
-          acc = fmaf(w[1], bf16hi(u.x), acc);
-          acc = fmaf(w[2], bf16lo(u.y), acc);
-          acc = fmaf(w[3], bf16hi(u.y), acc);
-          acc = fmaf(w[4], bf16lo(u.z), acc);
-          acc = fmaf(w[5], bf16hi(u.z), acc);
-          acc = fmaf(w[6], bf16lo(u.w), acc);
-          acc = fmaf(w[7], bf16hi(u.w), acc);
+          uint64_t acc2 = 0ull;
+          acc2 = ffma2(w2[0], f2pack(bf16lo(u.x), bf16hi(u.x)), acc2);
+          acc2 = ffma2(w2[1], f2pack(bf16lo(u.y), bf16hi(u.y)), acc2);
+          acc2 = ffma2(w2[2], f2pack(bf16lo(u.z), bf16hi(u.z)), acc2);
+          acc2 = ffma2(w2[3], f2pack(bf16lo(u.w), bf16hi(u.w)), acc2);
+          acc = f2sum(acc2);
         }
         v[q] = acc;
       }
@@ -187,8 +191,15 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int i = 0; i < KPL; ++i) nk[i] = mybuf[i * 32 + lane];
         __syncwarp();
-        bitonic_sort<KPL>(nk, false);
-        merge_top<KPL>(top, nk);
+        if (have_top) {
+          bitonic_sort<KPL>(nk, false);
+          merge_top<KPL>(top, nk);
+        } else {  // the first full buffer becomes the running list directly
+          bitonic_sort<KPL>(nk, true);
+#pragma unroll
+          for (int i = 0; i < KPL; ++i) top[i] = nk[i];
+          have_top = true;
+        }
         cnt = 0;
       }
     }
@@ -202,8 +213,14 @@ __global__ void __launch_bounds__(kThreads)
         nk[i] = e < cnt ? mybuf[e] : 0ull;
       }
       __syncwarp();
-      bitonic_sort<KPL>(nk, false);
-      merge_top<KPL>(top, nk);
+      if (have_top) {
+        bitonic_sort<KPL>(nk, false);
+        merge_top<KPL>(top, nk);
+      } else {
+        bitonic_sort<KPL>(nk, true);
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) top[i] = nk[i];
+      }
     }
   }
 
