@@ -20,8 +20,8 @@
  *       Sparse Prefetching" (agihunt.info summary), fetch-cap ablation);
  *   a5  the admitted blocks are gathered from pinned host memory into HBM on a
  *       side stream, overlapped with other work, and are used from step t+1
- *       on ([R] abstract: "staged in HBMs before being used in the next decode
- *       step").
+ *       on ([R] abstract: prefetched blocks land in HBM one step ahead of
+ *       their use).
  *
  * Conventions
  *   - Every call returns an oasis_status.  No call aborts, prints or exits.
@@ -114,8 +114,8 @@ typedef struct {
  * step's scans are done, so the scans run alone and the host-link gathers
  * start early and overlap the attention.  CONCURRENT: the attention starts at
  * once, sharing HBM with the scans.  THREE_STREAMS: the pipeline as the pages
- * describe it ([R] "three background CUDA streams per layer -- top-K
- * prediction, KV selection, and KV transfer"): a stand-alone scan + top-K, a
+ * describe it ([R] *What carries the argument*: per layer, one background
+ * stream each for ranking, selection and transfer): a stand-alone scan + top-K, a
  * stand-alone admission and the gathers on three streams, the attention
  * starting at once.  Results are identical. */
 #define OASIS_SCHEDULE_SCAN_FIRST 0
@@ -178,8 +178,8 @@ OASIS_API const char* oasis_last_error(const oasis_ctx* ctx);
 OASIS_API int oasis_sync(oasis_ctx* ctx, uint32_t* device_bits);
 
 /* Support (a0): per-block min/max key summaries of `layer` over the tokens
- * below ctx_len[table] ([R] "coordinate-wise min/max per block, in the style
- * of Quest").  Reads the pinned host store through its device mapping. */
+ * below ctx_len[table] ([R] *What carries the argument*: Quest-style
+ * per-block min/max key summaries).  Reads the pinned host store through its device mapping. */
 OASIS_API int oasis_build_summaries(oasis_ctx* ctx, int layer, int table,
                                     void* stream);
 
@@ -191,9 +191,9 @@ OASIS_API int oasis_build_summaries(oasis_ctx* ctx, int layer, int table,
 OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step,
                                   void* stream);
 
-/* a1: look-ahead attention ([R], [V]: "one shared attention kernel processes
- * the normal token and the draft token over the same resident sparse KV
- * set").  For every request r and query head j, separately for q and q_draft:
+/* a1: look-ahead attention ([R] *What carries the argument*, [V]
+ * key_machinery: a single attention pass serves both the normal and the draft
+ * token, reading one shared resident sparse set).  For every request r and query head j, separately for q and q_draft:
  * softmax(x . k / scale) . v over the valid tokens of the occupied slots of
  * KV head j / G in table (step & 1).  A block's valid tokens are those below
  * ctx_len[step & 1][r]; a head with no valid token outputs zeros. */
@@ -211,9 +211,9 @@ OASIS_API int oasis_dense_attn(oasis_ctx* ctx, const void* kv_dense, int table,
                                const void* q, const void* q_draft, void* out,
                                void* out_draft, void* stream);
 
-/* a2 + a3: summary scan and head-wise top-K ([R]: the draft query "scans
- * compressed key summaries ... produces a head-wise top-K ranking of all
- * logical blocks without restoring any keys").  For every (r, h) and every
+/* a2 + a3: summary scan and head-wise top-K ([R] *What carries the argument*:
+ * the draft query ranks every logical block per KV head from the compressed
+ * summaries alone, never touching the full keys).  For every (r, h) and every
  * logical block b < ceil(ctx_len[step & 1][r] / B):
  *   s[b] = sum_{j in group(h)} sum_i max(qd_ji * min_bi, qd_ji * max_bi)
  * then topk_ids = the first min(K, NB_r) blocks by (s desc, b asc), -1
@@ -222,9 +222,10 @@ OASIS_API int oasis_score_topk(oasis_ctx* ctx, int layer, int step,
                                const void* q_draft, int32_t* topk_ids,
                                float* topk_scores, void* stream);
 
-/* a4: capped least-recently-selected eviction ([R]: "a capped-eviction
- * policy pairs each admitted nonresident block with a least-recently-selected
- * resident block"), per (r, h), from table (step & 1) into table
+/* a4: capped least-recently-selected eviction ([R] *What carries the
+ * argument*: every admitted block that is not resident replaces the resident
+ * block selected least recently, under a per-step cap), per (r, h), from
+ * table (step & 1) into table
  * ((step + 1) & 1):
  *   (i)   stamp = step for every slot whose block is in topk_ids;
  *   (ii)  M = blocks of topk_ids not resident, in rank order;
@@ -241,8 +242,8 @@ OASIS_API int oasis_admit_evict(oasis_ctx* ctx, int layer, int step,
                                 int32_t* admit_slots, int32_t* evict_ids,
                                 int32_t* n_admit, void* stream);
 
-/* a5: prefetch gather ([V]: the "gather kernel" reading pinned CPU memory
- * through the CUDA UVA mapping).  For every (r, h) and i < n_admit: copy host
+/* a5: prefetch gather ([V] supporting_citations: a gather kernel reads the
+ * selected blocks from pinned CPU memory through CUDA UVA).  For every (r, h) and i < n_admit: copy host
  * unit (r, h, admit_ids[i]) into pool unit phys[(step + 1) & 1][admit_slots[i]]
  * (byte copy of keys and values).  Those units are spares of table (step & 1),
  * so the copy may run while step `step`'s attention reads that table. */
@@ -251,7 +252,8 @@ OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step,
                              const int32_t* admit_slots,
                              const int32_t* n_admit, void* stream);
 
-/* a1..a5 as one layer-step (a6, [R] "layer-local synchronization").
+/* a1..a5 as one layer-step (a6; [R] *What carries the argument*: the
+ * background work synchronises per layer).
  * q_draft is first copied (on `stream`) into a per-layer staging buffer.
  * Side work, on the context's two high-priority side streams, ordered after
  * everything already on `stream` (so after this layer's previous attention):

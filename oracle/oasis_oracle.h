@@ -41,16 +41,16 @@ extern "C" {
 #endif
 
 /* Per-block coordinate-wise min/max of the keys over the block's valid tokens
- * ([R] "compressed key summaries (coordinate-wise min/max per block, in the
- * style of Quest)").  Blocks b < ceil(ctx_len[r]/B) are written; others are
+ * ([R] *What carries the argument*: Quest-style compressed summaries, one
+ * min and one max per coordinate and block).  Blocks b < ceil(ctx_len[r]/B) are written; others are
  * left untouched. */
 int orc_summary_build(const uint16_t* host_kv, const int32_t* ctx_len, int R,
                       int Hkv, int NBmax, int B, int d, uint16_t* summ);
 
 /* Sparse attention of one (request r, KV head h) over its resident blocks,
  * for the normal query and the draft query of each of the G query heads of
- * the group ([R] "one shared attention kernel processes the normal token and
- * the draft token over the same resident sparse KV set").
+ * the group ([R] *What carries the argument*: one attention pass serves both
+ * tokens over the same resident sparse set).
  * out[2][G][d] (fp32): out[0] for q, out[1] for the draft query. */
 int orc_attention_rh(const uint16_t* host_kv, const int32_t* ctx_len,
                      const int32_t* res, const uint16_t* q, const uint16_t* qd,
@@ -59,8 +59,8 @@ int orc_attention_rh(const uint16_t* host_kv, const int32_t* ctx_len,
 
 /* Summary score of every logical block b < ceil(ctx_len[r]/B) for one
  * (r, h): s[b] = sum over the group's query heads j and dims i of
- * max(qd[j][i]*min[b][i], qd[j][i]*max[b][i])  ([R] the draft query "scans
- * compressed key summaries").  scores[NBmax] (fp32, one rounding of a double
+ * max(qd[j][i]*min[b][i], qd[j][i]*max[b][i])  ([R] *What carries the
+ * argument*: the draft query is scored against the summaries).  scores[NBmax] (fp32, one rounding of a double
  * sum); entries b >= NB_r are set to -inf. */
 int orc_score_rh(const uint16_t* summ, const int32_t* ctx_len,
                  const uint16_t* qd, int R, int Hq, int Hkv, int NBmax, int d,
@@ -68,12 +68,13 @@ int orc_score_rh(const uint16_t* summ, const int32_t* ctx_len,
 
 /* Head-wise top-K of one (r, h): the first min(K, NB) block ids ordered by
  * (score descending, id ascending); the rest of topk[K] is -1
- * ([R] "a head-wise top-K ranking of all logical blocks"). */
+ * ([R] *What carries the argument*: every logical block is ranked per KV
+ * head). */
 int orc_topk_rh(const float* scores, int NB, int K, int32_t* topk);
 
-/* Capped eviction for one (r, h) at step t ([R] "a capped-eviction policy
- * pairs each admitted nonresident block with a least-recently-selected
- * resident block"; [S] fetch cap).  Updates res[K] and stamp[K] in place and
+/* Capped eviction for one (r, h) at step t ([R] *What carries the
+ * argument*: each admitted non-resident block displaces the resident block
+ * selected least recently; [S] fetch cap).  Updates res[K] and stamp[K] in place and
  * writes admit_ids/admit_slots/evict_ids[C] (-1 padded) and *n_admit. */
 int orc_admit_evict_rh(int32_t* res, int32_t* stamp, const int32_t* topk,
                        int K, int C, int step, int32_t* admit_ids,
