@@ -48,13 +48,15 @@ cudaError_t launch_admit_kpl(const AdmitArgs& a, cudaStream_t s) {
 // mapping over the host link) into pool units, one warp per unit; every lane
 // issues all 16 of its 16-byte loads before storing, so each warp keeps a
 // whole unit in flight.  The grid is kept small: at most kGatherCtas CTAs of
-// 4 warps, 2 MiB of host reads in flight.  Measured on GB300 (pinned H2D
+// 4 warps, 1.25 MiB of host reads in flight.  Measured on GB300 (pinned H2D
 // ~210 GB/s): 16 / 32 / 64 / 96 CTAs move 131 / 174 / 199 / 206 GB/s, while a
 // concurrent HBM-streaming kernel slows by 1 / 9 / 35 / 48 %: the host reads
-// in flight compete with HBM traffic in the memory system, so the grid stops
-// where the link is nearly saturated.
+// in flight compete with HBM traffic in the memory system.  In the 128 x 16K
+// layer-step 24 / 32 / 40 / 48 / 64 CTAs give 3040 / 3036 / 3066 / 2980 /
+// 2787 layer-steps/s: 40 moves the units in time (266 us of a 326 us step)
+// while slowing the attention least.
 constexpr int kGatherThreads = 128;
-constexpr int kGatherCtas = 64;
+constexpr int kGatherCtas = 40;
 
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs a) {
   const int lane = threadIdx.x & 31;
