@@ -380,13 +380,17 @@ def run_oasis(args, ws, rank, local):
     link_bytes = adm_units * UNIT_BYTES
 
     # ---------------- end to end: host buffers through oasis_step_host
-    qh = torch.empty((shape.R, shape.Hq, 128), dtype=torch.bfloat16, pin_memory=True)
-    qdh = torch.empty_like(qh).pin_memory()
-    oh = torch.empty_like(qh).pin_memory()
-    odh = torch.empty_like(qh).pin_memory()
+    # Two sets of pinned host buffers: the host writes step i's inputs while
+    # the GPU runs step i - 1, and reads step i - 1's outputs once that step
+    # is done (one step of overlap, every copy inside the timed region).
+    def pinned():
+        return torch.empty((shape.R, shape.Hq, 128), dtype=torch.bfloat16, pin_memory=True)
+    qh, qdh, oh, odh = ([pinned(), pinned()] for _ in range(4))
+    done = [torch.cuda.Event(), torch.cuda.Event()]
     q_host = q[:min(nq, 8)].cpu()
     qd_host = qd[:min(nq, 8)].cpu()
     e2e_steps = args.steps
+    checksum = 0.0
     barrier(ws)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -394,11 +398,18 @@ def run_oasis(args, ws, rank, local):
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(main)
     for i in range(e2e_steps):
-        qh.copy_(q_host[i % q_host.shape[0]])       # the host-side input of this step
-        qdh.copy_(qd_host[i % qd_host.shape[0]])
-        eng.oasis_step_host(0, step, qh, qdh, oh, odh, main)
+        b = i & 1
+        if i >= 2:
+            done[b].synchronize()                   # step i - 2 finished: read its result
+            checksum += float(oh[b][0, 0, 0])
+        qh[b].copy_(q_host[i % q_host.shape[0]])    # the host-side input of this step
+        qdh[b].copy_(qd_host[i % qd_host.shape[0]])
+        eng.oasis_step_host(0, step, qh[b], qdh[b], oh[b], odh[b], main)
+        done[b].record(main)
         step += 1
-        main.synchronize()                          # the host reads this step's result
+    for i in range(max(e2e_steps - 2, 0), e2e_steps):
+        done[i & 1].synchronize()
+        checksum += float(oh[i & 1][0, 0, 0])
     eng.oasis_join(0, main)
     f1.record(main)
     torch.cuda.synchronize(dev)
@@ -465,8 +476,9 @@ def run_oasis(args, ws, rank, local):
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": 2 * R * Hq * 128 * 2,
                     "d2h_bytes_per_step": 2 * R * Hq * 128 * 2,
-                    "note": "oasis_step_host: pinned q/q_draft in, attention outputs out, "
-                            "host waits for each step's result"},
+                    "note": "oasis_step_host: pinned q/q_draft in, attention outputs out; "
+                            "two host buffer sets, the host fills step i's inputs while "
+                            "step i-1 runs and reads each step's result after it ends"},
             "gpu_launches": int(sum(counts)), "clocks": clk,
             "profiled_pass_ms_per_step": round(ms_prof / args.steps, 5)}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -754,6 +766,75 @@ def run_miss_stall(args, ws, rank, local):
                           "steps": args.steps, **results}), flush=True)
 
 
+def run_remote(args, ws, rank, local):
+    """Remote tier (emulated prefill-decode disaggregation with remote partial
+    fetch) on the single-layer shape: the full cache stays in the remote
+    store; the decode side holds a local host tier that a block enters the
+    first time it is needed (warm start, then admissions), moved by host
+    threads at an emulated network rate.  Every step uses a fresh query, so
+    the admitted blocks are not replayed.  Reports layer-steps/s, remote
+    traffic per step, and the decode-side host memory held at the end against
+    the full cache, next to the same steps without a remote tier."""
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = get_shape(args)
+    R, Hq, Hkv, K = shape.R, shape.Hq, shape.Hkv, shape.K
+    n = args.steps + args.warmup
+    q, qd = workload.queries(shape, args.seed, 0, n, device=dev)
+    lens = workload.ctx_lens(shape)
+    nb = np.array([-(-int(x) // 16) for x in lens], dtype=np.int64)
+    full_units = int(nb.sum()) * Hkv
+    results = {}
+    for mode in ["local"] + [f"remote_{g:g}GBps" for g in args.remote_gbps]:
+        eng, lens, host = build_layer(shape, args.seed, dev, args.side_groups, args.schedule)
+        rt = None
+        if mode != "local":
+            gbps = float(mode[len("remote_"):-len("GBps")])
+            rt = eng.oasis_remote_attach(0, shape.NBmax, gbps, args.remote_threads)
+        warm_start(eng, shape, q[0], dev)
+        out = torch.empty((R, Hq, 128), dtype=torch.bfloat16, device=dev)
+        outd = torch.empty_like(out)
+        st = torch.cuda.Stream(dev)
+        for t in range(args.warmup):
+            eng.oasis_step(0, t, q[t], qd[t], out, outd, st)
+        eng.oasis_join(0, st)
+        torch.cuda.synchronize(dev)
+        s0 = eng.oasis_remote_stats(0) if rt is not None else None
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for t in range(args.warmup, n):
+            eng.oasis_step(0, t, q[t], qd[t], out, outd, st)
+        eng.oasis_join(0, st)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        eng.oasis_sync()
+        ms = e0.elapsed_time(e1) / args.steps
+        r = {"ms_per_step": round(ms, 4), "layer_steps_per_s": round(1e3 / ms, 1)}
+        if rt is not None:
+            s1 = eng.oasis_remote_stats(0)
+            du = s1["units"] - s0["units"]
+            held = int(rt["local_count"].sum().item())
+            r.update({
+                "remote_units_per_step": round(du / args.steps, 1),
+                "remote_GB_per_step": round(du * 8192 / args.steps / 1e9, 4),
+                "transfer_ms_per_step": round((s1["seconds"] - s0["seconds"]) * 1e3 / args.steps, 4),
+                "transfer_GBps": round(du * 8192 / max(s1["seconds"] - s0["seconds"], 1e-9) / 1e9, 1),
+                "decode_host_units_held": held,
+                "full_cache_units": full_units,
+                "decode_host_fraction": round(held / full_units, 4),
+                "admission_fraction": round(R * Hkv * K / full_units, 4),
+                "bad_entries": s1["bad_entries"]})
+        results[mode] = r
+        eng.close()
+        del eng, host
+        torch.cuda.empty_cache()
+    if rank == 0:
+        print(json.dumps({"mode": "remote tier", "workload": workload_desc(shape),
+                          "steps": args.steps, "warmup": args.warmup,
+                          "remote_threads": args.remote_threads, **results}), flush=True)
+
+
 def run_cap_sweep(args, ws, rank, local):
     """Fetch-cap sweep on the single-layer shape: for each cap, layer-steps/s,
     host-to-device bytes per step, and the top-K agreement between the draft
@@ -856,6 +937,11 @@ def main():
                     help="request groups of the side work (0 = library default)")
     ap.add_argument("--schedule", type=int, default=0,
                     help="0 scan first, 1 concurrent, 2 the pages' three background streams")
+    ap.add_argument("--remote", action="store_true",
+                    help="remote tier (emulated disaggregated partial fetch) on the single-layer shape")
+    ap.add_argument("--remote-gbps", type=float, nargs="+", default=[0.0, 50.0, 25.0],
+                    help="emulated network rates for --remote (0 = unthrottled host copy)")
+    ap.add_argument("--remote-threads", type=int, default=8)
     ap.add_argument("--requests", type=int, default=0,
                     help="override the request count (small cases for profiling)")
     args = ap.parse_args()
@@ -870,6 +956,8 @@ def main():
         run_kernels_alone(args, ws, rank, local)
     elif args.miss_stall:
         run_miss_stall(args, ws, rank, local)
+    elif args.remote:
+        run_remote(args, ws, rank, local)
     elif workload.SHAPES[args.workload].layers > 1:
         run_oasis_layers(args, ws, rank, local)
     else:

@@ -91,6 +91,8 @@ typedef enum {
 #define OASIS_DEVERR_BAD_BLOCK_ID 0x1u /* a block id >= NBmax or past context */
 #define OASIS_DEVERR_TIMEOUT 0x2u      /* a kernel's bounded barrier wait expired */
 #define OASIS_DEVERR_BAD_UNIT 0x4u     /* a pool unit index >= U */
+#define OASIS_DEVERR_NOT_LOCAL 0x8u    /* remote tier: a block needed a local slot
+                                          but the local tier was full */
 
 typedef struct {
   int32_t num_layers;
@@ -303,6 +305,71 @@ OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step,
 /* ctx_len[(step + 1) & 1][r] = ctx_len[step & 1][r] + grow for every r. */
 OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
                                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * Remote tier: emulation of prefill-decode disaggregation with remote partial
+ * fetch ([R] abstract and *If this is right*: under disaggregation a request
+ * is admitted to the decode node with a fraction of its KV, and the decode
+ * node's host memory holds only part of the cache; [S] result table, PD row).
+ *
+ * Reading.  The full KV cache stays on the prefill side (the remote tier);
+ * the decode side keeps a host tier of `capacity` local slots per (r, h).  A
+ * block enters the local tier the first time the decode side needs it (the
+ * initial resident set at oasis_load_resident, then every admitted block that
+ * is not yet held) and stays there; the gather always copies from the local
+ * tier into HBM.  Local slots are assigned in list order (admission rank
+ * order) from 0 upwards.  Summaries are built from the remote store (they are
+ * shipped with the request).  The network transfer remote -> local is done on
+ * the host, as a NIC's DMA would be, by a CUDA host callback ordered between
+ * the slot assignment and the gather on the gather's stream, optionally
+ * throttled to `gbps`; it moves no data through the GPU.
+ *
+ * With a remote tier attached to a layer, host_kv (given to oasis_init) is the
+ * remote store, pinned and mapped as before; oasis_append_token is refused
+ * (OASIS_ESTATE) for that layer.
+ *
+ * Layouts:
+ *   local_tier pinned [R][Hkv][capacity][2][B][d]   bf16   local slots
+ *   local_map  dev    [R][Hkv][NBmax] int32 (local slot of each block, -1 =
+ *                     not held) followed by [R][Hkv] int32 (slots in use)
+ *   miss_lists pinned [R][Hkv] int32 n_miss, then [R][Hkv][M] int32 ids, then
+ *                     [R][Hkv][M] int32 slots, M = max(K, C): the blocks the
+ *                     last slot assignment of each (r, h) fetched, in order
+ * ------------------------------------------------------------------------ */
+typedef struct {
+  int32_t capacity; /* local slots per (r, h): K <= capacity <= NBmax */
+  float gbps;       /* emulated network bandwidth in 1e9 bytes/s; 0 = no throttle */
+  int32_t threads;  /* host copy threads per transfer, 1..16 (0 = 4) */
+} oasis_remote_config;
+
+typedef struct {
+  size_t local_tier_bytes; /* per layer, pinned host */
+  size_t local_map_bytes;  /* per layer, device */
+  size_t miss_lists_bytes; /* per layer, pinned host */
+} oasis_remote_sizes;
+
+OASIS_API int oasis_remote_query_sizes(const oasis_config* cfg,
+                                       const oasis_remote_config* rcfg,
+                                       oasis_remote_sizes* out);
+
+/* Attach a remote tier to `layer` before its oasis_load_resident.  The
+ * buffers are lent for the life of the context (16-byte aligned; local_tier
+ * and miss_lists page-locked and mapped for the device).  Clears local_map
+ * (every block not held, no slot in use); synchronises.  Errors: OASIS_EINVAL
+ * on a bad size or pointer, OASIS_ESTATE once the layer is loaded. */
+OASIS_API int oasis_remote_attach(oasis_ctx* ctx, int layer,
+                                  const oasis_remote_config* rcfg,
+                                  void* local_tier, int32_t* local_map,
+                                  int32_t* miss_lists);
+
+/* Totals of the layer's emulated network transfers since attach: units
+ * (8 KiB each) moved remote -> local, host callbacks run, and seconds those
+ * callbacks took (throttle included); bad_entries counts list entries the
+ * callbacks skipped as out of range (0 unless the lists were corrupted).
+ * Read after oasis_sync for a settled value.  Any output may be NULL. */
+OASIS_API int oasis_remote_stats(oasis_ctx* ctx, int layer, int64_t* units,
+                                 int64_t* transfers, double* seconds,
+                                 int64_t* bad_entries);
 
 /* Kernel timing: when enabled, oasis_step records CUDA events around each of
  * its kernels on the stream that launches it. */

@@ -54,6 +54,7 @@ def _load():
             "orc_step_rh": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, D,
                             I, I, P, P, P, P, P, P, P],
             "orc_append_token": [P, P, P, P, P, I, I, I, I, I, I],
+            "orc_remote_fetch_rh": [P, I, P, P, I, I, P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(L, name)
@@ -151,6 +152,24 @@ def append_token(host_kv, summ, ctx_len, k_new, v_new, r):
         "append_token")
 
 
+def remote_fetch_rh(ids, local_map_row, count, capacity):
+    """Remote-tier slot assignment of one (r, h).  ``local_map_row`` ([NBmax]
+    int32) is updated in place; ``count`` is a 1-element int32 array updated
+    in place.  Returns ``(miss_ids, miss_slots, full)``."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    n = ids.shape[0]
+    mi = np.full(max(n, 1), -1, dtype=np.int32)
+    ms = np.full(max(n, 1), -1, dtype=np.int32)
+    nm = np.zeros(1, dtype=np.int32)
+    rc = _load().orc_remote_fetch_rh(_p(ids, np.int32), n, _p(local_map_row, np.int32),
+                                     _p(count, np.int32), capacity, local_map_row.shape[0],
+                                     _p(mi, np.int32), _p(ms, np.int32), _p(nm, np.int32))
+    if rc < 0:
+        raise ValueError("oracle remote_fetch_rh rejected its arguments")
+    k = int(nm[0])
+    return mi[:k].copy(), ms[:k].copy(), bool(rc)
+
+
 class LayerOracle:
     """Oracle state of one layer restricted to a set of (r, h) pairs.
 
@@ -159,7 +178,8 @@ class LayerOracle:
     ``[R][Hkv][K]`` tables but only the tracked pairs are advanced.
     """
 
-    def __init__(self, host_kv, summ, ctx_len, res0, K, C, pairs, scale=None):
+    def __init__(self, host_kv, summ, ctx_len, res0, K, C, pairs, scale=None,
+                 remote_capacity=None):
         self.host_kv, self.summ, self.ctx_len = host_kv, summ, ctx_len
         self.R, self.Hkv, self.NBmax, _, self.B, self.d = host_kv.shape
         self.K, self.C = K, C
@@ -168,6 +188,22 @@ class LayerOracle:
         self.pairs = [tuple(int(x) for x in p) for p in pairs]
         self.scale = 1.0 / np.sqrt(self.d) if scale is None else scale
         self._scores = np.empty(self.NBmax, dtype=np.float32)
+        # Remote tier: the decode side's slot map and slot count per pair; the
+        # initial resident set is fetched first (in slot order).
+        self.remote_capacity = remote_capacity
+        self.initial_misses = {}
+        if remote_capacity is not None:
+            self.local_map = np.full((self.R, self.Hkv, self.NBmax), -1, dtype=np.int32)
+            self.local_count = np.zeros((self.R, self.Hkv), dtype=np.int32)
+            for (r, h) in self.pairs:
+                self.initial_misses[(r, h)] = self._fetch(r, h, self.res[r, h])
+
+    def _fetch(self, r, h, ids):
+        cnt = self.local_count[r, h:h + 1].copy()
+        row = self.local_map[r, h]
+        mi, ms, full = remote_fetch_rh(ids, row, cnt, self.remote_capacity)
+        self.local_count[r, h] = cnt[0]
+        return dict(miss_ids=mi, miss_slots=ms, n_miss=len(mi), full=full)
 
     def step(self, q, qd, t, topk_override=None):
         """Run one layer-step for every tracked pair.
@@ -203,4 +239,6 @@ class LayerOracle:
                                         self.C, t)
             out[(r, h)] = dict(attn=attn, scores=scores, topk=topk, admit_ids=a,
                                admit_slots=s, evict_ids=e, n_admit=n)
+            if self.remote_capacity is not None:
+                out[(r, h)].update(self._fetch(r, h, a[:n]))
         return out

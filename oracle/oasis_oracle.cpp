@@ -260,6 +260,33 @@ extern "C" int orc_step_rh(const uint16_t* host_kv, const uint16_t* summ,
                             admit_slots, evict_ids, n_admit);
 }
 
+extern "C" int orc_remote_fetch_rh(const int32_t* ids, int n, int32_t* local_map,
+                                   int32_t* count, int capacity, int NBmax,
+                                   int32_t* miss_ids, int32_t* miss_slots,
+                                   int32_t* n_miss) {
+  if (!ids || !local_map || !count || !miss_ids || !miss_slots || !n_miss ||
+      n < 0 || capacity < 0 || NBmax <= 0 || *count < 0)
+    return -1;
+  int full = 0;
+  *n_miss = 0;
+  for (int i = 0; i < n; ++i) {
+    const int id = ids[i];
+    if (id < 0) continue;
+    if (id >= NBmax) return -1;
+    if (local_map[id] >= 0) continue;  // already held by the decode side
+    if (*count >= capacity) {          // no slot left: stays remote
+      full = 1;
+      continue;
+    }
+    local_map[id] = *count;
+    miss_ids[*n_miss] = id;
+    miss_slots[*n_miss] = *count;
+    ++*n_miss;
+    ++*count;
+  }
+  return full;
+}
+
 extern "C" int orc_append_token(uint16_t* host_kv, uint16_t* summ,
                                 const int32_t* ctx_len, const uint16_t* k_new,
                                 const uint16_t* v_new, int R, int Hkv,

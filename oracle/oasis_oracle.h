@@ -94,6 +94,20 @@ int orc_step_rh(const uint16_t* host_kv, const uint16_t* summ,
                 int32_t* topk, int32_t* admit_ids, int32_t* admit_slots,
                 int32_t* evict_ids, int32_t* n_admit);
 
+/* Remote-tier partial fetch for one (r, h) (emulated prefill-decode
+ * disaggregation; [R] abstract: a request reaches the decode node with only
+ * part of its KV and the decode node's host memory holds only part of the
+ * cache; [S] result table, PD row).  The decode-side host tier has
+ * `capacity` slots; local_map[NBmax] gives each block's slot (-1 = not held)
+ * and *count the slots in use.  The ids ids[0..n) are visited in order; an id
+ * < 0 is skipped; an id not yet held takes slot *count (then *count grows by
+ * one) and is appended to miss_ids / miss_slots, *n_miss counting them.  When
+ * no slot is left the id stays not held and the function reports 1 after
+ * finishing the list; otherwise 0.  Ids are distinct and < NBmax. */
+int orc_remote_fetch_rh(const int32_t* ids, int n, int32_t* local_map,
+                        int32_t* count, int capacity, int NBmax,
+                        int32_t* miss_ids, int32_t* miss_slots, int32_t* n_miss);
+
 /* Append one decoded token to request r of one layer: write k_new/v_new
  * ([Hkv][d] each) at position pos = ctx_len[r] into the host store and fold
  * the key into the tail block's summary (a fresh block starts as min = max =

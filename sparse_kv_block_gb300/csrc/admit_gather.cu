@@ -81,8 +81,13 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
       if (lane == 0) raise_error(a.err, kErrBadUnit);
       continue;
     }
+    const int src_slot = a.local_map ? a.local_map[static_cast<size_t>(pair) * a.NBmax + id] : id;
+    if (src_slot < 0 || src_slot >= a.src_units) {
+      if (lane == 0) raise_error(a.err, kErrNotLocal);
+      continue;
+    }
     const uint4* src = static_cast<const uint4*>(a.host) +
-                       (static_cast<size_t>(pair) * a.NBmax + id) * (kUnitBytes / 16);
+                       (static_cast<size_t>(pair) * a.src_units + src_slot) * (kUnitBytes / 16);
     uint4* dst = static_cast<uint4*>(a.pool) +
                  (static_cast<size_t>(pair) * a.U + unit) * (kUnitBytes / 16);
     uint4 v[kUnitBytes / 16 / 32];
@@ -90,6 +95,53 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
     for (int j = 0; j < kUnitBytes / 16 / 32; ++j) v[j] = __ldcs(src + j * 32 + lane);
 #pragma unroll
     for (int j = 0; j < kUnitBytes / 16 / 32; ++j) dst[j * 32 + lane] = v[j];
+  }
+}
+
+// Remote tier slot assignment, one warp per pair: 32 items at a time, the
+// blocks that need a slot found by ballot and numbered by their rank among
+// them, so slots follow item order exactly as a sequential loop would give.
+constexpr int kRemoteWarps = 4;
+
+__global__ void __launch_bounds__(kRemoteWarps * 32) remote_assign_kernel(const RemoteArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int local = blockIdx.x * kRemoteWarps + (threadIdx.x >> 5);
+  if (local >= a.pairs) return;  // warp-uniform
+  const int pair = a.pair0 + local;
+  const size_t base_map = static_cast<size_t>(pair) * a.NBmax;
+  int count = a.count[pair];
+  int n = a.items;
+  if (a.n_valid) n = min(max(a.n_valid[pair], 0), a.items);
+  int nm = 0;
+  for (int b = 0; b < n; b += 32) {
+    const int i = b + lane;
+    const int id = i < n ? a.ids[static_cast<size_t>(pair) * a.items + i] : -1;
+    bool need = false;
+    if (id >= a.NBmax) {
+      raise_error(a.err, kErrBadBlock);
+    } else if (id >= 0) {
+      need = a.local_map[base_map + id] < 0;
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, need);
+    const int rank = __popc(ball & ((1u << lane) - 1u));
+    const int room = max(a.capacity - count, 0);
+    if (need) {
+      if (rank < room) {
+        const int slot = count + rank;
+        a.local_map[base_map + id] = slot;
+        a.miss_ids[static_cast<size_t>(pair) * a.M + nm + rank] = id;
+        a.miss_slots[static_cast<size_t>(pair) * a.M + nm + rank] = slot;
+      } else {
+        raise_error(a.err, kErrNotLocal);
+      }
+    }
+    const int got = min(__popc(ball), room);
+    count += got;
+    nm += got;
+  }
+  if (lane == 0) {
+    a.count[pair] = count;
+    a.n_miss[pair] = nm;
   }
 }
 
@@ -262,6 +314,12 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
   }();
   if (grid > cap) grid = cap;
   gather_kernel<<<static_cast<int>(grid), kGatherThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_remote_assign(const RemoteArgs& a, cudaStream_t s) {
+  if (a.pairs <= 0) return cudaSuccess;
+  remote_assign_kernel<<<(a.pairs + kRemoteWarps - 1) / kRemoteWarps, kRemoteWarps * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -2,11 +2,18 @@
 // the side stream and its events, the TMA descriptors and step orchestration.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <memory>
 #include <string>
+#include <thread>
+#include <tuple>
 #include <vector>
 
 #include "../../include/oasis.h"
@@ -19,6 +26,96 @@ namespace {
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Remote tier (emulated prefill-decode disaggregation).  The transfer
+// remote -> local tier of the blocks a slot assignment listed runs on the
+// host, in a CUDA host callback, as a network adapter's DMA would: no GPU
+// work.  One job per (pair range, item count) a layer uses; a job's fields
+// never change after creation, so a callback may still be queued when the
+// next step enqueues the same job again.
+struct RemoteStats {
+  std::atomic<int64_t> units{0}, transfers{0}, bad{0}, nanos{0};
+};
+
+struct RemoteJob {
+  const uint8_t* remote = nullptr;  // [pairs][NBmax] units
+  uint8_t* local = nullptr;         // [pairs][capacity] units
+  const int32_t* n_miss = nullptr;  // host view of the lists
+  const int32_t* miss_ids = nullptr;
+  const int32_t* miss_slots = nullptr;
+  int pair0 = 0, pairs = 0, M = 0, NBmax = 0, capacity = 0, threads = 1;
+  double gbps = 0.0;
+  RemoteStats* stats = nullptr;
+};
+
+void remote_copy_range(const RemoteJob& j, const std::vector<std::pair<int, int>>& items,
+                       size_t lo, size_t hi) {
+  for (size_t k = lo; k < hi; ++k) {
+    const int p = items[k].first, i = items[k].second;
+    const size_t li = static_cast<size_t>(p) * j.M + i;
+    std::memcpy(j.local + (static_cast<size_t>(p) * j.capacity + j.miss_slots[li]) * kUnitBytes,
+                j.remote + (static_cast<size_t>(p) * j.NBmax + j.miss_ids[li]) * kUnitBytes,
+                kUnitBytes);
+  }
+}
+
+void CUDART_CB remote_transfer(void* arg) {
+  const RemoteJob& j = *static_cast<const RemoteJob*>(arg);
+  const auto t0 = std::chrono::steady_clock::now();
+  std::vector<std::pair<int, int>> items;
+  int64_t bad = 0;
+  for (int p = j.pair0; p < j.pair0 + j.pairs; ++p) {
+    const int n = j.n_miss[p];
+    if (n < 0 || n > j.M) {
+      ++bad;
+      continue;
+    }
+    for (int i = 0; i < n; ++i) {
+      const size_t li = static_cast<size_t>(p) * j.M + i;
+      if (j.miss_ids[li] < 0 || j.miss_ids[li] >= j.NBmax || j.miss_slots[li] < 0 ||
+          j.miss_slots[li] >= j.capacity) {
+        ++bad;
+        continue;
+      }
+      items.emplace_back(p, i);
+    }
+  }
+  const size_t n = items.size();
+  const int nt = static_cast<int>(std::min<size_t>(j.threads, (n + 63) / 64));
+  if (nt <= 1) {
+    remote_copy_range(j, items, 0, n);
+  } else {
+    std::vector<std::thread> pool;
+    for (int t = 1; t < nt; ++t)
+      pool.emplace_back(remote_copy_range, std::cref(j), std::cref(items), n * t / nt,
+                        n * (t + 1) / nt);
+    remote_copy_range(j, items, 0, n / nt);
+    for (auto& th : pool) th.join();
+  }
+  if (j.gbps > 0.0) {
+    const double sec = static_cast<double>(n) * kUnitBytes / (j.gbps * 1e9);
+    std::this_thread::sleep_until(t0 + std::chrono::duration_cast<std::chrono::steady_clock::duration>(
+                                           std::chrono::duration<double>(sec)));
+  }
+  const auto dt = std::chrono::steady_clock::now() - t0;
+  j.stats->units += static_cast<int64_t>(n);
+  j.stats->transfers += 1;
+  j.stats->bad += bad;
+  j.stats->nanos += std::chrono::duration_cast<std::chrono::nanoseconds>(dt).count();
+}
+
+struct RemoteTier {
+  int capacity = 0, M = 0, threads = 4;
+  double gbps = 0.0;
+  uint8_t* local = nullptr;       // caller's pinned local tier
+  void* local_dev = nullptr;      // its device mapping
+  int32_t* map = nullptr;         // dev [pairs][NBmax]
+  int32_t* count = nullptr;       // dev [pairs]
+  int32_t* lists = nullptr;       // caller's pinned miss lists
+  int32_t* lists_dev = nullptr;   // their device mapping
+  RemoteStats stats;
+  std::map<std::tuple<int, int, int>, std::unique_ptr<RemoteJob>> jobs;
+};
 
 struct LayerState {
   void* pool = nullptr;
@@ -52,6 +149,7 @@ struct LayerState {
   std::vector<cudaEvent_t> ev_group2; // admissions done (three-stream schedule)
   bool side_pending = false;
   bool loaded = false;
+  std::unique_ptr<RemoteTier> remote;
 };
 
 struct ProfPair {
@@ -324,13 +422,74 @@ int run_admit(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t*
   return ctx->cuda(e, "admit_evict launch");
 }
 
+// Remote tier: assign local slots to the listed blocks not yet held, then
+// move them remote -> local on the host (a callback on the same stream), so
+// the gather that follows on `s` finds every block in the local tier.
+int run_remote_fetch(oasis_ctx* ctx, int layer, const int32_t* ids, const int32_t* n_valid,
+                     int items, int pair0, int pairs, cudaStream_t s) {
+  LayerState& L = ctx->layers[layer];
+  RemoteTier& T = *L.remote;
+  const int all = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
+  RemoteArgs r{};
+  r.ids = ids;
+  r.n_valid = n_valid;
+  r.local_map = T.map;
+  r.count = T.count;
+  r.n_miss = T.lists_dev;
+  r.miss_ids = T.lists_dev + all;
+  r.miss_slots = T.lists_dev + all + static_cast<size_t>(all) * T.M;
+  r.err = ctx->err;
+  r.pair0 = pair0;
+  r.pairs = pairs;
+  r.items = items;
+  r.NBmax = ctx->cfg.max_blocks;
+  r.capacity = T.capacity;
+  r.M = T.M;
+  if (int rc = ctx->cuda(launch_remote_assign(r, s), "remote slot assignment launch")) return rc;
+  auto& job = T.jobs[std::make_tuple(pair0, pairs, items)];
+  if (!job) {
+    job.reset(new (std::nothrow) RemoteJob());
+    if (!job) return ctx->fail(OASIS_ENOMEM, "remote job");
+    job->remote = static_cast<const uint8_t*>(L.host);
+    job->local = T.local;
+    job->n_miss = T.lists;
+    job->miss_ids = T.lists + all;
+    job->miss_slots = T.lists + all + static_cast<size_t>(all) * T.M;
+    job->pair0 = pair0;
+    job->pairs = pairs;
+    job->M = T.M;
+    job->NBmax = ctx->cfg.max_blocks;
+    job->capacity = T.capacity;
+    job->threads = T.threads;
+    job->gbps = T.gbps;
+    job->stats = &T.stats;
+  }
+  return ctx->cuda(cudaLaunchHostFunc(s, remote_transfer, job.get()), "remote transfer callback");
+}
+
+void gather_source(const oasis_ctx* ctx, const LayerState& L, GatherArgs& g) {
+  if (L.remote) {
+    g.host = L.remote->local_dev;
+    g.local_map = L.remote->map;
+    g.src_units = L.remote->capacity;
+  } else {
+    g.host = L.host_dev;
+    g.local_map = nullptr;
+    g.src_units = ctx->cfg.max_blocks;
+  }
+}
+
 int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
                  const int32_t* aslot, const int32_t* nadm, cudaStream_t s, int pair0 = 0,
                  int pairs = -1) {
   if (ctx->C == 0) return OASIS_OK;
   LayerState& L = ctx->layers[layer];
+  if (pairs < 0) pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
+  if (L.remote) {
+    if (int rc = run_remote_fetch(ctx, layer, aid, nadm, ctx->C, pair0, pairs, s)) return rc;
+  }
   GatherArgs g{};
-  g.host = L.host_dev;
+  gather_source(ctx, L, g);
   g.pool = L.pool;
   g.src_ids = aid;
   g.dst_slots = aslot;
@@ -338,7 +497,7 @@ int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
   g.phys = ctx->phys_tab(layer, step + 1);
   g.err = ctx->err;
   g.pair0 = pair0;
-  g.pairs = pairs < 0 ? ctx->cfg.num_requests * ctx->cfg.num_kv_heads : pairs;
+  g.pairs = pairs;
   g.items = ctx->C;
   g.NBmax = ctx->cfg.max_blocks;
   g.U = ctx->U;
@@ -506,6 +665,12 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side) cudaStreamSynchronize(ctx->side);
   if (ctx->side2) cudaStreamSynchronize(ctx->side2);
   if (ctx->side3) cudaStreamSynchronize(ctx->side3);
+  // Host callbacks of a remote tier may sit on a caller's stream.
+  for (auto& L : ctx->layers)
+    if (L.remote) {
+      cudaDeviceSynchronize();
+      break;
+    }
   for (auto& L : ctx->layers) {
     for (auto& e : L.ev_group)
       if (e) cudaEventDestroy(e);
@@ -577,8 +742,13 @@ OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step, voi
                                             ctx->cfg.topk, ctx->U, s),
                          "init tables launch"))
     return rc;
+  if (L.remote) {
+    if (int rc = run_remote_fetch(ctx, layer, ctx->res_tab(layer, first_step), nullptr,
+                                  ctx->cfg.topk, 0, pairs, s))
+      return rc;
+  }
   GatherArgs g{};
-  g.host = L.host_dev;
+  gather_source(ctx, L, g);
   g.pool = L.pool;
   g.src_ids = ctx->res_tab(layer, first_step);
   g.dst_slots = nullptr;
@@ -835,6 +1005,8 @@ OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step, const void
   if (int rc = ctx->set_device()) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LayerState& L = ctx->layers[layer];
+  if (L.remote)
+    return ctx->fail(OASIS_ESTATE, "append: layer %d has a remote tier attached", layer);
   // The token may land in a block this layer's side work is copying.
   if (L.side_pending) {
     if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
@@ -864,6 +1036,87 @@ OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow, void* st
   return ctx->cuda(launch_advance(ctx->ctx_tab(step), ctx->ctx_tab(step + 1),
                                   ctx->cfg.num_requests, grow, static_cast<cudaStream_t>(stream)),
                    "advance launch");
+}
+
+namespace {
+const char* remote_config_error(const oasis_config* cfg, const oasis_remote_config* r) {
+  if (!r) return "remote config is NULL";
+  if (r->capacity < cfg->topk || r->capacity > cfg->max_blocks)
+    return "remote capacity must be in [K, NBmax]";
+  if (!(r->gbps >= 0.f) || std::isinf(r->gbps)) return "remote gbps must be finite and >= 0";
+  if (r->threads < 0 || r->threads > 16) return "remote threads must be in 0..16";
+  return nullptr;
+}
+}  // namespace
+
+OASIS_API int oasis_remote_query_sizes(const oasis_config* cfg, const oasis_remote_config* rcfg,
+                                       oasis_remote_sizes* out) {
+  if (!out || config_error(cfg) || remote_config_error(cfg, rcfg)) return OASIS_EINVAL;
+  const size_t pairs = static_cast<size_t>(cfg->num_requests) * cfg->num_kv_heads;
+  const size_t M = std::max(cfg->topk, fetch_cap(*cfg));
+  out->local_tier_bytes = pairs * rcfg->capacity * kUnitBytes;
+  out->local_map_bytes = (pairs * cfg->max_blocks + pairs) * 4;
+  out->miss_lists_bytes = (pairs + 2 * pairs * M) * 4;
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_remote_attach(oasis_ctx* ctx, int layer, const oasis_remote_config* rcfg,
+                                  void* local_tier, int32_t* local_map, int32_t* miss_lists) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (const char* e = remote_config_error(&ctx->cfg, rcfg))
+    return ctx->fail(OASIS_EINVAL, "remote_attach: %s", e);
+  if (!local_tier || !local_map || !miss_lists || !aligned16(local_tier) ||
+      !aligned16(local_map) || !aligned16(miss_lists))
+    return ctx->fail(OASIS_EINVAL, "remote_attach: null or misaligned buffer");
+  LayerState& L = ctx->layers[layer];
+  if (L.loaded || L.remote)
+    return ctx->fail(OASIS_ESTATE, "remote_attach: layer %d already loaded or attached", layer);
+  if (int rc = ctx->set_device()) return rc;
+  std::unique_ptr<RemoteTier> T(new (std::nothrow) RemoteTier());
+  if (!T) return ctx->fail(OASIS_ENOMEM, "remote tier");
+  T->capacity = rcfg->capacity;
+  T->M = std::max(ctx->cfg.topk, ctx->C);
+  T->threads = rcfg->threads > 0 ? rcfg->threads : 4;
+  T->gbps = rcfg->gbps;
+  T->local = static_cast<uint8_t*>(local_tier);
+  T->lists = miss_lists;
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, local_tier, 0) != cudaSuccess || !d) {
+    cudaGetLastError();
+    return ctx->fail(OASIS_EINVAL, "remote_attach: local_tier is not mapped page-locked memory");
+  }
+  T->local_dev = d;
+  d = nullptr;
+  if (cudaHostGetDevicePointer(&d, miss_lists, 0) != cudaSuccess || !d) {
+    cudaGetLastError();
+    return ctx->fail(OASIS_EINVAL, "remote_attach: miss_lists is not mapped page-locked memory");
+  }
+  T->lists_dev = static_cast<int32_t*>(d);
+  const size_t pairs = static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_kv_heads;
+  T->map = local_map;
+  T->count = local_map + pairs * ctx->cfg.max_blocks;
+  if (int rc = ctx->cuda(cudaMemsetAsync(T->map, 0xff, pairs * ctx->cfg.max_blocks * 4, ctx->side2),
+                         "clear local map"))
+    return rc;
+  if (int rc = ctx->cuda(cudaMemsetAsync(T->count, 0, pairs * 4, ctx->side2), "clear slot counts"))
+    return rc;
+  if (int rc = ctx->cuda(cudaStreamSynchronize(ctx->side2), "remote attach sync")) return rc;
+  std::memset(miss_lists, 0, pairs * 4);
+  L.remote = std::move(T);
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_remote_stats(oasis_ctx* ctx, int layer, int64_t* units, int64_t* transfers,
+                                 double* seconds, int64_t* bad_entries) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  const LayerState& L = ctx->layers[layer];
+  if (!L.remote) return ctx->fail(OASIS_ESTATE, "remote_stats: layer %d has no remote tier", layer);
+  const RemoteStats& S = L.remote->stats;
+  if (units) *units = S.units.load();
+  if (transfers) *transfers = S.transfers.load();
+  if (seconds) *seconds = static_cast<double>(S.nanos.load()) * 1e-9;
+  if (bad_entries) *bad_entries = S.bad.load();
+  return OASIS_OK;
 }
 
 OASIS_API int oasis_profile_enable(oasis_ctx* ctx, int enable) {

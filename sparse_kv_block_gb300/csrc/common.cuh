@@ -22,6 +22,7 @@ constexpr int kMaxGroup = 4;
 constexpr uint32_t kErrBadBlock = 0x1u;
 constexpr uint32_t kErrTimeout = 0x2u;
 constexpr uint32_t kErrBadUnit = 0x4u;
+constexpr uint32_t kErrNotLocal = 0x8u;
 
 // Bounded barrier waits give up after about a second at 2 GHz.
 constexpr long long kWaitLimitCycles = 2000000000LL;

@@ -65,8 +65,29 @@ struct GatherArgs {
   const int32_t* dst_slots;  // may be null
   const int32_t* n_valid;    // may be null
   const int32_t* phys;
+  // Remote tier: when set, the host store is the local tier of src_units
+  // slots per pair and block id b of pair p is read from slot
+  // local_map[p*NBmax + b]; otherwise src_units = NBmax and slot = b.
+  const int32_t* local_map;
   uint32_t* err;
-  int pair0, pairs, items, NBmax, U;
+  int pair0, pairs, items, NBmax, U, src_units;
+};
+
+// Remote tier slot assignment: item i of pair p names block
+// ids[p*items + i] (skipped if < 0 or i >= n_valid[p]); every named block
+// without a local slot gets slot count[p]++ (in item order) while
+// count[p] < capacity, and is listed in miss_ids / miss_slots [p][M] with
+// n_miss[p] entries.  The lists may live in mapped host memory.
+struct RemoteArgs {
+  const int32_t* ids;
+  const int32_t* n_valid;    // may be null
+  int32_t* local_map;        // [R][Hkv][NBmax]
+  int32_t* count;            // [R][Hkv]
+  int32_t* n_miss;           // [R][Hkv]
+  int32_t* miss_ids;         // [R][Hkv][M]
+  int32_t* miss_slots;       // [R][Hkv][M]
+  uint32_t* err;
+  int pair0, pairs, items, NBmax, capacity, M;
 };
 
 struct SummaryArgs {
@@ -94,6 +115,7 @@ cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
 cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_admit(const AdmitArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
+cudaError_t launch_remote_assign(const RemoteArgs& a, cudaStream_t s);
 cudaError_t launch_init_tables(int32_t* phys, int32_t* stamps, int pairs,
                                int K, int U, cudaStream_t s);
 cudaError_t launch_summary_build(const SummaryArgs& a, cudaStream_t s);

@@ -49,6 +49,18 @@ class oasis_buffers(ctypes.Structure):
                 ("ctx_len", c_void_p), ("workspace", c_void_p)]
 
 
+class oasis_remote_config(ctypes.Structure):
+    _fields_ = [("capacity", c_int32), ("gbps", c_float), ("threads", c_int32)]
+
+
+class oasis_remote_sizes(ctypes.Structure):
+    _fields_ = [("local_tier_bytes", c_size_t), ("local_map_bytes", c_size_t),
+                ("miss_lists_bytes", c_size_t)]
+
+
+DEVERR_NOT_LOCAL = 0x8
+
+
 class OasisError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
@@ -80,6 +92,11 @@ EXPORTS = {
                                  POINTER(c_void_p)]),
     "oasis_append_token": (c_int, [_P, c_int, c_int, _P, _P, _P]),
     "oasis_advance_context": (c_int, [_P, c_int, c_int, _P]),
+    "oasis_remote_query_sizes": (c_int, [POINTER(oasis_config), POINTER(oasis_remote_config),
+                                         POINTER(oasis_remote_sizes)]),
+    "oasis_remote_attach": (c_int, [_P, c_int, POINTER(oasis_remote_config), _P, _P, _P]),
+    "oasis_remote_stats": (c_int, [_P, c_int, POINTER(c_int64), POINTER(c_int64),
+                                   POINTER(c_double), POINTER(c_int64)]),
     "oasis_profile_enable": (c_int, [_P, c_int]),
     "oasis_profile_read": (c_int, [_P, POINTER(c_double), POINTER(c_int64), POINTER(c_double)]),
 }
@@ -139,6 +156,14 @@ def oasis_query_sizes(cfg: oasis_config) -> oasis_sizes:
     rc = lib().oasis_query_sizes(ctypes.byref(cfg), ctypes.byref(out))
     if rc != OASIS_OK:
         raise OasisError(rc, oasis_config_error(cfg) or "query_sizes failed")
+    return out
+
+
+def oasis_remote_query_sizes(cfg: oasis_config, rcfg: oasis_remote_config) -> oasis_remote_sizes:
+    out = oasis_remote_sizes()
+    rc = lib().oasis_remote_query_sizes(ctypes.byref(cfg), ctypes.byref(rcfg), ctypes.byref(out))
+    if rc != OASIS_OK:
+        raise OasisError(rc, "remote_query_sizes: bad config or remote config")
     return out
 
 
@@ -273,6 +298,43 @@ class Oasis:
 
     def oasis_advance_context(self, step, grow=1, stream=None) -> None:
         self._check(lib().oasis_advance_context(self.ctx, step, grow, _stream(stream)))
+
+    def oasis_remote_attach(self, layer: int, capacity: int, gbps: float = 0.0,
+                            threads: int = 0) -> dict:
+        """Allocate the remote tier's buffers (pinned local tier and miss
+        lists, device local map), attach them to `layer` and return them as
+        tensors: local_tier [R][Hkv][capacity][2][16][128] bf16, local_map
+        [R][Hkv][NBmax] int32, local_count [R][Hkv] int32 (a view into the
+        same buffer), miss_lists (flat int32)."""
+        rcfg = oasis_remote_config(capacity, gbps, threads)
+        sz = oasis_remote_query_sizes(self.cfg, rcfg)
+        R, Hkv, NB = self.cfg.num_requests, self.cfg.num_kv_heads, self.cfg.max_blocks
+        local = torch.zeros((R, Hkv, capacity, 2, 16, 128), dtype=torch.bfloat16,
+                            pin_memory=True)
+        assert local.numel() * 2 == sz.local_tier_bytes
+        mp = torch.empty(sz.local_map_bytes // 4, dtype=torch.int32, device=self.device)
+        lists = torch.zeros(sz.miss_lists_bytes // 4, dtype=torch.int32, pin_memory=True)
+        self._check(lib().oasis_remote_attach(self.ctx, layer, ctypes.byref(rcfg),
+                                              local.data_ptr(), mp.data_ptr(),
+                                              lists.data_ptr()))
+        pairs = R * Hkv
+        M = max(self.cfg.topk, self.C)
+        t = dict(local_tier=local, local_map=mp[:pairs * NB].view(R, Hkv, NB),
+                 local_count=mp[pairs * NB:].view(R, Hkv), miss_lists=lists,
+                 n_miss=lists[:pairs].view(R, Hkv),
+                 miss_ids=lists[pairs:pairs + pairs * M].view(R, Hkv, M),
+                 miss_slots=lists[pairs + pairs * M:].view(R, Hkv, M))
+        if not hasattr(self, "remote"):
+            self.remote = {}
+        self.remote[layer] = t
+        return t
+
+    def oasis_remote_stats(self, layer: int) -> dict:
+        u, n, b = c_int64(0), c_int64(0), c_int64(0)
+        sec = c_double(0.0)
+        self._check(lib().oasis_remote_stats(self.ctx, layer, ctypes.byref(u), ctypes.byref(n),
+                                             ctypes.byref(sec), ctypes.byref(b)))
+        return dict(units=u.value, transfers=n.value, seconds=sec.value, bad_entries=b.value)
 
     def oasis_profile_enable(self, enable: bool = True) -> None:
         self._check(lib().oasis_profile_enable(self.ctx, 1 if enable else 0))

@@ -38,11 +38,12 @@ class Layer:
     orc: oracle.LayerOracle
     hb: np.ndarray
     summ: np.ndarray
+    remote: dict = None
 
 
 def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_fp32=False,
                gen_device="cpu", pairs=None, res0=None, side_groups=0,
-               schedule=0) -> Layer:
+               schedule=0, remote_capacity=None, remote_gbps=0.0) -> Layer:
     if K is not None or fetch_ratio is not None:
         shape = dataclasses.replace(shape, K=K if K is not None else shape.K,
                                     fetch_ratio=shape.fetch_ratio if fetch_ratio is None else fetch_ratio)
@@ -60,14 +61,40 @@ def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_
     eng.set_context(lens)
     eng.set_resident(0, res0, 0)
     eng.oasis_build_summaries(0, 0)
+    remote = None
+    if remote_capacity is not None:
+        remote = eng.oasis_remote_attach(0, remote_capacity, remote_gbps)
     eng.oasis_load_resident(0, 0)
     eng.oasis_sync()
     hb = workload.bf16_bits(host)
     summ = oracle.summary_build(hb, lens)
     if pairs is None:
         pairs = [(r, h) for r in range(shape.R) for h in range(shape.Hkv)]
-    orc = oracle.LayerOracle(hb, summ, lens, res0, shape.K, shape.C, pairs)
-    return Layer(shape, lens, host, q, qd, res0, eng, orc, hb, summ)
+    orc = oracle.LayerOracle(hb, summ, lens, res0, shape.K, shape.C, pairs,
+                             remote_capacity=remote_capacity)
+    return Layer(shape, lens, host, q, qd, res0, eng, orc, hb, summ, remote)
+
+
+def check_remote(L: Layer, misses: dict):
+    """Remote tier against the oracle: the last slot assignment's lists per
+    pair (bit-exact), the slot map and counts, and every held block's local
+    copy against the host store, byte for byte."""
+    T = L.remote
+    n_miss = T["n_miss"].numpy()
+    mi, ms = T["miss_ids"].numpy(), T["miss_slots"].numpy()
+    for (r, h), v in misses.items():
+        n = v["n_miss"]
+        assert n_miss[r, h] == n, (r, h)
+        assert (mi[r, h, :n] == v["miss_ids"]).all(), (r, h)
+        assert (ms[r, h, :n] == v["miss_slots"]).all(), (r, h)
+    lmap = T["local_map"].cpu().numpy()
+    cnt = T["local_count"].cpu().numpy()
+    local = workload.bf16_bits(T["local_tier"])
+    for (r, h) in misses:
+        assert (lmap[r, h] == L.orc.local_map[r, h]).all(), (r, h)
+        assert cnt[r, h] == L.orc.local_count[r, h], (r, h)
+        for b in np.nonzero(lmap[r, h] >= 0)[0]:
+            np.testing.assert_array_equal(local[r, h, lmap[r, h, b]], L.hb[r, h, b])
 
 
 def bits_to_float(bits: np.ndarray) -> np.ndarray:

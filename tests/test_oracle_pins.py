@@ -342,3 +342,85 @@ def test_append_token_matches_numpy_minmax():
         valid = min(B, lens[0] - b * B)
         np.testing.assert_array_equal(to_float(summ[:, :, b, 0]), kf[:, :, b, 0, :valid].min(axis=2))
         np.testing.assert_array_equal(to_float(summ[:, :, b, 1]), kf[:, :, b, 0, :valid].max(axis=2))
+
+
+# ------------------------------------------------------------ remote tier
+def test_remote_fetch_hand_worked():
+    g = json.load(open(os.path.join(GOLD, "remote_fetch_hand.json")))
+    local_map = np.full(g["NBmax"], -1, dtype=np.int32)
+    count = np.zeros(1, dtype=np.int32)
+    for c in g["calls"]:
+        mi, ms, full = oracle.remote_fetch_rh(c["ids"], local_map, count, g["capacity"])
+        assert mi.tolist() == c["miss_ids"], c["why"]
+        assert ms.tolist() == c["miss_slots"], c["why"]
+        assert int(count[0]) == c["count"] and full == c["full"], c["why"]
+    want = np.full(g["NBmax"], -1, dtype=np.int32)
+    for k, v in g["final_map"].items():
+        want[int(k)] = v
+    np.testing.assert_array_equal(local_map, want)
+
+
+@pytest.mark.parametrize("seed,capacity", [(0, 64), (1, 12), (2, 3)])
+def test_remote_fetch_matches_set_model(seed, capacity):
+    """Brute-force model with Python sets and a list of first appearances:
+    the held set is the first `capacity` distinct ids ever listed, slot =
+    position in that order, and each call fetches exactly the newly held
+    ids in list order."""
+    rng = np.random.default_rng(seed)
+    NB = 64
+    local_map = np.full(NB, -1, dtype=np.int32)
+    count = np.zeros(1, dtype=np.int32)
+    order = []
+    for _ in range(40):
+        n = int(rng.integers(0, 9))
+        ids = rng.choice(NB, size=n, replace=False).astype(np.int32)
+        ids[rng.random(n) < 0.15] = -1
+        before = list(order)
+        new = []
+        overflow = False
+        for x in ids.tolist():
+            if x < 0 or x in order:
+                continue
+            if len(order) < capacity:
+                order.append(x)
+                new.append(x)
+            else:
+                overflow = True
+        mi, ms, full = oracle.remote_fetch_rh(ids, local_map, count, capacity)
+        assert mi.tolist() == new
+        assert ms.tolist() == list(range(len(before), len(order)))
+        assert full == overflow
+        assert int(count[0]) == len(order)
+        held = {int(b) for b in np.nonzero(local_map >= 0)[0]}
+        assert held == set(order)
+        assert sorted(local_map[local_map >= 0].tolist()) == list(range(len(order)))
+        for slot, b in enumerate(order):
+            assert local_map[b] == slot
+
+
+def test_remote_fetch_oracle_layer_tracks_admissions():
+    """LayerOracle with a remote tier: the initial fetch is the resident set
+    in slot order, and every later fetch is the step's admitted blocks that
+    were never held before (capacity = NBmax, so nothing overflows)."""
+    from sparse_kv_block_gb300 import workload
+    shape = workload.SHAPES["tiny"]
+    lens = workload.ctx_lens(shape)
+    kv = workload.bf16_bits(workload.host_kv(shape, 0, 0, lens, device="cpu"))
+    summ = oracle.summary_build(kv, lens)
+    res0 = workload.initial_resident(shape, 0, 0, lens)
+    pairs = [(r, h) for r in range(shape.R) for h in range(shape.Hkv)]
+    orc = oracle.LayerOracle(kv, summ, lens, res0, shape.K, shape.C, pairs,
+                             remote_capacity=shape.NBmax)
+    seen = {p: [int(x) for x in res0[p] if x >= 0] for p in pairs}
+    for p in pairs:
+        assert orc.initial_misses[p]["miss_ids"].tolist() == seen[p]
+    q, qd = workload.queries(shape, 0, 0, 4, device="cpu")
+    for t in range(4):
+        out = orc.step(workload.bf16_bits(q[t]), workload.bf16_bits(qd[t]), t)
+        for p in pairs:
+            adm = out[p]["admit_ids"][:out[p]["n_admit"]].tolist()
+            new = [x for x in adm if x not in seen[p]]
+            assert out[p]["miss_ids"].tolist() == new
+            assert out[p]["miss_slots"].tolist() == list(range(len(seen[p]), len(seen[p]) + len(new)))
+            seen[p] += new
+            assert int(orc.local_count[p]) == len(seen[p])

@@ -1,0 +1,143 @@
+"""Remote tier (emulated prefill-decode disaggregation with remote partial
+fetch) on the GPU against the oracle: slot assignment lists, slot map and
+counts bit-exact, local tier and pool byte-exact, attention within the usual
+tolerance; tier overflow reported through the device error word; the
+throttle honoured."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_kv_block_gb300 import workload
+from sparse_kv_block_gb300.oasis import DEVERR_NOT_LOCAL, OASIS_ESTATE, OasisError
+from tests import _harness as H
+
+pytestmark = pytest.mark.gpu
+TINY = workload.SHAPES["tiny"]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda", 0)
+
+
+def test_remote_staged_steps_match_oracle(dev):
+    sh = dataclasses.replace(TINY, R=3)
+    L = H.make_layer(sh, seed=11, steps=6, fetch_ratio=0.25, remote_capacity=sh.NBmax)
+    H.check_remote(L, L.orc.initial_misses)
+    for t in range(6):
+        ref = H.run_staged_step(L, t, dev)
+        H.check_remote(L, ref)
+    st = L.eng.oasis_remote_stats(0)
+    assert st["units"] == int(L.orc.local_count.sum()) and st["bad_entries"] == 0
+    L.eng.close()
+
+
+@pytest.mark.parametrize("groups,schedule", [(0, 0), (3, 0), (2, 2)])
+def test_remote_fused_steps_match_oracle(dev, groups, schedule):
+    sh = dataclasses.replace(TINY, R=4)
+    L = H.make_layer(sh, seed=12, steps=6, fetch_ratio=0.25, out_fp32=True, side_groups=groups,
+                     schedule=schedule, remote_capacity=48)
+    eng = L.eng
+    out = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
+    outd = torch.empty_like(out)
+    for t in range(6):
+        eng.oasis_step(0, t, L.q[t].to(dev), L.qd[t].to(dev), out, outd)
+        eng.oasis_join(0)
+        eng.oasis_sync()
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
+        for (r, h), v in ref.items():
+            assert np.array_equal(lists["topk_ids"][r, h], v["topk"]), "tie window hit"
+            assert not v["full"]
+        H.check_attention([out.cpu().numpy(), outd.cpu().numpy()], ref, sh.G)
+        H.check_remote(L, ref)
+        H.check_pool(L, (t + 1) & 1)
+    eng.close()
+
+
+def test_remote_back_to_back_steps(dev):
+    # Host callbacks between the slot assignment and the gather of every step,
+    # steps issued without host synchronisation.
+    sh = dataclasses.replace(TINY, R=5)
+    L = H.make_layer(sh, seed=13, steps=8, fetch_ratio=0.25, out_fp32=True,
+                     remote_capacity=sh.NBmax)
+    eng = L.eng
+    outs = [torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev) for _ in range(16)]
+    qg, qdg = L.q.to(dev), L.qd.to(dev)
+    for t in range(8):
+        eng.oasis_step(0, t, qg[t], qdg[t], outs[2 * t], outs[2 * t + 1])
+    eng.oasis_join(0)
+    eng.oasis_sync()
+    for t in range(8):
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        H.check_attention([outs[2 * t].cpu().numpy(), outs[2 * t + 1].cpu().numpy()], ref, sh.G)
+    H.check_remote(L, ref)
+    H.check_pool(L, 8 & 1)
+    eng.close()
+
+
+def test_remote_tier_overflow_is_reported(dev):
+    # capacity K + 1: the first admissions overflow the tier.  Both sides run
+    # the slot assignment on the GPU's own admission lists.
+    sh = dataclasses.replace(TINY, R=2)
+    cap = sh.K + 1
+    L = H.make_layer(sh, seed=14, steps=4, fetch_ratio=0.25, remote_capacity=cap)
+    eng = L.eng
+    R, Hk, K, C = sh.R, sh.Hkv, sh.K, sh.C
+    lmap = L.orc.local_map.copy()
+    cnt = L.orc.local_count.copy()
+    saw_full = False
+    for t in range(4):
+        qdg = L.qd[t].to(dev)
+        topk = torch.empty((R, Hk, K), dtype=torch.int32, device=dev)
+        eng.oasis_score_topk(0, t, qdg, topk)
+        aid = torch.empty((R, Hk, C), dtype=torch.int32, device=dev)
+        asl, evi = torch.empty_like(aid), torch.empty_like(aid)
+        nad = torch.empty((R, Hk), dtype=torch.int32, device=dev)
+        eng.oasis_admit_evict(0, t, topk, aid, asl, evi, nad)
+        eng.oasis_prefetch(0, t, aid, asl, nad)
+        full = False
+        try:
+            eng.oasis_sync()
+        except OasisError as e:
+            assert f"0x{DEVERR_NOT_LOCAL:x}" in str(e)
+            full = True
+        a, n = aid.cpu().numpy(), nad.cpu().numpy()
+        want_full = False
+        for r in range(R):
+            for h in range(Hk):
+                c1 = cnt[r, h:h + 1].copy()
+                mi, ms, f = oracle.remote_fetch_rh(a[r, h, :n[r, h]], lmap[r, h], c1, cap)
+                cnt[r, h] = c1[0]
+                want_full |= f
+                assert L.remote["n_miss"][r, h].item() == len(mi)
+                assert (L.remote["miss_ids"][r, h, :len(mi)].numpy() == mi).all()
+        assert full == want_full
+        saw_full |= full
+        assert (L.remote["local_map"].cpu().numpy() == lmap).all()
+        assert (L.remote["local_count"].cpu().numpy() == cnt).all()
+    assert saw_full
+    eng.close()
+
+
+def test_remote_throttle_and_append_refused(dev):
+    sh = dataclasses.replace(TINY, R=2)
+    gbps = 0.25
+    L = H.make_layer(sh, seed=15, steps=3, fetch_ratio=0.25, remote_capacity=sh.NBmax,
+                     remote_gbps=gbps)
+    for t in range(3):
+        H.run_staged_step(L, t, dev)
+    st = L.eng.oasis_remote_stats(0)
+    assert st["transfers"] == 4   # the load, then one per step
+    assert st["units"] == int(L.orc.local_count.sum())
+    assert st["seconds"] >= st["units"] * 8192 / (gbps * 1e9) * 0.999
+    k = torch.zeros((sh.R, sh.Hkv, 128), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(OasisError) as e:
+        L.eng.oasis_append_token(0, 3, k, k)
+    assert e.value.status == OASIS_ESTATE
+    L.eng.close()
