@@ -320,9 +320,12 @@ OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
  * tier into HBM.  Local slots are assigned in list order (admission rank
  * order) from 0 upwards.  Summaries are built from the remote store (they are
  * shipped with the request).  The network transfer remote -> local is done on
- * the host, as a NIC's DMA would be, by a CUDA host callback ordered between
- * the slot assignment and the gather on the gather's stream, optionally
- * throttled to `gbps`; it moves no data through the GPU.
+ * the host, as a NIC's DMA would be: a CUDA host callback on the context's
+ * network stream, after the slot assignment, copies the listed units with a
+ * pool of `threads` host threads, optionally throttled to `gbps`; it moves no
+ * data through the GPU.  The gather then runs in two launches on its stream:
+ * the admitted units already held locally at once, beside the transfer, and
+ * the units just fetched once the transfer has ended.
  *
  * With a remote tier attached to a layer, host_kv (given to oasis_init) is the
  * remote store, pinned and mapped as before; oasis_append_token is refused
@@ -331,7 +334,8 @@ OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
  * Layouts:
  *   local_tier pinned [R][Hkv][capacity][2][B][d]   bf16   local slots
  *   local_map  dev    [R][Hkv][NBmax] int32 (local slot of each block, -1 =
- *                     not held) followed by [R][Hkv] int32 (slots in use)
+ *                     not held), then [R][Hkv] int32 (slots in use), then
+ *                     [R][Hkv] int32 (slots in use before the last assignment)
  *   miss_lists pinned [R][Hkv] int32 n_miss, then [R][Hkv][M] int32 ids, then
  *                     [R][Hkv][M] int32 slots, M = max(K, C): the blocks the
  *                     last slot assignment of each (r, h) fetched, in order

@@ -83,9 +83,10 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs
     }
     const int src_slot = a.local_map ? a.local_map[static_cast<size_t>(pair) * a.NBmax + id] : id;
     if (src_slot < 0 || src_slot >= a.src_units) {
-      if (lane == 0) raise_error(a.err, kErrNotLocal);
+      if (lane == 0 && a.phase != 2) raise_error(a.err, kErrNotLocal);
       continue;
     }
+    if (a.phase != 0 && (a.phase == 1) == (src_slot >= a.base[pair])) continue;
     const uint4* src = static_cast<const uint4*>(a.host) +
                        (static_cast<size_t>(pair) * a.src_units + src_slot) * (kUnitBytes / 16);
     uint4* dst = static_cast<uint4*>(a.pool) +
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(kRemoteWarps * 32) remote_assign_kernel(const 
   const int pair = a.pair0 + local;
   const size_t base_map = static_cast<size_t>(pair) * a.NBmax;
   int count = a.count[pair];
+  if (lane == 0) a.base[pair] = count;
   int n = a.items;
   if (a.n_valid) n = min(max(a.n_valid[pair], 0), a.items);
   int nm = 0;

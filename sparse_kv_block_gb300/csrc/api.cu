@@ -6,11 +6,14 @@
 #include <atomic>
 #include <chrono>
 #include <cmath>
+#include <condition_variable>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <map>
 #include <memory>
+#include <mutex>
 #include <string>
 #include <thread>
 #include <tuple>
@@ -37,27 +40,88 @@ struct RemoteStats {
   std::atomic<int64_t> units{0}, transfers{0}, bad{0}, nanos{0};
 };
 
+// Persistent host copy threads of one remote tier.  run(n, f) calls
+// f(lo, hi) over [0, n) in chunks claimed from an atomic counter by the
+// workers and the calling thread, and returns when all chunks are done.
+class CopyPool {
+ public:
+  explicit CopyPool(int threads) {
+    for (int i = 1; i < threads; ++i) th_.emplace_back([this] { loop(); });
+  }
+  ~CopyPool() {
+    {
+      std::lock_guard<std::mutex> g(m_);
+      stop_ = true;
+    }
+    cv_.notify_all();
+    for (auto& t : th_) t.join();
+  }
+  void run(size_t n, const std::function<void(size_t, size_t)>& f) {
+    std::lock_guard<std::mutex> one(run_m_);
+    if (th_.empty() || n <= kChunk) {
+      f(0, n);
+      return;
+    }
+    {
+      std::lock_guard<std::mutex> g(m_);
+      f_ = &f;
+      n_ = n;
+      next_ = 0;
+      busy_ = th_.size();
+      ++gen_;
+    }
+    cv_.notify_all();
+    work();
+    std::unique_lock<std::mutex> l(m_);
+    done_.wait(l, [this] { return busy_ == 0; });
+    f_ = nullptr;
+  }
+
+ private:
+  static constexpr size_t kChunk = 8;  // units (64 KiB) per claim
+  void work() {
+    for (;;) {
+      const size_t k = next_.fetch_add(kChunk);
+      if (k >= n_) return;
+      (*f_)(k, std::min(k + kChunk, n_));
+    }
+  }
+  void loop() {
+    uint64_t seen = 0;
+    for (;;) {
+      {
+        std::unique_lock<std::mutex> l(m_);
+        cv_.wait(l, [&] { return stop_ || gen_ != seen; });
+        if (stop_) return;
+        seen = gen_;
+      }
+      work();
+      std::lock_guard<std::mutex> g(m_);
+      if (--busy_ == 0) done_.notify_one();
+    }
+  }
+  std::vector<std::thread> th_;
+  std::mutex m_, run_m_;
+  std::condition_variable cv_, done_;
+  const std::function<void(size_t, size_t)>* f_ = nullptr;
+  size_t n_ = 0;
+  std::atomic<size_t> next_{0};
+  size_t busy_ = 0;
+  uint64_t gen_ = 0;
+  bool stop_ = false;
+};
+
 struct RemoteJob {
   const uint8_t* remote = nullptr;  // [pairs][NBmax] units
   uint8_t* local = nullptr;         // [pairs][capacity] units
   const int32_t* n_miss = nullptr;  // host view of the lists
   const int32_t* miss_ids = nullptr;
   const int32_t* miss_slots = nullptr;
-  int pair0 = 0, pairs = 0, M = 0, NBmax = 0, capacity = 0, threads = 1;
+  int pair0 = 0, pairs = 0, M = 0, NBmax = 0, capacity = 0;
   double gbps = 0.0;
   RemoteStats* stats = nullptr;
+  CopyPool* pool = nullptr;
 };
-
-void remote_copy_range(const RemoteJob& j, const std::vector<std::pair<int, int>>& items,
-                       size_t lo, size_t hi) {
-  for (size_t k = lo; k < hi; ++k) {
-    const int p = items[k].first, i = items[k].second;
-    const size_t li = static_cast<size_t>(p) * j.M + i;
-    std::memcpy(j.local + (static_cast<size_t>(p) * j.capacity + j.miss_slots[li]) * kUnitBytes,
-                j.remote + (static_cast<size_t>(p) * j.NBmax + j.miss_ids[li]) * kUnitBytes,
-                kUnitBytes);
-  }
-}
 
 void CUDART_CB remote_transfer(void* arg) {
   const RemoteJob& j = *static_cast<const RemoteJob*>(arg);
@@ -81,17 +145,15 @@ void CUDART_CB remote_transfer(void* arg) {
     }
   }
   const size_t n = items.size();
-  const int nt = static_cast<int>(std::min<size_t>(j.threads, (n + 63) / 64));
-  if (nt <= 1) {
-    remote_copy_range(j, items, 0, n);
-  } else {
-    std::vector<std::thread> pool;
-    for (int t = 1; t < nt; ++t)
-      pool.emplace_back(remote_copy_range, std::cref(j), std::cref(items), n * t / nt,
-                        n * (t + 1) / nt);
-    remote_copy_range(j, items, 0, n / nt);
-    for (auto& th : pool) th.join();
-  }
+  j.pool->run(n, [&](size_t lo, size_t hi) {
+    for (size_t k = lo; k < hi; ++k) {
+      const int p = items[k].first, i = items[k].second;
+      const size_t li = static_cast<size_t>(p) * j.M + i;
+      std::memcpy(j.local + (static_cast<size_t>(p) * j.capacity + j.miss_slots[li]) * kUnitBytes,
+                  j.remote + (static_cast<size_t>(p) * j.NBmax + j.miss_ids[li]) * kUnitBytes,
+                  kUnitBytes);
+    }
+  });
   if (j.gbps > 0.0) {
     const double sec = static_cast<double>(n) * kUnitBytes / (j.gbps * 1e9);
     std::this_thread::sleep_until(t0 + std::chrono::duration_cast<std::chrono::steady_clock::duration>(
@@ -110,11 +172,19 @@ struct RemoteTier {
   uint8_t* local = nullptr;       // caller's pinned local tier
   void* local_dev = nullptr;      // its device mapping
   int32_t* map = nullptr;         // dev [pairs][NBmax]
-  int32_t* count = nullptr;       // dev [pairs]
+  int32_t* count = nullptr;       // dev [pairs]: slots in use
+  int32_t* base = nullptr;        // dev [pairs]: slots in use before the last assignment
   int32_t* lists = nullptr;       // caller's pinned miss lists
   int32_t* lists_dev = nullptr;   // their device mapping
+  cudaEvent_t ev_assigned = nullptr;
+  cudaEvent_t ev_moved = nullptr;
   RemoteStats stats;
+  std::unique_ptr<CopyPool> pool;
   std::map<std::tuple<int, int, int>, std::unique_ptr<RemoteJob>> jobs;
+  ~RemoteTier() {
+    if (ev_assigned) cudaEventDestroy(ev_assigned);
+    if (ev_moved) cudaEventDestroy(ev_moved);
+  }
 };
 
 struct LayerState {
@@ -253,6 +323,7 @@ struct oasis_ctx {
   cudaStream_t side = nullptr;   // scan + top-K + admission
   cudaStream_t side2 = nullptr;  // host -> HBM gathers
   cudaStream_t side3 = nullptr;  // admissions (three-stream schedule only)
+  cudaStream_t net = nullptr;    // remote tier transfers (host callbacks)
   std::string last_error;
   bool prof = false;
   std::vector<ProfPair> prof_pool;
@@ -422,9 +493,9 @@ int run_admit(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t*
   return ctx->cuda(e, "admit_evict launch");
 }
 
-// Remote tier: assign local slots to the listed blocks not yet held, then
-// move them remote -> local on the host (a callback on the same stream), so
-// the gather that follows on `s` finds every block in the local tier.
+// Remote tier: assign local slots to the listed blocks not yet held (on
+// `s`), then move them remote -> local on the host in a callback on the
+// context's network stream; ev_moved marks the end of that transfer.
 int run_remote_fetch(oasis_ctx* ctx, int layer, const int32_t* ids, const int32_t* n_valid,
                      int items, int pair0, int pairs, cudaStream_t s) {
   LayerState& L = ctx->layers[layer];
@@ -435,6 +506,7 @@ int run_remote_fetch(oasis_ctx* ctx, int layer, const int32_t* ids, const int32_
   r.n_valid = n_valid;
   r.local_map = T.map;
   r.count = T.count;
+  r.base = T.base;
   r.n_miss = T.lists_dev;
   r.miss_ids = T.lists_dev + all;
   r.miss_slots = T.lists_dev + all + static_cast<size_t>(all) * T.M;
@@ -460,17 +532,39 @@ int run_remote_fetch(oasis_ctx* ctx, int layer, const int32_t* ids, const int32_
     job->M = T.M;
     job->NBmax = ctx->cfg.max_blocks;
     job->capacity = T.capacity;
-    job->threads = T.threads;
     job->gbps = T.gbps;
     job->stats = &T.stats;
+    job->pool = T.pool.get();
   }
-  return ctx->cuda(cudaLaunchHostFunc(s, remote_transfer, job.get()), "remote transfer callback");
+  if (int rc = ctx->cuda(cudaEventRecord(T.ev_assigned, s), "record assignment")) return rc;
+  if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->net, T.ev_assigned, 0), "net wait")) return rc;
+  if (int rc = ctx->cuda(cudaLaunchHostFunc(ctx->net, remote_transfer, job.get()),
+                         "remote transfer callback"))
+    return rc;
+  return ctx->cuda(cudaEventRecord(T.ev_moved, ctx->net), "record transfer");
+}
+
+// With a remote tier the gather runs in two launches: the units already held
+// in the local tier (slot < base) at once, beside the network transfer, and
+// the units this assignment fetched (slot >= base) after it.
+int launch_gather_split(oasis_ctx* ctx, const LayerState& L, GatherArgs g, cudaStream_t s) {
+  if (!L.remote) {
+    g.phase = 0;
+    return ctx->cuda(launch_gather(g, s), "gather launch");
+  }
+  g.phase = 1;
+  if (int rc = ctx->cuda(launch_gather(g, s), "gather launch (held units)")) return rc;
+  if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.remote->ev_moved, 0), "wait transfer"))
+    return rc;
+  g.phase = 2;
+  return ctx->cuda(launch_gather(g, s), "gather launch (fetched units)");
 }
 
 void gather_source(const oasis_ctx* ctx, const LayerState& L, GatherArgs& g) {
   if (L.remote) {
     g.host = L.remote->local_dev;
     g.local_map = L.remote->map;
+    g.base = L.remote->base;
     g.src_units = L.remote->capacity;
   } else {
     g.host = L.host_dev;
@@ -502,9 +596,9 @@ int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
   g.NBmax = ctx->cfg.max_blocks;
   g.U = ctx->U;
   cudaEvent_t* pe = ctx->prof_begin(3, s);
-  cudaError_t e = launch_gather(g, s);
+  const int rc = launch_gather_split(ctx, L, g, s);
   ctx->prof_end(pe, s);
-  return ctx->cuda(e, "prefetch launch");
+  return rc;
 }
 
 }  // namespace
@@ -688,6 +782,8 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side) cudaStreamDestroy(ctx->side);
   if (ctx->side2) cudaStreamDestroy(ctx->side2);
   if (ctx->side3) cudaStreamDestroy(ctx->side3);
+  ctx->layers.clear();  // remote tiers: copy threads joined, events destroyed
+  if (ctx->net) cudaStreamDestroy(ctx->net);
   delete ctx;
   return OASIS_OK;
 }
@@ -760,7 +856,7 @@ OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step, voi
   g.items = ctx->cfg.topk;
   g.NBmax = ctx->cfg.max_blocks;
   g.U = ctx->U;
-  if (int rc = ctx->cuda(launch_gather(g, s), "load gather launch")) return rc;
+  if (int rc = launch_gather_split(ctx, L, g, s)) return rc;
   L.loaded = true;
   L.side_pending = false;
   return OASIS_OK;
@@ -1055,7 +1151,7 @@ OASIS_API int oasis_remote_query_sizes(const oasis_config* cfg, const oasis_remo
   const size_t pairs = static_cast<size_t>(cfg->num_requests) * cfg->num_kv_heads;
   const size_t M = std::max(cfg->topk, fetch_cap(*cfg));
   out->local_tier_bytes = pairs * rcfg->capacity * kUnitBytes;
-  out->local_map_bytes = (pairs * cfg->max_blocks + pairs) * 4;
+  out->local_map_bytes = (pairs * cfg->max_blocks + 2 * pairs) * 4;
   out->miss_lists_bytes = (pairs + 2 * pairs * M) * 4;
   return OASIS_OK;
 }
@@ -1095,10 +1191,22 @@ OASIS_API int oasis_remote_attach(oasis_ctx* ctx, int layer, const oasis_remote_
   const size_t pairs = static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_kv_heads;
   T->map = local_map;
   T->count = local_map + pairs * ctx->cfg.max_blocks;
+  T->base = T->count + pairs;
+  if (cudaEventCreateWithFlags(&T->ev_assigned, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&T->ev_moved, cudaEventDisableTiming) != cudaSuccess)
+    return ctx->fail(OASIS_ENOMEM, "remote_attach: events");
+  if (!ctx->net) {
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&ctx->net, cudaStreamNonBlocking, hi) != cudaSuccess)
+      return ctx->fail(OASIS_ENOMEM, "remote_attach: network stream");
+  }
+  T->pool.reset(new (std::nothrow) CopyPool(T->threads));
+  if (!T->pool) return ctx->fail(OASIS_ENOMEM, "remote_attach: copy threads");
   if (int rc = ctx->cuda(cudaMemsetAsync(T->map, 0xff, pairs * ctx->cfg.max_blocks * 4, ctx->side2),
                          "clear local map"))
     return rc;
-  if (int rc = ctx->cuda(cudaMemsetAsync(T->count, 0, pairs * 4, ctx->side2), "clear slot counts"))
+  if (int rc = ctx->cuda(cudaMemsetAsync(T->count, 0, 2 * pairs * 4, ctx->side2), "clear slot counts"))
     return rc;
   if (int rc = ctx->cuda(cudaStreamSynchronize(ctx->side2), "remote attach sync")) return rc;
   std::memset(miss_lists, 0, pairs * 4);

@@ -69,6 +69,10 @@ struct GatherArgs {
   // slots per pair and block id b of pair p is read from slot
   // local_map[p*NBmax + b]; otherwise src_units = NBmax and slot = b.
   const int32_t* local_map;
+  // phase 0: every item; 1: only items whose local slot < base[p] (held
+  // before the last slot assignment); 2: only the others.
+  const int32_t* base;
+  int phase;
   uint32_t* err;
   int pair0, pairs, items, NBmax, U, src_units;
 };
@@ -77,12 +81,14 @@ struct GatherArgs {
 // ids[p*items + i] (skipped if < 0 or i >= n_valid[p]); every named block
 // without a local slot gets slot count[p]++ (in item order) while
 // count[p] < capacity, and is listed in miss_ids / miss_slots [p][M] with
-// n_miss[p] entries.  The lists may live in mapped host memory.
+// n_miss[p] entries; base[p] receives count[p] before the assignment.  The
+// lists may live in mapped host memory.
 struct RemoteArgs {
   const int32_t* ids;
   const int32_t* n_valid;    // may be null
   int32_t* local_map;        // [R][Hkv][NBmax]
   int32_t* count;            // [R][Hkv]
+  int32_t* base;             // [R][Hkv]
   int32_t* n_miss;           // [R][Hkv]
   int32_t* miss_ids;         // [R][Hkv][M]
   int32_t* miss_slots;       // [R][Hkv][M]

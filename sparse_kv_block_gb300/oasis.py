@@ -320,7 +320,8 @@ class Oasis:
         pairs = R * Hkv
         M = max(self.cfg.topk, self.C)
         t = dict(local_tier=local, local_map=mp[:pairs * NB].view(R, Hkv, NB),
-                 local_count=mp[pairs * NB:].view(R, Hkv), miss_lists=lists,
+                 local_count=mp[pairs * NB:pairs * NB + pairs].view(R, Hkv),
+                 local_base=mp[pairs * NB + pairs:].view(R, Hkv), miss_lists=lists,
                  n_miss=lists[:pairs].view(R, Hkv),
                  miss_ids=lists[pairs:pairs + pairs * M].view(R, Hkv, M),
                  miss_slots=lists[pairs + pairs * M:].view(R, Hkv, M))

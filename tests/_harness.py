@@ -89,6 +89,9 @@ def check_remote(L: Layer, misses: dict):
         assert (ms[r, h, :n] == v["miss_slots"]).all(), (r, h)
     lmap = T["local_map"].cpu().numpy()
     cnt = T["local_count"].cpu().numpy()
+    base = T["local_base"].cpu().numpy()
+    for (r, h) in misses:
+        assert base[r, h] == cnt[r, h] - n_miss[r, h], (r, h)
     local = workload.bf16_bits(T["local_tier"])
     for (r, h) in misses:
         assert (lmap[r, h] == L.orc.local_map[r, h]).all(), (r, h)
