@@ -49,8 +49,8 @@ int orc_summary_build(const uint16_t* host_kv, const int32_t* ctx_len, int R,
 
 /* Sparse attention of one (request r, KV head h) over its resident blocks,
  * for the normal query and the draft query of each of the G query heads of
- * the group ([R] *What carries the argument*: one attention pass serves both
- * tokens over the same resident sparse set).
+ * the group ([R] *What carries the argument*: one attention pass handles the
+ * normal and the draft token, both reading the one resident block set).
  * out[2][G][d] (fp32): out[0] for q, out[1] for the draft query. */
 int orc_attention_rh(const uint16_t* host_kv, const int32_t* ctx_len,
                      const int32_t* res, const uint16_t* q, const uint16_t* qd,

@@ -2,9 +2,10 @@
 // (request, KV head) by one warp (step a4), shared by the stand-alone admit
 // kernel and the tail of the fused score + top-K + admit kernel.
 //
-// "Pith review of OasisKV", section "What carries the argument": a
-// capped-eviction policy pairs each admitted nonresident block with a
-// least-recently-selected resident block so per-step traffic is bounded.
+// "Pith review of OasisKV", section "What carries the argument": eviction is
+// capped, and every block admitted from outside the resident set replaces
+// the resident block selected least recently, which bounds the traffic of a
+// step.
 // Reading of the pages: (i) stamp re-selected residents with the step;
 // (ii) missing top-K blocks in rank order; (iii) eviction candidates = slots
 // whose block is not selected, empty first, then (stamp, block id, slot)

@@ -2,8 +2,8 @@
 //
 // One shared pass serves the normal and the draft query of every query head
 // of a KV head over that head's resident blocks ("Pith review of OasisKV",
-// section "What carries the argument": one shared attention kernel processes
-// the normal token and the draft token over the same resident sparse KV set).
+// section "What carries the argument": a single attention kernel handles both
+// tokens of a decode step, reading one resident block set for the two).
 //
 // GB300 mapping.  One CTA per (request, KV head); four warps, each streaming
 // its own share of the resident units through a private two-deep ring of

@@ -3,9 +3,9 @@
 // The draft query scores every logical block of its request from the
 // per-block min/max key summaries and the blocks are ranked head-wise
 // ("Pith review of OasisKV", section "What carries the argument": the draft
-// query scans compressed key summaries, coordinate-wise min/max per block in
-// the style of Quest, and produces a head-wise top-K ranking of all logical
-// blocks without restoring any keys).
+// query is scored against Quest-style per-block minima and maxima of the
+// keys, and every logical block is ranked per KV head from those summaries
+// alone; the full keys are never read).
 //
 // Score of block b for KV head h (group = the G query heads of h):
 //   s[b] = sum_j sum_i max(qd_ji * mn_bi, qd_ji * mx_bi).
