@@ -1059,10 +1059,9 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
   if (!L.loaded) return ctx->fail(OASIS_ESTATE, "layer %d: oasis_load_resident first", layer);
   if (int rc = ctx->set_device()) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The side work of the previous step still reads the staged draft query.
-  if (L.side_pending) {
-    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
-  }
+  // The staging buffers are read only by work on `stream` (the attention and
+  // oasis_step's copy of q_draft into its ring), so the copies below need no
+  // wait for the previous step's side work.
   const size_t qb = static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_q_heads * kHeadDim * 2;
   const size_t ob = qb * (ctx->cfg.out_fp32 ? 2 : 1);
   if (int rc = ctx->cuda(cudaMemcpyAsync(L.q_stage, q_host, qb, cudaMemcpyHostToDevice, s), "h2d q"))

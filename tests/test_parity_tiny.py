@@ -123,6 +123,31 @@ def test_host_buffer_step_matches_device_step(dev):
     eng.close()
 
 
+def test_host_buffer_steps_back_to_back(dev):
+    # oasis_step_host issued for consecutive steps with no host wait between
+    # them: step t + 1's input copies may overlap step t's side work.
+    sh = dataclasses.replace(TINY, R=5)
+    L = H.make_layer(sh, seed=9, steps=6, fetch_ratio=0.25, out_fp32=False)
+    eng = L.eng
+
+    def pinned():
+        return torch.empty((sh.R, sh.Hq, 128), dtype=torch.bfloat16, pin_memory=True)
+    bufs = [[pinned() for _ in range(4)] for _ in range(6)]
+    for t in range(6):
+        bufs[t][0].copy_(L.q[t])
+        bufs[t][1].copy_(L.qd[t])
+        eng.oasis_step_host(0, t, *bufs[t])
+    torch.cuda.synchronize()
+    eng.oasis_join(0)
+    eng.oasis_sync()
+    for t in range(6):
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        H.check_attention([bufs[t][2].float().numpy(), bufs[t][3].float().numpy()], ref, sh.G)
+    assert (eng.res_ids[0][6 & 1].cpu().numpy() == L.orc.res).all()
+    H.check_pool(L, 6 & 1)
+    eng.close()
+
+
 def test_device_error_word_on_bad_block_id(dev):
     # An id past the context is reported through oasis_sync, not a fault:
     # the kernels skip it and set a bit in the device error word.
