@@ -167,36 +167,49 @@ def warm_start(eng, shape, q0, dev):
     eng.oasis_sync()
 
 
-def oracle_rate(shape, host, lens, q, qd, budget_s: float, steps_hint: int = 1):
-    """Time the CPU oracle on whole (request, all KV heads) samples.
+def oracle_rate(shape, host, lens, q, qd, budget_s: float, threads: int = 1):
+    """Time the CPU oracle on whole (request, all KV heads) samples, on
+    `threads` host threads at once (each steps its own requests; the oracle's
+    C functions release the interpreter lock).
 
-    Returns (layer-steps/s extrapolated to the whole batch, pairs timed,
-    seconds, sample description)."""
+    Returns (layer-steps/s extrapolated to the whole batch = the sum of the
+    threads' pair-step rates over the batch's pairs, pairs timed, busy
+    seconds summed over threads, sample description)."""
+    import concurrent.futures
     import oracle
     hb = workload.bf16_bits(host)
-    nreq = 1
-    t_pairs, t_sec = 0, 0.0
     res0 = workload.initial_resident(shape, 0, 0, lens)
-    r = 0
-    while t_sec < budget_s:
-        sub = np.ascontiguousarray(hb[r:r + nreq])
-        sl = np.ascontiguousarray(lens[r:r + nreq])
-        summ = oracle.summary_build(sub, sl)
-        orc = oracle.LayerOracle(sub, summ, sl, res0[r:r + nreq], shape.K, shape.C,
-                                 [(0, h) for h in range(shape.Hkv)])
-        qb = np.ascontiguousarray(workload.bf16_bits(q[0][r:r + nreq].cpu().contiguous()))
-        qdb = np.ascontiguousarray(workload.bf16_bits(qd[0][r:r + nreq].cpu().contiguous()))
-        t0 = time.perf_counter()
-        for t in range(steps_hint):
-            orc.step(qb, qdb, t)
-        t_sec += time.perf_counter() - t0
-        t_pairs += shape.Hkv * steps_hint
-        r = (r + 1) % shape.R
-    pairs_per_s = t_pairs / t_sec
+    qb_all = workload.bf16_bits(q[0].cpu().contiguous())
+    qdb_all = workload.bf16_bits(qd[0].cpu().contiguous())
+    oracle.build()
+
+    def worker(k):
+        t_pairs, t_sec, r = 0, 0.0, k % shape.R
+        while t_sec < budget_s:
+            sub = np.ascontiguousarray(hb[r:r + 1])
+            sl = np.ascontiguousarray(lens[r:r + 1])
+            summ = oracle.summary_build(sub, sl)
+            orc = oracle.LayerOracle(sub, summ, sl, res0[r:r + 1], shape.K, shape.C,
+                                     [(0, h) for h in range(shape.Hkv)])
+            qb = np.ascontiguousarray(qb_all[r:r + 1])
+            qdb = np.ascontiguousarray(qdb_all[r:r + 1])
+            t0 = time.perf_counter()
+            orc.step(qb, qdb, 0)
+            t_sec += time.perf_counter() - t0
+            t_pairs += shape.Hkv
+            r = (r + threads) % shape.R
+        return t_pairs, t_sec
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+        res = list(ex.map(worker, range(threads)))
+    pairs_per_s = sum(p / s for p, s in res)
+    t_pairs = sum(p for p, _ in res)
+    t_sec = sum(s for _, s in res)
     rate = pairs_per_s / (shape.R * shape.Hkv)
     desc = (f"oracle_step (attention + summary score + top-K + capped eviction, fp64) on "
             f"{t_pairs} (request, KV head) pair-steps of the {shape.name} layer, "
-            f"{t_sec:.1f} s single-threaded, extrapolated to {shape.R * shape.Hkv} pairs")
+            f"{budget_s:.0f} s on each of {threads} host thread(s) (rates summed), "
+            f"extrapolated to {shape.R * shape.Hkv} pairs")
     return rate, t_pairs, t_sec, desc
 
 
@@ -380,15 +393,21 @@ def run_oasis(args, ws, rank, local):
     link_bytes = adm_units * UNIT_BYTES
 
     # ---------------- end to end: host buffers through oasis_step_host
-    # Two sets of pinned host buffers: the host writes step i's inputs while
-    # the GPU runs step i - 1, and reads step i - 1's outputs once that step
-    # is done (one step of overlap, every copy inside the timed region).
+    # Inputs: the step's queries in pinned host memory (a ring of 8 distinct
+    # steps, filled before timing); each step copies its own inputs to the
+    # device.  Outputs: two pinned sets, the host reading step i - 2's result
+    # once that step has ended while steps i - 1 and i are in flight; every
+    # copy is inside the timed region.
     def pinned():
         return torch.empty((shape.R, shape.Hq, 128), dtype=torch.bfloat16, pin_memory=True)
-    qh, qdh, oh, odh = ([pinned(), pinned()] for _ in range(4))
+    n_in = min(nq, 8)
+    qh = [pinned() for _ in range(n_in)]
+    qdh = [pinned() for _ in range(n_in)]
+    for j in range(n_in):
+        qh[j].copy_(q[j].cpu())
+        qdh[j].copy_(qd[j].cpu())
+    oh, odh = [pinned(), pinned()], [pinned(), pinned()]
     done = [torch.cuda.Event(), torch.cuda.Event()]
-    q_host = q[:min(nq, 8)].cpu()
-    qd_host = qd[:min(nq, 8)].cpu()
     e2e_steps = args.steps
     checksum = 0.0
     barrier(ws)
@@ -402,9 +421,7 @@ def run_oasis(args, ws, rank, local):
         if i >= 2:
             done[b].synchronize()                   # step i - 2 finished: read its result
             checksum += float(oh[b][0, 0, 0])
-        qh[b].copy_(q_host[i % q_host.shape[0]])    # the host-side input of this step
-        qdh[b].copy_(qd_host[i % qd_host.shape[0]])
-        eng.oasis_step_host(0, step, qh[b], qdh[b], oh[b], odh[b], main)
+        eng.oasis_step_host(0, step, qh[i % n_in], qdh[i % n_in], oh[b], odh[b], main)
         done[b].record(main)
         step += 1
     for i in range(max(e2e_steps - 2, 0), e2e_steps):
@@ -483,16 +500,23 @@ def run_oasis(args, ws, rank, local):
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": 2 * R * Hq * 128 * 2,
                     "d2h_bytes_per_step": 2 * R * Hq * 128 * 2,
-                    "note": "oasis_step_host: pinned q/q_draft in, attention outputs out; "
-                            "two host buffer sets, the host fills step i's inputs while "
-                            "step i-1 runs and reads each step's result after it ends"},
+                    "note": "oasis_step_host: each step copies its q/q_draft from pinned "
+                            "host memory (a ring of 8 steps' inputs) and its attention "
+                            "outputs back; the host reads every result once its step ends, "
+                            "two steps in flight"},
             "gpu_launches": int(sum(counts)), "clocks": clk,
             "profiled_pass_ms_per_step": round(ms_prof / args.steps, 5)}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        # The oracle on every host core (its (request, KV head) pairs are
+        # independent), and on one core for reference.
+        ncores = os.cpu_count() or 1
         rate, pairs, sec, desc = oracle_rate(shape, host, lens, q.cpu(), qd.cpu(),
-                                             budget_s=args.cpu_budget)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": desc}
+                                             budget_s=args.cpu_budget / 2, threads=ncores)
+        rate1, _, _, desc1 = oracle_rate(shape, host, lens, q.cpu(), qd.cpu(),
+                                         budget_s=args.cpu_budget / 2, threads=1)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": ncores, "kind": "oracle",
+                                "sample": desc, "single_thread_value": rate1,
+                                "single_thread_sample": desc1}
     if rank == 0:
         print(json.dumps(line), flush=True)
     eng.close()
@@ -503,7 +527,12 @@ def run_oasis_layers(args, ws, rank, local):
     order on one main stream; each layer's side work overlaps the next
     layers.  Host stores are shared by layers l and l + M when the host
     cannot pin one per layer (M = --host-stores); every layer keeps its own
-    summaries, resident pool and tables."""
+    summaries, resident pool and tables, and its queries point at its
+    store's hot blocks.  With hot-block drift (the 36-layer workload), the
+    hot blocks move between steps, untimed: the pipeline is drained, the
+    host stores rewritten, and each layer's summaries and resident copies of
+    the moved blocks refreshed (oasis_refresh_blocks); each step is then
+    timed on its own and the steps' times are summed."""
     from sparse_kv_block_gb300.oasis import Oasis, lib, make_config
     lib()
     dev = torch.device("cuda", local)
@@ -525,7 +554,8 @@ def run_oasis_layers(args, ws, rank, local):
     eng.set_context(lens)
     qs, qds = [], []
     for l in range(L):
-        q, qd = workload.queries(shape, args.seed + rank, l, nq, device=dev)
+        q, qd = workload.queries(shape, args.seed + rank, l, nq, device=dev,
+                                 direction_layer=l % M)
         qs.append(q)
         qds.append(qd)
         eng.oasis_build_summaries(l, 0)
@@ -547,6 +577,40 @@ def run_oasis_layers(args, ws, rank, local):
     if grow:   # a few distinct new tokens, cycled (drawn untimed)
         toks = [workload.new_tokens(shape, args.seed + rank, 0, i, device=dev) for i in range(4)]
 
+    drift = shape.hot_move_prob > 0 and not args.no_hot_drift
+    if drift:
+        hots = [workload.hot_blocks(shape, args.seed + rank, m, lens) for m in range(M)]
+        max_ids = 2 * max(len(x) for row in hots[0] for x in row)
+        ids_h = torch.full((shape.R, shape.Hkv, max_ids), -1, dtype=torch.int32)
+        nid_h = torch.zeros((shape.R, shape.Hkv), dtype=torch.int32)
+        ids_d = [torch.empty((shape.R, shape.Hkv, max_ids), dtype=torch.int32, device=dev)
+                 for _ in range(M)]
+        nid_d = [torch.empty((shape.R, shape.Hkv), dtype=torch.int32, device=dev)
+                 for _ in range(M)]
+    moved = [0]
+
+    def drift_between_steps():
+        """Untimed: drain, move hot blocks in every host store, refresh."""
+        for l in range(L):
+            eng.oasis_join(l, main)
+        main.synchronize()
+        for m in range(M):
+            mv = workload.move_hot_blocks(shape, args.seed + rank, m, step, hots[m], lens)
+            workload.apply_hot_moves(shape, args.seed + rank, m, stores[m], mv, lens)
+            moved[0] += len(mv)
+            ids_h.fill_(-1)
+            nid_h.zero_()
+            for (r, h, old, new) in mv:
+                n = int(nid_h[r, h])
+                ids_h[r, h, n] = old
+                ids_h[r, h, n + 1] = new
+                nid_h[r, h] = n + 2
+            ids_d[m].copy_(ids_h)
+            nid_d[m].copy_(nid_h)
+        for l in range(L):
+            eng.oasis_refresh_blocks(l, step, ids_d[l % M], nid_d[l % M], main)
+        main.synchronize()
+
     def one_step():
         nonlocal step
         for l in range(L):
@@ -562,27 +626,43 @@ def run_oasis_layers(args, ws, rank, local):
 
     for _ in range(args.warmup):
         one_step()
+        if drift:
+            drift_between_steps()
     for l in range(L):
         eng.oasis_join(l, main)
     torch.cuda.synchronize(dev)
     eng.oasis_sync()
+    moved[0] = 0
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     eng.oasis_profile_enable(True)
     barrier(ws)
     torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(main)
-    for _ in range(args.steps):
-        one_step()
-    for l in range(L):
-        eng.oasis_join(l, main)
-    e1.record(main)
-    torch.cuda.synchronize(dev)
+    if drift:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            ev[i][0].record(main)
+            one_step()
+            for l in range(L):
+                eng.oasis_join(l, main)
+            ev[i][1].record(main)
+            drift_between_steps()
+        torch.cuda.synchronize(dev)
+        ms = sum(a.elapsed_time(b) for a, b in ev)
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for _ in range(args.steps):
+            one_step()
+        for l in range(L):
+            eng.oasis_join(l, main)
+        e1.record(main)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
     barrier(ws)
-    ms = e0.elapsed_time(e1)
     ms_sum, counts, off_sum = eng.oasis_profile_read()
     eng.oasis_profile_enable(False)
     clk = clocks.stop()
@@ -611,7 +691,10 @@ def run_oasis_layers(args, ws, rank, local):
             "config": {"workload": workload_desc(shape), "host_stores": M,
                        "note": f"layers l and l+{M} share one pinned host store"
                                + ("; one token appended per request per step (timed)"
-                                  if grow else ""),
+                                  if grow else "")
+                               + (f"; hot blocks moved between steps (untimed, "
+                                  f"{moved[0] / args.steps:.0f} moves per step over "
+                                  f"{M} stores), each step timed alone" if drift else ""),
                        "tokens_per_s": round(value * R / L, 1),
                        "l2": "inputs larger than L2"},
             "roofline": {"bound": "hbm", "kernel": "attention",
@@ -936,6 +1019,8 @@ def main():
                     help="fetch-cap sweep (0.01, 0.05, 0.25, 1.0) on the single-layer shape")
     ap.add_argument("--host-stores", type=int, default=12,
                     help="distinct pinned host stores of a multi-layer workload")
+    ap.add_argument("--no-hot-drift", action="store_true",
+                    help="36-layer workload: keep the hot blocks in place (one timed region)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--queries", type=int, default=64, help="distinct query steps, cycled")
     ap.add_argument("--cpu-budget", type=float, default=12.0)

@@ -302,6 +302,17 @@ OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step,
                                  const void* k_new, const void* v_new,
                                  void* stream);
 
+/* Support: blocks the caller rewrote in `layer`'s host store before step
+ * `step` (a workload whose hot blocks move between steps).  ids: dev
+ * [R][Hkv][max_ids] int32, n_ids: dev [R][Hkv] int32; for every (r, h) and
+ * i < n_ids, block ids[.., i] (< NBmax; -1 = skip) gets its summary rebuilt
+ * over the tokens below ctx_len[step & 1][r] and, if it is resident in table
+ * (step & 1), its pool unit rewritten from the host store.  Runs after the
+ * layer's side work of step - 1.  Refused (OASIS_ESTATE) with a remote tier. */
+OASIS_API int oasis_refresh_blocks(oasis_ctx* ctx, int layer, int step,
+                                   const int32_t* ids, const int32_t* n_ids,
+                                   int max_ids, void* stream);
+
 /* ctx_len[(step + 1) & 1][r] = ctx_len[step & 1][r] + grow for every r. */
 OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
                                     void* stream);

@@ -165,6 +165,45 @@ __global__ void init_tables_kernel(int32_t* phys, int32_t* stamps, int pairs, in
 // Per-block coordinate-wise min/max of the keys over the valid tokens, one
 // warp per (request, KV head, block); lanes 0-15 take even tokens, 16-31 odd
 // tokens, 8 dims per lane; bf16 min/max are exact.
+// Min/max of one block's keys over its `valid` tokens by one warp: lanes
+// 0-15 take even tokens, 16-31 odd tokens, 8 dims per lane; the min row is
+// written by lanes 0-15 and the max row by lanes 16-31.
+__device__ __forceinline__ void warp_block_summary(const uint4* keys, int valid, uint4* dst,
+                                                   int lane) {
+  const int dch = lane & 15;
+  __nv_bfloat162 mn[4], mx[4];
+  const __nv_bfloat162 pinf = __floats2bfloat162_rn(INFINITY, INFINITY);
+  const __nv_bfloat162 ninf = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    mn[i] = pinf;
+    mx[i] = ninf;
+  }
+  for (int tkn = lane >> 4; tkn < valid; tkn += 2) {
+    const uint4 v = keys[tkn * (kHeadDim / 8) + dch];
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      mn[i] = __hmin2(mn[i], p[i]);
+      mx[i] = __hmax2(mx[i], p[i]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t mnb = *reinterpret_cast<uint32_t*>(&mn[i]);
+    uint32_t mxb = *reinterpret_cast<uint32_t*>(&mx[i]);
+    mnb = __shfl_xor_sync(0xffffffffu, mnb, 16);
+    mxb = __shfl_xor_sync(0xffffffffu, mxb, 16);
+    mn[i] = __hmin2(mn[i], *reinterpret_cast<__nv_bfloat162*>(&mnb));
+    mx[i] = __hmax2(mx[i], *reinterpret_cast<__nv_bfloat162*>(&mxb));
+  }
+  uint4 outv;
+  __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(&outv);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = (lane < 16) ? mn[i] : mx[i];
+  dst[(lane >> 4) * (kHeadDim / 8) + dch] = outv;
+}
+
 __global__ void summary_build_kernel(const SummaryArgs a) {
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
@@ -179,39 +218,54 @@ __global__ void summary_build_kernel(const SummaryArgs a) {
     if (valid <= 0) continue;
     const uint4* keys = static_cast<const uint4*>(a.host) +
                         static_cast<size_t>(it) * (kUnitBytes / 16);  // K rows first
-    const int dch = lane & 15;
-    __nv_bfloat162 mn[4], mx[4];
-    const __nv_bfloat162 pinf = __floats2bfloat162_rn(INFINITY, INFINITY);
-    const __nv_bfloat162 ninf = __floats2bfloat162_rn(-INFINITY, -INFINITY);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      mn[i] = pinf;
-      mx[i] = ninf;
+    warp_block_summary(keys, valid, static_cast<uint4*>(a.summ) +
+                                        static_cast<size_t>(it) * (kSummBytes / 16),
+                       lane);
+  }
+}
+
+// Blocks rewritten in the host store: one warp per listed (pair, block)
+// rebuilds the block's summary and, when the block is resident in the given
+// table, copies the new contents into its pool unit.
+__global__ void refresh_kernel(const RefreshArgs a) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  const long long total = static_cast<long long>(a.R) * a.Hkv * a.max_ids;
+  for (long long it = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); it < total;
+       it += warps) {
+    const int pair = static_cast<int>(it / a.max_ids);
+    const int i = static_cast<int>(it - static_cast<long long>(pair) * a.max_ids);
+    if (i >= a.n_ids[pair]) continue;
+    const int b = a.ids[it];
+    if (b < 0) continue;
+    if (b >= a.NBmax) {
+      if (lane == 0) raise_error(a.err, kErrBadBlock);
+      continue;
     }
-    for (int tkn = lane >> 4; tkn < valid; tkn += 2) {
-      const uint4 v = keys[tkn * (kHeadDim / 8) + dch];
-      const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        mn[i] = __hmin2(mn[i], p[i]);
-        mx[i] = __hmax2(mx[i], p[i]);
-      }
+    const int r = pair / a.Hkv;
+    const int valid = min(kBlock, a.ctx_len[r] - b * kBlock);
+    const size_t blk = static_cast<size_t>(pair) * a.NBmax + b;
+    const uint4* src = static_cast<const uint4*>(a.host) + blk * (kUnitBytes / 16);
+    if (valid > 0)
+      warp_block_summary(src, valid, static_cast<uint4*>(a.summ) + blk * (kSummBytes / 16), lane);
+    int slot = -1;
+    for (int s0 = 0; s0 < a.K && slot < 0; s0 += 32) {
+      const int s = s0 + lane;
+      const unsigned hit = __ballot_sync(0xffffffffu, s < a.K && a.res[static_cast<size_t>(pair) * a.K + s] == b);
+      if (hit) slot = s0 + __ffs(hit) - 1;
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t mnb = *reinterpret_cast<uint32_t*>(&mn[i]);
-      uint32_t mxb = *reinterpret_cast<uint32_t*>(&mx[i]);
-      mnb = __shfl_xor_sync(0xffffffffu, mnb, 16);
-      mxb = __shfl_xor_sync(0xffffffffu, mxb, 16);
-      mn[i] = __hmin2(mn[i], *reinterpret_cast<__nv_bfloat162*>(&mnb));
-      mx[i] = __hmax2(mx[i], *reinterpret_cast<__nv_bfloat162*>(&mxb));
+    if (slot < 0) continue;
+    const int unit = a.phys[static_cast<size_t>(pair) * a.U + slot];
+    if (unit < 0 || unit >= a.U) {
+      if (lane == 0) raise_error(a.err, kErrBadUnit);
+      continue;
     }
-    uint4 outv;
-    __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(&outv);
+    uint4* dst = static_cast<uint4*>(a.pool) + (static_cast<size_t>(pair) * a.U + unit) * (kUnitBytes / 16);
+    uint4 v[kUnitBytes / 16 / 32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = (lane < 16) ? mn[i] : mx[i];
-    uint4* dst = static_cast<uint4*>(a.summ) + static_cast<size_t>(it) * (kSummBytes / 16);
-    dst[(lane >> 4) * (kHeadDim / 8) + dch] = outv;
+    for (int j = 0; j < kUnitBytes / 16 / 32; ++j) v[j] = src[j * 32 + lane];
+#pragma unroll
+    for (int j = 0; j < kUnitBytes / 16 / 32; ++j) dst[j * 32 + lane] = v[j];
   }
 }
 
@@ -335,6 +389,15 @@ cudaError_t launch_init_tables(int32_t* phys, int32_t* stamps, int pairs, int K,
 cudaError_t launch_summary_build(const SummaryArgs& a, cudaStream_t s) {
   if (a.R * a.Hkv * a.NBmax == 0) return cudaSuccess;
   summary_build_kernel<<<8 * sm_count(), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_refresh(const RefreshArgs& a, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.R) * a.Hkv * a.max_ids;
+  if (total == 0) return cudaSuccess;
+  long long grid = (total + 7) / 8;
+  if (grid > 8 * sm_count()) grid = 8 * sm_count();
+  refresh_kernel<<<static_cast<int>(grid), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -1124,6 +1124,39 @@ OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step, const void
   return ctx->cuda(launch_append(a, s), "append launch");
 }
 
+OASIS_API int oasis_refresh_blocks(oasis_ctx* ctx, int layer, int step, const int32_t* ids,
+                                   const int32_t* n_ids, int max_ids, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !ids || !n_ids || max_ids < 0)
+    return ctx->fail(OASIS_EINVAL, "refresh: bad argument");
+  if (int rc = ctx->set_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerState& L = ctx->layers[layer];
+  if (L.remote)
+    return ctx->fail(OASIS_ESTATE, "refresh: layer %d has a remote tier attached", layer);
+  // The previous step's gathers write units of table (step & 1).
+  if (L.side_pending) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
+  }
+  RefreshArgs a{};
+  a.host = L.host_dev;
+  a.summ = L.summ;
+  a.pool = L.pool;
+  a.ids = ids;
+  a.n_ids = n_ids;
+  a.ctx_len = ctx->ctx_tab(step);
+  a.res = ctx->res_tab(layer, step);
+  a.phys = ctx->phys_tab(layer, step);
+  a.err = ctx->err;
+  a.R = ctx->cfg.num_requests;
+  a.Hkv = ctx->cfg.num_kv_heads;
+  a.NBmax = ctx->cfg.max_blocks;
+  a.K = ctx->cfg.topk;
+  a.U = ctx->U;
+  a.max_ids = max_ids;
+  return ctx->cuda(launch_refresh(a, s), "refresh launch");
+}
+
 OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow, void* stream) {
   if (!ctx) return OASIS_EINVAL;
   if (step < 0 || grow < 0) return ctx->fail(OASIS_EINVAL, "advance: bad argument");

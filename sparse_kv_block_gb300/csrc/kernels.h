@@ -103,6 +103,22 @@ struct SummaryArgs {
   int R, Hkv, NBmax;
 };
 
+// Blocks the caller rewrote in the host store: for every pair p and
+// i < n_ids[p], block ids[p*max_ids + i] gets its summary rebuilt (tokens
+// below ctx_len[r]) and, if resident in (res, phys), its pool unit rewritten.
+struct RefreshArgs {
+  const void* host;          // device alias of the pinned store
+  void* summ;
+  void* pool;
+  const int32_t* ids;        // [R][Hkv][max_ids]
+  const int32_t* n_ids;      // [R][Hkv]
+  const int32_t* ctx_len;    // [R]
+  const int32_t* res;        // [R][Hkv][K]
+  const int32_t* phys;       // [R][Hkv][U]
+  uint32_t* err;
+  int R, Hkv, NBmax, K, U, max_ids;
+};
+
 struct AppendArgs {
   const void* k_new;         // [R][Hkv][d]
   const void* v_new;
@@ -126,11 +142,12 @@ cudaError_t launch_init_tables(int32_t* phys, int32_t* stamps, int pairs,
                                int K, int U, cudaStream_t s);
 cudaError_t launch_summary_build(const SummaryArgs& a, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_refresh(const RefreshArgs& a, cudaStream_t s);
 cudaError_t launch_advance(const int32_t* cur, int32_t* nxt, int R, int grow,
                            cudaStream_t s);
 
 size_t attention_smem_bytes();
-size_t score_topk_smem_bytes(int K);
+size_t score_topk_smem_bytes(int K, int NBmax);
 
 // Largest NBmax the fused score + admit kernel can hold in shared memory.
 constexpr int kMaxBlocksPerHead = 131072;

@@ -16,12 +16,17 @@
 // scan is a pure HBM stream.
 //
 // GB300 mapping.  One CTA per (request, KV head): a producer warp streams the
-// request's contiguous summary rows through a 2-deep ring of 16 KiB stages
-// with 1-D bulk copies; eight consumer warps each score 4 blocks per stage
-// (one 16-byte load per lane per block, packed fp32x2 multiply-adds,
-// transposed shuffle reduction), keep a running top-KP list in registers
-// (bitonic sort of each filled buffer of KP keys, then a bitonic merge), and
-// finally merge their lists in a tree.
+// request's contiguous summary rows through a 2-deep ring of stages (4
+// blocks per consumer warp, 2 KiB) with 1-D bulk copies; CW consumer warps
+// each score 4 blocks per stage (one 16-byte load per lane per block, packed
+// fp32x2 multiply-adds, transposed shuffle reduction), keep a running top-KP
+// list in registers (bitonic sort of each filled buffer of KP keys, then a
+// bitonic merge), and finally merge their lists in a tree.  Shared memory is
+// sized from the actual NBmax (the fused admission reuses the ring).  CW = 8
+// (16 KiB stages, 4 CTAs per SM) by default; CW = 4 (8 KiB stages, ~21 KB and
+// 48 registers per thread: 8 CTAs per SM, a 128-request x 8-head layer in one
+// wave) is faster alone on GB300 (92 vs 98 us) but slower inside the step,
+// beside the host-link gather (129 vs 120 us; 2872 vs 3108 layer-steps/s).
 // Keys are 64-bit: order-preserving score bits above the complemented block
 // id, so ties break to the lower id and all keys are distinct.
 #include <cstdlib>
@@ -34,35 +39,39 @@
 namespace oasis {
 namespace {
 
-constexpr int kCW = 8;                       // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;     // + one producer warp
-constexpr int kChunk = 32;                   // blocks per stage
-constexpr int kChunkBytes = kChunk * kSummBytes;  // 16 KiB
-constexpr int kAdmitScratch = sizeof(AdmitWarpSmem) + 2 * 4 * (kMaxBlocksPerHead / 32);
+constexpr int kStages = 2;                   // ring depth
 
-// Shared memory: the ring of ST stages (reused by the fused admission once
-// every stage has been consumed, so at least kAdmitScratch bytes), the
-// stage barriers, and the per-warp key buffers.
-template <int KPL, int ST>
+// Shared memory: the ring of kStages stages (reused by the fused admission
+// once every stage has been consumed, so at least the admission's scratch
+// for this NBmax), the stage barriers, and the per-warp key buffers.  The
+// same arithmetic runs on the host (launch size) and in the kernel.
+template <int KPL, int CW>
 struct Layout {
   static constexpr int KP = 32 * KPL;
-  static constexpr int ring = 0;
-  static constexpr int bars =
-      ((ST * kChunkBytes > kAdmitScratch ? ST * kChunkBytes : kAdmitScratch) + 127) / 128 * 128;
-  static constexpr int keys = bars + 64;     // [kCW][KP] uint64
-  static constexpr int total = keys + kCW * KP * 8 + 128;
+  static constexpr int kChunk = 4 * CW;                    // blocks per stage
+  static constexpr int kChunkBytes = kChunk * kSummBytes;  // 2 KiB per warp
+  __host__ __device__ static int bars(int NBmax) {
+    const size_t ring = static_cast<size_t>(kStages) * kChunkBytes;
+    const size_t adm = admit_warp_smem_bytes(NBmax);
+    return static_cast<int>(((ring > adm ? ring : adm) + 127) / 128 * 128);
+  }
+  __host__ __device__ static int keys(int NBmax) { return bars(NBmax) + 64; }  // [CW][KP] u64
+  __host__ __device__ static int total(int NBmax) { return keys(NBmax) + CW * KP * 8 + 128; }
 };
 
-template <int KPL, int kStages>
-__global__ void __launch_bounds__(kThreads)
+template <int KPL, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32)
     score_topk_kernel(const ScoreArgs a) {
-  using L = Layout<KPL, kStages>;
+  using L = Layout<KPL, CW>;
   constexpr int KP = L::KP;
+  constexpr int kCW = CW;
+  constexpr int kChunk = L::kChunk;
+  constexpr int kChunkBytes = L::kChunkBytes;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem + L::ring;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars);
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars(a.NBmax));
   uint64_t* empty = full + kStages;
-  uint64_t* keybuf = reinterpret_cast<uint64_t*>(smem + L::keys);
+  uint64_t* keybuf = reinterpret_cast<uint64_t*>(smem + L::keys(a.NBmax));
 
   const int pair = a.pair0 + blockIdx.x;
   const int r = pair / a.Hkv;
@@ -266,47 +275,48 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int KPL, int ST>
-cudaError_t launch_kpl_st(const ScoreArgs& a, cudaStream_t s) {
+template <int KPL, int CW>
+cudaError_t launch_kpl_cw(const ScoreArgs& a, cudaStream_t s) {
+  if (a.pairs <= 0) return cudaSuccess;
+  const int smem = Layout<KPL, CW>::total(a.NBmax);
   static int configured_device = -1;
+  static int configured_smem = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(score_topk_kernel<KPL, ST>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Layout<KPL, ST>::total);
+  if (configured_device != dev || smem > configured_smem) {
+    e = cudaFuncSetAttribute(score_topk_kernel<KPL, CW>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured_device = dev;
+    configured_smem = smem;
   }
-  if (a.pairs <= 0) return cudaSuccess;
-  score_topk_kernel<KPL, ST><<<a.pairs, kThreads, Layout<KPL, ST>::total, s>>>(a);
+  score_topk_kernel<KPL, CW><<<a.pairs, (CW + 1) * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-// Ring depth: 2 stages by default (~49 KB of shared memory, 4 CTAs per SM:
-// measured 100 us alone on the 128 x 16K layer against 105 us with 3 stages
-// and 3 CTAs per SM); OASIS_SCAN_STAGES=3 is a tuning override.
-int scan_stages() {
-  static const int st = [] {
-    const char* e = std::getenv("OASIS_SCAN_STAGES");
-    return (e && std::atoi(e) == 3) ? 3 : 2;
+// Consumer warps per CTA: 8 by default; OASIS_SCAN_WARPS=4 is a tuning
+// override (see the file comment for the measurements).
+int scan_warps() {
+  static const int cw = [] {
+    const char* e = std::getenv("OASIS_SCAN_WARPS");
+    return (e && std::atoi(e) == 4) ? 4 : 8;
   }();
-  return st;
+  return cw;
 }
 
 template <int KPL>
 cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
-  return scan_stages() == 2 ? launch_kpl_st<KPL, 2>(a, s) : launch_kpl_st<KPL, 3>(a, s);
+  return scan_warps() == 4 ? launch_kpl_cw<KPL, 4>(a, s) : launch_kpl_cw<KPL, 8>(a, s);
 }
 
 }  // namespace
 
-size_t score_topk_smem_bytes(int K) {
-  if (K <= 32) return Layout<1, 3>::total;
-  if (K <= 64) return Layout<2, 3>::total;
-  if (K <= 128) return Layout<4, 3>::total;
-  return Layout<8, 3>::total;
+size_t score_topk_smem_bytes(int K, int NBmax) {
+  if (K <= 32) return Layout<1, 8>::total(NBmax);
+  if (K <= 64) return Layout<2, 8>::total(NBmax);
+  if (K <= 128) return Layout<4, 8>::total(NBmax);
+  return Layout<8, 8>::total(NBmax);
 }
 
 cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s) {

@@ -91,6 +91,7 @@ EXPORTS = {
                                  POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
                                  POINTER(c_void_p)]),
     "oasis_append_token": (c_int, [_P, c_int, c_int, _P, _P, _P]),
+    "oasis_refresh_blocks": (c_int, [_P, c_int, c_int, _P, _P, c_int, _P]),
     "oasis_advance_context": (c_int, [_P, c_int, c_int, _P]),
     "oasis_remote_query_sizes": (c_int, [POINTER(oasis_config), POINTER(oasis_remote_config),
                                          POINTER(oasis_remote_sizes)]),
@@ -295,6 +296,11 @@ class Oasis:
     def oasis_append_token(self, layer, step, k_new, v_new, stream=None) -> None:
         self._check(lib().oasis_append_token(self.ctx, layer, step, _ptr(k_new), _ptr(v_new),
                                              _stream(stream)))
+
+    def oasis_refresh_blocks(self, layer, step, ids, n_ids, stream=None) -> None:
+        """ids: int32 [R][Hkv][max_ids] (device), n_ids: int32 [R][Hkv] (device)."""
+        self._check(lib().oasis_refresh_blocks(self.ctx, layer, step, _ptr(ids), _ptr(n_ids),
+                                               int(ids.shape[-1]), _stream(stream)))
 
     def oasis_advance_context(self, step, grow=1, stream=None) -> None:
         self._check(lib().oasis_advance_context(self.ctx, step, grow, _stream(stream)))

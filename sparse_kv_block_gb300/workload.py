@@ -158,8 +158,10 @@ def host_kv(shape: Shape, seed: int, layer: int, lens: np.ndarray,
 
 
 def queries(shape: Shape, seed: int, layer: int, steps: int,
-            device="cpu") -> tuple:
-    """(q, qd) for `steps` consecutive steps: [steps][R][Hq][d] bf16 each."""
+            device="cpu", direction_layer: Optional[int] = None) -> tuple:
+    """(q, qd) for `steps` consecutive steps: [steps][R][Hq][d] bf16 each.
+    The query mean points along the head directions of `direction_layer`
+    (default `layer`): the layer whose host store the queries read."""
     R, Hq, d, G = shape.R, shape.Hq, shape.d, shape.G
     g = _gen(device, seed, layer, 4)
     z = torch.randn((steps + 1, R, Hq, d), generator=g, device=device)
@@ -168,12 +170,57 @@ def queries(shape: Shape, seed: int, layer: int, steps: int,
         q = z[:steps]
         qd = q + shape.draft_sigma * e
     else:
-        u = head_directions(shape, seed, layer).to(device)
+        u = head_directions(shape, seed, layer if direction_layer is None
+                            else direction_layer).to(device)
         mean = (shape.q_mean * u).repeat_interleave(G, dim=0)  # [Hq][d]
         rho = shape.draft_corr
         q = mean + z[:steps]
         qd = mean + rho * z[1:] + math.sqrt(1.0 - rho * rho) * e
     return q.to(torch.bfloat16), qd.to(torch.bfloat16)
+
+
+def move_hot_blocks(shape: Shape, seed: int, layer: int, step: int, hot: list,
+                    lens: np.ndarray) -> list:
+    """Drift of the planted structure between two steps: every hot block of
+    every (r, h) moves, with probability hot_move_prob, to a block drawn
+    uniformly from the request's blocks that are not hot.  Updates `hot` in
+    place and returns the moves as (r, h, old, new) tuples."""
+    rng = np.random.default_rng([seed, layer, 7, step])
+    moves = []
+    for r in range(shape.R):
+        nb = -(-int(lens[r]) // shape.B) if lens[r] > 0 else 0
+        for h in range(shape.Hkv):
+            ids = hot[r][h]
+            if len(ids) == 0 or len(ids) >= nb:
+                continue
+            go = np.nonzero(rng.random(len(ids)) < shape.hot_move_prob)[0]
+            for k in go:
+                taken = set(int(x) for x in ids)
+                new = int(rng.integers(0, nb))
+                while new in taken:
+                    new = int(rng.integers(0, nb))
+                moves.append((r, h, int(ids[k]), new))
+                ids[k] = new
+    return moves
+
+
+def apply_hot_moves(shape: Shape, seed: int, layer: int, store: torch.Tensor,
+                    moves: list, lens: np.ndarray) -> None:
+    """Rewrite the keys of moved hot blocks in a host store: the old block
+    loses the hot_shift * u_h offset, the new block gains it (valid tokens
+    only; tokens past the context stay zero)."""
+    if not moves:
+        return
+    u = head_directions(shape, seed, layer)
+    m = torch.as_tensor(moves, dtype=torch.int64)
+    r, h, old, new = m[:, 0], m[:, 1], m[:, 2], m[:, 3]
+    tok = torch.arange(shape.B)
+    L = torch.as_tensor(lens, dtype=torch.int64)
+    for blk, sign in ((old, -1.0), (new, 1.0)):
+        valid = (blk[:, None] * shape.B + tok[None, :]) < L[r][:, None]      # [n][B]
+        x = store[r, h, blk, 0].float()                                       # [n][B][d]
+        x += sign * shape.hot_shift * u[h][:, None, :] * valid[:, :, None]
+        store[r, h, blk, 0] = x.to(torch.bfloat16)
 
 
 def initial_resident(shape: Shape, seed: int, layer: int,
