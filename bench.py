@@ -157,6 +157,31 @@ def build_layer(shape, seed, dev, side_groups=0, schedule=0):
     return eng, lens, host
 
 
+class _DeviceView:
+    """__cuda_array_interface__ of a pinned host tensor at its device address."""
+
+    def __init__(self, t: torch.Tensor, dev_ptr: int):
+        self.__cuda_array_interface__ = {"shape": (t.numel(),), "typestr": "<i2",
+                                         "data": (dev_ptr, False), "version": 2,
+                                         "strides": None}
+
+
+def pinned_device_alias(t: torch.Tensor, dev) -> torch.Tensor:
+    """A CUDA tensor over a pinned host bf16 tensor's memory (its device
+    mapping), so torch kernels read and write it over the host link."""
+    from sparse_kv_block_gb300.oasis import lib
+    import ctypes
+    fn = lib().cudaHostGetDevicePointer
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p, ctypes.c_uint]
+    p = ctypes.c_void_p()
+    if fn(ctypes.byref(p), ctypes.c_void_p(t.data_ptr()), 0) != 0 or not p.value:
+        raise RuntimeError("store is not mapped page-locked memory")
+    with torch.cuda.device(dev):
+        flat = torch.as_tensor(_DeviceView(t, p.value), device=dev)
+    return flat.view(torch.bfloat16).view(t.shape)
+
+
 def warm_start(eng, shape, q0, dev):
     """Resident set = the summary-ranked top-K of the first query (warm cache)."""
     topk = torch.empty((shape.R, shape.Hkv, shape.K), dtype=torch.int32, device=dev)
@@ -589,6 +614,14 @@ def run_oasis_layers(args, ws, rank, local):
                  for _ in range(M)]
     moved = [0]
 
+    if drift:
+        # The moved blocks are rewritten by GPU kernels through the stores'
+        # device mappings: CPU stores would leave the lines dirty in the host
+        # caches, and the next steps' gathers of those blocks (they are the
+        # new hot blocks, soon admitted) then run at about half speed
+        # (measured: 2082 against 3127 layer-steps/s without rewriting).
+        views = [pinned_device_alias(st, dev) for st in stores]
+
     def drift_between_steps():
         """Untimed: drain, move hot blocks in every host store, refresh."""
         for l in range(L):
@@ -596,7 +629,8 @@ def run_oasis_layers(args, ws, rank, local):
         main.synchronize()
         for m in range(M):
             mv = workload.move_hot_blocks(shape, args.seed + rank, m, step, hots[m], lens)
-            workload.apply_hot_moves(shape, args.seed + rank, m, stores[m], mv, lens)
+            with torch.cuda.stream(main):
+                workload.apply_hot_moves(shape, args.seed + rank, m, views[m], mv, lens)
             moved[0] += len(mv)
             ids_h.fill_(-1)
             nid_h.zero_()

@@ -275,9 +275,12 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
 OASIS_API int oasis_join(oasis_ctx* ctx, int layer, void* stream);
 
 /* oasis_step with host buffers: q/q_draft are copied from (pinned) host
- * memory into the workspace, the step runs, and out/out_draft are copied back
- * to host memory, all on `stream`.  Host buffers must stay valid until the
- * stream reaches the copies. */
+ * memory into a workspace slot of the step's parity on the context's input
+ * stream (after the slot's previous reader, step - 2, is done, so the copies
+ * can overlap the previous step), `stream` waits for them, the step runs, and
+ * out/out_draft are copied back to host memory on `stream`.  Everything is
+ * complete when `stream` passes the call; host buffers must stay valid until
+ * then. */
 OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step,
                               const void* q_host, const void* q_draft_host,
                               void* out_host, void* out_draft_host,

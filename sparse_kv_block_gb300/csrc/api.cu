@@ -207,8 +207,13 @@ struct LayerState {
     int32_t* evict_ids = nullptr;
     int32_t* n_admit = nullptr;
   } lists[2];
-  void* q_stage = nullptr;
-  void* qd_stage = nullptr;
+  // oasis_step_host's input staging, by step parity: the copies of step
+  // t + 1 run on the context's input stream while step t computes.
+  void* q_stage[2] = {nullptr, nullptr};
+  void* qd_stage[2] = {nullptr, nullptr};
+  cudaEvent_t ev_in[2] = {nullptr, nullptr};          // inputs of the slot copied
+  cudaEvent_t ev_stage_free[2] = {nullptr, nullptr};  // last reader of the slot done
+  bool stage_used[2] = {false, false};
   void* out_stage = nullptr;
   void* outd_stage = nullptr;
   void* qd_ring[2] = {nullptr, nullptr};  // staged draft queries, by step parity
@@ -231,7 +236,7 @@ struct ProfPair {
 struct WsLayout {
   size_t err, per_layer;
   size_t topk_ids, topk_scores, admit_ids, admit_slots, evict_ids, n_admit;
-  size_t q_stage, qd_stage, out_stage, outd_stage, qd_ring0, qd_ring1;
+  size_t q_stage, qd_stage, q_stage1, qd_stage1, out_stage, outd_stage, qd_ring0, qd_ring1;
   size_t total;
 };
 
@@ -256,6 +261,8 @@ WsLayout ws_layout(const oasis_config& c) {
   w.n_admit = o;     o += 2 * align_up(pairs * 4);
   w.q_stage = o;     o += align_up(qbytes);
   w.qd_stage = o;    o += align_up(qbytes);
+  w.q_stage1 = o;    o += align_up(qbytes);
+  w.qd_stage1 = o;   o += align_up(qbytes);
   w.out_stage = o;   o += align_up(obytes);
   w.outd_stage = o;  o += align_up(obytes);
   w.qd_ring0 = o;    o += align_up(qbytes);
@@ -324,6 +331,7 @@ struct oasis_ctx {
   cudaStream_t side2 = nullptr;  // host -> HBM gathers
   cudaStream_t side3 = nullptr;  // admissions (three-stream schedule only)
   cudaStream_t net = nullptr;    // remote tier transfers (host callbacks)
+  cudaStream_t io = nullptr;     // oasis_step_host input copies
   std::string last_error;
   bool prof = false;
   std::vector<ProfPair> prof_pool;
@@ -669,7 +677,8 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
   if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return bail(OASIS_ECUDA);
   if (cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, hi) != cudaSuccess ||
       cudaStreamCreateWithPriority(&c->side2, cudaStreamNonBlocking, hi) != cudaSuccess ||
-      cudaStreamCreateWithPriority(&c->side3, cudaStreamNonBlocking, hi) != cudaSuccess)
+      cudaStreamCreateWithPriority(&c->side3, cudaStreamNonBlocking, hi) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&c->io, cudaStreamNonBlocking, hi) != cudaSuccess)
     return bail(OASIS_ENOMEM);
   {
     const int pairs = cfg->num_requests * cfg->num_kv_heads;
@@ -727,8 +736,14 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
         Lp.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.n_admit - b0) + p * na);
       }
     }
-    S.q_stage = w + (c->wl.q_stage - b0);
-    S.qd_stage = w + (c->wl.qd_stage - b0);
+    S.q_stage[0] = w + (c->wl.q_stage - b0);
+    S.qd_stage[0] = w + (c->wl.qd_stage - b0);
+    S.q_stage[1] = w + (c->wl.q_stage1 - b0);
+    S.qd_stage[1] = w + (c->wl.qd_stage1 - b0);
+    for (int k = 0; k < 2; ++k)
+      if (cudaEventCreateWithFlags(&S.ev_in[k], cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&S.ev_stage_free[k], cudaEventDisableTiming) != cudaSuccess)
+        return bail(OASIS_ENOMEM);
     S.qd_ring[0] = w + (c->wl.qd_ring0 - b0);
     S.qd_ring[1] = w + (c->wl.qd_ring1 - b0);
     S.out_stage = w + (c->wl.out_stage - b0);
@@ -759,6 +774,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side) cudaStreamSynchronize(ctx->side);
   if (ctx->side2) cudaStreamSynchronize(ctx->side2);
   if (ctx->side3) cudaStreamSynchronize(ctx->side3);
+  if (ctx->io) cudaStreamSynchronize(ctx->io);
   // Host callbacks of a remote tier may sit on a caller's stream.
   for (auto& L : ctx->layers)
     if (L.remote) {
@@ -773,6 +789,10 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
     if (L.ev_start) cudaEventDestroy(L.ev_start);
     if (L.ev_side_done) cudaEventDestroy(L.ev_side_done);
     if (L.ev_scan_done) cudaEventDestroy(L.ev_scan_done);
+    for (int k = 0; k < 2; ++k) {
+      if (L.ev_in[k]) cudaEventDestroy(L.ev_in[k]);
+      if (L.ev_stage_free[k]) cudaEventDestroy(L.ev_stage_free[k]);
+    }
   }
   for (auto& p : ctx->prof_pool) {
     cudaEventDestroy(p.a);
@@ -782,6 +802,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side) cudaStreamDestroy(ctx->side);
   if (ctx->side2) cudaStreamDestroy(ctx->side2);
   if (ctx->side3) cudaStreamDestroy(ctx->side3);
+  if (ctx->io) cudaStreamDestroy(ctx->io);
   ctx->layers.clear();  // remote tiers: copy threads joined, events destroyed
   if (ctx->net) cudaStreamDestroy(ctx->net);
   delete ctx;
@@ -1059,18 +1080,30 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
   if (!L.loaded) return ctx->fail(OASIS_ESTATE, "layer %d: oasis_load_resident first", layer);
   if (int rc = ctx->set_device()) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The staging buffers are read only by work on `stream` (the attention and
-  // oasis_step's copy of q_draft into its ring), so the copies below need no
-  // wait for the previous step's side work.
+  // Inputs go to the staging slot of this step's parity on the input stream,
+  // as soon as the slot's last reader (step - 2's attention and q_draft copy
+  // on `stream`) is done, so they usually land while the previous step still
+  // computes; `stream` waits for them before the step.
+  const int slot = step & 1;
   const size_t qb = static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_q_heads * kHeadDim * 2;
   const size_t ob = qb * (ctx->cfg.out_fp32 ? 2 : 1);
-  if (int rc = ctx->cuda(cudaMemcpyAsync(L.q_stage, q_host, qb, cudaMemcpyHostToDevice, s), "h2d q"))
+  if (L.stage_used[slot]) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->io, L.ev_stage_free[slot], 0), "wait stage"))
+      return rc;
+  }
+  if (int rc = ctx->cuda(cudaMemcpyAsync(L.q_stage[slot], q_host, qb, cudaMemcpyHostToDevice,
+                                         ctx->io), "h2d q"))
     return rc;
-  if (int rc = ctx->cuda(cudaMemcpyAsync(L.qd_stage, q_draft_host, qb, cudaMemcpyHostToDevice, s),
-                         "h2d q_draft"))
+  if (int rc = ctx->cuda(cudaMemcpyAsync(L.qd_stage[slot], q_draft_host, qb,
+                                         cudaMemcpyHostToDevice, ctx->io), "h2d q_draft"))
     return rc;
-  if (int rc = oasis_step(ctx, layer, step, L.q_stage, L.qd_stage, L.out_stage, L.outd_stage, stream))
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_in[slot], ctx->io), "record inputs")) return rc;
+  if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_in[slot], 0), "wait inputs")) return rc;
+  if (int rc = oasis_step(ctx, layer, step, L.q_stage[slot], L.qd_stage[slot], L.out_stage,
+                          L.outd_stage, stream))
     return rc;
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_stage_free[slot], s), "record stage")) return rc;
+  L.stage_used[slot] = true;
   if (int rc = ctx->cuda(cudaMemcpyAsync(out_host, L.out_stage, ob, cudaMemcpyDeviceToHost, s), "d2h out"))
     return rc;
   return ctx->cuda(cudaMemcpyAsync(out_draft_host, L.outd_stage, ob, cudaMemcpyDeviceToHost, s),

@@ -208,14 +208,16 @@ def apply_hot_moves(shape: Shape, seed: int, layer: int, store: torch.Tensor,
                     moves: list, lens: np.ndarray) -> None:
     """Rewrite the keys of moved hot blocks in a host store: the old block
     loses the hot_shift * u_h offset, the new block gains it (valid tokens
-    only; tokens past the context stay zero)."""
+    only; tokens past the context stay zero).  `store` may be a CPU tensor or
+    a CUDA view of a pinned store (the rewrite then runs on the GPU)."""
     if not moves:
         return
-    u = head_directions(shape, seed, layer)
-    m = torch.as_tensor(moves, dtype=torch.int64)
+    dev = store.device
+    u = head_directions(shape, seed, layer).to(dev)
+    m = torch.as_tensor(moves, dtype=torch.int64, device=dev)
     r, h, old, new = m[:, 0], m[:, 1], m[:, 2], m[:, 3]
-    tok = torch.arange(shape.B)
-    L = torch.as_tensor(lens, dtype=torch.int64)
+    tok = torch.arange(shape.B, device=dev)
+    L = torch.as_tensor(lens, dtype=torch.int64, device=dev)
     for blk, sign in ((old, -1.0), (new, 1.0)):
         valid = (blk[:, None] * shape.B + tok[None, :]) < L[r][:, None]      # [n][B]
         x = store[r, h, blk, 0].float()                                       # [n][B][d]
