@@ -244,6 +244,27 @@ OASIS_API int oasis_admit_evict(oasis_ctx* ctx, int layer, int step,
                                 int32_t* admit_slots, int32_t* evict_ids,
                                 int32_t* n_admit, void* stream);
 
+/* a2 + a3 + a4 without caller scratch: oasis_score_topk followed by
+ * oasis_admit_evict on `stream`, with the top-K list between the two held in
+ * a fixed file-scope device array of the library (1 MiB: at most 262144 =
+ * R x Hkv x K entries; a larger configuration is refused with OASIS_EINVAL
+ * and a message) instead of a buffer the caller allocates.  The pages have
+ * no counterpart: it exists for callers that cannot allocate device memory
+ * where they issue the step (device memory fully committed to the KV pool
+ * and summaries, or an allocator that may not be entered from the thread
+ * driving the decode loop).  Outputs and table updates are those of the two
+ * calls.  The scratch's device address is looked up once per device, with
+ * that device current, on the first call: make that first call before any
+ * stream capture.  Nothing in the scratch needs to start at zero.  The
+ * scratch is shared by every context and layer in the process: two calls
+ * whose work may overlap on the device (other streams, layers or contexts
+ * without ordering between them) race on it, so order them (one stream, or
+ * events). */
+OASIS_API int oasis_score_admit_noalloc(oasis_ctx* ctx, int layer, int step,
+                                        const void* q_draft, int32_t* admit_ids,
+                                        int32_t* admit_slots, int32_t* evict_ids,
+                                        int32_t* n_admit, void* stream);
+
 /* a5: prefetch gather ([V] supporting_citations: a gather kernel reads the
  * selected blocks from pinned CPU memory through CUDA UVA).  For every (r, h) and i < n_admit: copy host
  * unit (r, h, admit_ids[i]) into pool unit phys[(step + 1) & 1][admit_slots[i]]

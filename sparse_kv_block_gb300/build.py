@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liboasis.so")
-SOURCES = ["api.cu", "attn.cu", "score_topk.cu", "admit_gather.cu"]
+SOURCES = ["api.cu", "attn.cu", "score_topk.cu", "admit_gather.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.h"]
 
 

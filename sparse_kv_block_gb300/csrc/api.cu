@@ -958,6 +958,30 @@ OASIS_API int oasis_admit_evict(oasis_ctx* ctx, int layer, int step, const int32
                    static_cast<cudaStream_t>(stream));
 }
 
+OASIS_API int oasis_score_admit_noalloc(oasis_ctx* ctx, int layer, int step,
+                                        const void* q_draft, int32_t* admit_ids,
+                                        int32_t* admit_slots, int32_t* evict_ids,
+                                        int32_t* n_admit, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || step > (1 << 30) || !q_draft || !admit_ids || !admit_slots || !evict_ids ||
+      !n_admit)
+    return ctx->fail(OASIS_EINVAL, "score_admit_noalloc: bad step or null pointer");
+  const size_t need = static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_kv_heads *
+                      ctx->cfg.topk;
+  if (need > kNoAllocTopkEntries)
+    return ctx->fail(OASIS_EINVAL,
+                     "score_admit_noalloc: the top-K lists need %zu entries, the fixed "
+                     "scratch holds %zu (1 MiB); use oasis_score_topk + oasis_admit_evict",
+                     need, kNoAllocTopkEntries);
+  if (int rc = ctx->set_device()) return rc;
+  int32_t* topk = nullptr;
+  if (int rc = ctx->cuda(noalloc_topk_scratch(ctx->cfg.device, &topk), "scratch address"))
+    return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = run_score(ctx, layer, step, q_draft, topk, nullptr, s)) return rc;
+  return run_admit(ctx, layer, step, topk, admit_ids, admit_slots, evict_ids, n_admit, s);
+}
+
 OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* admit_ids,
                              const int32_t* admit_slots, const int32_t* n_admit,
                              void* stream) {

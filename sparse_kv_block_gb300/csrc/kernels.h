@@ -152,4 +152,10 @@ size_t score_topk_smem_bytes(int K, int NBmax);
 // Largest NBmax the fused score + admit kernel can hold in shared memory.
 constexpr int kMaxBlocksPerHead = 131072;
 
+// oasis_score_admit_noalloc: entries of its file-scope top-K scratch, and the
+// scratch's device address (looked up once per device, with that device
+// current, on the first call).
+constexpr size_t kNoAllocTopkEntries = 262144;
+cudaError_t noalloc_topk_scratch(int device, int32_t** ptr);
+
 }  // namespace oasis

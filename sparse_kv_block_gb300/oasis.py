@@ -83,6 +83,7 @@ EXPORTS = {
     "oasis_dense_attn": (c_int, [_P, _P, c_int, _P, _P, _P, _P, _P]),
     "oasis_score_topk": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
     "oasis_admit_evict": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P, _P]),
+    "oasis_score_admit_noalloc": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P, _P]),
     "oasis_prefetch": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
     "oasis_step": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
     "oasis_join": (c_int, [_P, c_int, _P]),
@@ -269,6 +270,13 @@ class Oasis:
         self._check(lib().oasis_admit_evict(self.ctx, layer, step, _ptr(topk_ids),
                                             _ptr(admit_ids), _ptr(admit_slots),
                                             _ptr(evict_ids), _ptr(n_admit), _stream(stream)))
+
+    def oasis_score_admit_noalloc(self, layer, step, qd, admit_ids, admit_slots, evict_ids,
+                                  n_admit, stream=None) -> None:
+        self._check(lib().oasis_score_admit_noalloc(self.ctx, layer, step, _ptr(qd),
+                                                    _ptr(admit_ids), _ptr(admit_slots),
+                                                    _ptr(evict_ids), _ptr(n_admit),
+                                                    _stream(stream)))
 
     def oasis_prefetch(self, layer, step, admit_ids, admit_slots, n_admit, stream=None) -> None:
         self._check(lib().oasis_prefetch(self.ctx, layer, step, _ptr(admit_ids),
