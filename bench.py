@@ -1004,7 +1004,7 @@ def run_cap_sweep(args, ws, rank, local):
         outd = torch.empty_like(out)
         true_topk = torch.empty((shape.R, shape.Hkv, shape.K), dtype=torch.int32, device=dev)
         P, NB, K = shape.R * shape.Hkv, shape.NBmax, shape.K
-        agree, agree_x, adm = [], [], []
+        agree, agree_x, agree_s, adm = [], [], [], []
         step = 0
         for _ in range(args.warmup):
             eng.oasis_step(0, step, q[step % nq], qd[step % nq], out, outd, main)
@@ -1029,6 +1029,9 @@ def run_cap_sweep(args, ws, rank, local):
             ax.scatter_(1, lists["topk_ids"][:ns].reshape(-1, K).long() + 1, 1.0)
             bx.scatter_(1, ex.reshape(-1, K) + 1, 1.0)
             agree_x.append(float(((ax * bx)[:, 1:].sum(1) / K).mean()))
+            cx = torch.zeros((ns * shape.Hkv, NB + 1), device=dev)
+            cx.scatter_(1, true_topk[:ns].reshape(-1, K).long() + 1, 1.0)
+            agree_s.append(float(((cx * bx)[:, 1:].sum(1) / K).mean()))
             adm.append(int(lists["n_admit"].sum()))
             step += 1
         torch.cuda.synchronize(dev)
@@ -1050,7 +1053,9 @@ def run_cap_sweep(args, ws, rank, local):
                         "admitted_units_per_step": sum(adm) / len(adm),
                         "topk_agreement_draft_vs_next": round(sum(agree) / len(agree), 5),
                         "topk_agreement_draft_vs_next_exact":
-                            round(sum(agree_x) / len(agree_x), 5)})
+                            round(sum(agree_x) / len(agree_x), 5),
+                        "topk_agreement_summary_vs_exact_same_query":
+                            round(sum(agree_s) / len(agree_s), 5)})
         eng.close()
         del eng
         torch.cuda.empty_cache()
