@@ -14,21 +14,26 @@
 // N: S^T = K_unit * Q^T, online softmax over tokens, then O^T += V^T * P^T
 // with P^T moved into the B-operand layout by movmatrix.  The kernel is
 // bound by HBM reads of the resident units (8 KiB per unit).
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace oasis {
 namespace {
 
-constexpr int kWarps = 4;
 constexpr int kStages = 2;
-constexpr int kThreads = kWarps * 32;
 constexpr int kStageBytes = kUnitBytes;            // 8 KiB: [half][32 rows][128 B]
-constexpr int kRingBytes = kWarps * kStages * kStageBytes;
-constexpr int kBarOffset = kRingBytes;
-constexpr int kListOffset = kBarOffset + 256;
-constexpr int kCountOffset = kListOffset + kMaxTopK * 8;
-constexpr int kSmemBytes = kCountOffset + 16 + 1024;  // + alignment slack
+
+// Shared memory of a CTA of W warps: W private rings, barriers, unit list.
+template <int W>
+struct AttnLayout {
+  static constexpr int kRingBytes = W * kStages * kStageBytes;
+  static constexpr int kBarOffset = kRingBytes;
+  static constexpr int kListOffset = kBarOffset + 256;
+  static constexpr int kCountOffset = kListOffset + kMaxTopK * 8;
+  static constexpr int kSmemBytes = kCountOffset + 16 + 1024;  // + alignment slack
+};
 
 struct UnitRef {
   int unit;   // global pool unit index (pair * U + phys slot unit)
@@ -46,8 +51,14 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(kThreads)
+template <int kWarps>
+__global__ void __launch_bounds__(kWarps * 32)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap pool_map) {
+  using Lay = AttnLayout<kWarps>;
+  constexpr int kThreads = kWarps * 32;
+  constexpr int kBarOffset = Lay::kBarOffset;
+  constexpr int kListOffset = Lay::kListOffset;
+  constexpr int kCountOffset = Lay::kCountOffset;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOffset);
@@ -312,24 +323,55 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace
 
-size_t attention_smem_bytes() { return kSmemBytes; }
+size_t attention_smem_bytes() { return AttnLayout<4>::kSmemBytes; }
 
-cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
-                             cudaStream_t s) {
+namespace {
+
+template <int W>
+cudaError_t configure_attn() {
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = cudaFuncSetAttribute(attn_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttnLayout<W>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
+  return cudaSuccess;
+}
+
+// Warps per CTA: 4 (3 CTAs per SM).  A 3-warp variant (4 CTAs per SM, the
+// same bytes in flight per SM) fills the last wave of some grids better and
+// is faster alone there (64 requests x 8 heads: 86.6 against 96.6 us), but
+// measured inside the decode loops it was not (32-layer, 64-request loop:
+// 3692 / 3636 against 3822 / 3731 layer-steps/s; 128 requests: equal), so it
+// is only a tuning override: OASIS_ATTN_WARPS=3.
+int attn_warps() {
+  static const int forced = [] {
+    const char* e = std::getenv("OASIS_ATTN_WARPS");
+    return (e && std::atoi(e) == 3) ? 3 : 4;
+  }();
+  return forced;
+}
+
+template <int W>
+cudaError_t launch_w(const AttnArgs& a, const CUtensorMap* pool_map, int grid, cudaStream_t s) {
+  cudaError_t e = configure_attn<W>();
+  if (e != cudaSuccess) return e;
+  attn_kernel<W><<<grid, W * 32, AttnLayout<W>::kSmemBytes, s>>>(a, *pool_map);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
+                             cudaStream_t s) {
   const int grid = a.R * a.Hkv;
   if (grid == 0) return cudaSuccess;
-  attn_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, *pool_map);
-  return cudaGetLastError();
+  return attn_warps() == 3 ? launch_w<3>(a, pool_map, grid, s)
+                           : launch_w<4>(a, pool_map, grid, s);
 }
 
 }  // namespace oasis

@@ -22,11 +22,12 @@
 // fp32x2 multiply-adds, transposed shuffle reduction), keep a running top-KP
 // list in registers (bitonic sort of each filled buffer of KP keys, then a
 // bitonic merge), and finally merge their lists in a tree.  Shared memory is
-// sized from the actual NBmax (the fused admission reuses the ring).  CW = 8
-// (16 KiB stages, 4 CTAs per SM) by default; CW = 4 (8 KiB stages, ~21 KB and
-// 48 registers per thread: 8 CTAs per SM, a 128-request x 8-head layer in one
-// wave) is faster alone on GB300 (92 vs 98 us) but slower inside the step,
-// beside the host-link gather (129 vs 120 us; 2872 vs 3108 layer-steps/s).
+// sized from the actual NBmax (the fused admission reuses the ring).  Two
+// variants: CW = 8 (16 KiB stages, ~41 KB, 4 CTAs per SM) and CW = 4 (8 KiB
+// stages, ~21 KB and 48 registers per thread, 8 CTAs per SM); the launcher
+// picks one by wave quantisation (see scan_warps).  Alone on the 128 x 16K
+// layer CW = 4 is faster (92 vs 98 us) but inside the step, beside the
+// host-link gather, CW = 8 is (120 vs 129 us).
 // Keys are 64-bit: order-preserving score bits above the complemented block
 // id, so ties break to the lower id and all keys are distinct.
 #include <cstdlib>
@@ -275,10 +276,10 @@ __global__ void __launch_bounds__((CW + 1) * 32)
   }
 }
 
+// Raise the kernel's dynamic shared memory limit to `smem` (once per device
+// and size).
 template <int KPL, int CW>
-cudaError_t launch_kpl_cw(const ScoreArgs& a, cudaStream_t s) {
-  if (a.pairs <= 0) return cudaSuccess;
-  const int smem = Layout<KPL, CW>::total(a.NBmax);
+cudaError_t configure(int smem) {
   static int configured_device = -1;
   static int configured_smem = 0;
   int dev = 0;
@@ -291,23 +292,70 @@ cudaError_t launch_kpl_cw(const ScoreArgs& a, cudaStream_t s) {
     configured_device = dev;
     configured_smem = smem;
   }
+  return cudaSuccess;
+}
+
+template <int KPL, int CW>
+cudaError_t launch_kpl_cw(const ScoreArgs& a, cudaStream_t s) {
+  if (a.pairs <= 0) return cudaSuccess;
+  const int smem = Layout<KPL, CW>::total(a.NBmax);
+  cudaError_t e = configure<KPL, CW>(smem);
+  if (e != cudaSuccess) return e;
   score_topk_kernel<KPL, CW><<<a.pairs, (CW + 1) * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-// Consumer warps per CTA: 8 by default; OASIS_SCAN_WARPS=4 is a tuning
-// override (see the file comment for the measurements).
-int scan_warps() {
-  static const int cw = [] {
+// CTAs of a variant resident on the whole GPU at once (0 if unknown).
+template <int KPL, int CW>
+int grid_slots(int NBmax) {
+  const int smem = Layout<KPL, CW>::total(NBmax);
+  int dev = 0, sms = 0, per = 0;
+  if (configure<KPL, CW>(smem) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, score_topk_kernel<KPL, CW>,
+                                                    (CW + 1) * 32, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per * sms;
+}
+
+// Consumer warps per CTA, chosen by wave quantisation of the one-CTA-per-pair
+// grid.  8 warps (twice the bytes in flight per CTA) unless that grid needs a
+// second wave that would run less than half full while the 4-warp grid fits
+// in one: measured on GB300, 720 pairs (36-layer loop, 90 requests): 4 warps
+// 3657 against 3392 layer-steps/s (scan 91 vs 109 us); 1024 pairs (last
+// 8-warp wave 68 % full): 8 warps 3108 against 2872; 512 pairs of 2048
+// blocks (one wave either way): 8 warps 3685 against 3630.
+// OASIS_SCAN_WARPS=4 or 8 forces a variant.
+template <int KPL>
+int scan_warps(int pairs, int NBmax) {
+  static const int forced = [] {
     const char* e = std::getenv("OASIS_SCAN_WARPS");
-    return (e && std::atoi(e) == 4) ? 4 : 8;
+    const int v = e ? std::atoi(e) : 0;
+    return (v == 4 || v == 8) ? v : 0;
   }();
-  return cw;
+  if (forced) return forced;
+  static int cached_dev = -1, cached_nb = -1, s8 = 0, s4 = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 8;
+  if (dev != cached_dev || NBmax != cached_nb) {
+    s8 = grid_slots<KPL, 8>(NBmax);
+    s4 = grid_slots<KPL, 4>(NBmax);
+    cached_dev = dev;
+    cached_nb = NBmax;
+  }
+  if (s8 > 0 && s4 > 0 && pairs > s8 && pairs <= s4) {
+    const int last = pairs % s8;  // CTAs of the 8-warp grid's last wave
+    if (last != 0 && 2 * last < s8) return 4;
+  }
+  return 8;
 }
 
 template <int KPL>
 cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
-  return scan_warps() == 4 ? launch_kpl_cw<KPL, 4>(a, s) : launch_kpl_cw<KPL, 8>(a, s);
+  return scan_warps<KPL>(a.pairs, a.NBmax) == 4 ? launch_kpl_cw<KPL, 4>(a, s)
+                                                : launch_kpl_cw<KPL, 8>(a, s);
 }
 
 }  // namespace
