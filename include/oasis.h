@@ -291,6 +291,13 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
                          const void* q_draft, void* out, void* out_draft,
                          void* stream);
 
+/* Host-side bounded wait for this layer's outstanding side work (the last
+ * oasis_step's scan, admission and gathers; with a remote tier also its
+ * network transfers): polls an event until it completes (OASIS_OK) or
+ * `timeout_ms` passes (OASIS_ETIMEOUT; the work keeps running and a later
+ * wait may succeed).  OASIS_OK at once when no side work is outstanding. */
+OASIS_API int oasis_wait(oasis_ctx* ctx, int layer, double timeout_ms);
+
 /* Make `stream` wait for this layer's outstanding side work (event wait, no
  * host block). */
 OASIS_API int oasis_join(oasis_ctx* ctx, int layer, void* stream);
@@ -355,12 +362,13 @@ OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
  * tier into HBM.  Local slots are assigned in list order (admission rank
  * order) from 0 upwards.  Summaries are built from the remote store (they are
  * shipped with the request).  The network transfer remote -> local is done on
- * the host, as a NIC's DMA would be: a CUDA host callback on the context's
- * network stream, after the slot assignment, copies the listed units with a
- * pool of `threads` host threads, optionally throttled to `gbps`; it moves no
+ * the host, as a NIC's DMA would be: a worker thread of the tier, told by the
+ * stream (a 32-bit write after the slot assignment) that the lists are ready,
+ * copies the listed units with a pool of `threads` host threads, optionally
+ * throttled to `gbps`, and writes the transfer's number back; it moves no
  * data through the GPU.  The gather then runs in two launches on its stream:
  * the admitted units already held locally at once, beside the transfer, and
- * the units just fetched once the transfer has ended.
+ * the units just fetched after a stream wait for that number.
  *
  * With a remote tier attached to a layer, host_kv (given to oasis_init) is the
  * remote store, pinned and mapped as before; oasis_append_token is refused
@@ -373,7 +381,9 @@ OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
  *                     [R][Hkv] int32 (slots in use before the last assignment)
  *   miss_lists pinned [R][Hkv] int32 n_miss, then [R][Hkv][M] int32 ids, then
  *                     [R][Hkv][M] int32 slots, M = max(K, C): the blocks the
- *                     last slot assignment of each (r, h) fetched, in order
+ *                     last slot assignment of each (r, h) fetched, in order;
+ *                     then (16-byte aligned) two uint32 sequence words the
+ *                     stream and the tier's worker thread hand over with
  * ------------------------------------------------------------------------ */
 typedef struct {
   int32_t capacity; /* local slots per (r, h): K <= capacity <= NBmax */

@@ -415,4 +415,22 @@ cudaError_t launch_advance(const int32_t* cur, int32_t* nxt, int R, int grow,
   return cudaGetLastError();
 }
 
+cudaError_t preload_support_kernels() {
+  cudaFuncAttributes at;
+  const void* fns[] = {
+      reinterpret_cast<const void*>(admit_kernel<1>), reinterpret_cast<const void*>(admit_kernel<2>),
+      reinterpret_cast<const void*>(admit_kernel<4>), reinterpret_cast<const void*>(admit_kernel<8>),
+      reinterpret_cast<const void*>(gather_kernel),
+      reinterpret_cast<const void*>(remote_assign_kernel),
+      reinterpret_cast<const void*>(init_tables_kernel),
+      reinterpret_cast<const void*>(summary_build_kernel),
+      reinterpret_cast<const void*>(refresh_kernel), reinterpret_cast<const void*>(append_kernel),
+      reinterpret_cast<const void*>(advance_kernel)};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncGetAttributes(&at, f);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace oasis

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI (include/oasis.h): argument validation, the context,
 // the side stream and its events, the TMA descriptors and step orchestration.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
@@ -10,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <deque>
 #include <functional>
 #include <map>
 #include <memory>
@@ -32,10 +34,14 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Remote tier (emulated prefill-decode disaggregation).  The transfer
 // remote -> local tier of the blocks a slot assignment listed runs on the
-// host, in a CUDA host callback, as a network adapter's DMA would: no GPU
-// work.  One job per (pair range, item count) a layer uses; a job's fields
-// never change after creation, so a callback may still be queued when the
-// next step enqueues the same job again.
+// host, as a network adapter's DMA would: no GPU work.  A worker thread per
+// tier takes the transfers in issue order; the GPU and the worker hand over
+// through two sequence words in mapped host memory: the stream writes a
+// transfer's number after its slot assignment (the worker then reads the
+// lists) and waits, before gathering the fetched units, until the worker
+// has written the number back.  (A CUDA host callback doing the copy was
+// measured to hold up the issuing thread's CUDA calls for as long as the
+// callback ran.)
 struct RemoteStats {
   std::atomic<int64_t> units{0}, transfers{0}, bad{0}, nanos{0};
 };
@@ -112,78 +118,155 @@ class CopyPool {
 };
 
 struct RemoteJob {
-  const uint8_t* remote = nullptr;  // [pairs][NBmax] units
-  uint8_t* local = nullptr;         // [pairs][capacity] units
-  const int32_t* n_miss = nullptr;  // host view of the lists
-  const int32_t* miss_ids = nullptr;
-  const int32_t* miss_slots = nullptr;
-  int pair0 = 0, pairs = 0, M = 0, NBmax = 0, capacity = 0;
-  double gbps = 0.0;
-  RemoteStats* stats = nullptr;
-  CopyPool* pool = nullptr;
+  uint32_t seq = 0;                 // transfer number
+  int pair0 = 0, pairs = 0;
 };
 
-void CUDART_CB remote_transfer(void* arg) {
-  const RemoteJob& j = *static_cast<const RemoteJob*>(arg);
-  const auto t0 = std::chrono::steady_clock::now();
-  std::vector<std::pair<int, int>> items;
-  int64_t bad = 0;
-  for (int p = j.pair0; p < j.pair0 + j.pairs; ++p) {
-    const int n = j.n_miss[p];
-    if (n < 0 || n > j.M) {
-      ++bad;
-      continue;
-    }
-    for (int i = 0; i < n; ++i) {
-      const size_t li = static_cast<size_t>(p) * j.M + i;
-      if (j.miss_ids[li] < 0 || j.miss_ids[li] >= j.NBmax || j.miss_slots[li] < 0 ||
-          j.miss_slots[li] >= j.capacity) {
-        ++bad;
-        continue;
-      }
-      items.emplace_back(p, i);
-    }
-  }
-  const size_t n = items.size();
-  j.pool->run(n, [&](size_t lo, size_t hi) {
-    for (size_t k = lo; k < hi; ++k) {
-      const int p = items[k].first, i = items[k].second;
-      const size_t li = static_cast<size_t>(p) * j.M + i;
-      std::memcpy(j.local + (static_cast<size_t>(p) * j.capacity + j.miss_slots[li]) * kUnitBytes,
-                  j.remote + (static_cast<size_t>(p) * j.NBmax + j.miss_ids[li]) * kUnitBytes,
-                  kUnitBytes);
-    }
-  });
-  if (j.gbps > 0.0) {
-    const double sec = static_cast<double>(n) * kUnitBytes / (j.gbps * 1e9);
-    std::this_thread::sleep_until(t0 + std::chrono::duration_cast<std::chrono::steady_clock::duration>(
-                                           std::chrono::duration<double>(sec)));
-  }
-  const auto dt = std::chrono::steady_clock::now() - t0;
-  j.stats->units += static_cast<int64_t>(n);
-  j.stats->transfers += 1;
-  j.stats->bad += bad;
-  j.stats->nanos += std::chrono::duration_cast<std::chrono::nanoseconds>(dt).count();
+// Driver entry points of the stream memory operations.
+using PFN_WaitValue32 = CUresult(CUDAAPI*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+using PFN_WriteValue32 = CUresult(CUDAAPI*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+PFN_WaitValue32 get_wait_value32() {
+  static PFN_WaitValue32 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &p, 11070, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_WaitValue32>(p);
+    return static_cast<PFN_WaitValue32>(nullptr);
+  }();
+  return fn;
+}
+PFN_WriteValue32 get_write_value32() {
+  static PFN_WriteValue32 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 11070, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_WriteValue32>(p);
+    return static_cast<PFN_WriteValue32>(nullptr);
+  }();
+  return fn;
 }
 
+// True when sequence word value v has reached s (wrap-around safe).
+inline bool seq_reached(uint32_t v, uint32_t s) { return static_cast<int32_t>(v - s) >= 0; }
+
 struct RemoteTier {
-  int capacity = 0, M = 0, threads = 4;
+  int capacity = 0, M = 0, threads = 4, NBmax = 0, all_pairs = 0;
   double gbps = 0.0;
-  uint8_t* local = nullptr;       // caller's pinned local tier
-  void* local_dev = nullptr;      // its device mapping
-  int32_t* map = nullptr;         // dev [pairs][NBmax]
-  int32_t* count = nullptr;       // dev [pairs]: slots in use
-  int32_t* base = nullptr;        // dev [pairs]: slots in use before the last assignment
-  int32_t* lists = nullptr;       // caller's pinned miss lists
-  int32_t* lists_dev = nullptr;   // their device mapping
-  cudaEvent_t ev_assigned = nullptr;
-  cudaEvent_t ev_moved = nullptr;
+  const uint8_t* remote = nullptr; // the remote store, [pairs][NBmax] units
+  uint8_t* local = nullptr;        // caller's pinned local tier
+  void* local_dev = nullptr;       // its device mapping
+  int32_t* map = nullptr;          // dev [pairs][NBmax]
+  int32_t* count = nullptr;        // dev [pairs]: slots in use
+  int32_t* base = nullptr;         // dev [pairs]: slots in use before the last assignment
+  int32_t* lists = nullptr;        // caller's pinned miss lists
+  int32_t* lists_dev = nullptr;    // their device mapping
+  volatile uint32_t* assigned = nullptr;  // host view: last assignment done (GPU writes)
+  volatile uint32_t* moved = nullptr;     // host view: last transfer done (worker writes)
+  CUdeviceptr assigned_dev = 0, moved_dev = 0;
+  uint32_t next_seq = 0;           // issue counter (API thread)
   RemoteStats stats;
   std::unique_ptr<CopyPool> pool;
-  std::map<std::tuple<int, int, int>, std::unique_ptr<RemoteJob>> jobs;
+  std::thread worker;
+  std::mutex qm;
+  std::condition_variable qcv;
+  std::deque<RemoteJob> queue;
+  bool stop = false;
+
+  void start() { worker = std::thread([this] { run(); }); }
+  void post(const RemoteJob& j) {
+    {
+      std::lock_guard<std::mutex> g(qm);
+      queue.push_back(j);
+    }
+    qcv.notify_one();
+  }
   ~RemoteTier() {
-    if (ev_assigned) cudaEventDestroy(ev_assigned);
-    if (ev_moved) cudaEventDestroy(ev_moved);
+    {
+      std::lock_guard<std::mutex> g(qm);
+      stop = true;
+    }
+    qcv.notify_one();
+    if (worker.joinable()) worker.join();
+    if (moved) *moved = next_seq;  // nothing may wait on a transfer any more
+  }
+
+ private:
+  // Transfers in issue order.  Waits (bounded, ~60 s) for the GPU to finish
+  // the transfer's slot assignment, copies the listed units, holds the
+  // throttle, then publishes the number; on a timeout it publishes without
+  // copying and counts the lists as bad, so no stream waits forever.
+  void run() {
+    for (;;) {
+      RemoteJob j;
+      {
+        std::unique_lock<std::mutex> l(qm);
+        qcv.wait(l, [this] { return stop || !queue.empty(); });
+        if (queue.empty()) return;
+        j = queue.front();
+        queue.pop_front();
+      }
+      const auto t0 = std::chrono::steady_clock::now();
+      bool ready = true;
+      for (int spin = 0; !seq_reached(*assigned, j.seq); ++spin) {
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(60)) {
+          ready = false;
+          break;
+        }
+        if (spin > 64) std::this_thread::sleep_for(std::chrono::microseconds(20));
+      }
+      std::atomic_thread_fence(std::memory_order_acquire);
+      const auto t1 = std::chrono::steady_clock::now();
+      size_t n = 0;
+      int64_t bad = ready ? 0 : 1;
+      if (ready) {
+        const int32_t* n_miss = lists;
+        const int32_t* ids = lists + all_pairs;
+        const int32_t* slots = lists + all_pairs + static_cast<size_t>(all_pairs) * M;
+        std::vector<std::pair<int, int>> items;
+        for (int p = j.pair0; p < j.pair0 + j.pairs; ++p) {
+          const int c = n_miss[p];
+          if (c < 0 || c > M) {
+            ++bad;
+            continue;
+          }
+          for (int i = 0; i < c; ++i) {
+            const size_t li = static_cast<size_t>(p) * M + i;
+            if (ids[li] < 0 || ids[li] >= NBmax || slots[li] < 0 || slots[li] >= capacity) {
+              ++bad;
+              continue;
+            }
+            items.emplace_back(p, i);
+          }
+        }
+        n = items.size();
+        pool->run(n, [&](size_t lo, size_t hi) {
+          for (size_t k = lo; k < hi; ++k) {
+            const int p = items[k].first, i = items[k].second;
+            const size_t li = static_cast<size_t>(p) * M + i;
+            std::memcpy(local + (static_cast<size_t>(p) * capacity + slots[li]) * kUnitBytes,
+                        remote + (static_cast<size_t>(p) * NBmax + ids[li]) * kUnitBytes,
+                        kUnitBytes);
+          }
+        });
+        if (gbps > 0.0) {
+          const double sec = static_cast<double>(n) * kUnitBytes / (gbps * 1e9);
+          std::this_thread::sleep_until(
+              t1 + std::chrono::duration_cast<std::chrono::steady_clock::duration>(
+                       std::chrono::duration<double>(sec)));
+        }
+      }
+      const auto dt = std::chrono::steady_clock::now() - t1;
+      std::atomic_thread_fence(std::memory_order_release);
+      *moved = j.seq;
+      stats.units += static_cast<int64_t>(n);
+      stats.transfers += 1;
+      stats.bad += bad;
+      stats.nanos += std::chrono::duration_cast<std::chrono::nanoseconds>(dt).count();
+    }
   }
 };
 
@@ -330,7 +413,6 @@ struct oasis_ctx {
   cudaStream_t side = nullptr;   // scan + top-K + admission
   cudaStream_t side2 = nullptr;  // host -> HBM gathers
   cudaStream_t side3 = nullptr;  // admissions (three-stream schedule only)
-  cudaStream_t net = nullptr;    // remote tier transfers (host callbacks)
   cudaStream_t io = nullptr;     // oasis_step_host input copies
   std::string last_error;
   bool prof = false;
@@ -397,6 +479,13 @@ struct oasis_ctx {
 };
 
 namespace {
+
+// NVTX range for the host-side issue of one call (visible in a timeline
+// profiler; without one attached the calls return at once).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 int check_layer(oasis_ctx* ctx, int layer) {
   if (!ctx) return OASIS_EINVAL;
@@ -502,8 +591,7 @@ int run_admit(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t*
 }
 
 // Remote tier: assign local slots to the listed blocks not yet held (on
-// `s`), then move them remote -> local on the host in a callback on the
-// context's network stream; ev_moved marks the end of that transfer.
+// `s`), then hand the transfer remote -> local to the tier's worker thread.
 int run_remote_fetch(oasis_ctx* ctx, int layer, const int32_t* ids, const int32_t* n_valid,
                      int items, int pair0, int pairs, cudaStream_t s) {
   LayerState& L = ctx->layers[layer];
@@ -526,30 +614,19 @@ int run_remote_fetch(oasis_ctx* ctx, int layer, const int32_t* ids, const int32_
   r.capacity = T.capacity;
   r.M = T.M;
   if (int rc = ctx->cuda(launch_remote_assign(r, s), "remote slot assignment launch")) return rc;
-  auto& job = T.jobs[std::make_tuple(pair0, pairs, items)];
-  if (!job) {
-    job.reset(new (std::nothrow) RemoteJob());
-    if (!job) return ctx->fail(OASIS_ENOMEM, "remote job");
-    job->remote = static_cast<const uint8_t*>(L.host);
-    job->local = T.local;
-    job->n_miss = T.lists;
-    job->miss_ids = T.lists + all;
-    job->miss_slots = T.lists + all + static_cast<size_t>(all) * T.M;
-    job->pair0 = pair0;
-    job->pairs = pairs;
-    job->M = T.M;
-    job->NBmax = ctx->cfg.max_blocks;
-    job->capacity = T.capacity;
-    job->gbps = T.gbps;
-    job->stats = &T.stats;
-    job->pool = T.pool.get();
-  }
-  if (int rc = ctx->cuda(cudaEventRecord(T.ev_assigned, s), "record assignment")) return rc;
-  if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->net, T.ev_assigned, 0), "net wait")) return rc;
-  if (int rc = ctx->cuda(cudaLaunchHostFunc(ctx->net, remote_transfer, job.get()),
-                         "remote transfer callback"))
-    return rc;
-  return ctx->cuda(cudaEventRecord(T.ev_moved, ctx->net), "record transfer");
+  // The stream publishes the transfer number once the assignment is done
+  // (with a memory barrier, so the lists are visible); the worker copies.
+  const uint32_t seq = ++T.next_seq;
+  auto write = get_write_value32();
+  if (!write) return ctx->fail(OASIS_ECUDA, "cuStreamWriteValue32 unavailable");
+  if (write(s, T.assigned_dev, seq, 0) != CUDA_SUCCESS)
+    return ctx->fail(OASIS_ECUDA, "remote: stream write of the assignment number failed");
+  RemoteJob j;
+  j.seq = seq;
+  j.pair0 = pair0;
+  j.pairs = pairs;
+  T.post(j);
+  return OASIS_OK;
 }
 
 // With a remote tier the gather runs in two launches: the units already held
@@ -562,8 +639,10 @@ int launch_gather_split(oasis_ctx* ctx, const LayerState& L, GatherArgs g, cudaS
   }
   g.phase = 1;
   if (int rc = ctx->cuda(launch_gather(g, s), "gather launch (held units)")) return rc;
-  if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.remote->ev_moved, 0), "wait transfer"))
-    return rc;
+  auto wait = get_wait_value32();
+  if (!wait) return ctx->fail(OASIS_ECUDA, "cuStreamWaitValue32 unavailable");
+  if (wait(s, L.remote->moved_dev, L.remote->next_seq, CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS)
+    return ctx->fail(OASIS_ECUDA, "remote: stream wait for the transfer failed");
   g.phase = 2;
   return ctx->cuda(launch_gather(g, s), "gather launch (fetched units)");
 }
@@ -691,6 +770,14 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
   }
   auto encode = get_encode();
   if (!encode) return bail(OASIS_ECUDA);
+  // Load all kernels up front: a kernel's first launch otherwise loads its
+  // module lazily, and that load waits for the work already queued on the
+  // device (measured: a first oasis_step issued while a throttled remote
+  // transfer was pending blocked the calling thread for the transfer's
+  // 130 ms).
+  if (preload_attention_kernels() != cudaSuccess || preload_score_kernels() != cudaSuccess ||
+      preload_support_kernels() != cudaSuccess)
+    return bail(OASIS_ECUDA);
 
   const size_t R = cfg->num_requests, H = cfg->num_kv_heads;
   for (int l = 0; l < L; ++l) {
@@ -775,7 +862,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side2) cudaStreamSynchronize(ctx->side2);
   if (ctx->side3) cudaStreamSynchronize(ctx->side3);
   if (ctx->io) cudaStreamSynchronize(ctx->io);
-  // Host callbacks of a remote tier may sit on a caller's stream.
+  // A remote tier's transfers may sit on a caller's stream.
   for (auto& L : ctx->layers)
     if (L.remote) {
       cudaDeviceSynchronize();
@@ -803,8 +890,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side2) cudaStreamDestroy(ctx->side2);
   if (ctx->side3) cudaStreamDestroy(ctx->side3);
   if (ctx->io) cudaStreamDestroy(ctx->io);
-  ctx->layers.clear();  // remote tiers: copy threads joined, events destroyed
-  if (ctx->net) cudaStreamDestroy(ctx->net);
+  ctx->layers.clear();  // remote tiers: worker and copy threads joined
   delete ctx;
   return OASIS_OK;
 }
@@ -995,6 +1081,7 @@ OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t*
 
 OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
                          const void* q_draft, void* out, void* out_draft, void* stream) {
+  NvtxRange nvtx("oasis_step");
   if (int rc = check_layer(ctx, layer)) return rc;
   if (step < 0 || step > (1 << 30) || !q || !q_draft || !out || !out_draft)
     return ctx->fail(OASIS_EINVAL, "step: bad step or null pointer");
@@ -1083,6 +1170,27 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_side_done, ctx->side2), "record side")) return rc;
   L.side_pending = true;
   return OASIS_OK;
+}
+
+OASIS_API int oasis_wait(oasis_ctx* ctx, int layer, double timeout_ms) {
+  NvtxRange nvtx("oasis_wait");
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (!(timeout_ms >= 0.0)) return ctx->fail(OASIS_EINVAL, "wait: timeout must be >= 0");
+  if (int rc = ctx->set_device()) return rc;
+  LayerState& L = ctx->layers[layer];
+  if (!L.side_pending) return OASIS_OK;
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(L.ev_side_done);
+    if (e == cudaSuccess) return OASIS_OK;
+    if (e != cudaErrorNotReady) return ctx->cuda(e, "wait: event query");
+    const double ms =
+        std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    if (ms >= timeout_ms)
+      return ctx->fail(OASIS_ETIMEOUT, "wait: layer %d side work not done after %.1f ms", layer,
+                       timeout_ms);
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
 }
 
 OASIS_API int oasis_join(oasis_ctx* ctx, int layer, void* stream) {
@@ -1241,7 +1349,8 @@ OASIS_API int oasis_remote_query_sizes(const oasis_config* cfg, const oasis_remo
   const size_t M = std::max(cfg->topk, fetch_cap(*cfg));
   out->local_tier_bytes = pairs * rcfg->capacity * kUnitBytes;
   out->local_map_bytes = (pairs * cfg->max_blocks + 2 * pairs) * 4;
-  out->miss_lists_bytes = (pairs + 2 * pairs * M) * 4;
+  // the lists, then two 32-bit sequence words (16-byte aligned)
+  out->miss_lists_bytes = ((pairs + 2 * pairs * M) * 4 + 15) / 16 * 16 + 16;
   return OASIS_OK;
 }
 
@@ -1281,17 +1390,25 @@ OASIS_API int oasis_remote_attach(oasis_ctx* ctx, int layer, const oasis_remote_
   T->map = local_map;
   T->count = local_map + pairs * ctx->cfg.max_blocks;
   T->base = T->count + pairs;
-  if (cudaEventCreateWithFlags(&T->ev_assigned, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&T->ev_moved, cudaEventDisableTiming) != cudaSuccess)
-    return ctx->fail(OASIS_ENOMEM, "remote_attach: events");
-  if (!ctx->net) {
-    int lo = 0, hi = 0;
-    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
-        cudaStreamCreateWithPriority(&ctx->net, cudaStreamNonBlocking, hi) != cudaSuccess)
-      return ctx->fail(OASIS_ENOMEM, "remote_attach: network stream");
+  if (!get_wait_value32() || !get_write_value32())
+    return ctx->fail(OASIS_ECUDA, "remote_attach: stream memory operations unavailable");
+  {
+    const size_t words = ((pairs + 2 * pairs * static_cast<size_t>(T->M)) * 4 + 15) / 16 * 16;
+    uint8_t* hb = reinterpret_cast<uint8_t*>(miss_lists) + words;
+    uint8_t* db = reinterpret_cast<uint8_t*>(T->lists_dev) + words;
+    T->assigned = reinterpret_cast<volatile uint32_t*>(hb);
+    T->moved = reinterpret_cast<volatile uint32_t*>(hb + 4);
+    T->assigned_dev = reinterpret_cast<CUdeviceptr>(db);
+    T->moved_dev = reinterpret_cast<CUdeviceptr>(db + 4);
+    *T->assigned = 0;
+    *T->moved = 0;
   }
+  T->remote = static_cast<const uint8_t*>(L.host);
+  T->NBmax = ctx->cfg.max_blocks;
+  T->all_pairs = static_cast<int>(pairs);
   T->pool.reset(new (std::nothrow) CopyPool(T->threads));
   if (!T->pool) return ctx->fail(OASIS_ENOMEM, "remote_attach: copy threads");
+  T->start();
   if (int rc = ctx->cuda(cudaMemsetAsync(T->map, 0xff, pairs * ctx->cfg.max_blocks * 4, ctx->side2),
                          "clear local map"))
     return rc;

@@ -374,4 +374,11 @@ cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
                            : launch_w<4>(a, pool_map, grid, s);
 }
 
+cudaError_t preload_attention_kernels() {
+  cudaFuncAttributes at;
+  cudaError_t e = cudaFuncGetAttributes(&at, attn_kernel<4>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&at, attn_kernel<3>);
+  return e;
+}
+
 }  // namespace oasis

@@ -374,4 +374,22 @@ cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s) {
   return launch_kpl<8>(a, s);
 }
 
+cudaError_t preload_score_kernels() {
+  cudaFuncAttributes at;
+  const void* fns[] = {
+      reinterpret_cast<const void*>(score_topk_kernel<1, 8>),
+      reinterpret_cast<const void*>(score_topk_kernel<2, 8>),
+      reinterpret_cast<const void*>(score_topk_kernel<4, 8>),
+      reinterpret_cast<const void*>(score_topk_kernel<8, 8>),
+      reinterpret_cast<const void*>(score_topk_kernel<1, 4>),
+      reinterpret_cast<const void*>(score_topk_kernel<2, 4>),
+      reinterpret_cast<const void*>(score_topk_kernel<4, 4>),
+      reinterpret_cast<const void*>(score_topk_kernel<8, 4>)};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncGetAttributes(&at, f);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace oasis

@@ -86,6 +86,7 @@ EXPORTS = {
     "oasis_score_admit_noalloc": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P, _P]),
     "oasis_prefetch": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
     "oasis_step": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
+    "oasis_wait": (c_int, [_P, c_int, c_double]),
     "oasis_join": (c_int, [_P, c_int, _P]),
     "oasis_step_host": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
     "oasis_step_lists": (c_int, [_P, c_int, c_int, POINTER(c_void_p), POINTER(c_void_p),
@@ -286,6 +287,14 @@ class Oasis:
         self._check(lib().oasis_step(self.ctx, layer, step, _ptr(q), _ptr(qd), _ptr(out),
                                      _ptr(outd), _stream(stream)))
 
+    def oasis_wait(self, layer: int, timeout_ms: float) -> bool:
+        """True when the layer's side work is done, False on timeout."""
+        rc = lib().oasis_wait(self.ctx, layer, float(timeout_ms))
+        if rc == OASIS_ETIMEOUT:
+            return False
+        self._check(rc)
+        return True
+
     def oasis_join(self, layer, stream=None) -> None:
         self._check(lib().oasis_join(self.ctx, layer, _stream(stream)))
 
@@ -338,7 +347,7 @@ class Oasis:
                  local_base=mp[pairs * NB + pairs:].view(R, Hkv), miss_lists=lists,
                  n_miss=lists[:pairs].view(R, Hkv),
                  miss_ids=lists[pairs:pairs + pairs * M].view(R, Hkv, M),
-                 miss_slots=lists[pairs + pairs * M:].view(R, Hkv, M))
+                 miss_slots=lists[pairs + pairs * M:pairs + 2 * pairs * M].view(R, Hkv, M))
         if not hasattr(self, "remote"):
             self.remote = {}
         self.remote[layer] = t
