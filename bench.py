@@ -1094,7 +1094,7 @@ def main():
                     help="remote tier (emulated disaggregated partial fetch) on the single-layer shape")
     ap.add_argument("--remote-gbps", type=float, nargs="+", default=[0.0, 50.0, 25.0],
                     help="emulated network rates for --remote (0 = unthrottled host copy)")
-    ap.add_argument("--remote-threads", type=int, default=8)
+    ap.add_argument("--remote-threads", type=int, default=16)
     ap.add_argument("--requests", type=int, default=0,
                     help="override the request count (small cases for profiling)")
     args = ap.parse_args()
