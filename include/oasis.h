@@ -193,6 +193,15 @@ OASIS_API int oasis_build_summaries(oasis_ctx* ctx, int layer, int table,
 OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step,
                                   void* stream);
 
+/* Support (resume from saved state): oasis_load_resident that keeps the
+ * stamps the caller wrote into the stamps buffer.  The state of a layer
+ * between steps is its caller-owned buffers: res_ids[t & 1], stamps and
+ * ctx_len[t & 1] (plus, with a remote tier, its local map and tier); saving
+ * them after step t - 1 and resuming with this call at first_step = t gives
+ * the same results as continuing. */
+OASIS_API int oasis_resume_resident(oasis_ctx* ctx, int layer, int first_step,
+                                    void* stream);
+
 /* a1: look-ahead attention ([R] *What carries the argument*, [V]
  * key_machinery: a single attention pass serves both the normal and the draft
  * token, reading one shared resident sparse set).  For every request r and query head j, separately for q and q_draft:

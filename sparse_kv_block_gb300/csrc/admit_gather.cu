@@ -154,6 +154,7 @@ __global__ void init_tables_kernel(int32_t* phys, int32_t* stamps, int pairs, in
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     phys[i] = static_cast<int32_t>(i % U);
   }
+  if (!stamps) return;  // resume: the caller's stamps stay
   const long long m = static_cast<long long>(pairs) * K;
   for (long long i = blockIdx.x * blockDim.x + threadIdx.x; i < m;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {

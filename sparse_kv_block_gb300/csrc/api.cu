@@ -931,7 +931,10 @@ OASIS_API int oasis_build_summaries(oasis_ctx* ctx, int layer, int table, void* 
                    "summary_build launch");
 }
 
-OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step, void* stream) {
+namespace {
+// Resident set res_ids[first_step & 1] into the pool, phys[first_step & 1]
+// reset to the identity; stamps reset to -1 unless keep_stamps.
+int load_resident(oasis_ctx* ctx, int layer, int first_step, bool keep_stamps, void* stream) {
   if (int rc = check_layer(ctx, layer)) return rc;
   if (first_step < 0) return ctx->fail(OASIS_EINVAL, "first_step must be >= 0");
   if (int rc = ctx->set_device()) return rc;
@@ -941,7 +944,8 @@ OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step, voi
     if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
   }
   const int pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
-  if (int rc = ctx->cuda(launch_init_tables(ctx->phys_tab(layer, first_step), L.stamps, pairs,
+  if (int rc = ctx->cuda(launch_init_tables(ctx->phys_tab(layer, first_step),
+                                            keep_stamps ? nullptr : L.stamps, pairs,
                                             ctx->cfg.topk, ctx->U, s),
                          "init tables launch"))
     return rc;
@@ -967,6 +971,16 @@ OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step, voi
   L.loaded = true;
   L.side_pending = false;
   return OASIS_OK;
+}
+
+}  // namespace
+
+OASIS_API int oasis_load_resident(oasis_ctx* ctx, int layer, int first_step, void* stream) {
+  return load_resident(ctx, layer, first_step, false, stream);
+}
+
+OASIS_API int oasis_resume_resident(oasis_ctx* ctx, int layer, int first_step, void* stream) {
+  return load_resident(ctx, layer, first_step, true, stream);
 }
 
 OASIS_API int oasis_lookahead_attn(oasis_ctx* ctx, int layer, int step, const void* q,

@@ -79,6 +79,7 @@ EXPORTS = {
     "oasis_sync": (c_int, [_P, POINTER(c_uint32)]),
     "oasis_build_summaries": (c_int, [_P, c_int, c_int, _P]),
     "oasis_load_resident": (c_int, [_P, c_int, c_int, _P]),
+    "oasis_resume_resident": (c_int, [_P, c_int, c_int, _P]),
     "oasis_lookahead_attn": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
     "oasis_dense_attn": (c_int, [_P, _P, c_int, _P, _P, _P, _P, _P]),
     "oasis_score_topk": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
@@ -253,6 +254,9 @@ class Oasis:
 
     def oasis_load_resident(self, layer: int, first_step: int = 0, stream=None) -> None:
         self._check(lib().oasis_load_resident(self.ctx, layer, first_step, _stream(stream)))
+
+    def oasis_resume_resident(self, layer: int, first_step: int, stream=None) -> None:
+        self._check(lib().oasis_resume_resident(self.ctx, layer, first_step, _stream(stream)))
 
     def oasis_lookahead_attn(self, layer, step, q, qd, out, outd, stream=None) -> None:
         self._check(lib().oasis_lookahead_attn(self.ctx, layer, step, _ptr(q), _ptr(qd),
