@@ -141,7 +141,7 @@ class ClockSampler:
                 "samples_under_load": len(loaded)}
 
 
-def build_layer(shape, seed, dev, side_groups=0, schedule=0):
+def build_layer(shape, seed, dev, side_groups=0, schedule=3):
     """Allocate and fill one layer (untimed setup); returns (engine, q, qd, lens, host)."""
     from sparse_kv_block_gb300.oasis import Oasis, make_config
     lens = workload.ctx_lens(shape)
@@ -1088,8 +1088,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--side-groups", type=int, default=0,
                     help="request groups of the side work (0 = library default)")
-    ap.add_argument("--schedule", type=int, default=0,
-                    help="0 scan first, 1 concurrent, 2 the pages' three background streams")
+    ap.add_argument("--schedule", type=int, default=3,
+                    help="0 scan first, 1 concurrent, 2 the pages' three background streams, "
+                         "3 auto (scan first on device buffers, concurrent on host buffers)")
     ap.add_argument("--remote", action="store_true",
                     help="remote tier (emulated disaggregated partial fetch) on the single-layer shape")
     ap.add_argument("--remote-gbps", type=float, nargs="+", default=[0.0, 50.0, 25.0],

@@ -373,7 +373,7 @@ const char* config_error(const oasis_config* c) {
   if (c->max_blocks > kMaxBlocksPerHead) return "max_blocks must be <= 131072";
   if (c->side_groups < 0 || c->side_groups > 64) return "side_groups must be in 0..64";
   if (c->schedule != OASIS_SCHEDULE_SCAN_FIRST && c->schedule != OASIS_SCHEDULE_CONCURRENT &&
-      c->schedule != OASIS_SCHEDULE_THREE_STREAMS)
+      c->schedule != OASIS_SCHEDULE_THREE_STREAMS && c->schedule != OASIS_SCHEDULE_AUTO)
     return "schedule must be one of OASIS_SCHEDULE_*";
   const double units = static_cast<double>(c->num_requests) * c->num_kv_heads *
                        (c->topk + fetch_cap(*c)) * 2 * kBlock;
@@ -1093,9 +1093,23 @@ OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t*
                       static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_draft, void* out,
+              void* out_draft, void* stream, int schedule);
+}  // namespace
+
 OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
                          const void* q_draft, void* out, void* out_draft, void* stream) {
   NvtxRange nvtx("oasis_step");
+  if (!ctx) return OASIS_EINVAL;
+  const int sched = ctx->cfg.schedule == OASIS_SCHEDULE_AUTO ? OASIS_SCHEDULE_SCAN_FIRST
+                                                              : ctx->cfg.schedule;
+  return step_impl(ctx, layer, step, q, q_draft, out, out_draft, stream, sched);
+}
+
+namespace {
+int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_draft, void* out,
+              void* out_draft, void* stream, int schedule) {
   if (int rc = check_layer(ctx, layer)) return rc;
   if (step < 0 || step > (1 << 30) || !q || !q_draft || !out || !out_draft)
     return ctx->fail(OASIS_EINVAL, "step: bad step or null pointer");
@@ -1131,7 +1145,7 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
     const int p0 = static_cast<int>(static_cast<long long>(pairs) * g / ctx->groups);
     const int p1 = static_cast<int>(static_cast<long long>(pairs) * (g + 1) / ctx->groups);
     const LayerState::Lists& Ls = L.lists[step & 1];
-    if (ctx->cfg.schedule == OASIS_SCHEDULE_THREE_STREAMS) {
+    if (schedule == OASIS_SCHEDULE_THREE_STREAMS) {
       // The pages' pipeline: top-K prediction, KV selection and KV transfer
       // on three streams, each stage of a group ordered by an event.
       if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side,
@@ -1173,7 +1187,7 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
     if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[0], 0), "group wait"))
       return rc;
   }
-  if (ctx->cfg.schedule == OASIS_SCHEDULE_SCAN_FIRST) {
+  if (schedule == OASIS_SCHEDULE_SCAN_FIRST) {
     // The scan gets the whole HBM bandwidth and the SMs first, so the
     // gathers (host-link bound) start as early as possible; the attention
     // then overlaps the gathers, which write only spare units.
@@ -1185,6 +1199,8 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
   L.side_pending = true;
   return OASIS_OK;
 }
+
+}  // namespace
 
 OASIS_API int oasis_wait(oasis_ctx* ctx, int layer, double timeout_ms) {
   NvtxRange nvtx("oasis_wait");
@@ -1245,8 +1261,13 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
     return rc;
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_in[slot], ctx->io), "record inputs")) return rc;
   if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_in[slot], 0), "wait inputs")) return rc;
-  if (int rc = oasis_step(ctx, layer, step, L.q_stage[slot], L.qd_stage[slot], L.out_stage,
-                          L.outd_stage, stream))
+  // AUTO: with host buffers the attention starts at once, so the output
+  // copy back to the host overlaps the next step's scan instead of delaying
+  // it (measured end to end: 2912 against 2814 layer-steps/s scan-first).
+  const int sched = ctx->cfg.schedule == OASIS_SCHEDULE_AUTO ? OASIS_SCHEDULE_CONCURRENT
+                                                              : ctx->cfg.schedule;
+  if (int rc = step_impl(ctx, layer, step, L.q_stage[slot], L.qd_stage[slot], L.out_stage,
+                         L.outd_stage, stream, sched))
     return rc;
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_stage_free[slot], s), "record stage")) return rc;
   L.stage_used[slot] = true;

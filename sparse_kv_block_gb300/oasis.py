@@ -31,7 +31,7 @@ class oasis_config(ctypes.Structure):
                 ("side_groups", c_int32), ("schedule", c_int32)]
 
 
-SCHEDULE_SCAN_FIRST, SCHEDULE_CONCURRENT, SCHEDULE_THREE_STREAMS = 0, 1, 2
+SCHEDULE_SCAN_FIRST, SCHEDULE_CONCURRENT, SCHEDULE_THREE_STREAMS, SCHEDULE_AUTO = 0, 1, 2, 3
 
 
 class oasis_sizes(ctypes.Structure):
@@ -145,7 +145,7 @@ def _stream(s) -> Optional[int]:
 
 def make_config(R, NBmax, Hq, Hkv, K, fetch_ratio, layers=1, softmax_scale=0.0,
                 out_fp32=False, device=0, d=128, B=16, side_groups=0,
-                schedule=0) -> oasis_config:
+                schedule=SCHEDULE_AUTO) -> oasis_config:
     return oasis_config(layers, R, NBmax, Hq, Hkv, d, B, K, fetch_ratio, softmax_scale,
                         1 if out_fp32 else 0, device, side_groups, schedule)
 

@@ -123,11 +123,13 @@ def test_host_buffer_step_matches_device_step(dev):
     eng.close()
 
 
-def test_host_buffer_steps_back_to_back(dev):
+@pytest.mark.parametrize("schedule", [0, 3])
+def test_host_buffer_steps_back_to_back(dev, schedule):
     # oasis_step_host issued for consecutive steps with no host wait between
-    # them: step t + 1's input copies may overlap step t's side work.
+    # them: step t + 1's input copies may overlap step t's side work.  The
+    # automatic schedule runs host-buffer steps concurrently.
     sh = dataclasses.replace(TINY, R=5)
-    L = H.make_layer(sh, seed=9, steps=6, fetch_ratio=0.25, out_fp32=False)
+    L = H.make_layer(sh, seed=9, steps=6, fetch_ratio=0.25, out_fp32=False, schedule=schedule)
     eng = L.eng
 
     def pinned():
