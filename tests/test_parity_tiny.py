@@ -72,7 +72,7 @@ def test_small_groups_and_many_requests(dev):
 
 
 @pytest.mark.parametrize("groups,R,schedule", [(0, 2, 0), (3, 5, 0), (10, 5, 0), (3, 5, 1),
-                                               (3, 5, 2), (0, 2, 2)])
+                                               (3, 5, 2), (0, 2, 2), (0, 5, 3)])
 def test_fused_step_matches_oracle(dev, groups, R, schedule):
     # oasis_step: fused scan + top-K + admission per request group on one side
     # stream, gathers per group on another; uneven and one-pair groups too;
