@@ -673,6 +673,7 @@ def run_oasis_layers(args, ws, rank, local):
     eng.oasis_profile_enable(True)
     barrier(ws)
     torch.cuda.synchronize(dev)
+    step_spread = None
     if drift:
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
@@ -684,7 +685,11 @@ def run_oasis_layers(args, ws, rank, local):
             ev[i][1].record(main)
             drift_between_steps()
         torch.cuda.synchronize(dev)
-        ms = sum(a.elapsed_time(b) for a, b in ev)
+        per_step = sorted(a.elapsed_time(b) for a, b in ev)
+        ms = sum(per_step)
+        step_spread = {"min": round(per_step[0], 3),
+                       "median": round(per_step[len(per_step) // 2], 3),
+                       "max": round(per_step[-1], 3)}
     else:
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -742,6 +747,8 @@ def run_oasis_layers(args, ws, rank, local):
                           "bytes_per_layer_step": int(link_bytes),
                           "achieved_gbs_whole_step": round(link_bytes * value / 1e9, 1)},
             "kernels": per, "gpu_launches": int(sum(counts)), "clocks": clk}
+    if step_spread is not None:
+        line["step_ms_spread"] = step_spread
     if rank == 0:
         print(json.dumps(line), flush=True)
     eng.close()
