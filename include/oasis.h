@@ -30,7 +30,8 @@
  *     of the context and reports deferred device-side errors.
  *   - Ownership: every buffer is allocated by the caller and lent to the
  *     library for the life of the context; the library never frees it.  The
- *     library itself allocates only CUDA streams and events.  oasis_query_sizes
+ *     library itself allocates only CUDA streams and events (and, with a
+ *     remote tier, host threads and their queues).  oasis_query_sizes
  *     reports every buffer size.
  *   - Shapes: R requests, Hq query heads, Hkv KV heads (G = Hq/Hkv <= 4), head
  *     dim d = 128, block size B = 16, K resident blocks per (request, KV head),
@@ -426,9 +427,10 @@ OASIS_API int oasis_remote_attach(oasis_ctx* ctx, int layer,
                                   int32_t* miss_lists);
 
 /* Totals of the layer's emulated network transfers since attach: units
- * (8 KiB each) moved remote -> local, host callbacks run, and seconds those
- * callbacks took (throttle included); bad_entries counts list entries the
- * callbacks skipped as out of range (0 unless the lists were corrupted).
+ * (8 KiB each) moved remote -> local, transfers made, and seconds the
+ * worker spent copying (throttle included); bad_entries counts list entries
+ * the worker skipped as out of range, plus transfers it gave up waiting for
+ * (0 unless something went wrong).
  * Read after oasis_sync for a settled value.  Any output may be NULL. */
 OASIS_API int oasis_remote_stats(oasis_ctx* ctx, int layer, int64_t* units,
                                  int64_t* transfers, double* seconds,
