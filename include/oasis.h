@@ -340,10 +340,11 @@ OASIS_API int oasis_step_lists(oasis_ctx* ctx, int layer, int step,
 
 /* Support (a0, growing contexts): append one token per request to `layer`.
  * k_new, v_new: dev [R][Hkv][d] bf16.  The token goes to position
- * p = ctx_len[step & 1][r]: written into the host store, folded into the
- * tail block's summary (a new block starts at min = max = key), and written
- * into the resident copy if block p / B is resident in table
- * ((step + 1) & 1).  Runs after the layer's side work of step `step`. */
+ * p = ctx_len[step & 1][r]: written into the host store (with a remote tier:
+ * into the block's local slot, see below), folded into the tail block's
+ * summary (a new block starts at min = max = key), and written into the
+ * resident copy if block p / B is resident in table ((step + 1) & 1).  Runs
+ * after the layer's side work of step `step`. */
 OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step,
                                  const void* k_new, const void* v_new,
                                  void* stream);
@@ -386,8 +387,12 @@ OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow,
  * the units just fetched after a stream wait for that number.
  *
  * With a remote tier attached to a layer, host_kv (given to oasis_init) is the
- * remote store, pinned and mapped as before; oasis_append_token is refused
- * (OASIS_ESTATE) for that layer.
+ * remote store, pinned and mapped as before.  oasis_load_resident also brings
+ * the block each request's context ends in (if it ends inside a block) to the
+ * local tier, since decoding appends there; oasis_append_token then writes a
+ * decoded token into its block's local slot, a block the token opens taking
+ * the next free slot (OASIS_DEVERR_NOT_LOCAL if none is left), and never into
+ * the remote store.  oasis_refresh_blocks is refused (OASIS_ESTATE).
  *
  * Layouts:
  *   local_tier pinned [R][Hkv][capacity][2][B][d]   bf16   local slots

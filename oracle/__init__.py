@@ -188,15 +188,31 @@ class LayerOracle:
         self.pairs = [tuple(int(x) for x in p) for p in pairs]
         self.scale = 1.0 / np.sqrt(self.d) if scale is None else scale
         self._scores = np.empty(self.NBmax, dtype=np.float32)
-        # Remote tier: the decode side's slot map and slot count per pair; the
-        # initial resident set is fetched first (in slot order).
+        # Remote tier: the decode side's slot map and slot count per pair.
+        # At load the initial resident set is fetched (in slot order), then
+        # the block each context ends in when it ends inside a block (decoding
+        # appends there).  initial_misses is that last assignment.
         self.remote_capacity = remote_capacity
-        self.initial_misses = {}
+        self.resident_misses, self.initial_misses = {}, {}
         if remote_capacity is not None:
             self.local_map = np.full((self.R, self.Hkv, self.NBmax), -1, dtype=np.int32)
             self.local_count = np.zeros((self.R, self.Hkv), dtype=np.int32)
             for (r, h) in self.pairs:
-                self.initial_misses[(r, h)] = self._fetch(r, h, self.res[r, h])
+                self.resident_misses[(r, h)] = self._fetch(r, h, self.res[r, h])
+                c = int(self.ctx_len[r])
+                tail = [c // self.B] if c > 0 and c % self.B else []
+                self.initial_misses[(r, h)] = self._fetch(r, h, np.array(tail, dtype=np.int32))
+
+    def append_local(self, r):
+        """Remote tier: a token appended to request r at position ctx_len[r]
+        goes to its block's local slot; a block it opens takes the next slot.
+        Returns True if some head found no slot left."""
+        full = False
+        c = int(self.ctx_len[r])
+        for (rr, h) in self.pairs:
+            if rr == r:
+                full |= self._fetch(r, h, np.array([c // self.B], dtype=np.int32))["full"]
+        return full
 
     def _fetch(self, r, h, ids):
         cnt = self.local_count[r, h:h + 1].copy()

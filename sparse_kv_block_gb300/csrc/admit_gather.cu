@@ -288,7 +288,29 @@ __global__ void append_kernel(const AppendArgs a) {
   const uint4 v = (kvsel ? static_cast<const uint4*>(a.v_new)
                          : static_cast<const uint4*>(a.k_new))[static_cast<size_t>(pair) * 16 + dch];
   const size_t unit_host = static_cast<size_t>(pair) * a.NBmax + b;
-  uint4* hrow = static_cast<uint4*>(a.host) + unit_host * (kUnitBytes / 16) +
+  size_t unit_store = unit_host;
+  if (a.local_map) {
+    // The decode side's copy of block b: its local slot, or a fresh slot for
+    // a block this token opens.  One warp per pair: no other writer.
+    int slot = a.local_map[unit_host];
+    if (slot < 0 && tk == 0) {
+      const int c = a.local_count[pair];
+      if (c < a.capacity) {
+        slot = c;
+        __syncwarp();
+        if (lane == 0) {
+          a.local_count[pair] = c + 1;
+          a.local_map[unit_host] = c;
+        }
+      }
+    }
+    if (slot < 0) {
+      if (lane == 0) raise_error(a.err, kErrNotLocal);
+      return;
+    }
+    unit_store = static_cast<size_t>(pair) * a.capacity + slot;
+  }
+  uint4* hrow = static_cast<uint4*>(a.host) + unit_store * (kUnitBytes / 16) +
                 (kvsel * kBlock + tk) * (kHeadDim / 8) + dch;
   *hrow = v;
   if (kvsel == 0) {
@@ -402,6 +424,21 @@ cudaError_t launch_refresh(const RefreshArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+__global__ void tail_blocks_kernel(const int32_t* ctx_len, int R, int Hkv, int32_t* tail) {
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= R * Hkv) return;
+  const int c = ctx_len[p / Hkv];
+  tail[p] = (c > 0 && c % kBlock != 0) ? c / kBlock : -1;
+}
+
+cudaError_t launch_tail_blocks(const int32_t* ctx_len, int R, int Hkv, int32_t* tail,
+                               cudaStream_t s) {
+  const int pairs = R * Hkv;
+  if (pairs == 0) return cudaSuccess;
+  tail_blocks_kernel<<<(pairs + 255) / 256, 256, 0, s>>>(ctx_len, R, Hkv, tail);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
   const int pairs = a.R * a.Hkv;
   if (pairs == 0) return cudaSuccess;
@@ -426,7 +463,8 @@ cudaError_t preload_support_kernels() {
       reinterpret_cast<const void*>(init_tables_kernel),
       reinterpret_cast<const void*>(summary_build_kernel),
       reinterpret_cast<const void*>(refresh_kernel), reinterpret_cast<const void*>(append_kernel),
-      reinterpret_cast<const void*>(advance_kernel)};
+      reinterpret_cast<const void*>(advance_kernel),
+      reinterpret_cast<const void*>(tail_blocks_kernel)};
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncGetAttributes(&at, f);
     if (e != cudaSuccess) return e;

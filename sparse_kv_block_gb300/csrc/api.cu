@@ -629,6 +629,15 @@ int run_remote_fetch(oasis_ctx* ctx, int layer, const int32_t* ids, const int32_
   return OASIS_OK;
 }
 
+// Make `s` wait until the tier's worker has finished the latest transfer.
+int wait_remote(oasis_ctx* ctx, const RemoteTier& T, cudaStream_t s) {
+  auto wait = get_wait_value32();
+  if (!wait) return ctx->fail(OASIS_ECUDA, "cuStreamWaitValue32 unavailable");
+  if (wait(s, T.moved_dev, T.next_seq, CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS)
+    return ctx->fail(OASIS_ECUDA, "remote: stream wait for the transfer failed");
+  return OASIS_OK;
+}
+
 // With a remote tier the gather runs in two launches: the units already held
 // in the local tier (slot < base) at once, beside the network transfer, and
 // the units this assignment fetched (slot >= base) after it.
@@ -639,10 +648,7 @@ int launch_gather_split(oasis_ctx* ctx, const LayerState& L, GatherArgs g, cudaS
   }
   g.phase = 1;
   if (int rc = ctx->cuda(launch_gather(g, s), "gather launch (held units)")) return rc;
-  auto wait = get_wait_value32();
-  if (!wait) return ctx->fail(OASIS_ECUDA, "cuStreamWaitValue32 unavailable");
-  if (wait(s, L.remote->moved_dev, L.remote->next_seq, CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS)
-    return ctx->fail(OASIS_ECUDA, "remote: stream wait for the transfer failed");
+  if (int rc = wait_remote(ctx, *L.remote, s)) return rc;
   g.phase = 2;
   return ctx->cuda(launch_gather(g, s), "gather launch (fetched units)");
 }
@@ -968,6 +974,18 @@ int load_resident(oasis_ctx* ctx, int layer, int first_step, bool keep_stamps, v
   g.NBmax = ctx->cfg.max_blocks;
   g.U = ctx->U;
   if (int rc = launch_gather_split(ctx, L, g, s)) return rc;
+  if (L.remote) {
+    // The block each request's context ends in (decoding appends there
+    // first) also travels to the local tier; the list borrows a workspace
+    // buffer no step uses yet.
+    int32_t* tail = L.lists[1].topk_ids;
+    if (int rc = ctx->cuda(launch_tail_blocks(ctx->ctx_tab(first_step), ctx->cfg.num_requests,
+                                              ctx->cfg.num_kv_heads, tail, s),
+                           "tail blocks launch"))
+      return rc;
+    if (int rc = run_remote_fetch(ctx, layer, tail, nullptr, 1, 0, pairs, s)) return rc;
+    if (int rc = wait_remote(ctx, *L.remote, s)) return rc;
+  }
   L.loaded = true;
   L.side_pending = false;
   return OASIS_OK;
@@ -1300,8 +1318,6 @@ OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step, const void
   if (int rc = ctx->set_device()) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   LayerState& L = ctx->layers[layer];
-  if (L.remote)
-    return ctx->fail(OASIS_ESTATE, "append: layer %d has a remote tier attached", layer);
   // The token may land in a block this layer's side work is copying.
   if (L.side_pending) {
     if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
@@ -1309,7 +1325,10 @@ OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step, const void
   AppendArgs a{};
   a.k_new = k_new;
   a.v_new = v_new;
-  a.host = L.host_dev;
+  a.host = L.remote ? L.remote->local_dev : L.host_dev;
+  a.local_map = L.remote ? L.remote->map : nullptr;
+  a.local_count = L.remote ? L.remote->count : nullptr;
+  a.capacity = L.remote ? L.remote->capacity : 0;
   a.summ = L.summ;
   a.pool = L.pool;
   a.ctx_len = ctx->ctx_tab(step);

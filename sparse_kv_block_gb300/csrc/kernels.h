@@ -122,7 +122,13 @@ struct RefreshArgs {
 struct AppendArgs {
   const void* k_new;         // [R][Hkv][d]
   const void* v_new;
-  void* host;                // device alias of the pinned store
+  void* host;                // device alias of the pinned store (or local tier)
+  // Remote tier: the token goes to the block's local slot; a block that
+  // starts with this token gets the next free slot (count[p]++ while below
+  // capacity).  Null without a remote tier.
+  int32_t* local_map;        // [R][Hkv][NBmax]
+  int32_t* local_count;      // [R][Hkv]
+  int capacity;
   void* summ;
   void* pool;
   const int32_t* ctx_len;    // the step's table
@@ -143,6 +149,10 @@ cudaError_t launch_init_tables(int32_t* phys, int32_t* stamps, int pairs,
 cudaError_t launch_summary_build(const SummaryArgs& a, cudaStream_t s);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_refresh(const RefreshArgs& a, cudaStream_t s);
+// tail[p] = last block of request p / Hkv if its context ends inside a block,
+// else -1 (the blocks a decode side appends into first).
+cudaError_t launch_tail_blocks(const int32_t* ctx_len, int R, int Hkv, int32_t* tail,
+                               cudaStream_t s);
 cudaError_t launch_advance(const int32_t* cur, int32_t* nxt, int R, int grow,
                            cudaStream_t s);
 

@@ -413,7 +413,8 @@ def test_remote_fetch_oracle_layer_tracks_admissions():
                              remote_capacity=shape.NBmax)
     seen = {p: [int(x) for x in res0[p] if x >= 0] for p in pairs}
     for p in pairs:
-        assert orc.initial_misses[p]["miss_ids"].tolist() == seen[p]
+        assert orc.resident_misses[p]["miss_ids"].tolist() == seen[p]
+        assert orc.initial_misses[p]["n_miss"] == 0          # 1024-token contexts: no tail
     q, qd = workload.queries(shape, 0, 0, 4, device="cpu")
     for t in range(4):
         out = orc.step(workload.bf16_bits(q[t]), workload.bf16_bits(qd[t]), t)
@@ -424,3 +425,30 @@ def test_remote_fetch_oracle_layer_tracks_admissions():
             assert out[p]["miss_slots"].tolist() == list(range(len(seen[p]), len(seen[p]) + len(new)))
             seen[p] += new
             assert int(orc.local_count[p]) == len(seen[p])
+
+
+def test_remote_oracle_tail_fetch_and_appends():
+    """Remote tier with ragged contexts: the load fetches the resident set and
+    then each context's partial tail block; appends inside a held block take
+    no slot, an append that opens a block takes the next one."""
+    from sparse_kv_block_gb300 import workload
+    shape = workload.SHAPES["tiny"]
+    lens = np.array([1000, 32], dtype=np.int32)          # 1000 = 62*16 + 8; 32 = 2*16
+    kv = workload.bf16_bits(workload.host_kv(shape, 0, 0, lens, device="cpu"))
+    summ = oracle.summary_build(kv, lens)
+    res0 = workload.initial_resident(shape, 0, 0, lens)
+    pairs = [(0, 0), (1, 0)]
+    orc = oracle.LayerOracle(kv, summ, lens.copy(), res0, shape.K, shape.C, pairs,
+                             remote_capacity=shape.NBmax)
+    # request 0: tail block 62 fetched unless resident already
+    tail0 = orc.initial_misses[(0, 0)]
+    assert tail0["miss_ids"].tolist() == ([] if 62 in res0[0, 0] else [62])
+    assert orc.local_map[0, 0, 62] >= 0
+    # request 1: context ends on a block boundary, nothing extra
+    assert orc.initial_misses[(1, 0)]["n_miss"] == 0
+    c0 = orc.local_count.copy()
+    assert orc.append_local(0) is False                  # position 1000: inside block 62
+    assert (orc.local_count == c0).all()
+    assert orc.append_local(1) is False                  # position 32: opens block 2
+    assert orc.local_count[1, 0] == c0[1, 0] + (0 if 2 in res0[1, 0] else 1)
+    assert orc.local_map[1, 0, 2] >= 0

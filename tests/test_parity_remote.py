@@ -125,7 +125,7 @@ def test_remote_tier_overflow_is_reported(dev):
     eng.close()
 
 
-def test_remote_throttle_and_append_refused(dev):
+def test_remote_throttle_and_refresh_refused(dev):
     sh = dataclasses.replace(TINY, R=2)
     gbps = 0.25
     L = H.make_layer(sh, seed=15, steps=3, fetch_ratio=0.25, remote_capacity=sh.NBmax,
@@ -133,11 +133,65 @@ def test_remote_throttle_and_append_refused(dev):
     for t in range(3):
         H.run_staged_step(L, t, dev)
     st = L.eng.oasis_remote_stats(0)
-    assert st["transfers"] == 4   # the load, then one per step
+    assert st["transfers"] == 5   # the load (resident set, then tail blocks), one per step
     assert st["units"] == int(L.orc.local_count.sum())
     assert st["seconds"] >= st["units"] * 8192 / (gbps * 1e9) * 0.999
-    k = torch.zeros((sh.R, sh.Hkv, 128), dtype=torch.bfloat16, device=dev)
+    ids = torch.zeros((sh.R, sh.Hkv, 1), dtype=torch.int32, device=dev)
+    n = torch.zeros((sh.R, sh.Hkv), dtype=torch.int32, device=dev)
     with pytest.raises(OasisError) as e:
-        L.eng.oasis_append_token(0, 3, k, k)
+        L.eng.oasis_refresh_blocks(0, 3, ids, n)
     assert e.value.status == OASIS_ESTATE
     L.eng.close()
+
+
+@pytest.mark.parametrize("lens0", [[1000, 37], [992, 16]])
+def test_remote_with_growing_contexts(dev, lens0):
+    # Decoding with a remote tier: the load also brings each context's
+    # partial tail block to the local tier; appended tokens go to local slots
+    # (a block a token opens takes the next slot); the remote store is never
+    # written.  The oracle keeps its own copy of the store with the appends.
+    steps = 30
+    sh = dataclasses.replace(TINY, ctx=max(lens0), grow_steps=steps)
+    lens = np.array(lens0, dtype=np.int32)
+    L = H.make_layer(sh, seed=16, steps=steps, lens=lens, fetch_ratio=0.25, out_fp32=True,
+                     remote_capacity=sh.NBmax)
+    eng = L.eng
+    remote_before = L.hb.copy()
+    hb_orc, summ_orc, lens_o = L.hb.copy(), L.summ.copy(), L.lens.copy()
+    orc = oracle.LayerOracle(hb_orc, summ_orc, lens_o, L.res0, sh.K, sh.C, L.orc.pairs,
+                             remote_capacity=sh.NBmax)
+    T = L.remote
+    assert (T["local_map"].cpu().numpy() == orc.local_map).all()
+    out = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
+    outd = torch.empty_like(out)
+    for t in range(steps):
+        eng.oasis_step(0, t, L.q[t].to(dev), L.qd[t].to(dev), out, outd)
+        k_new, v_new = workload.new_tokens(sh, 16, 0, t)
+        eng.oasis_append_token(0, t, k_new.to(dev), v_new.to(dev))
+        eng.oasis_advance_context(t, 1)
+        eng.oasis_join(0)
+        eng.oasis_sync()
+        ref = orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        kb, vb = workload.bf16_bits(k_new), workload.bf16_bits(v_new)
+        for r in range(sh.R):
+            assert not orc.append_local(r)
+            oracle.append_token(hb_orc, summ_orc, lens_o, kb[r], vb[r], r)
+        lens_o += 1
+        H.check_attention([out.cpu().numpy(), outd.cpu().numpy()], ref, sh.G)
+        lmap = T["local_map"].cpu().numpy()
+        assert (lmap == orc.local_map).all(), t
+        assert (T["local_count"].cpu().numpy() == orc.local_count).all(), t
+        local = workload.bf16_bits(T["local_tier"])
+        for (r, h) in orc.pairs:
+            for b in np.nonzero(lmap[r, h] >= 0)[0]:
+                np.testing.assert_array_equal(local[r, h, lmap[r, h, b]], hb_orc[r, h, b])
+        nxt = (t + 1) & 1
+        res = eng.res_ids[0][nxt].cpu().numpy()
+        phys = eng.phys[0][nxt].cpu().numpy()
+        pool = workload.bf16_bits(eng.kv_pool[0].cpu())
+        for (r, h) in orc.pairs:
+            for s_ in range(sh.K):
+                if res[r, h, s_] >= 0:
+                    np.testing.assert_array_equal(pool[r, h, phys[r, h, s_]], hb_orc[r, h, res[r, h, s_]])
+    np.testing.assert_array_equal(L.hb, remote_before)      # the remote store is untouched
+    eng.close()
