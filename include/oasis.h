@@ -166,21 +166,25 @@ OASIS_API const char* oasis_config_error(const oasis_config* cfg);
  * no GPU).  EINVAL on an unsupported configuration. */
 OASIS_API int oasis_query_sizes(const oasis_config* cfg, oasis_sizes* out);
 
-/* Validate cfg and bufs, map the host stores, build the TMA descriptors and
- * create the side stream and events.  Buffers are not initialised: call
- * oasis_build_summaries and oasis_load_resident per layer before its first
- * step. */
+/* Validate cfg and bufs, map the host stores, build the TMA descriptors,
+ * create the streams and events and load every kernel.  Buffers are not
+ * initialised: call oasis_build_summaries and oasis_load_resident per layer
+ * before its first step.  Errors: OASIS_EINVAL for a bad configuration, a
+ * null or misaligned buffer (16 bytes; the workspace 256) or a host store
+ * that is not page-locked memory mapped for the device; OASIS_ENOMEM if a
+ * stream or event cannot be created; OASIS_ECUDA for a failed CUDA call.
+ * *out is NULL on failure. */
 OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
                          oasis_ctx** out);
 
-/* Wait for the context's work and release its streams and events (not the
- * caller's buffers).  NULL is accepted. */
+/* Wait for the context's work and release its streams, events and threads
+ * (not the caller's buffers).  NULL is accepted. */
 OASIS_API int oasis_destroy(oasis_ctx* ctx);
 
 /* Message for the last failed call on ctx (never NULL). */
 OASIS_API const char* oasis_last_error(const oasis_ctx* ctx);
 
-/* Wait for all work of the context (both streams) and return OASIS_EDEVICE if
+/* Wait for all work of the device and return OASIS_EDEVICE if
  * a kernel raised a device error bit since the last oasis_sync (the bits are
  * then cleared; *device_bits receives them when non-NULL). */
 OASIS_API int oasis_sync(oasis_ctx* ctx, uint32_t* device_bits);
