@@ -1,15 +1,15 @@
 """Soak: thousands of fused steps issued back to back (double-buffered
 tables and lists, side streams reused every step) keep every invariant: no
-device error bits, distinct resident ids, each table's units a permutation,
-every resident pool unit byte-equal to its host block, and attention equal
-to the oracle's over the GPU's own resident table."""
+device error bits, a full set of distinct resident ids in range, each
+table's units a permutation, and every resident pool unit byte-equal to its
+host block.  (Parity with the oracle is covered by the lockstep tests; here
+no oracle is fed anything the GPU produced.)"""
 import dataclasses
 
 import numpy as np
 import pytest
 import torch
 
-import oracle
 from sparse_kv_block_gb300 import workload
 from tests import _harness as H
 
@@ -42,15 +42,6 @@ def test_three_thousand_steps(dev):
         step += 1
         eng.oasis_join(0)
         assert eng.oasis_sync() == 0
-        # attention of step t against the oracle over the table step t read
-        res = eng.res_ids[0][t & 1].cpu().numpy()
-        o = out.cpu().numpy()
-        qb, qdb = workload.bf16_bits(L.q[t % nq]), workload.bf16_bits(L.qd[t % nq])
-        for r in range(sh.R):
-            for h in range(sh.Hkv):
-                ref = oracle.attention_rh(L.hb, L.lens, res, qb, qdb, r, h)
-                got = o[r, h * sh.G:(h + 1) * sh.G]
-                assert np.abs(got - ref[0]).max() <= H.ATT_MAX_ABS
         # tables after step t (the next step's) and the pool
         nxt = (t + 1) & 1
         resn = eng.res_ids[0][nxt].cpu().numpy()
@@ -58,5 +49,6 @@ def test_three_thousand_steps(dev):
             for h in range(sh.Hkv):
                 ids = resn[r, h][resn[r, h] >= 0]
                 assert len(set(ids.tolist())) == len(ids) == sh.K
+                assert ids.min() >= 0 and ids.max() < sh.NBmax
         H.check_pool(L, nxt)
     eng.close()
