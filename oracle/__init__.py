@@ -221,15 +221,11 @@ class LayerOracle:
         self.local_count[r, h] = cnt[0]
         return dict(miss_ids=mi, miss_slots=ms, n_miss=len(mi), full=full)
 
-    def step(self, q, qd, t, topk_override=None):
-        """Run one layer-step for every tracked pair.
-
-        ``topk_override`` maps (r, h) -> a top-K list to use for the eviction
-        in place of the oracle's own (used to hold both sides in lockstep when
-        an id inside the tie window differs).  Returns a dict keyed by (r, h)
-        with attn [2][G][d], scores, topk, admit_ids, admit_slots, evict_ids,
-        n_admit.
-        """
+    def step(self, q, qd, t):
+        """Run one layer-step for every tracked pair, on the oracle's own
+        state only.  Returns a dict keyed by (r, h) with attn [2][G][d],
+        scores, topk, admit_ids, admit_slots, evict_ids, n_admit (and, with
+        a remote tier, the slot assignment's miss lists)."""
         L = _load()
         Hq = q.shape[1]
         out = {}
@@ -248,10 +244,7 @@ class LayerOracle:
                 "score_rh")
             nb = min(num_blocks(int(self.ctx_len[r]), self.B), self.NBmax)
             topk = topk_rh(scores, nb, self.K)
-            used = topk
-            if topk_override is not None and (r, h) in topk_override:
-                used = np.ascontiguousarray(topk_override[(r, h)], dtype=np.int32)
-            a, s, e, n = admit_evict_rh(self.res[r, h], self.stamp[r, h], used,
+            a, s, e, n = admit_evict_rh(self.res[r, h], self.stamp[r, h], topk,
                                         self.C, t)
             out[(r, h)] = dict(attn=attn, scores=scores, topk=topk, admit_ids=a,
                                admit_slots=s, evict_ids=e, n_admit=n)
