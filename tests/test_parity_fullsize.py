@@ -135,3 +135,21 @@ def test_fetch_cap_extremes_full_layer(dev, ratio):
         for v in ref.values():
             assert v["n_admit"] <= L.shape.C
     L.eng.close()
+
+
+def test_remote_tier_full_layer(dev):
+    # The remote tier on the 128 x 16K layer (local tier of NBmax slots): the
+    # sampled pairs' slot assignment, slot map, local copies and pool follow
+    # the oracle through staged and fused steps.
+    sh = workload.SHAPES["qwen3_8b_16k"]
+    sample = [(3, 1), (64, 5), (126, 2)]
+    L = H.make_layer(sh, seed=94, steps=4, gen_device="cuda", pairs=sample,
+                     remote_capacity=sh.NBmax)
+    H.check_remote(L, L.orc.initial_misses)
+    for t in range(2):
+        ref = H.run_staged_step(L, t, dev, check_pool_every=False)
+        H.check_remote(L, ref)
+        H.check_pool(L, (t + 1) & 1, sample)
+    live = fused_steps(L, dev, range(2, 4), sample, sh.K)
+    assert L.eng.oasis_remote_stats(0)["bad_entries"] == 0
+    L.eng.close()
