@@ -153,3 +153,60 @@ def test_remote_tier_full_layer(dev):
     live = fused_steps(L, dev, range(2, 4), sample, sh.K)
     assert L.eng.oasis_remote_stats(0)["bad_entries"] == 0
     L.eng.close()
+
+
+def test_two_layers_of_the_36_layer_workload(dev):
+    # Two full-size layers (90 x 16K each, own stores) stepped in layer order
+    # on one stream without host synchronisation, as the multi-layer
+    # benchmark does: each layer's side work overlaps the next layer.
+    from sparse_kv_block_gb300.oasis import Oasis, make_config
+    sh = workload.SHAPES["qwen3_8b_36l"]
+    nl, steps = 2, 3
+    sample = [(2, 0), (45, 6), (88, 3)]
+    lens = workload.ctx_lens(sh)
+    hosts, qs, qds, res0s, orcs = [], [], [], [], []
+    for l in range(nl):
+        h = torch.empty((sh.R, sh.Hkv, sh.NBmax, 2, 16, 128), dtype=torch.bfloat16,
+                        pin_memory=True)
+        workload.host_kv(sh, 95, l, lens, device="cuda", out=h)
+        q, qd = workload.queries(sh, 95, l, steps, device="cuda")
+        hosts.append(h)
+        qs.append(q.cpu())
+        qds.append(qd.cpu())
+        res0s.append(workload.initial_resident(sh, 95, l, lens))
+    eng = Oasis(make_config(sh.R, sh.NBmax, sh.Hq, sh.Hkv, sh.K, sh.fetch_ratio, layers=nl,
+                            out_fp32=True), host_kv=hosts)
+    eng.set_context(lens)
+    for l in range(nl):
+        eng.set_resident(l, res0s[l], 0)
+        eng.oasis_build_summaries(l, 0)
+        eng.oasis_load_resident(l, 0)
+        hb = workload.bf16_bits(hosts[l])
+        orcs.append(oracle.LayerOracle(hb, oracle.summary_build(hb, lens), lens, res0s[l],
+                                       sh.K, sh.C, sample))
+    eng.oasis_sync()
+    outs = [torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev) for _ in range(nl)]
+    outds = [torch.empty_like(o) for o in outs]
+    live = [list(sample) for _ in range(nl)]
+    for t in range(steps):
+        for l in range(nl):
+            eng.oasis_step(l, t, qs[l][t].to(dev), qds[l][t].to(dev), outs[l], outds[l])
+        for l in range(nl):
+            eng.oasis_join(l)
+        eng.oasis_sync()
+        for l in range(nl):
+            orcs[l].pairs = live[l]
+            ref = orcs[l].step(workload.bf16_bits(qs[l][t]), workload.bf16_bits(qds[l][t]), t)
+            H.check_attention([outs[l].cpu().numpy(), outds[l].cpu().numpy()], ref, sh.G)
+            lists = {k: v.cpu().numpy() for k, v in eng.step_lists(l, t).items()}
+            res_n = eng.res_ids[l][(t + 1) & 1].cpu().numpy()
+            keep = []
+            for (r, h), v in ref.items():
+                assert H.topk_agrees(lists["topk_ids"][r, h], v["topk"], v["scores"], sh.K)
+                if np.array_equal(lists["topk_ids"][r, h], v["topk"]):
+                    assert (lists["admit_ids"][r, h, :sh.C] == v["admit_ids"]).all()
+                    assert (res_n[r, h] == orcs[l].res[r, h]).all()
+                    keep.append((r, h))
+            live[l] = keep
+            assert len(keep) >= len(sample) - 1
+    eng.close()
