@@ -47,11 +47,11 @@ def _load():
         P, I, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
         sig = {
             "orc_summary_build": [P, P, I, I, I, I, I, P],
-            "orc_attention_rh": [P, P, P, P, P, I, I, I, I, I, I, I, D, I, I, P],
-            "orc_score_rh": [P, P, P, I, I, I, I, I, I, I, I, P],
+            "orc_attention_rh": [P, P, P, P, P, I, I, I, I, I, I, I, I, D, I, I, P],
+            "orc_score_rh": [P, P, P, I, I, I, I, I, I, I, I, I, P],
             "orc_topk_rh": [P, I, I, P],
             "orc_admit_evict_rh": [P, P, P, I, I, I, P, P, P, P],
-            "orc_step_rh": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, D,
+            "orc_step_rh": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, D,
                             I, I, P, P, P, P, P, P, P],
             "orc_append_token": [P, P, P, P, P, I, I, I, I, I, I],
             "orc_remote_fetch_rh": [P, I, P, P, I, I, P, P, P],
@@ -91,17 +91,29 @@ def summary_build(host_kv: np.ndarray, ctx_len: np.ndarray) -> np.ndarray:
     return summ
 
 
+def drafts(qd: np.ndarray) -> int:
+    """Number of draft queries D in ``qd``: ``[R][Hq][d]`` is one draft,
+    ``[D][R][Hq][d]`` is D of them."""
+    if qd.ndim == 3:
+        return 1
+    if qd.ndim == 4 and qd.shape[0] >= 1:
+        return qd.shape[0]
+    raise ValueError("draft queries must be [R][Hq][d] or [D][R][Hq][d]")
+
+
 def attention_rh(host_kv, ctx_len, res, q, qd, r, h, scale=None):
-    """Attention outputs ``[2][G][d]`` float32 of one (r, h)."""
+    """Attention outputs ``[1 + D][G][d]`` float32 of one (r, h): the normal
+    query, then each draft query."""
     R, Hkv, NBmax, _, B, d = host_kv.shape
     Hq = q.shape[1]
     K = res.shape[-1]
+    D = drafts(qd)
     if scale is None:
         scale = 1.0 / np.sqrt(d)
-    out = np.empty((2, Hq // Hkv, d), dtype=np.float32)
+    out = np.empty((1 + D, Hq // Hkv, d), dtype=np.float32)
     _ok(_load().orc_attention_rh(
         _p(host_kv, np.uint16), _p(ctx_len, np.int32), _p(res, np.int32),
-        _p(q, np.uint16), _p(qd, np.uint16), R, Hq, Hkv, NBmax, B, d, K,
+        _p(q, np.uint16), _p(qd, np.uint16), D, R, Hq, Hkv, NBmax, B, d, K,
         float(scale), r, h, _p(out, np.float32)), "attention_rh")
     return out
 
@@ -109,10 +121,11 @@ def attention_rh(host_kv, ctx_len, res, q, qd, r, h, scale=None):
 def score_rh(summ, ctx_len, qd, r, h, B):
     """Summary scores ``[NBmax]`` float32 of one (r, h) (-inf past the context)."""
     R, Hkv, NBmax, _, d = summ.shape
-    Hq = qd.shape[1]
+    D = drafts(qd)
+    Hq = qd.shape[-2]
     s = np.empty(NBmax, dtype=np.float32)
     _ok(_load().orc_score_rh(_p(summ, np.uint16), _p(ctx_len, np.int32),
-                             _p(qd, np.uint16), R, Hq, Hkv, NBmax, d, B, r, h,
+                             _p(qd, np.uint16), D, R, Hq, Hkv, NBmax, d, B, r, h,
                              _p(s, np.float32)), "score_rh")
     return s
 
@@ -223,23 +236,25 @@ class LayerOracle:
 
     def step(self, q, qd, t):
         """Run one layer-step for every tracked pair, on the oracle's own
-        state only.  Returns a dict keyed by (r, h) with attn [2][G][d],
+        state only.  ``qd`` holds one draft ``[R][Hq][d]`` or D of them
+        ``[D][R][Hq][d]``.  Returns a dict keyed by (r, h) with attn [1+D][G][d],
         scores, topk, admit_ids, admit_slots, evict_ids, n_admit (and, with
         a remote tier, the slot assignment's miss lists)."""
         L = _load()
         Hq = q.shape[1]
+        D = drafts(qd)
         out = {}
         for (r, h) in self.pairs:
-            attn = np.empty((2, Hq // self.Hkv, self.d), dtype=np.float32)
+            attn = np.empty((1 + D, Hq // self.Hkv, self.d), dtype=np.float32)
             scores = np.empty(self.NBmax, dtype=np.float32)
             _ok(L.orc_attention_rh(_p(self.host_kv, np.uint16),
                                    _p(self.ctx_len, np.int32), _p(self.res, np.int32),
-                                   _p(q, np.uint16), _p(qd, np.uint16), self.R, Hq,
+                                   _p(q, np.uint16), _p(qd, np.uint16), D, self.R, Hq,
                                    self.Hkv, self.NBmax, self.B, self.d, self.K,
                                    float(self.scale), r, h, _p(attn, np.float32)),
                 "attention_rh")
             _ok(L.orc_score_rh(_p(self.summ, np.uint16), _p(self.ctx_len, np.int32),
-                               _p(qd, np.uint16), self.R, Hq, self.Hkv, self.NBmax,
+                               _p(qd, np.uint16), D, self.R, Hq, self.Hkv, self.NBmax,
                                self.d, self.B, r, h, _p(scores, np.float32)),
                 "score_rh")
             nb = min(num_blocks(int(self.ctx_len[r]), self.B), self.NBmax)

@@ -108,12 +108,12 @@ extern "C" int orc_summary_build(const uint16_t* host_kv, const int32_t* ctx_len
 
 extern "C" int orc_attention_rh(const uint16_t* host_kv, const int32_t* ctx_len,
                                 const int32_t* res, const uint16_t* q,
-                                const uint16_t* qd, int R, int Hq, int Hkv,
+                                const uint16_t* qd, int D, int R, int Hq, int Hkv,
                                 int NBmax, int B, int d, int K, double scale,
                                 int r, int h, float* out) {
   if (!host_kv || !ctx_len || !res || !q || !qd || !out ||
-      !dims_ok(R, Hq, Hkv, NBmax, B, d) || K <= 0 || r < 0 || r >= R || h < 0 ||
-      h >= Hkv)
+      !dims_ok(R, Hq, Hkv, NBmax, B, d) || D < 1 || K <= 0 || r < 0 || r >= R ||
+      h < 0 || h >= Hkv)
     return -1;
   const int G = Hq / Hkv;
   const int ctx = ctx_len[r];
@@ -129,8 +129,10 @@ extern "C" int orc_attention_rh(const uint16_t* host_kv, const int32_t* ctx_len,
       vals.push_back(host_kv + kv_index(r, h, id, 1, t, 0, Hkv, NBmax, B, d));
     }
   }
-  for (int which = 0; which < 2; ++which) {
-    const uint16_t* src = which == 0 ? q : qd;
+  // Query vector `which`: 0 = the normal query, 1 + e = draft e.
+  const size_t plane = static_cast<size_t>(R) * Hq * d;
+  for (int which = 0; which <= D; ++which) {
+    const uint16_t* src = which == 0 ? q : qd + (which - 1) * plane;
     for (int g = 0; g < G; ++g) {
       const int j = h * G + g;
       const uint16_t* x = src + (static_cast<size_t>(r) * Hq + j) * d;
@@ -141,11 +143,11 @@ extern "C" int orc_attention_rh(const uint16_t* host_kv, const int32_t* ctx_len,
 }
 
 extern "C" int orc_score_rh(const uint16_t* summ, const int32_t* ctx_len,
-                            const uint16_t* qd, int R, int Hq, int Hkv,
+                            const uint16_t* qd, int D, int R, int Hq, int Hkv,
                             int NBmax, int d, int B, int r, int h,
                             float* scores) {
   if (!summ || !ctx_len || !qd || !scores || !dims_ok(R, Hq, Hkv, NBmax, B, d) ||
-      r < 0 || r >= R || h < 0 || h >= Hkv)
+      D < 1 || r < 0 || r >= R || h < 0 || h >= Hkv)
     return -1;
   const int G = Hq / Hkv;
   const int nb = std::min(blocks_of(ctx_len[r], B), NBmax);
@@ -155,15 +157,17 @@ extern "C" int orc_score_rh(const uint16_t* summ, const int32_t* ctx_len,
       continue;
     }
     double acc = 0.0;
-    for (int g = 0; g < G; ++g) {
-      const uint16_t* x = qd + (static_cast<size_t>(r) * Hq + h * G + g) * d;
-      for (int i = 0; i < d; ++i) {
-        const double xi = widen(x[i]);
-        const double lo = widen(summ[summ_index(r, h, b, 0, i, Hkv, NBmax, d)]);
-        const double hi = widen(summ[summ_index(r, h, b, 1, i, Hkv, NBmax, d)]);
-        acc += std::max(xi * lo, xi * hi);
+    for (int e = 0; e < D; ++e)
+      for (int g = 0; g < G; ++g) {
+        const uint16_t* x =
+            qd + ((static_cast<size_t>(e) * R + r) * Hq + h * G + g) * d;
+        for (int i = 0; i < d; ++i) {
+          const double xi = widen(x[i]);
+          const double lo = widen(summ[summ_index(r, h, b, 0, i, Hkv, NBmax, d)]);
+          const double hi = widen(summ[summ_index(r, h, b, 1, i, Hkv, NBmax, d)]);
+          acc += std::max(xi * lo, xi * hi);
+        }
       }
-    }
     scores[b] = static_cast<float>(acc);
   }
   return 0;
@@ -240,17 +244,17 @@ extern "C" int orc_admit_evict_rh(int32_t* res, int32_t* stamp,
 
 extern "C" int orc_step_rh(const uint16_t* host_kv, const uint16_t* summ,
                            const int32_t* ctx_len, int32_t* res, int32_t* stamp,
-                           const uint16_t* q, const uint16_t* qd, int R, int Hq,
-                           int Hkv, int NBmax, int B, int d, int K, int C,
+                           const uint16_t* q, const uint16_t* qd, int D, int R,
+                           int Hq, int Hkv, int NBmax, int B, int d, int K, int C,
                            int step, double scale, int r, int h,
                            float* attn_out, float* scores_scratch,
                            int32_t* topk, int32_t* admit_ids,
                            int32_t* admit_slots, int32_t* evict_ids,
                            int32_t* n_admit) {
-  if (orc_attention_rh(host_kv, ctx_len, res, q, qd, R, Hq, Hkv, NBmax, B, d, K,
-                       scale, r, h, attn_out))
+  if (orc_attention_rh(host_kv, ctx_len, res, q, qd, D, R, Hq, Hkv, NBmax, B, d,
+                       K, scale, r, h, attn_out))
     return -1;
-  if (orc_score_rh(summ, ctx_len, qd, R, Hq, Hkv, NBmax, d, B, r, h,
+  if (orc_score_rh(summ, ctx_len, qd, D, R, Hq, Hkv, NBmax, d, B, r, h,
                    scores_scratch))
     return -1;
   const int nb = std::min(blocks_of(ctx_len[r], B), NBmax);

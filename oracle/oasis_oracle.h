@@ -22,7 +22,8 @@
  * Layouts (row-major, innermost last):
  *   host_kv [R][Hkv][NBmax][2][B][d]  bf16   (index 0 = keys, 1 = values)
  *   summ    [R][Hkv][NBmax][2][d]     bf16   (index 0 = min row, 1 = max row)
- *   q, qd   [R][Hq][d]                bf16   (normal and draft queries)
+ *   q       [R][Hq][d]                bf16   (normal queries)
+ *   qd      [D][R][Hq][d]             bf16   (D >= 1 draft queries per step)
  *   res     [R][Hkv][K]               int32  (logical block id per slot, -1 = empty)
  *   stamp   [R][Hkv][K]               int32  (step of last selection, -1 = never)
  *   topk    [R][Hkv][K]               int32  (block ids in rank order, -1 pad)
@@ -48,23 +49,26 @@ int orc_summary_build(const uint16_t* host_kv, const int32_t* ctx_len, int R,
                       int Hkv, int NBmax, int B, int d, uint16_t* summ);
 
 /* Sparse attention of one (request r, KV head h) over its resident blocks,
- * for the normal query and the draft query of each of the G query heads of
+ * for the normal query and every draft query of each of the G query heads of
  * the group ([R] *What carries the argument*: one attention pass handles the
- * normal and the draft token, both reading the one resident block set).
- * out[2][G][d] (fp32): out[0] for q, out[1] for the draft query. */
+ * normal and the draft token, both reading the one resident block set; with
+ * D > 1 drafts every draft reads that same set).
+ * out[1 + D][G][d] (fp32): out[0] for q, out[1 + e] for draft e. */
 int orc_attention_rh(const uint16_t* host_kv, const int32_t* ctx_len,
                      const int32_t* res, const uint16_t* q, const uint16_t* qd,
-                     int R, int Hq, int Hkv, int NBmax, int B, int d, int K,
-                     double scale, int r, int h, float* out);
+                     int D, int R, int Hq, int Hkv, int NBmax, int B, int d,
+                     int K, double scale, int r, int h, float* out);
 
 /* Summary score of every logical block b < ceil(ctx_len[r]/B) for one
- * (r, h): s[b] = sum over the group's query heads j and dims i of
- * max(qd[j][i]*min[b][i], qd[j][i]*max[b][i])  ([R] *What carries the
- * argument*: the draft query is scored against the summaries).  scores[NBmax] (fp32, one rounding of a double
- * sum); entries b >= NB_r are set to -inf. */
+ * (r, h): s[b] = sum over the drafts e, the group's query heads j and dims i
+ * of max(qd[e][j][i]*min[b][i], qd[e][j][i]*max[b][i])  ([R] *What carries
+ * the argument*: the draft query is scored against the summaries; several
+ * drafts are read as further query vectors of the group, their bounds summed
+ * like those of the group's heads).  scores[NBmax] (fp32, one rounding of a
+ * double sum); entries b >= NB_r are set to -inf. */
 int orc_score_rh(const uint16_t* summ, const int32_t* ctx_len,
-                 const uint16_t* qd, int R, int Hq, int Hkv, int NBmax, int d,
-                 int B, int r, int h, float* scores);
+                 const uint16_t* qd, int D, int R, int Hq, int Hkv, int NBmax,
+                 int d, int B, int r, int h, float* scores);
 
 /* Head-wise top-K of one (r, h): the first min(K, NB) block ids ordered by
  * (score descending, id ascending); the rest of topk[K] is -1
@@ -88,8 +92,8 @@ int orc_admit_evict_rh(int32_t* res, int32_t* stamp, const int32_t* topk,
  * NBmax floats.  Outputs as in the functions above. */
 int orc_step_rh(const uint16_t* host_kv, const uint16_t* summ,
                 const int32_t* ctx_len, int32_t* res, int32_t* stamp,
-                const uint16_t* q, const uint16_t* qd, int R, int Hq, int Hkv,
-                int NBmax, int B, int d, int K, int C, int step, double scale,
+                const uint16_t* q, const uint16_t* qd, int D, int R, int Hq,
+                int Hkv, int NBmax, int B, int d, int K, int C, int step, double scale,
                 int r, int h, float* attn_out, float* scores_scratch,
                 int32_t* topk, int32_t* admit_ids, int32_t* admit_slots,
                 int32_t* evict_ids, int32_t* n_admit);

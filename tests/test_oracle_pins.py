@@ -109,6 +109,50 @@ def test_score_upper_bounds_every_key_and_sums_group():
         np.testing.assert_allclose(s, np.sum(single, axis=0), rtol=1e-6)
 
 
+def test_score_two_drafts_hand_worked():
+    gold = json.load(open(os.path.join(GOLD, "quest_bound_hand.json")))
+    for c in gold["draft_cases"]:
+        kv = make_store(c["keys"], np.zeros_like(c["keys"]), B=2)
+        lens = np.array([2], dtype=np.int32)
+        summ = oracle.summary_build(kv, lens)
+        qd = to_bits(np.asarray(c["drafts"], dtype=np.float32).reshape(len(c["drafts"]), 1, 1, 2))
+        s = oracle.score_rh(summ, lens, qd, 0, 0, B=2)
+        assert s[0] == np.float32(c["score"])
+        kf = to_float(kv)[0, 0, 0, 0].astype(np.float64)
+        best = sum((to_float(qd)[e, 0, 0] @ kf.T).max() for e in range(qd.shape[0]))
+        assert best == c["sum_max_qk"]
+        assert s[0] >= best
+
+
+def test_score_drafts_bound_each_draft_and_add_up():
+    # Several drafts on a multi-request layer (so a wrong draft or request
+    # stride shows): the score bounds the sum over drafts of each draft's
+    # best key in every block, equals the sum of the single-draft scores, and
+    # two identical drafts give exactly twice the single-draft score.
+    rng = np.random.default_rng(4)
+    R, Hkv, G, NB, B, d, D = 3, 2, 2, 10, 16, 128, 3
+    kv = to_bits(rng.standard_normal((R, Hkv, NB, 2, B, d)))
+    lens = np.array([NB * B, NB * B - 21, 37], dtype=np.int32)
+    summ = oracle.summary_build(kv, lens)
+    qd = to_bits(rng.standard_normal((D, R, Hkv * G, d)) * 1.5)
+    kf, qf = to_float(kv).astype(np.float64), to_float(qd).astype(np.float64)
+    for r in range(R):
+        nb = -(-lens[r] // B)
+        for h in range(Hkv):
+            s = oracle.score_rh(summ, lens, qd, r, h, B)
+            single = [oracle.score_rh(summ, lens, np.ascontiguousarray(qd[e]), r, h, B)
+                      for e in range(D)]
+            np.testing.assert_allclose(s[:nb], np.sum(single, axis=0)[:nb], rtol=1e-6)
+            assert np.isneginf(s[nb:]).all()
+            for b in range(nb):
+                valid = min(B, lens[r] - b * B)
+                best = sum((kf[r, h, b, 0, :valid] @ qf[e, r, h * G:(h + 1) * G].T).max(axis=0).sum()
+                           for e in range(D))
+                assert s[b] >= best - 1e-6 * abs(best)
+            twice = oracle.score_rh(summ, lens, np.stack([qd[1], qd[1]]), r, h, B)
+            np.testing.assert_array_equal(twice, 2 * single[1])
+
+
 def test_score_single_token_block_is_exact_dot():
     # one valid token: min = max = k, so the bound collapses to q.k
     rng = np.random.default_rng(2)
@@ -271,6 +315,55 @@ def test_attention_masks_tail_and_empty_slots_and_routes_heads():
     perm = res[:, :, ::-1].copy()
     np.testing.assert_allclose(oracle.attention_rh(kv, lens, perm, q, qd, 0, 0), o,
                                rtol=1e-6, atol=1e-7)
+
+
+def test_attention_each_draft_reads_the_one_resident_set():
+    # D drafts: row 0 is the normal query's output, row 1 + e equals the
+    # one-draft output for draft e (pinned above against dense softmax),
+    # on a multi-request layer so a wrong draft or request stride shows.
+    rng = np.random.default_rng(14)
+    R, Hkv, G, NB, B, d, D = 3, 2, 4, 6, 16, 128, 3
+    kv, q, _ = rand_layer(rng, R, Hkv, G, NB)
+    qd = to_bits(rng.standard_normal((D, R, Hkv * G, d)))
+    lens = np.array([NB * B, 3 * B + 2, NB * B - 1], dtype=np.int32)
+    res = np.stack([np.stack([rng.permutation(NB)[:4] for _ in range(Hkv)])
+                    for _ in range(R)]).astype(np.int32)
+    res[1, 1, 2] = -1
+    for r in range(R):
+        for h in range(Hkv):
+            o = oracle.attention_rh(kv, lens, res, q, qd, r, h)
+            assert o.shape == (1 + D, G, d)
+            for e in range(D):
+                one = oracle.attention_rh(kv, lens, res, q, np.ascontiguousarray(qd[e]), r, h)
+                np.testing.assert_array_equal(o[0], one[0])
+                np.testing.assert_array_equal(o[1 + e], one[1])
+
+
+def test_step_with_two_identical_drafts_ranks_as_one():
+    # Doubling every score (exact in binary floating point) changes no rank:
+    # two copies of one draft give the one-draft top-K and eviction.
+    from sparse_kv_block_gb300 import workload
+    shape = workload.SHAPES["tiny"]
+    lens = workload.ctx_lens(shape)
+    kv = workload.bf16_bits(workload.host_kv(shape, 0, 0, lens, device="cpu"))
+    summ = oracle.summary_build(kv, lens)
+    res0 = workload.initial_resident(shape, 0, 0, lens)
+    pairs = [(r, h) for r in range(shape.R) for h in range(shape.Hkv)]
+    one = oracle.LayerOracle(kv, summ, lens, res0, shape.K, shape.C, pairs)
+    two = oracle.LayerOracle(kv, summ, lens, res0, shape.K, shape.C, pairs)
+    q, qd = workload.queries(shape, 0, 0, 3, device="cpu")
+    for t in range(3):
+        qb, qdb = workload.bf16_bits(q[t]), workload.bf16_bits(qd[t])
+        a = one.step(qb, qdb, t)
+        b = two.step(qb, np.stack([qdb, qdb]), t)
+        for p in pairs:
+            np.testing.assert_array_equal(b[p]["scores"], 2 * a[p]["scores"])
+            np.testing.assert_array_equal(b[p]["topk"], a[p]["topk"])
+            np.testing.assert_array_equal(b[p]["admit_ids"], a[p]["admit_ids"])
+            np.testing.assert_array_equal(b[p]["attn"][:2], a[p]["attn"])
+            np.testing.assert_array_equal(b[p]["attn"][2], a[p]["attn"][1])
+    np.testing.assert_array_equal(one.res, two.res)
+    np.testing.assert_array_equal(one.stamp, two.stamp)
 
 
 # ----------------------------------------------------------------- eviction
