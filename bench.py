@@ -141,7 +141,7 @@ class ClockSampler:
                 "samples_under_load": len(loaded)}
 
 
-def build_layer(shape, seed, dev, side_groups=0, schedule=3):
+def build_layer(shape, seed, dev, side_groups=0, schedule=3, num_drafts=1):
     """Allocate and fill one layer (untimed setup); returns (engine, q, qd, lens, host)."""
     from sparse_kv_block_gb300.oasis import Oasis, make_config
     lens = workload.ctx_lens(shape)
@@ -150,7 +150,8 @@ def build_layer(shape, seed, dev, side_groups=0, schedule=3):
     gen = dev if dev.type == "cuda" else "cpu"
     workload.host_kv(shape, seed, 0, lens, device=gen, out=host)
     cfg = make_config(shape.R, shape.NBmax, shape.Hq, shape.Hkv, shape.K, shape.fetch_ratio,
-                      device=dev.index or 0, side_groups=side_groups, schedule=schedule)
+                      device=dev.index or 0, side_groups=side_groups, schedule=schedule,
+                      num_drafts=num_drafts)
     eng = Oasis(cfg, host_kv=[host])
     eng.set_context(lens)
     eng.oasis_build_summaries(0, 0)
@@ -897,6 +898,89 @@ def run_miss_stall(args, ws, rank, local):
                           "steps": args.steps, **results}), flush=True)
 
 
+def run_drafts(args, ws, rank, local):
+    """Several draft queries per step (an option of the three-stream
+    pipeline): the look-ahead step with D = 1, 2, 3 drafts on the same
+    workload, each draft attending over the one resident set and the drafts'
+    summary bounds summed for the ranking.  Reports the step rate and the
+    attention kernel alone (same resident bytes, 1 + D query kinds)."""
+    from sparse_kv_block_gb300.oasis import lib
+    lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = get_shape(args)
+    R, Hq, Hkv, K = shape.R, shape.Hq, shape.Hkv, shape.K
+    nq = min(args.queries, 16)
+    peak = measured_peaks().get("hbm_gbs")
+    results = {}
+    for D in (1, 2, 3):
+        eng, lens, host = build_layer(shape, args.seed, dev, args.side_groups, args.schedule,
+                                      num_drafts=D)
+        q, qd = workload.draft_queries(shape, args.seed, 0, nq, D, device=dev)
+        warm_start(eng, shape, qd[0], dev)
+        out = torch.empty((R, Hq, 128), dtype=torch.bfloat16, device=dev)
+        outd = torch.empty((D, R, Hq, 128), dtype=torch.bfloat16, device=dev)
+        st = torch.cuda.Stream(dev)
+        for i in range(args.warmup):
+            eng.oasis_step(0, i, q[i % nq], qd[i % nq], out, outd, st)
+        eng.oasis_join(0, st)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for i in range(args.warmup, args.warmup + args.steps):
+            eng.oasis_step(0, i, q[i % nq], qd[i % nq], out, outd, st)
+        eng.oasis_join(0, st)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        eng.oasis_sync()
+        ms = e0.elapsed_time(e1) / args.steps
+        last = args.warmup + args.steps - 1
+        admitted = float(eng.step_lists(0, last)["n_admit"].float().mean())
+        # a profiled pass (per-kernel durations and start offsets in the step)
+        n_prof = min(args.steps, 200)
+        eng.oasis_profile_enable(True)
+        for i in range(last + 1, last + 1 + n_prof):
+            eng.oasis_step(0, i, q[i % nq], qd[i % nq], out, outd, st)
+        eng.oasis_join(0, st)
+        torch.cuda.synchronize(dev)
+        ms_sum, counts, off_sum = eng.oasis_profile_read()
+        eng.oasis_profile_enable(False)
+        names = ("attention", "score_topk", "admit_evict", "prefetch")
+        kern = {n: {"ms": round(ms_sum[k] / max(counts[k], 1), 4),
+                    "start_ms": round(off_sum[k] / max(counts[k], 1), 4)}
+                for k, n in enumerate(names) if counts[k]}
+        # attention alone on the resident set the loops left behind
+        nxt = last + 1 + n_prof
+        n_attn = 50
+        for _ in range(3):
+            eng.oasis_lookahead_attn(0, nxt, q[0], qd[0], out, outd, st)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(st)
+        for _ in range(n_attn):
+            eng.oasis_lookahead_attn(0, nxt, q[0], qd[0], out, outd, st)
+        a1.record(st)
+        torch.cuda.synchronize(dev)
+        eng.oasis_sync()
+        ams = a0.elapsed_time(a1) / n_attn
+        # resident units + q and the D draft planes read + 1 + D outputs written
+        nbytes = R * Hkv * K * 8192 + 2 * (1 + D) * R * Hq * 128 * 2
+        gbs = nbytes / (ams * 1e-3) / 1e9
+        results[f"drafts_{D}"] = {
+            "ms_per_step": round(ms, 4), "layer_steps_per_s": round(1e3 / ms, 1),
+            "admitted_per_head": round(admitted, 3), "profiled_kernels": kern,
+            "attention_alone_us": round(ams * 1e3, 1), "attention_gbs": round(gbs, 1),
+            "attention_frac_of_measured_hbm": round(gbs / peak, 4) if peak else None}
+        eng.close()
+        del eng, host
+        torch.cuda.empty_cache()
+    if rank == 0:
+        print(json.dumps({"mode": "draft queries per step", "workload": workload_desc(shape),
+                          "steps": args.steps, "l2": "attention reads 1 GiB of units per launch",
+                          **results}), flush=True)
+
+
 def run_remote(args, ws, rank, local):
     """Remote tier (emulated prefill-decode disaggregation with remote partial
     fetch) on the single-layer shape: the full cache stays in the remote
@@ -1098,6 +1182,8 @@ def main():
     ap.add_argument("--schedule", type=int, default=3,
                     help="0 scan first, 1 concurrent, 2 the pages' three background streams, "
                          "3 auto (scan first on device buffers, concurrent on host buffers)")
+    ap.add_argument("--drafts", action="store_true",
+                    help="step rate and attention time with 1, 2 and 3 draft queries per step")
     ap.add_argument("--remote", action="store_true",
                     help="remote tier (emulated disaggregated partial fetch) on the single-layer shape")
     ap.add_argument("--remote-gbps", type=float, nargs="+", default=[0.0, 50.0, 25.0],
@@ -1119,6 +1205,8 @@ def main():
         run_miss_stall(args, ws, rank, local)
     elif args.remote:
         run_remote(args, ws, rank, local)
+    elif args.drafts:
+        run_drafts(args, ws, rank, local)
     elif workload.SHAPES[args.workload].layers > 1:
         run_oasis_layers(args, ws, rank, local)
     else:

@@ -55,8 +55,10 @@
  *   stamps     dev    [R][Hkv][K]               int32  step of last selection, -1 never
  *   phys       dev    [2][R][Hkv][U]            int32  pool unit per slot; [K..U) spares
  *   ctx_len    dev    [2][R]                    int32  tokens per request
- *   q, q_draft dev    [R][Hq][d]                bf16
+ *   q          dev    [R][Hq][d]                bf16
+ *   q_draft    dev    [D][R][Hq][d]             bf16   D = draft queries per step
  *   out        dev    [R][Hq][d]                bf16, or fp32 if cfg.out_fp32
+ *   out_draft  dev    [D][R][Hq][d]             as out
  *   topk_ids   dev    [R][Hkv][K]               int32  rank order, -1 padded
  *   topk_scores dev   [R][Hkv][K]               fp32   (nullable)
  *   admit_ids, admit_slots, evict_ids  dev [R][Hkv][C] int32 (-1 padded)
@@ -111,6 +113,12 @@ typedef struct {
   int32_t side_groups;   /* request groups oasis_step pipelines its side work
                             in (0 = one per 256 (request, KV head) pairs, <= 8) */
   int32_t schedule;      /* OASIS_SCHEDULE_*: how a step orders a1 */
+  int32_t num_drafts;    /* D, draft queries per step: 0 or 1 = one, <= 3.
+                            Several drafts (an option of the three-stream
+                            pipeline) all read the one resident set in a1 and
+                            their bounds add up in a2 like those of a group's
+                            query heads; q_draft and out_draft hold D planes
+                            of [R][Hq][d]. */
 } oasis_config;
 
 /* oasis_step schedules.  SCAN_FIRST: the attention of a step starts when the
@@ -214,7 +222,8 @@ OASIS_API int oasis_resume_resident(oasis_ctx* ctx, int layer, int first_step,
 
 /* a1: look-ahead attention ([R] *What carries the argument*, [V]
  * key_machinery: a single attention pass serves both the normal and the draft
- * token, reading one shared resident sparse set).  For every request r and query head j, separately for q and q_draft:
+ * token, reading one shared resident sparse set).  For every request r and
+ * query head j, separately for q and each of the D draft planes of q_draft:
  * softmax(x . k / scale) . v over the valid tokens of the occupied slots of
  * KV head j / G in table (step & 1).  A block's valid tokens are those below
  * ctx_len[step & 1][r]; a head with no valid token outputs zeros. */
@@ -236,7 +245,8 @@ OASIS_API int oasis_dense_attn(oasis_ctx* ctx, const void* kv_dense, int table,
  * the draft query ranks every logical block per KV head from the compressed
  * summaries alone, never touching the full keys).  For every (r, h) and every
  * logical block b < ceil(ctx_len[step & 1][r] / B):
- *   s[b] = sum_{j in group(h)} sum_i max(qd_ji * min_bi, qd_ji * max_bi)
+ *   s[b] = sum_{e < D} sum_{j in group(h)} sum_i
+ *            max(qd_eji * min_bi, qd_eji * max_bi)
  * then topk_ids = the first min(K, NB_r) blocks by (s desc, b asc), -1
  * padded; topk_scores (nullable) the matching s (fp32) or -inf. */
 OASIS_API int oasis_score_topk(oasis_ctx* ctx, int layer, int step,

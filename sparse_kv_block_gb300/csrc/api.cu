@@ -327,12 +327,16 @@ int fetch_cap(const oasis_config& c) {
   return static_cast<int>(std::floor(static_cast<double>(c.fetch_ratio) * c.topk + 1e-9));
 }
 
+// Draft queries per step (0 in the config means one).
+int num_drafts(const oasis_config& c) { return c.num_drafts > 0 ? c.num_drafts : 1; }
+
 WsLayout ws_layout(const oasis_config& c) {
   WsLayout w{};
   const size_t pairs = static_cast<size_t>(c.num_requests) * c.num_kv_heads;
   const size_t C = static_cast<size_t>(fetch_cap(c));
   const size_t qbytes = static_cast<size_t>(c.num_requests) * c.num_q_heads * c.head_dim * 2;
   const size_t obytes = qbytes * (c.out_fp32 ? 2 : 1);
+  const size_t D = static_cast<size_t>(num_drafts(c));
   w.err = 0;
   size_t o = kAlign;
   // each list twice (step parity 0 and 1), the copies adjacent
@@ -343,13 +347,13 @@ WsLayout ws_layout(const oasis_config& c) {
   w.evict_ids = o;   o += 2 * align_up(pairs * (C ? C : 1) * 4);
   w.n_admit = o;     o += 2 * align_up(pairs * 4);
   w.q_stage = o;     o += align_up(qbytes);
-  w.qd_stage = o;    o += align_up(qbytes);
+  w.qd_stage = o;    o += align_up(D * qbytes);
   w.q_stage1 = o;    o += align_up(qbytes);
-  w.qd_stage1 = o;   o += align_up(qbytes);
+  w.qd_stage1 = o;   o += align_up(D * qbytes);
   w.out_stage = o;   o += align_up(obytes);
-  w.outd_stage = o;  o += align_up(obytes);
-  w.qd_ring0 = o;    o += align_up(qbytes);
-  w.qd_ring1 = o;    o += align_up(qbytes);
+  w.outd_stage = o;  o += align_up(D * obytes);
+  w.qd_ring0 = o;    o += align_up(D * qbytes);
+  w.qd_ring1 = o;    o += align_up(D * qbytes);
   w.per_layer = o - kAlign;
   w.total = kAlign + w.per_layer * static_cast<size_t>(c.num_layers);
   return w;
@@ -372,6 +376,7 @@ const char* config_error(const oasis_config* c) {
   if (c->device < 0) return "device must be >= 0";
   if (c->max_blocks > kMaxBlocksPerHead) return "max_blocks must be <= 131072";
   if (c->side_groups < 0 || c->side_groups > 64) return "side_groups must be in 0..64";
+  if (c->num_drafts < 0 || c->num_drafts > kMaxDrafts) return "num_drafts must be in 0..3";
   if (c->schedule != OASIS_SCHEDULE_SCAN_FIRST && c->schedule != OASIS_SCHEDULE_CONCURRENT &&
       c->schedule != OASIS_SCHEDULE_THREE_STREAMS && c->schedule != OASIS_SCHEDULE_AUTO)
     return "schedule must be one of OASIS_SCHEDULE_*";
@@ -403,6 +408,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct oasis_ctx {
   oasis_config cfg{};
   int G = 0, C = 0, U = 0;
+  int D = 1;  // draft queries per step
   int groups = 1;  // request groups the side work is pipelined in
   float scale_log2 = 0.f;
   std::vector<LayerState> layers;
@@ -510,6 +516,7 @@ int run_attention(oasis_ctx* ctx, int layer, int step, const void* q, const void
   a.Hq = ctx->cfg.num_q_heads;
   a.Hkv = ctx->cfg.num_kv_heads;
   a.G = ctx->G;
+  a.D = ctx->D;
   a.K = ctx->cfg.topk;
   a.U = ctx->U;
   a.NBmax = ctx->cfg.max_blocks;
@@ -563,6 +570,7 @@ int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
   a.Hq = ctx->cfg.num_q_heads;
   a.Hkv = ctx->cfg.num_kv_heads;
   a.G = ctx->G;
+  a.D = ctx->D;
   a.K = ctx->cfg.topk;
   a.NBmax = ctx->cfg.max_blocks;
   a.pair0 = pair0;
@@ -743,6 +751,7 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
   if (!c) return OASIS_ENOMEM;
   c->cfg = *cfg;
   c->G = cfg->num_q_heads / cfg->num_kv_heads;
+  c->D = num_drafts(*cfg);
   c->C = fetch_cap(*cfg);
   c->U = cfg->topk + c->C;
   const double scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0 / std::sqrt(128.0);
@@ -1046,6 +1055,7 @@ OASIS_API int oasis_dense_attn(oasis_ctx* ctx, const void* kv_dense, int table, 
   a.Hq = ctx->cfg.num_q_heads;
   a.Hkv = ctx->cfg.num_kv_heads;
   a.G = ctx->G;
+  a.D = ctx->D;
   a.NBmax = ctx->cfg.max_blocks;
   a.scale_log2 = ctx->scale_log2;
   a.out_fp32 = ctx->cfg.out_fp32;
@@ -1138,8 +1148,8 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
   // The side work reads the draft query from a per-layer double buffer, so
   // the caller may reuse its buffer as soon as `stream` passes this call.
   void* qd_copy = L.qd_ring[step & 1];
-  const size_t qbytes =
-      static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_q_heads * kHeadDim * 2;
+  const size_t qbytes = static_cast<size_t>(ctx->D) * ctx->cfg.num_requests *
+                        ctx->cfg.num_q_heads * kHeadDim * 2;
   if (int rc = ctx->cuda(cudaMemcpyAsync(qd_copy, q_draft, qbytes, cudaMemcpyDeviceToDevice, s),
                          "stage q_draft"))
     return rc;
@@ -1274,7 +1284,7 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
   if (int rc = ctx->cuda(cudaMemcpyAsync(L.q_stage[slot], q_host, qb, cudaMemcpyHostToDevice,
                                          ctx->io), "h2d q"))
     return rc;
-  if (int rc = ctx->cuda(cudaMemcpyAsync(L.qd_stage[slot], q_draft_host, qb,
+  if (int rc = ctx->cuda(cudaMemcpyAsync(L.qd_stage[slot], q_draft_host, ctx->D * qb,
                                          cudaMemcpyHostToDevice, ctx->io), "h2d q_draft"))
     return rc;
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_in[slot], ctx->io), "record inputs")) return rc;
@@ -1291,7 +1301,8 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
   L.stage_used[slot] = true;
   if (int rc = ctx->cuda(cudaMemcpyAsync(out_host, L.out_stage, ob, cudaMemcpyDeviceToHost, s), "d2h out"))
     return rc;
-  return ctx->cuda(cudaMemcpyAsync(out_draft_host, L.outd_stage, ob, cudaMemcpyDeviceToHost, s),
+  return ctx->cuda(cudaMemcpyAsync(out_draft_host, L.outd_stage, ctx->D * ob,
+                                   cudaMemcpyDeviceToHost, s),
                    "d2h out_draft");
 }
 

@@ -12,8 +12,10 @@
 // unit is tiny (16 tokens x 8 query vectors x 128 dims), so it runs on
 // mma.sync m16n8k16 with the tokens as M and the 2 x G <= 8 query vectors as
 // N: S^T = K_unit * Q^T, online softmax over tokens, then O^T += V^T * P^T
-// with P^T moved into the B-operand layout by movmatrix.  The kernel is
-// bound by HBM reads of the resident units (8 KiB per unit).
+// with P^T moved into the B-operand layout by movmatrix.  With several draft
+// queries per step the (1 + D) x G query vectors take two such 8-column
+// tiles (kNT = 2), reading each staged unit once for all of them.  The
+// kernel is bound by HBM reads of the resident units (8 KiB per unit).
 #include <cstdlib>
 
 #include "common.cuh"
@@ -28,6 +30,10 @@ constexpr int kStageBytes = kUnitBytes;            // 8 KiB: [half][32 rows][128
 // Shared memory of a CTA of W warps: W private rings, barriers, unit list.
 template <int W>
 struct AttnLayout {
+  // The merge space ([W][16][128] fp32 partial outputs at most) reuses the
+  // ring, so the ring must hold it.
+  static_assert(W * kStages * kStageBytes >= W * 16 * 128 * 4 + 2 * W * 16 * 4,
+                "merge space exceeds the ring");
   static constexpr int kRingBytes = W * kStages * kStageBytes;
   static constexpr int kBarOffset = kRingBytes;
   static constexpr int kListOffset = kBarOffset + 256;
@@ -51,11 +57,14 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int kWarps>
+// kNT tiles of 8 query columns: column n = which * 4 + gi, which 0 = the
+// normal query, 1 + e = draft e; gi = query head within the group.
+template <int kWarps, int kNT>
 __global__ void __launch_bounds__(kWarps * 32)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap pool_map) {
   using Lay = AttnLayout<kWarps>;
   constexpr int kThreads = kWarps * 32;
+  constexpr int kCols = 8 * kNT;
   constexpr int kBarOffset = Lay::kBarOffset;
   constexpr int kListOffset = Lay::kListOffset;
   constexpr int kCountOffset = Lay::kCountOffset;
@@ -121,25 +130,29 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (lane == 0) *count_s = n;
   }
 
-  // B fragments of Q^T (d x 8 query vectors): column n = which * 4 + gi,
-  // which 0 = normal query, 1 = draft query; gi = query head within the group.
+  // B fragments of Q^T (d x 8 query vectors) per column tile; this lane
+  // loads column g of each tile.
   const int g = lane >> 2;
   const int t = lane & 3;
-  uint32_t qf[8][2];
-  {
-    const int which = g >> 2, gi = g & 3;
-    if (gi < a.G) {
+  const size_t plane = static_cast<size_t>(a.R) * a.Hq * kHeadDim;
+  uint32_t qf[kNT][8][2];
+#pragma unroll
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int which = nt * 2 + (g >> 2), gi = g & 3;
+    if (gi < a.G && which <= a.D) {
+      const __nv_bfloat16* base_q = which == 0
+          ? static_cast<const __nv_bfloat16*>(a.q)
+          : static_cast<const __nv_bfloat16*>(a.qd) + (which - 1) * plane;
       const uint32_t* src = reinterpret_cast<const uint32_t*>(
-          static_cast<const __nv_bfloat16*>(which ? a.qd : a.q) +
-          (static_cast<size_t>(r) * a.Hq + h * a.G + gi) * kHeadDim);
+          base_q + (static_cast<size_t>(r) * a.Hq + h * a.G + gi) * kHeadDim);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        qf[kk][0] = __ldg(src + 8 * kk + t);
-        qf[kk][1] = __ldg(src + 8 * kk + 4 + t);
+        qf[nt][kk][0] = __ldg(src + 8 * kk + t);
+        qf[nt][kk][1] = __ldg(src + 8 * kk + 4 + t);
       }
     } else {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) qf[kk][0] = qf[kk][1] = 0u;
+      for (int kk = 0; kk < 8; ++kk) qf[nt][kk][0] = qf[nt][kk][1] = 0u;
     }
   }
   __syncthreads();
@@ -177,10 +190,16 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int vrow = kBlock + (lane & 7) + ((lane >> 4) & 1) * 8;  // V rows
   const int vch = (lane >> 3) & 1;
 
-  float o[8][4];
+  // Per column tile: O^T accumulators, running max and sum of columns 2t, 2t+1.
+  float o[kNT][8][4];
+  float m0[kNT], m1[kNT], l0[kNT], l1[kNT];
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+    m0[nt] = m1[nt] = -INFINITY;
+    l0[nt] = l1[nt] = 0.f;
+  }
   const float sc = a.scale_log2;
 
   int k = 0;
@@ -196,44 +215,53 @@ __global__ void __launch_bounds__(kWarps * 32)
     uint8_t* stage = my_ring + st * kStageBytes;
     const uint32_t sb = smem_u32(stage);
 
-    // S^T (16 tokens x 8 queries) = K_unit (16 x 128) * Q^T (128 x 8)
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    // S^T (16 tokens x 8 queries) = K_unit (16 x 128) * Q^T (128 x 8), per
+    // column tile; each K fragment is loaded once for all tiles.
+    float s[kNT][4];
+#pragma unroll
+    for (int nt = 0; nt < kNT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const int half = kk >> 2;
       const int chunk = (kk & 3) * 2 + kch;
       uint32_t a0, a1, a2, a3;
       ldsm_x4(sb + half * (kStageBytes / 2) + swz(krow, chunk), a0, a1, a2, a3);
-      mma_bf16_16816(s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt)
+        mma_bf16_16816(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
     }
 
     // Online softmax over tokens (rows g, g+8) per query column (2t, 2t+1).
-    float x0 = s[0] * sc, x1 = s[1] * sc, x2 = s[2] * sc, x3 = s[3] * sc;
-    if (g >= valid) x0 = x1 = -INFINITY;
-    if (g + 8 >= valid) x2 = x3 = -INFINITY;
-    float t0 = fmaxf(x0, x2), t1 = fmaxf(x1, x3);
+    uint32_t b0[kNT], b1[kNT];
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
-      t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
-    }
-    const float mn0 = fmaxf(m0, t0), mn1 = fmaxf(m1, t1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
-    l0 = l0 * al0 + p0 + p2;
-    l1 = l1 * al1 + p1 + p3;
+    for (int nt = 0; nt < kNT; ++nt) {
+      float x0 = s[nt][0] * sc, x1 = s[nt][1] * sc, x2 = s[nt][2] * sc, x3 = s[nt][3] * sc;
+      if (g >= valid) x0 = x1 = -INFINITY;
+      if (g + 8 >= valid) x2 = x3 = -INFINITY;
+      float t0 = fmaxf(x0, x2), t1 = fmaxf(x1, x3);
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
+      for (int off = 4; off < 32; off <<= 1) {
+        t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+        t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+      }
+      const float mn0 = fmaxf(m0[nt], t0), mn1 = fmaxf(m1[nt], t1);
+      const float al0 = exp2f(m0[nt] - mn0), al1 = exp2f(m1[nt] - mn1);
+      m0[nt] = mn0;
+      m1[nt] = mn1;
+      const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
+      const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+      l0[nt] = l0[nt] * al0 + p0 + p2;
+      l1[nt] = l1[nt] * al1 + p1 + p3;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[nt][mt][0] *= al0;
+        o[nt][mt][1] *= al1;
+        o[nt][mt][2] *= al0;
+        o[nt][mt][3] *= al1;
+      }
+      b0[nt] = movmatrix_t(pack_bf16x2(p0, p1));
+      b1[nt] = movmatrix_t(pack_bf16x2(p2, p3));
     }
-    const uint32_t b0 = movmatrix_t(pack_bf16x2(p0, p1));
-    const uint32_t b1 = movmatrix_t(pack_bf16x2(p2, p3));
 
     if (valid < kBlock) {
       // Zero the value rows past the context so that 0 * garbage stays 0.
@@ -255,7 +283,8 @@ __global__ void __launch_bounds__(kWarps * 32)
       const int chunk = (mt & 3) * 2 + vch;
       uint32_t a0, a1, a2, a3;
       ldsm_x4_t(sb + half * (kStageBytes / 2) + swz(vrow, chunk), a0, a1, a2, a3);
-      mma_bf16_16816(o[mt], a0, a1, a2, a3, b0, b1);
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) mma_bf16_16816(o[nt][mt], a0, a1, a2, a3, b0[nt], b1[nt]);
     }
     __syncwarp();
     if (lane == 0 && k + kStages < my_count) issue(k + kStages);
@@ -269,50 +298,58 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   // Row sums: reduce over the 8 lanes that share t.
 #pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0[nt] += __shfl_xor_sync(0xffffffffu, l0[nt], off);
+      l1[nt] += __shfl_xor_sync(0xffffffffu, l1[nt], off);
+    }
   }
 
   __syncthreads();  // every ring slot has been consumed: reuse as merge space
-  float* mo = reinterpret_cast<float*>(base);           // [kWarps][8][128]
-  float* mm = mo + kWarps * 8 * kHeadDim;               // [kWarps][8]
-  float* ml = mm + kWarps * 8;                          // [kWarps][8]
+  float* mo = reinterpret_cast<float*>(base);           // [kWarps][kCols][128]
+  float* mm = mo + kWarps * kCols * kHeadDim;           // [kWarps][kCols]
+  float* ml = mm + kWarps * kCols;                      // [kWarps][kCols]
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int d0 = mt * 16 + g;
-    mo[(warp * 8 + 2 * t) * kHeadDim + d0] = o[mt][0];
-    mo[(warp * 8 + 2 * t + 1) * kHeadDim + d0] = o[mt][1];
-    mo[(warp * 8 + 2 * t) * kHeadDim + d0 + 8] = o[mt][2];
-    mo[(warp * 8 + 2 * t + 1) * kHeadDim + d0 + 8] = o[mt][3];
-  }
-  if (g == 0) {
-    mm[warp * 8 + 2 * t] = m0;
-    mm[warp * 8 + 2 * t + 1] = m1;
-    ml[warp * 8 + 2 * t] = l0;
-    ml[warp * 8 + 2 * t + 1] = l1;
+  for (int nt = 0; nt < kNT; ++nt) {
+    const int c0 = warp * kCols + nt * 8 + 2 * t;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d0 = mt * 16 + g;
+      mo[c0 * kHeadDim + d0] = o[nt][mt][0];
+      mo[(c0 + 1) * kHeadDim + d0] = o[nt][mt][1];
+      mo[c0 * kHeadDim + d0 + 8] = o[nt][mt][2];
+      mo[(c0 + 1) * kHeadDim + d0 + 8] = o[nt][mt][3];
+    }
+    if (g == 0) {
+      mm[c0] = m0[nt];
+      mm[c0 + 1] = m1[nt];
+      ml[c0] = l0[nt];
+      ml[c0 + 1] = l1[nt];
+    }
   }
   __syncthreads();
 
-  for (int e = threadIdx.x; e < 8 * kHeadDim; e += kThreads) {
+  for (int e = threadIdx.x; e < kCols * kHeadDim; e += kThreads) {
     const int n = e >> 7;
     const int dd = e & (kHeadDim - 1);
     const int which = n >> 2, gi = n & 3;
-    if (gi >= a.G) continue;
+    if (gi >= a.G || which > a.D) continue;
     float mx = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, mm[w * 8 + n]);
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, mm[w * kCols + n]);
     float acc = 0.f, den = 0.f;
     if (mx > -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float f = exp2f(mm[w * 8 + n] - mx);
-        acc += f * mo[(w * 8 + n) * kHeadDim + dd];
-        den += f * ml[w * 8 + n];
+        const float f = exp2f(mm[w * kCols + n] - mx);
+        acc += f * mo[(w * kCols + n) * kHeadDim + dd];
+        den += f * ml[w * kCols + n];
       }
     }
     const float v = den > 0.f ? acc / den : 0.f;
-    const size_t idx = (static_cast<size_t>(r) * a.Hq + h * a.G + gi) * kHeadDim + dd;
+    const size_t idx = (which ? (which - 1) * plane : 0) +
+                       (static_cast<size_t>(r) * a.Hq + h * a.G + gi) * kHeadDim + dd;
     void* dst = which ? a.outd : a.out;
     if (a.out_fp32)
       static_cast<float*>(dst)[idx] = v;
@@ -327,14 +364,14 @@ size_t attention_smem_bytes() { return AttnLayout<4>::kSmemBytes; }
 
 namespace {
 
-template <int W>
+template <int W, int NT>
 cudaError_t configure_attn() {
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(attn_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_kernel<W, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttnLayout<W>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
@@ -356,11 +393,11 @@ int attn_warps() {
   return forced;
 }
 
-template <int W>
+template <int W, int NT>
 cudaError_t launch_w(const AttnArgs& a, const CUtensorMap* pool_map, int grid, cudaStream_t s) {
-  cudaError_t e = configure_attn<W>();
+  cudaError_t e = configure_attn<W, NT>();
   if (e != cudaSuccess) return e;
-  attn_kernel<W><<<grid, W * 32, AttnLayout<W>::kSmemBytes, s>>>(a, *pool_map);
+  attn_kernel<W, NT><<<grid, W * 32, AttnLayout<W>::kSmemBytes, s>>>(a, *pool_map);
   return cudaGetLastError();
 }
 
@@ -370,15 +407,25 @@ cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
                              cudaStream_t s) {
   const int grid = a.R * a.Hkv;
   if (grid == 0) return cudaSuccess;
-  return attn_warps() == 3 ? launch_w<3>(a, pool_map, grid, s)
-                           : launch_w<4>(a, pool_map, grid, s);
+  if (a.D < 1 || a.D > kMaxDrafts) return cudaErrorInvalidValue;
+  if (a.D > 1)  // 12 or 16 query columns: two tiles
+    return attn_warps() == 3 ? launch_w<3, 2>(a, pool_map, grid, s)
+                             : launch_w<4, 2>(a, pool_map, grid, s);
+  return attn_warps() == 3 ? launch_w<3, 1>(a, pool_map, grid, s)
+                           : launch_w<4, 1>(a, pool_map, grid, s);
 }
 
 cudaError_t preload_attention_kernels() {
   cudaFuncAttributes at;
-  cudaError_t e = cudaFuncGetAttributes(&at, attn_kernel<4>);
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&at, attn_kernel<3>);
-  return e;
+  const void* fns[] = {reinterpret_cast<const void*>(attn_kernel<4, 1>),
+                       reinterpret_cast<const void*>(attn_kernel<3, 1>),
+                       reinterpret_cast<const void*>(attn_kernel<4, 2>),
+                       reinterpret_cast<const void*>(attn_kernel<3, 2>)};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncGetAttributes(&at, f);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace oasis

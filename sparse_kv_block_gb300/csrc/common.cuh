@@ -17,6 +17,7 @@ constexpr int kSummElems = 2 * kHeadDim;             // min row + max row
 constexpr int kSummBytes = kSummElems * 2;           // 512 B
 constexpr int kMaxTopK = 256;
 constexpr int kMaxGroup = 4;
+constexpr int kMaxDrafts = 3;   // draft queries per step (1 + 3 query kinds x 4 heads = 16)
 
 // Device error word bits (mirrors OASIS_DEVERR_* in oasis.h).
 constexpr uint32_t kErrBadBlock = 0x1u;

@@ -10,14 +10,15 @@ namespace oasis {
 
 struct AttnArgs {
   const void* q;         // [R][Hq][d] bf16
-  const void* qd;        // [R][Hq][d] bf16
+  const void* qd;        // [D][R][Hq][d] bf16
   void* out;             // [R][Hq][d] bf16 or fp32
-  void* outd;            // [R][Hq][d] bf16 or fp32
+  void* outd;            // [D][R][Hq][d] bf16 or fp32
   const int32_t* res;    // [R][Hkv][K]  table of this step
   const int32_t* phys;   // [R][Hkv][U]  table of this step
   const int32_t* ctx_len;  // [R]        table of this step
   uint32_t* err;
   int R, Hq, Hkv, G, K, U, NBmax;
+  int D;                 // draft queries per step, 1..3
   float scale_log2;      // softmax scale * log2(e)
   int out_fp32;
   // dense = 1: no resident table; every block b < ceil(ctx_len / B) of a pair
@@ -43,13 +44,14 @@ struct AdmitArgs {
 };
 
 struct ScoreArgs {
-  const void* qd;        // [R][Hq][d] bf16
+  const void* qd;        // [D][R][Hq][d] bf16
   const void* summ;      // [R][Hkv][NBmax][2][d] bf16
   const int32_t* ctx_len;  // [R]
   int32_t* topk_ids;     // [R][Hkv][K]
   float* topk_scores;    // [R][Hkv][K] or null
   uint32_t* err;
   int R, Hq, Hkv, G, K, NBmax;
+  int D;                 // draft queries per step, 1..3 (their bounds add up)
   int pair0, pairs;
   int fuse_admit;        // run the capped eviction of each pair in the tail
   AdmitArgs admit;       // used when fuse_admit (its topk field is ignored)

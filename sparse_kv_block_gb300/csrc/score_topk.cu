@@ -7,13 +7,15 @@
 // keys, and every logical block is ranked per KV head from those summaries
 // alone; the full keys are never read).
 //
-// Score of block b for KV head h (group = the G query heads of h):
-//   s[b] = sum_j sum_i max(qd_ji * mn_bi, qd_ji * mx_bi).
+// Score of block b for KV head h (group = the G query heads of h; with D
+// draft queries per step, every draft's G vectors count as group members):
+//   s[b] = sum_e sum_j sum_i max(qd_eji * mn_bi, qd_eji * mx_bi).
 // Because mn <= mx, max(x*mn, x*mx) = max(x,0)*mx + min(x,0)*mn, so the sum
-// over the group folds into one dot product of length 2d with the weights
-// W+ = sum_j max(qd_j, 0) (on the max row) and W- = sum_j min(qd_j, 0) (on
-// the min row).  Each block then costs 256 multiply-adds on 512 bytes: the
-// scan is a pure HBM stream.
+// over the group (and the drafts) folds into one dot product of length 2d
+// with the weights W+ = sum_j max(qd_j, 0) (on the max row) and
+// W- = sum_j min(qd_j, 0) (on the min row): more drafts cost no scan time.
+// Each block then costs 256 multiply-adds on 512 bytes: the scan is a pure
+// HBM stream.
 //
 // GB300 mapping.  One CTA per (request, KV head): a producer warp streams the
 // request's contiguous summary rows through a 2-deep ring of stages (4
@@ -132,16 +134,20 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     float w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = 0.f;
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.qd) +
-                              (static_cast<size_t>(r) * a.Hq + h * a.G) * kHeadDim + d0;
-    for (int gi = 0; gi < a.G; ++gi) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qg + gi * kHeadDim));
-      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    // Every draft plane adds its group's vectors to the same two weights.
+    const size_t plane = static_cast<size_t>(a.R) * a.Hq * kHeadDim;
+    for (int e = 0; e < a.D; ++e) {
+      const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.qd) + e * plane +
+                                (static_cast<size_t>(r) * a.Hq + h * a.G) * kHeadDim + d0;
+      for (int gi = 0; gi < a.G; ++gi) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(qg + gi * kHeadDim));
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float lo = bf16lo(wd[i]), hi = bf16hi(wd[i]);
-        w[2 * i] += row ? fmaxf(lo, 0.f) : fminf(lo, 0.f);
-        w[2 * i + 1] += row ? fmaxf(hi, 0.f) : fminf(hi, 0.f);
+        for (int i = 0; i < 4; ++i) {
+          const float lo = bf16lo(wd[i]), hi = bf16hi(wd[i]);
+          w[2 * i] += row ? fmaxf(lo, 0.f) : fminf(lo, 0.f);
+          w[2 * i + 1] += row ? fmaxf(hi, 0.f) : fminf(hi, 0.f);
+        }
       }
     }
     // Weights as fp32 pairs for the packed fp32x2 multiply-add.

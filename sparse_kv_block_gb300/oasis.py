@@ -28,7 +28,7 @@ class oasis_config(ctypes.Structure):
                 ("num_q_heads", c_int32), ("num_kv_heads", c_int32), ("head_dim", c_int32),
                 ("block_size", c_int32), ("topk", c_int32), ("fetch_ratio", c_float),
                 ("softmax_scale", c_float), ("out_fp32", c_int32), ("device", c_int32),
-                ("side_groups", c_int32), ("schedule", c_int32)]
+                ("side_groups", c_int32), ("schedule", c_int32), ("num_drafts", c_int32)]
 
 
 SCHEDULE_SCAN_FIRST, SCHEDULE_CONCURRENT, SCHEDULE_THREE_STREAMS, SCHEDULE_AUTO = 0, 1, 2, 3
@@ -145,9 +145,11 @@ def _stream(s) -> Optional[int]:
 
 def make_config(R, NBmax, Hq, Hkv, K, fetch_ratio, layers=1, softmax_scale=0.0,
                 out_fp32=False, device=0, d=128, B=16, side_groups=0,
-                schedule=SCHEDULE_AUTO) -> oasis_config:
+                schedule=SCHEDULE_AUTO, num_drafts=1) -> oasis_config:
+    """``num_drafts`` D: draft queries per step; q_draft / out_draft then hold
+    D planes ``[D][R][Hq][d]`` (a ``[R][Hq][d]`` tensor is the one-draft case)."""
     return oasis_config(layers, R, NBmax, Hq, Hkv, d, B, K, fetch_ratio, softmax_scale,
-                        1 if out_fp32 else 0, device, side_groups, schedule)
+                        1 if out_fp32 else 0, device, side_groups, schedule, num_drafts)
 
 
 def oasis_config_error(cfg: oasis_config) -> Optional[str]:
@@ -258,15 +260,31 @@ class Oasis:
     def oasis_resume_resident(self, layer: int, first_step: int, stream=None) -> None:
         self._check(lib().oasis_resume_resident(self.ctx, layer, first_step, _stream(stream)))
 
+    def _sized(self, q=None, qd=None, out=None, outd=None) -> None:
+        """Refuse torch tensors smaller than the call reads or writes (the
+        library takes plain pointers and cannot check their extent)."""
+        c = self.cfg
+        D = c.num_drafts if c.num_drafts > 0 else 1
+        qb = c.num_requests * c.num_q_heads * c.head_dim * 2
+        ob = qb * (2 if c.out_fp32 else 1)
+        for name, x, need in (("q", q, qb), ("q_draft", qd, D * qb), ("out", out, ob),
+                              ("out_draft", outd, D * ob)):
+            if isinstance(x, torch.Tensor) and x.numel() * x.element_size() < need:
+                raise ValueError(f"{name} holds {x.numel() * x.element_size()} bytes, "
+                                 f"the call needs {need}")
+
     def oasis_lookahead_attn(self, layer, step, q, qd, out, outd, stream=None) -> None:
+        self._sized(q, qd, out, outd)
         self._check(lib().oasis_lookahead_attn(self.ctx, layer, step, _ptr(q), _ptr(qd),
                                                _ptr(out), _ptr(outd), _stream(stream)))
 
     def oasis_dense_attn(self, kv_dense, table, q, qd, out, outd, stream=None) -> None:
+        self._sized(q, qd, out, outd)
         self._check(lib().oasis_dense_attn(self.ctx, _ptr(kv_dense), table, _ptr(q), _ptr(qd),
                                            _ptr(out), _ptr(outd), _stream(stream)))
 
     def oasis_score_topk(self, layer, step, qd, topk_ids, topk_scores=None, stream=None) -> None:
+        self._sized(qd=qd)
         self._check(lib().oasis_score_topk(self.ctx, layer, step, _ptr(qd), _ptr(topk_ids),
                                            _ptr(topk_scores), _stream(stream)))
 
@@ -278,6 +296,7 @@ class Oasis:
 
     def oasis_score_admit_noalloc(self, layer, step, qd, admit_ids, admit_slots, evict_ids,
                                   n_admit, stream=None) -> None:
+        self._sized(qd=qd)
         self._check(lib().oasis_score_admit_noalloc(self.ctx, layer, step, _ptr(qd),
                                                     _ptr(admit_ids), _ptr(admit_slots),
                                                     _ptr(evict_ids), _ptr(n_admit),
@@ -288,6 +307,7 @@ class Oasis:
                                          _ptr(admit_slots), _ptr(n_admit), _stream(stream)))
 
     def oasis_step(self, layer, step, q, qd, out, outd, stream=None) -> None:
+        self._sized(q, qd, out, outd)
         self._check(lib().oasis_step(self.ctx, layer, step, _ptr(q), _ptr(qd), _ptr(out),
                                      _ptr(outd), _stream(stream)))
 
@@ -304,6 +324,7 @@ class Oasis:
 
     def oasis_step_host(self, layer, step, q_host, qd_host, out_host, outd_host,
                         stream=None) -> None:
+        self._sized(q_host, qd_host, out_host, outd_host)
         self._check(lib().oasis_step_host(self.ctx, layer, step, _ptr(q_host), _ptr(qd_host),
                                           _ptr(out_host), _ptr(outd_host), _stream(stream)))
 

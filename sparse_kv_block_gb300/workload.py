@@ -162,20 +162,42 @@ def queries(shape: Shape, seed: int, layer: int, steps: int,
     """(q, qd) for `steps` consecutive steps: [steps][R][Hq][d] bf16 each.
     The query mean points along the head directions of `direction_layer`
     (default `layer`): the layer whose host store the queries read."""
+    q, qd = draft_queries(shape, seed, layer, steps, 1, device, direction_layer)
+    return q, qd[:, 0]
+
+
+def draft_queries(shape: Shape, seed: int, layer: int, steps: int, num_drafts: int,
+                  device="cpu", direction_layer: Optional[int] = None) -> tuple:
+    """(q, qd) with D = num_drafts draft queries per step: q [steps][R][Hq][d],
+    qd [steps][D][R][Hq][d] bf16.  Draft 0 is the draft of `queries` (the same
+    draws).  Draft e > 0 looks e steps further: in the correlated recipe it
+    follows the query noise of step t + 1 + e; in the plain recipe it is the
+    step's query plus fresh noise."""
     R, Hq, d, G = shape.R, shape.Hq, shape.d, shape.G
+    D = int(num_drafts)
+    if D < 1:
+        raise ValueError("num_drafts must be >= 1")
     g = _gen(device, seed, layer, 4)
     z = torch.randn((steps + 1, R, Hq, d), generator=g, device=device)
     e = torch.randn((steps, R, Hq, d), generator=g, device=device)
+    if D > 1:  # drawn after the one-draft stream, which stays unchanged
+        z = torch.cat([z, torch.randn((D - 1, R, Hq, d), generator=g, device=device)])
+        e_more = torch.randn((D - 1, steps, R, Hq, d), generator=g, device=device)
+        e = torch.stack([e] + list(e_more))
+    else:
+        e = e.unsqueeze(0)
     if shape.draft_corr is None:
         q = z[:steps]
-        qd = q + shape.draft_sigma * e
+        qd = torch.stack([q + shape.draft_sigma * e[k] for k in range(D)], dim=1)
     else:
         u = head_directions(shape, seed, layer if direction_layer is None
                             else direction_layer).to(device)
         mean = (shape.q_mean * u).repeat_interleave(G, dim=0)  # [Hq][d]
         rho = shape.draft_corr
         q = mean + z[:steps]
-        qd = mean + rho * z[1:] + math.sqrt(1.0 - rho * rho) * e
+        c = math.sqrt(1.0 - rho * rho)
+        qd = torch.stack([mean + rho * z[1 + k:1 + k + steps] + c * e[k] for k in range(D)],
+                         dim=1)
     return q.to(torch.bfloat16), qd.to(torch.bfloat16)
 
 

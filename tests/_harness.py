@@ -39,11 +39,12 @@ class Layer:
     hb: np.ndarray
     summ: np.ndarray
     remote: dict = None
+    D: int = 1  # draft queries per step; qd is [steps][D][R][Hq][d] when D > 1
 
 
 def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_fp32=False,
                gen_device="cpu", pairs=None, res0=None, side_groups=0,
-               schedule=0, remote_capacity=None, remote_gbps=0.0) -> Layer:
+               schedule=0, remote_capacity=None, remote_gbps=0.0, num_drafts=1) -> Layer:
     if K is not None or fetch_ratio is not None:
         shape = dataclasses.replace(shape, K=K if K is not None else shape.K,
                                     fetch_ratio=shape.fetch_ratio if fetch_ratio is None else fetch_ratio)
@@ -51,12 +52,16 @@ def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_
     host = torch.empty((shape.R, shape.Hkv, shape.NBmax, 2, 16, 128), dtype=torch.bfloat16,
                        pin_memory=True)
     workload.host_kv(shape, seed, 0, lens, device=gen_device, out=host)
-    q, qd = workload.queries(shape, seed, 0, steps, device=gen_device)
+    if num_drafts == 1:
+        q, qd = workload.queries(shape, seed, 0, steps, device=gen_device)
+    else:
+        q, qd = workload.draft_queries(shape, seed, 0, steps, num_drafts, device=gen_device)
     q, qd = q.cpu(), qd.cpu()
     if res0 is None:
         res0 = workload.initial_resident(shape, seed, 0, lens)
     cfg = make_config(shape.R, shape.NBmax, shape.Hq, shape.Hkv, shape.K, shape.fetch_ratio,
-                      out_fp32=out_fp32, side_groups=side_groups, schedule=schedule)
+                      out_fp32=out_fp32, side_groups=side_groups, schedule=schedule,
+                      num_drafts=num_drafts)
     eng = Oasis(cfg, host_kv=[host])
     eng.set_context(lens)
     eng.set_resident(0, res0, 0)
@@ -72,7 +77,7 @@ def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_
         pairs = [(r, h) for r in range(shape.R) for h in range(shape.Hkv)]
     orc = oracle.LayerOracle(hb, summ, lens, res0, shape.K, shape.C, pairs,
                              remote_capacity=remote_capacity)
-    return Layer(shape, lens, host, q, qd, res0, eng, orc, hb, summ, remote)
+    return Layer(shape, lens, host, q, qd, res0, eng, orc, hb, summ, remote, num_drafts)
 
 
 def check_remote(L: Layer, misses: dict):
@@ -129,11 +134,17 @@ def topk_agrees(gpu_ids, ref_ids, ref_scores, K):
     return True
 
 
-def check_attention(out_gpu: np.ndarray, ref: dict, G: int):
+def check_attention(out_gpu: list, ref: dict, G: int):
+    """out_gpu = [out, out_draft]; out_draft is [R][Hq][d] for one draft or
+    [D][R][Hq][d] for D of them (compared plane by plane)."""
+    planes = [out_gpu[0]]
+    for x in out_gpu[1:]:
+        planes += list(x) if x.ndim == 4 else [x]
     errs = []
     for (r, h), v in ref.items():
-        for which in range(2):
-            d = np.abs(out_gpu[which][r, h * G:(h + 1) * G].astype(np.float64) - v["attn"][which])
+        assert len(planes) == v["attn"].shape[0]
+        for which in range(len(planes)):
+            d = np.abs(planes[which][r, h * G:(h + 1) * G].astype(np.float64) - v["attn"][which])
             errs.append(d)
     e = np.concatenate([x.ravel() for x in errs])
     assert e.max() <= ATT_MAX_ABS, f"attention max-abs {e.max():.3e}"
@@ -164,7 +175,7 @@ def run_staged_step(L: Layer, t: int, dev, check_pool_every=True):
     qg, qdg = L.q[t].to(dev), L.qd[t].to(dev)
     odt = torch.float32 if eng.cfg.out_fp32 else torch.bfloat16
     out = torch.empty((sh.R, sh.Hq, 128), dtype=odt, device=dev)
-    outd = torch.empty_like(out)
+    outd = torch.empty(tuple(L.qd[t].shape), dtype=odt, device=dev)
     R, H, K, C = sh.R, sh.Hkv, sh.K, max(sh.C, 1)
     topk = torch.empty((R, H, K), dtype=torch.int32, device=dev)
     scores = torch.empty((R, H, K), dtype=torch.float32, device=dev)

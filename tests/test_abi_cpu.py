@@ -45,6 +45,21 @@ def test_query_sizes_qwen3_8b_layer():
     assert s.workspace_bytes % 256 == 0
 
 
+def test_workspace_grows_with_draft_planes():
+    # q_draft / out_draft staging holds D planes; nothing else changes.
+    base = ob.make_config(R=128, NBmax=1024, Hq=32, Hkv=8, K=128, fetch_ratio=0.05)
+    plane = 128 * 32 * 128 * 2
+    w = [ob.oasis_query_sizes(ob.make_config(R=128, NBmax=1024, Hq=32, Hkv=8, K=128,
+                                             fetch_ratio=0.05, num_drafts=D)).workspace_bytes
+         for D in (1, 2, 3)]
+    assert ob.oasis_query_sizes(base).workspace_bytes == w[0]
+    # qd_stage x2, qd_ring x2 (plane each) and outd_stage (bf16 plane) per extra draft
+    assert w[1] - w[0] == 5 * plane and w[2] - w[1] == 5 * plane
+    zero = ob.make_config(R=128, NBmax=1024, Hq=32, Hkv=8, K=128, fetch_ratio=0.05,
+                          num_drafts=0)
+    assert ob.oasis_query_sizes(zero).workspace_bytes == w[0]
+
+
 @pytest.mark.parametrize("ratio,K,cap", [(0.05, 128, 6), (0.01, 128, 1), (0.25, 128, 32),
                                          (1.0, 128, 128), (0.25, 16, 4), (0.0, 16, 0)])
 def test_fetch_cap_is_floor(ratio, K, cap):
@@ -57,6 +72,7 @@ def test_fetch_cap_is_floor(ratio, K, cap):
     ("topk", 0, "topk"), ("topk", 300, "topk"), ("num_q_heads", 40, "per KV head"),
     ("num_q_heads", 31, "multiple"), ("fetch_ratio", 1.5, "fetch_ratio"),
     ("max_blocks", 8, "topk must be <= max_blocks"), ("num_requests", 0, "num_requests"),
+    ("num_drafts", 4, "num_drafts"), ("num_drafts", -1, "num_drafts"),
 ])
 def test_config_errors(field, value, msg):
     cfg = ob.make_config(R=2, NBmax=64, Hq=8, Hkv=2, K=16, fetch_ratio=0.25)
