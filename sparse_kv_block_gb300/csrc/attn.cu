@@ -59,8 +59,14 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 // kNT tiles of 8 query columns: column n = which * 4 + gi, which 0 = the
 // normal query, 1 + e = draft e; gi = query head within the group.
+// Register caps: three CTAs of this kernel fill an SM's shared memory, and
+// the host-link gather of the same step must still find registers for one of
+// its 128-thread CTAs (80 registers per thread) beside them.  Two tiles need
+// up to 166 registers uncapped (3 x 128 x 166 fills the whole register file,
+// which held the gathers back: 2538 against 3101 layer-steps/s at D = 2); at
+// 144 there is no spill and 3 x 128 x 144 + 128 x 80 = 65536.
 template <int kWarps, int kNT>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __maxnreg__(kNT == 2 ? 144 : 96)
     attn_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap pool_map) {
   using Lay = AttnLayout<kWarps>;
   constexpr int kThreads = kWarps * 32;
