@@ -137,6 +137,19 @@ typedef struct {
 #define OASIS_SCHEDULE_CONCURRENT 1
 #define OASIS_SCHEDULE_THREE_STREAMS 2
 #define OASIS_SCHEDULE_AUTO 3
+/* EARLY_SCAN: the scan + top-K of step t runs on its own stream as soon as
+ * its inputs exist, beside the previous step's attention, instead of after
+ * the work already on `stream`; only the admission waits for that work (it
+ * rewrites the table the previous attention read).  Contract: the draft
+ * queries must be ready when oasis_step is called (oasis_step_host's host
+ * buffers always are), and the summaries and context lengths may change
+ * between steps only through this library's calls (build_summaries,
+ * append_token, refresh_blocks, advance_context), which the early scan
+ * follows, or with the device idle.  Results are identical.  Measured on
+ * GB300 (128 x 16K layer, oasis_step): 3177 against 3079 layer-steps/s
+ * scan-first at cap 0.05, 3497-4129 against 3467 at cap 0.01; through
+ * oasis_step_host 2864-2875 against 2904 for AUTO, so AUTO never picks it. */
+#define OASIS_SCHEDULE_EARLY_SCAN 4
 
 typedef struct {
   size_t kv_pool_bytes;   /* per layer */

@@ -303,6 +303,16 @@ struct LayerState {
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_side_done = nullptr;
   cudaEvent_t ev_scan_done = nullptr;
+  // Early-scan schedule: the draft queries staged on the scan stream; the
+  // admissions of a step parity done (the next scan of that parity rewrites
+  // the top-K lists they read).
+  cudaEvent_t ev_qd_copied = nullptr;
+  cudaEvent_t ev_admitted[2] = {nullptr, nullptr};
+  bool admitted_pending[2] = {false, false};
+  // The library's last write of this layer's summaries (build, append,
+  // refresh), which an early scan must follow.
+  cudaEvent_t ev_mut = nullptr;
+  bool mut_pending = false;
   std::vector<cudaEvent_t> ev_group;  // one per side-work request group
   std::vector<cudaEvent_t> ev_group2; // admissions done (three-stream schedule)
   bool side_pending = false;
@@ -378,7 +388,8 @@ const char* config_error(const oasis_config* c) {
   if (c->side_groups < 0 || c->side_groups > 64) return "side_groups must be in 0..64";
   if (c->num_drafts < 0 || c->num_drafts > kMaxDrafts) return "num_drafts must be in 0..3";
   if (c->schedule != OASIS_SCHEDULE_SCAN_FIRST && c->schedule != OASIS_SCHEDULE_CONCURRENT &&
-      c->schedule != OASIS_SCHEDULE_THREE_STREAMS && c->schedule != OASIS_SCHEDULE_AUTO)
+      c->schedule != OASIS_SCHEDULE_THREE_STREAMS && c->schedule != OASIS_SCHEDULE_AUTO &&
+      c->schedule != OASIS_SCHEDULE_EARLY_SCAN)
     return "schedule must be one of OASIS_SCHEDULE_*";
   const double units = static_cast<double>(c->num_requests) * c->num_kv_heads *
                        (c->topk + fetch_cap(*c)) * 2 * kBlock;
@@ -418,7 +429,9 @@ struct oasis_ctx {
   WsLayout wl{};
   cudaStream_t side = nullptr;   // scan + top-K + admission
   cudaStream_t side2 = nullptr;  // host -> HBM gathers
-  cudaStream_t side3 = nullptr;  // admissions (three-stream schedule only)
+  cudaStream_t side3 = nullptr;  // admissions (three-stream) or scans (early scan)
+  cudaEvent_t ev_ctx_mut = nullptr;  // the library's last write of ctx_len
+  bool ctx_mut_pending = false;
   cudaStream_t io = nullptr;     // oasis_step_host input copies
   std::string last_error;
   bool prof = false;
@@ -772,7 +785,8 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
   if (cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, hi) != cudaSuccess ||
       cudaStreamCreateWithPriority(&c->side2, cudaStreamNonBlocking, hi) != cudaSuccess ||
       cudaStreamCreateWithPriority(&c->side3, cudaStreamNonBlocking, hi) != cudaSuccess ||
-      cudaStreamCreateWithPriority(&c->io, cudaStreamNonBlocking, hi) != cudaSuccess)
+      cudaStreamCreateWithPriority(&c->io, cudaStreamNonBlocking, hi) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_ctx_mut, cudaEventDisableTiming) != cudaSuccess)
     return bail(OASIS_ENOMEM);
   {
     const int pairs = cfg->num_requests * cfg->num_kv_heads;
@@ -852,7 +866,11 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
     S.outd_stage = w + (c->wl.outd_stage - b0);
     if (cudaEventCreateWithFlags(&S.ev_start, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_side_done, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&S.ev_scan_done, cudaEventDisableTiming) != cudaSuccess)
+        cudaEventCreateWithFlags(&S.ev_scan_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_qd_copied, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_admitted[0], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_admitted[1], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_mut, cudaEventDisableTiming) != cudaSuccess)
       return bail(OASIS_ENOMEM);
     S.ev_group.assign(c->groups, nullptr);
     S.ev_group2.assign(c->groups, nullptr);
@@ -891,7 +909,10 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
     if (L.ev_start) cudaEventDestroy(L.ev_start);
     if (L.ev_side_done) cudaEventDestroy(L.ev_side_done);
     if (L.ev_scan_done) cudaEventDestroy(L.ev_scan_done);
+    if (L.ev_qd_copied) cudaEventDestroy(L.ev_qd_copied);
+    if (L.ev_mut) cudaEventDestroy(L.ev_mut);
     for (int k = 0; k < 2; ++k) {
+      if (L.ev_admitted[k]) cudaEventDestroy(L.ev_admitted[k]);
       if (L.ev_in[k]) cudaEventDestroy(L.ev_in[k]);
       if (L.ev_stage_free[k]) cudaEventDestroy(L.ev_stage_free[k]);
     }
@@ -904,6 +925,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side) cudaStreamDestroy(ctx->side);
   if (ctx->side2) cudaStreamDestroy(ctx->side2);
   if (ctx->side3) cudaStreamDestroy(ctx->side3);
+  if (ctx->ev_ctx_mut) cudaEventDestroy(ctx->ev_ctx_mut);
   if (ctx->io) cudaStreamDestroy(ctx->io);
   ctx->layers.clear();  // remote tiers: worker and copy threads joined
   delete ctx;
@@ -932,18 +954,34 @@ OASIS_API int oasis_sync(oasis_ctx* ctx, uint32_t* device_bits) {
   return OASIS_OK;
 }
 
+namespace {
+// A library call wrote this layer's summaries on `s`: an early scan issued
+// later waits for it (the other schedules follow the caller's stream).
+int note_summary_write(oasis_ctx* ctx, LayerState& L, cudaStream_t s) {
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_mut, s), "record summary write")) return rc;
+  L.mut_pending = true;
+  return OASIS_OK;
+}
+}  // namespace
+
 OASIS_API int oasis_build_summaries(oasis_ctx* ctx, int layer, int table, void* stream) {
   if (int rc = check_layer(ctx, layer)) return rc;
   if (int rc = ctx->set_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerState& L = ctx->layers[layer];
+  // A scan of an earlier step may still read the summaries.
+  if (L.side_pending) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
+  }
   SummaryArgs a{};
-  a.host = ctx->layers[layer].host_dev;
-  a.summ = ctx->layers[layer].summ;
+  a.host = L.host_dev;
+  a.summ = L.summ;
   a.ctx_len = ctx->ctx_tab(table);
   a.R = ctx->cfg.num_requests;
   a.Hkv = ctx->cfg.num_kv_heads;
   a.NBmax = ctx->cfg.max_blocks;
-  return ctx->cuda(launch_summary_build(a, static_cast<cudaStream_t>(stream)),
-                   "summary_build launch");
+  if (int rc = ctx->cuda(launch_summary_build(a, s), "summary_build launch")) return rc;
+  return note_summary_write(ctx, L, s);
 }
 
 namespace {
@@ -1123,7 +1161,7 @@ OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t*
 
 namespace {
 int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_draft, void* out,
-              void* out_draft, void* stream, int schedule);
+              void* out_draft, void* stream, int schedule, cudaEvent_t inputs_ready);
 }  // namespace
 
 OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
@@ -1132,12 +1170,14 @@ OASIS_API int oasis_step(oasis_ctx* ctx, int layer, int step, const void* q,
   if (!ctx) return OASIS_EINVAL;
   const int sched = ctx->cfg.schedule == OASIS_SCHEDULE_AUTO ? OASIS_SCHEDULE_SCAN_FIRST
                                                               : ctx->cfg.schedule;
-  return step_impl(ctx, layer, step, q, q_draft, out, out_draft, stream, sched);
+  return step_impl(ctx, layer, step, q, q_draft, out, out_draft, stream, sched, nullptr);
 }
 
 namespace {
+// inputs_ready: with the early-scan schedule, the event after which the draft
+// queries may be read (null: they are ready when the call is made).
 int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_draft, void* out,
-              void* out_draft, void* stream, int schedule) {
+              void* out_draft, void* stream, int schedule, cudaEvent_t inputs_ready) {
   if (int rc = check_layer(ctx, layer)) return rc;
   if (step < 0 || step > (1 << 30) || !q || !q_draft || !out || !out_draft)
     return ctx->fail(OASIS_EINVAL, "step: bad step or null pointer");
@@ -1145,14 +1185,46 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
   if (!L.loaded) return ctx->fail(OASIS_ESTATE, "layer %d: oasis_load_resident first", layer);
   if (int rc = ctx->set_device()) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool early = schedule == OASIS_SCHEDULE_EARLY_SCAN;
   // The side work reads the draft query from a per-layer double buffer, so
   // the caller may reuse its buffer as soon as `stream` passes this call.
   void* qd_copy = L.qd_ring[step & 1];
   const size_t qbytes = static_cast<size_t>(ctx->D) * ctx->cfg.num_requests *
                         ctx->cfg.num_q_heads * kHeadDim * 2;
-  if (int rc = ctx->cuda(cudaMemcpyAsync(qd_copy, q_draft, qbytes, cudaMemcpyDeviceToDevice, s),
-                         "stage q_draft"))
+  if (early) {
+    // Early scan: the scans run on their own stream as soon as the draft
+    // queries, the summaries and the context lengths they read exist, not
+    // after the work already on `stream` (the previous attention).  They
+    // write only this step's top-K lists, whose previous readers (the
+    // admissions two steps back) must be done.
+    cudaStream_t sc = ctx->side3;
+    if (inputs_ready) {
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(sc, inputs_ready, 0), "scan wait inputs"))
+        return rc;
+    }
+    if (L.mut_pending) {
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(sc, L.ev_mut, 0), "scan wait summaries"))
+        return rc;
+    }
+    if (ctx->ctx_mut_pending) {
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(sc, ctx->ev_ctx_mut, 0), "scan wait ctx_len"))
+        return rc;
+    }
+    if (L.admitted_pending[step & 1]) {
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(sc, L.ev_admitted[step & 1], 0),
+                             "scan wait lists"))
+        return rc;
+    }
+    if (int rc = ctx->cuda(cudaMemcpyAsync(qd_copy, q_draft, qbytes, cudaMemcpyDeviceToDevice,
+                                           sc), "stage q_draft"))
+      return rc;
+    if (int rc = ctx->cuda(cudaEventRecord(L.ev_qd_copied, sc), "record q_draft staged"))
+      return rc;
+  } else if (int rc = ctx->cuda(cudaMemcpyAsync(qd_copy, q_draft, qbytes,
+                                                cudaMemcpyDeviceToDevice, s),
+                                "stage q_draft")) {
     return rc;
+  }
   // Start of this step's side work: everything earlier on `stream`, which
   // includes the previous step's attention of this layer.  That is all the
   // scan and the admission need (the admission rewrites the table the
@@ -1173,6 +1245,31 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
     const int p0 = static_cast<int>(static_cast<long long>(pairs) * g / ctx->groups);
     const int p1 = static_cast<int>(static_cast<long long>(pairs) * (g + 1) / ctx->groups);
     const LayerState::Lists& Ls = L.lists[step & 1];
+    if (early) {
+      // Scan + top-K on side3 (already running ahead); the group's
+      // admission on `side` after the step start and the group's scan; its
+      // gather on side2.
+      if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side3,
+                             p0, p1 - p0, false))
+        return rc;
+      if (int rc = ctx->cuda(cudaEventRecord(L.ev_group2[g], ctx->side3), "record top-k"))
+        return rc;
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side, L.ev_group2[g], 0), "wait top-k"))
+        return rc;
+      if (int rc = run_admit(ctx, layer, step, Ls.topk_ids, Ls.admit_ids, Ls.admit_slots,
+                             Ls.evict_ids, Ls.n_admit, ctx->side, p0, p1 - p0))
+        return rc;
+      if (int rc = ctx->cuda(cudaEventRecord(L.ev_group[g], ctx->side), "record group"))
+        return rc;
+      if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[g], 0), "group wait"))
+        return rc;
+      if (ctx->C > 0) {
+        if (int rc = run_prefetch(ctx, layer, step, Ls.admit_ids, Ls.admit_slots, Ls.n_admit,
+                                  ctx->side2, p0, p1 - p0))
+          return rc;
+      }
+      continue;
+    }
     if (schedule == OASIS_SCHEDULE_THREE_STREAMS) {
       // The pages' pipeline: top-K prediction, KV selection and KV transfer
       // on three streams, each stage of a group ordered by an event.
@@ -1213,6 +1310,14 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
   if (ctx->C == 0) {
     if (int rc = ctx->cuda(cudaEventRecord(L.ev_group[0], ctx->side), "record group")) return rc;
     if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[0], 0), "group wait"))
+      return rc;
+  }
+  if (early) {
+    if (int rc = ctx->cuda(cudaEventRecord(L.ev_admitted[step & 1], ctx->side), "record admitted"))
+      return rc;
+    L.admitted_pending[step & 1] = true;
+    // The caller may reuse q_draft once `stream` passes this call.
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_qd_copied, 0), "wait q_draft staged"))
       return rc;
   }
   if (schedule == OASIS_SCHEDULE_SCAN_FIRST) {
@@ -1295,7 +1400,7 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
   const int sched = ctx->cfg.schedule == OASIS_SCHEDULE_AUTO ? OASIS_SCHEDULE_CONCURRENT
                                                               : ctx->cfg.schedule;
   if (int rc = step_impl(ctx, layer, step, L.q_stage[slot], L.qd_stage[slot], L.out_stage,
-                         L.outd_stage, stream, sched))
+                         L.outd_stage, stream, sched, L.ev_in[slot]))
     return rc;
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_stage_free[slot], s), "record stage")) return rc;
   L.stage_used[slot] = true;
@@ -1351,7 +1456,8 @@ OASIS_API int oasis_append_token(oasis_ctx* ctx, int layer, int step, const void
   a.NBmax = ctx->cfg.max_blocks;
   a.K = ctx->cfg.topk;
   a.U = ctx->U;
-  return ctx->cuda(launch_append(a, s), "append launch");
+  if (int rc = ctx->cuda(launch_append(a, s), "append launch")) return rc;
+  return note_summary_write(ctx, L, s);
 }
 
 OASIS_API int oasis_refresh_blocks(oasis_ctx* ctx, int layer, int step, const int32_t* ids,
@@ -1384,16 +1490,23 @@ OASIS_API int oasis_refresh_blocks(oasis_ctx* ctx, int layer, int step, const in
   a.K = ctx->cfg.topk;
   a.U = ctx->U;
   a.max_ids = max_ids;
-  return ctx->cuda(launch_refresh(a, s), "refresh launch");
+  if (int rc = ctx->cuda(launch_refresh(a, s), "refresh launch")) return rc;
+  return note_summary_write(ctx, L, s);
 }
 
 OASIS_API int oasis_advance_context(oasis_ctx* ctx, int step, int grow, void* stream) {
   if (!ctx) return OASIS_EINVAL;
   if (step < 0 || grow < 0) return ctx->fail(OASIS_EINVAL, "advance: bad argument");
   if (int rc = ctx->set_device()) return rc;
-  return ctx->cuda(launch_advance(ctx->ctx_tab(step), ctx->ctx_tab(step + 1),
-                                  ctx->cfg.num_requests, grow, static_cast<cudaStream_t>(stream)),
-                   "advance launch");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = ctx->cuda(launch_advance(ctx->ctx_tab(step), ctx->ctx_tab(step + 1),
+                                        ctx->cfg.num_requests, grow, s),
+                         "advance launch"))
+    return rc;
+  // An early scan of a later step reads the new table: it waits for this.
+  if (int rc = ctx->cuda(cudaEventRecord(ctx->ev_ctx_mut, s), "record ctx write")) return rc;
+  ctx->ctx_mut_pending = true;
+  return OASIS_OK;
 }
 
 namespace {

@@ -32,6 +32,7 @@ class oasis_config(ctypes.Structure):
 
 
 SCHEDULE_SCAN_FIRST, SCHEDULE_CONCURRENT, SCHEDULE_THREE_STREAMS, SCHEDULE_AUTO = 0, 1, 2, 3
+SCHEDULE_EARLY_SCAN = 4
 
 
 class oasis_sizes(ctypes.Structure):

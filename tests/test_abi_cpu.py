@@ -73,6 +73,7 @@ def test_fetch_cap_is_floor(ratio, K, cap):
     ("num_q_heads", 31, "multiple"), ("fetch_ratio", 1.5, "fetch_ratio"),
     ("max_blocks", 8, "topk must be <= max_blocks"), ("num_requests", 0, "num_requests"),
     ("num_drafts", 4, "num_drafts"), ("num_drafts", -1, "num_drafts"),
+    ("schedule", 5, "schedule"), ("schedule", -1, "schedule"),
 ])
 def test_config_errors(field, value, msg):
     cfg = ob.make_config(R=2, NBmax=64, Hq=8, Hkv=2, K=16, fetch_ratio=0.25)

@@ -61,10 +61,11 @@ def test_small_groups_ragged_contexts(dev, D, Hq, lens):
     L.eng.close()
 
 
-@pytest.mark.parametrize("schedule,groups", [(0, 0), (1, 3), (2, 3), (3, 0)])
+@pytest.mark.parametrize("schedule,groups", [(0, 0), (1, 3), (2, 3), (3, 0), (4, 2)])
 def test_fused_steps_back_to_back(dev, schedule, groups):
     # oasis_step with three drafts, six steps issued with no host wait between
-    # them; the draft planes are staged per step by the library.
+    # them; the draft planes are staged per step by the library (on the scan
+    # stream under the early-scan schedule).
     D = 3
     sh = dataclasses.replace(TINY, R=5)
     L = H.make_layer(sh, seed=22, steps=6, out_fp32=True, side_groups=groups,

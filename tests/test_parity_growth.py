@@ -74,3 +74,53 @@ def test_append_and_advance_match_oracle(dev, ctx0, steps):
                         np.testing.assert_array_equal(pool[r, h, phys[r, h, s]],
                                                       hb_orc[r, h, res[r, h, s]])
     eng.close()
+
+
+@pytest.mark.parametrize("schedule", [0, 4])
+def test_growth_steps_back_to_back(dev, schedule):
+    # Steps, appends and context advances issued with no host wait at all.
+    # Under the early-scan schedule the scan of step t + 1 runs on its own
+    # stream and must still see the token appended after step t (the tail
+    # summary) and the advanced context length.
+    steps = 24
+    sh = dataclasses.replace(workload.SHAPES["tiny"], R=3, ctx=990, grow_steps=steps)
+    L = H.make_layer(sh, seed=12, lens=[990, 1000, 31], steps=steps, out_fp32=True,
+                     schedule=schedule)
+    eng = L.eng
+    hb_orc = L.hb.copy()
+    summ_orc = L.summ.copy()
+    lens = L.lens.copy()
+    orc = oracle.LayerOracle(hb_orc, summ_orc, lens, L.res0, sh.K, sh.C, L.orc.pairs)
+    outs = [torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
+            for _ in range(2 * steps)]
+    qg, qdg = L.q.to(dev), L.qd.to(dev)
+    toks = [workload.new_tokens(sh, 12, 0, t) for t in range(steps)]
+    toks_d = [(k.to(dev), v.to(dev)) for k, v in toks]
+    for t in range(steps):
+        eng.oasis_step(0, t, qg[t], qdg[t], outs[2 * t], outs[2 * t + 1])
+        eng.oasis_append_token(0, t, *toks_d[t])
+        eng.oasis_advance_context(t, 1)
+    eng.oasis_join(0)
+    eng.oasis_sync()
+    for t in range(steps):
+        ref = orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        kb, vb = workload.bf16_bits(toks[t][0]), workload.bf16_bits(toks[t][1])
+        for r in range(sh.R):
+            oracle.append_token(hb_orc, summ_orc, lens, kb[r], vb[r], r)
+        lens += 1
+        H.check_attention([outs[2 * t].cpu().numpy(), outs[2 * t + 1].cpu().numpy()], ref, sh.G)
+        if t >= steps - 2:   # the lists of the last two steps are still in place
+            lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
+            for (r, h), v in ref.items():
+                assert np.array_equal(lists["topk_ids"][r, h], v["topk"])
+    nxt = steps & 1
+    assert (eng.ctx_len[nxt].cpu().numpy() == lens).all()
+    assert (eng.res_ids[0][nxt].cpu().numpy() == orc.res).all()
+    assert (eng.stamps[0].cpu().numpy() == orc.stamp).all()
+    np.testing.assert_array_equal(L.hb, hb_orc)
+    gs = workload.bf16_bits(eng.summaries[0].cpu())
+    for r in range(sh.R):
+        nb = -(-int(lens[r]) // 16)
+        np.testing.assert_array_equal(H.bits_to_float(gs[r, :, :nb]),
+                                      H.bits_to_float(summ_orc[r, :, :nb]))
+    eng.close()

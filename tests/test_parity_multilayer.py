@@ -25,7 +25,7 @@ def dev():
     return torch.device("cuda", 0)
 
 
-@pytest.mark.parametrize("schedule", [0, 1, 2, 3])
+@pytest.mark.parametrize("schedule", [0, 1, 2, 3, 4])
 def test_three_layers_interleaved(dev, schedule):
     sh = dataclasses.replace(workload.SHAPES["tiny"], R=3, ctx=900, layers=3)
     nl, steps = 3, 5

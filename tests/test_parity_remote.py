@@ -37,7 +37,7 @@ def test_remote_staged_steps_match_oracle(dev):
     L.eng.close()
 
 
-@pytest.mark.parametrize("groups,schedule", [(0, 0), (3, 0), (2, 2)])
+@pytest.mark.parametrize("groups,schedule", [(0, 0), (3, 0), (2, 2), (2, 4)])
 def test_remote_fused_steps_match_oracle(dev, groups, schedule):
     sh = dataclasses.replace(TINY, R=4)
     L = H.make_layer(sh, seed=12, steps=6, fetch_ratio=0.25, out_fp32=True, side_groups=groups,

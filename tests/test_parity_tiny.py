@@ -72,7 +72,8 @@ def test_small_groups_and_many_requests(dev):
 
 
 @pytest.mark.parametrize("groups,R,schedule", [(0, 2, 0), (3, 5, 0), (10, 5, 0), (3, 5, 1),
-                                               (3, 5, 2), (0, 2, 2), (0, 5, 3)])
+                                               (3, 5, 2), (0, 2, 2), (0, 5, 3), (0, 2, 4),
+                                               (3, 5, 4)])
 def test_fused_step_matches_oracle(dev, groups, R, schedule):
     # oasis_step: fused scan + top-K + admission per request group on one side
     # stream, gathers per group on another; uneven and one-pair groups too;
@@ -123,7 +124,7 @@ def test_host_buffer_step_matches_device_step(dev):
     eng.close()
 
 
-@pytest.mark.parametrize("schedule", [0, 3])
+@pytest.mark.parametrize("schedule", [0, 3, 4])
 def test_host_buffer_steps_back_to_back(dev, schedule):
     # oasis_step_host issued for consecutive steps with no host wait between
     # them: step t + 1's input copies may overlap step t's side work.  The
@@ -168,7 +169,7 @@ def test_device_error_word_on_bad_block_id(dev):
 
 
 @pytest.mark.parametrize("ratio,groups,schedule", [(1.0, 3, 0), (0.25, 0, 1), (1.0, 1, 1),
-                                                    (1.0, 3, 2)])
+                                                    (1.0, 3, 2), (0.25, 0, 4), (1.0, 3, 4)])
 def test_back_to_back_steps_without_host_sync(dev, ratio, groups, schedule):
     # Steps issued back to back: step t+1's scan and admission may run while
     # step t's gathers are still copying, so the step lists must be per step.
