@@ -492,14 +492,13 @@ def run_oasis(args, ws, rank, local):
         k["peak_source"] = (hbm_src if k["bound"] == "hbm" else
                             "pinned cudaMemcpyAsync H2D, 256 MiB, measured in this run")
     # DRAM bytes per launch from ncu dram__bytes_read.sum + dram__bytes_write.sum
-    # (profiles/dram_traffic_qwen3_8b_16k.md): attention on the 32-request
-    # case scaled by the 4x units of this workload (full size: 1.08 GB +
-    # 2.12 MB), the scan at full size; the gather's 50 MB of HBM writes are
-    # still in L2 when it ends, so its DRAM count is small.
+    # at full size, mean of two launches (profiles/dram_traffic_qwen3_8b_16k.md);
+    # the gather's 50 MB of HBM writes are still in L2 when it ends, so its
+    # DRAM count is small.
     if shape.name == "qwen3_8b_16k":
-        measured = {"attention": int(4 * (269.256192e6 + 0.12646e6)),
-                    "score_topk": int(539.64e6 + 4.83e6),
-                    "prefetch": int((0.39859e6 + 4.14e6 + 0.44058e6 + 3.47e6) / 2)}
+        measured = {"attention": (1076977920 + 1741056 + 1077071104 + 2078720) // 2,
+                    "score_topk": (539654912 + 4669696 + 539656448 + 1666816) // 2,
+                    "prefetch": (394240 + 3492096 + 397568 + 3322112) // 2}
         for n, v in measured.items():
             if n in per_kernel:
                 per_kernel[n]["traffic"] = v
