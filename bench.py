@@ -749,6 +749,14 @@ def run_oasis_layers(args, ws, rank, local):
             "kernels": per, "gpu_launches": int(sum(counts)), "clocks": clk}
     if step_spread is not None:
         line["step_ms_spread"] = step_spread
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        # Every layer-step does the same work, so the oracle is timed on layer
+        # 0's store and first step (a bounded sample), on every host core.
+        ncores = os.cpu_count() or 1
+        rate, pairs, sec, desc = oracle_rate(shape, stores[0], lens, qs[0].cpu(), qds[0].cpu(),
+                                             budget_s=args.cpu_budget / 2, threads=ncores)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": ncores, "kind": "oracle",
+                                "sample": desc + " (layer 0, first step)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     eng.close()
