@@ -62,14 +62,18 @@ struct Layout {
   __host__ __device__ static int total(int NBmax) { return keys(NBmax) + CW * KP * 8 + 128; }
 };
 
+// The launch bounds pin the occupancy the 8-warp variants are sized for: 4
+// CTAs per SM (K <= 128) and 3 (K > 128); the 4-warp variants reach 8 and 5
+// unbounded.
 template <int KPL, int CW>
-__global__ void __launch_bounds__((CW + 1) * 32)
+__global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : (KPL <= 4 ? 4 : 3))
     score_topk_kernel(const ScoreArgs a) {
   using L = Layout<KPL, CW>;
   constexpr int KP = L::KP;
   constexpr int kCW = CW;
   constexpr int kChunk = L::kChunk;
   constexpr int kChunkBytes = L::kChunkBytes;
+  constexpr bool kRunsEarly = CW == 8;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::bars(a.NBmax));
@@ -157,6 +161,48 @@ __global__ void __launch_bounds__((CW + 1) * 32)
     uint64_t* mybuf = keybuf + warp * KP;
     int cnt = 0;
     bool have_top = false;  // false while `top` still holds only empty keys
+    // The buffer's keys as sorted 32-key runs (run i = keys i*32 .. i*32+31),
+    // nrun of them complete.  With 8 consumer warps each run is sorted as
+    // soon as its 32 keys exist (the sorts then overlap the stream: 94.2
+    // against 97.9 us alone on 1024 pairs); with 4, whose warps each see
+    // twice the keys, the whole buffer is sorted when full (92.5 against
+    // 96.9 us the other way).
+    uint64_t run[KPL];
+    int nrun = 0;
+    // Run i of a buffer sorted in the direction the bitonic network over the
+    // whole buffer gives it (descending for even i when the buffer is sorted
+    // descending), so finishing the network needs only the merges of size
+    // 64 and up.
+    auto sort_run = [&](uint64_t& x, int i, bool desc) {
+      uint64_t one[1] = {x};
+      bitonic_sort<1>(one, ((i & 1) == 0) == desc);
+      x = one[0];
+    };
+    // A full (or final, zero-padded) unsorted buffer: sort it and fold it
+    // into `top` (the first buffer becomes `top`, later ones are merged).
+    auto fold_buffer = [&](uint64_t(&nk)[KPL]) {
+      if (have_top) {
+        bitonic_sort<KPL>(nk, false);
+        merge_top<KPL>(top, nk);
+      } else {
+        bitonic_sort<KPL>(nk, true);
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) top[i] = nk[i];
+        have_top = true;
+      }
+    };
+    // The same for a buffer already held as sorted runs: finish its network.
+    auto finish_buffer = [&]() {
+      if (have_top) {
+        bitonic_finish<KPL>(run, false);
+        merge_top<KPL>(top, run);
+      } else {
+        bitonic_finish<KPL>(run, true);
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) top[i] = run[i];
+        have_top = true;
+      }
+    };
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
       const int st = c % kStages;
@@ -201,41 +247,62 @@ __global__ void __launch_bounds__((CW + 1) * 32)
         mybuf[cnt + q] = (static_cast<uint64_t>(float_key(x)) << 32) | (~b);
       }
       cnt += nv;
-      if (cnt == KP) {
+      if constexpr (kRunsEarly) {
+        // Every 32 keys are sorted as soon as they exist, while the stream
+        // still runs, into the run their place in the buffer's bitonic
+        // network calls for; a full buffer then needs only the network's
+        // last merges.
+        if (cnt >= 32 * (nrun + 1)) {
+          __syncwarp();
+          uint64_t x = mybuf[nrun * 32 + lane];
+          __syncwarp();
+          sort_run(x, nrun, !have_top);
+#pragma unroll
+          for (int i = 0; i < KPL; ++i)
+            if (i == nrun) run[i] = x;
+          ++nrun;
+        }
+        if (nrun == KPL) {
+          finish_buffer();
+          cnt = 0;
+          nrun = 0;
+        }
+      } else if (cnt == KP) {
         __syncwarp();
         uint64_t nk[KPL];
 #pragma unroll
         for (int i = 0; i < KPL; ++i) nk[i] = mybuf[i * 32 + lane];
         __syncwarp();
-        if (have_top) {
-          bitonic_sort<KPL>(nk, false);
-          merge_top<KPL>(top, nk);
-        } else {  // the first full buffer becomes the running list directly
-          bitonic_sort<KPL>(nk, true);
-#pragma unroll
-          for (int i = 0; i < KPL; ++i) top[i] = nk[i];
-          have_top = true;
-        }
+        fold_buffer(nk);
         cnt = 0;
       }
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
     if (cnt > 0) {
-      __syncwarp();
-      uint64_t nk[KPL];
+      if constexpr (kRunsEarly) {
+        // The runs not sorted yet (zero keys pad the partial one), then the
+        // rest of the network.
+        __syncwarp();
 #pragma unroll
-      for (int i = 0; i < KPL; ++i) {
-        const int e = i * 32 + lane;
-        nk[i] = e < cnt ? mybuf[e] : 0ull;
-      }
-      __syncwarp();
-      if (have_top) {
-        bitonic_sort<KPL>(nk, false);
-        merge_top<KPL>(top, nk);
+        for (int i = 0; i < KPL; ++i) {
+          if (i >= nrun) {
+            const int e = i * 32 + lane;
+            run[i] = e < cnt ? mybuf[e] : 0ull;
+            sort_run(run[i], i, !have_top);
+          }
+        }
+        __syncwarp();
+        finish_buffer();
       } else {
-        bitonic_sort<KPL>(nk, true);
+        __syncwarp();
+        uint64_t nk[KPL];
 #pragma unroll
-        for (int i = 0; i < KPL; ++i) top[i] = nk[i];
+        for (int i = 0; i < KPL; ++i) {
+          const int e = i * 32 + lane;
+          nk[i] = e < cnt ? mybuf[e] : 0ull;
+        }
+        __syncwarp();
+        fold_buffer(nk);
       }
     }
   }

@@ -50,6 +50,18 @@ __device__ __forceinline__ void bitonic_sort(uint64_t (&x)[KPL], bool desc) {
   }
 }
 
+// The stages of bitonic_sort of size 64 and up: x holds KPL runs of 32 keys,
+// run i already sorted descending iff ((i & 1) == 0) == desc.
+template <int KPL>
+__device__ __forceinline__ void bitonic_finish(uint64_t (&x)[KPL], bool desc) {
+  constexpr int E = 32 * KPL;
+#pragma unroll
+  for (int size = 64; size <= E; size <<= 1) {
+#pragma unroll
+    for (int j = size >> 1; j > 0; j >>= 1) bitonic_stage<KPL>(x, size, j, desc);
+  }
+}
+
 // a (descending) <- the top E keys of a and b, descending; b must be ascending.
 template <int KPL>
 __device__ __forceinline__ void merge_top(uint64_t (&a)[KPL], const uint64_t (&b)[KPL]) {
