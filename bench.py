@@ -496,9 +496,9 @@ def run_oasis(args, ws, rank, local):
     # the gather's 50 MB of HBM writes are still in L2 when it ends, so its
     # DRAM count is small.
     if shape.name == "qwen3_8b_16k":
-        measured = {"attention": (1076977920 + 1741056 + 1077071104 + 2078720) // 2,
-                    "score_topk": (539654912 + 4669696 + 539656448 + 1666816) // 2,
-                    "prefetch": (394240 + 3492096 + 397568 + 3322112) // 2}
+        measured = {"attention": (1076981248 + 1761280 + 1076978688 + 1692672) // 2,
+                    "score_topk": (539682560 + 4603392 + 539652096 + 2043904) // 2,
+                    "prefetch": (434944 + 3588352 + 397568 + 3309312) // 2}
         for n, v in measured.items():
             if n in per_kernel:
                 per_kernel[n]["traffic"] = v
