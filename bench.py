@@ -1188,7 +1188,8 @@ def main():
                     help="request groups of the side work (0 = library default)")
     ap.add_argument("--schedule", type=int, default=3,
                     help="0 scan first, 1 concurrent, 2 the pages' three background streams, "
-                         "3 auto (scan first on device buffers, concurrent on host buffers)")
+                         "3 auto (scan first on device buffers, concurrent on host buffers), "
+                         "4 early scan (the scan of step t beside the attention of step t-1)")
     ap.add_argument("--drafts", action="store_true",
                     help="step rate and attention time with 1, 2 and 3 draft queries per step")
     ap.add_argument("--remote", action="store_true",
