@@ -75,6 +75,7 @@ def test_fused_steps_back_to_back(dev, schedule, groups):
     outds = [torch.empty((D, sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
              for _ in range(6)]
     qg, qdg = L.q.to(dev), L.qd.to(dev)
+    torch.cuda.synchronize()  # the early-scan schedule reads q_draft when the call is made
     for t in range(6):
         eng.oasis_step(0, t, qg[t], qdg[t], outs[t], outds[t])
     eng.oasis_join(0)

@@ -96,6 +96,7 @@ def test_growth_steps_back_to_back(dev, schedule):
     qg, qdg = L.q.to(dev), L.qd.to(dev)
     toks = [workload.new_tokens(sh, 12, 0, t) for t in range(steps)]
     toks_d = [(k.to(dev), v.to(dev)) for k, v in toks]
+    torch.cuda.synchronize()  # the early-scan schedule reads q_draft when the call is made
     for t in range(steps):
         eng.oasis_step(0, t, qg[t], qdg[t], outs[2 * t], outs[2 * t + 1])
         eng.oasis_append_token(0, t, *toks_d[t])

@@ -58,6 +58,7 @@ def test_three_layers_interleaved(dev, schedule):
     outds = [torch.empty_like(o) for o in outs]
     qg = [q.to(dev) for q in qs]
     qdg = [q.to(dev) for q in qds]
+    torch.cuda.synchronize()  # the early-scan schedule reads q_draft when the call is made
     for t in range(steps):
         for l in range(nl):      # no host sync between layers
             eng.oasis_step(l, t, qg[l][t], qdg[l][t], outs[l], outds[l])

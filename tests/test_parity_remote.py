@@ -46,7 +46,9 @@ def test_remote_fused_steps_match_oracle(dev, groups, schedule):
     out = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
     outd = torch.empty_like(out)
     for t in range(6):
-        eng.oasis_step(0, t, L.q[t].to(dev), L.qd[t].to(dev), out, outd)
+        qg, qdg = L.q[t].to(dev), L.qd[t].to(dev)
+        torch.cuda.synchronize()  # the early-scan schedule reads q_draft when the call is made
+        eng.oasis_step(0, t, qg, qdg, out, outd)
         eng.oasis_join(0)
         eng.oasis_sync()
         ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)

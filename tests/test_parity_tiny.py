@@ -85,6 +85,7 @@ def test_fused_step_matches_oracle(dev, groups, R, schedule):
     outd = torch.empty_like(out)
     for t in range(6):
         qg, qdg = L.q[t].to(dev), L.qd[t].to(dev)
+        torch.cuda.synchronize()  # the early-scan schedule reads q_draft when the call is made
         eng.oasis_step(0, t, qg, qdg, out, outd)
         eng.oasis_join(0)
         eng.oasis_sync()
@@ -179,6 +180,7 @@ def test_back_to_back_steps_without_host_sync(dev, ratio, groups, schedule):
     eng, sh = L.eng, L.shape
     outs = [torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev) for _ in range(16)]
     qg, qdg = L.q.to(dev), L.qd.to(dev)
+    torch.cuda.synchronize()  # the early-scan schedule reads q_draft when the call is made
     for t in range(8):
         eng.oasis_step(0, t, qg[t], qdg[t], outs[2 * t], outs[2 * t + 1])
     eng.oasis_join(0)
