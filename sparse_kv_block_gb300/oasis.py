@@ -148,7 +148,9 @@ def make_config(R, NBmax, Hq, Hkv, K, fetch_ratio, layers=1, softmax_scale=0.0,
                 out_fp32=False, device=0, d=128, B=16, side_groups=0,
                 schedule=SCHEDULE_AUTO, num_drafts=1) -> oasis_config:
     """``num_drafts`` D: draft queries per step; q_draft / out_draft then hold
-    D planes ``[D][R][Hq][d]`` (a ``[R][Hq][d]`` tensor is the one-draft case)."""
+    D planes ``[D][R][Hq][d]`` (a ``[R][Hq][d]`` tensor is the one-draft case).
+    ``schedule``: one of SCHEDULE_*; with SCHEDULE_EARLY_SCAN the device-buffer
+    oasis_step reads q_draft when it is called, so it must be complete then."""
     return oasis_config(layers, R, NBmax, Hq, Hkv, d, B, K, fetch_ratio, softmax_scale,
                         1 if out_fp32 else 0, device, side_groups, schedule, num_drafts)
 
