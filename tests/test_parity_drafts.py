@@ -183,3 +183,62 @@ def test_full_size_layer_three_drafts_sampled(dev):
         assert len(live) >= len(sample) - 1
         H.check_pool(L, (t + 1) & 1, live)
     eng.close()
+
+
+def test_drafts_with_remote_tier(dev):
+    # Three drafts with the emulated remote tier: the admitted blocks that the
+    # drafts' summed bounds select are fetched into the local tier first.
+    D = 3
+    sh = dataclasses.replace(TINY, R=4)
+    L = H.make_layer(sh, seed=27, steps=5, fetch_ratio=0.25, out_fp32=True, side_groups=2,
+                     remote_capacity=48, num_drafts=D)
+    eng = L.eng
+    out = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
+    outd = torch.empty((D, sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
+    for t in range(5):
+        eng.oasis_step(0, t, L.q[t].to(dev), L.qd[t].to(dev), out, outd)
+        eng.oasis_join(0)
+        eng.oasis_sync()
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        check_lists(eng, t, ref, sh.C)
+        H.check_attention([out.cpu().numpy(), outd.cpu().numpy()], ref, sh.G)
+        H.check_remote(L, ref)
+        H.check_pool(L, (t + 1) & 1)
+    eng.close()
+
+
+@pytest.mark.parametrize("schedule", [0, 4])
+def test_drafts_with_growing_contexts(dev, schedule):
+    # Two drafts while every request grows by one token per step (appends and
+    # context advances issued back to back with the steps, no host wait).
+    D, steps = 2, 20
+    sh = dataclasses.replace(TINY, R=3, ctx=990, grow_steps=steps)
+    L = H.make_layer(sh, seed=28, lens=[990, 1000, 47], steps=steps, out_fp32=True,
+                     schedule=schedule, num_drafts=D)
+    eng = L.eng
+    hb_orc, summ_orc, lens = L.hb.copy(), L.summ.copy(), L.lens.copy()
+    orc = oracle.LayerOracle(hb_orc, summ_orc, lens, L.res0, sh.K, sh.C, L.orc.pairs)
+    outs = [torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev) for _ in range(steps)]
+    outds = [torch.empty((D, sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
+             for _ in range(steps)]
+    qg, qdg = L.q.to(dev), L.qd.to(dev)
+    toks = [workload.new_tokens(sh, 28, 0, t) for t in range(steps)]
+    toks_d = [(k.to(dev), v.to(dev)) for k, v in toks]
+    torch.cuda.synchronize()  # the early-scan schedule reads q_draft when the call is made
+    for t in range(steps):
+        eng.oasis_step(0, t, qg[t], qdg[t], outs[t], outds[t])
+        eng.oasis_append_token(0, t, *toks_d[t])
+        eng.oasis_advance_context(t, 1)
+    eng.oasis_join(0)
+    eng.oasis_sync()
+    for t in range(steps):
+        ref = orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        kb, vb = workload.bf16_bits(toks[t][0]), workload.bf16_bits(toks[t][1])
+        for r in range(sh.R):
+            oracle.append_token(hb_orc, summ_orc, lens, kb[r], vb[r], r)
+        lens += 1
+        H.check_attention([outs[t].cpu().numpy(), outds[t].cpu().numpy()], ref, sh.G)
+    assert (eng.res_ids[0][steps & 1].cpu().numpy() == orc.res).all()
+    assert (eng.stamps[0].cpu().numpy() == orc.stamp).all()
+    np.testing.assert_array_equal(L.hb, hb_orc)
+    eng.close()
