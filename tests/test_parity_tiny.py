@@ -125,6 +125,26 @@ def test_host_buffer_step_matches_device_step(dev):
     eng.close()
 
 
+def test_host_buffer_step_pageable_outputs(dev):
+    # Outputs in pageable host memory cannot be written through a device
+    # mapping: the step falls back to the workspace and a copy back.
+    L = H.make_layer(TINY, seed=10, steps=2, out_fp32=True)
+    sh, eng = L.shape, L.eng
+    for t in range(2):
+        qh = L.q[t].clone().pin_memory()
+        qdh = L.qd[t].clone().pin_memory()
+        oh = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32)      # pageable
+        odh = torch.empty_like(oh)
+        assert not oh.is_pinned()
+        eng.oasis_step_host(0, t, qh, qdh, oh, odh)
+        torch.cuda.synchronize()
+        eng.oasis_join(0)
+        eng.oasis_sync()
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        H.check_attention([oh.numpy(), odh.numpy()], ref, sh.G)
+    eng.close()
+
+
 @pytest.mark.parametrize("schedule", [0, 3, 4])
 def test_host_buffer_steps_back_to_back(dev, schedule):
     # oasis_step_host issued for consecutive steps with no host wait between
