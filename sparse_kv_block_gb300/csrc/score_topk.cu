@@ -22,14 +22,15 @@
 // blocks per consumer warp, 2 KiB) with 1-D bulk copies; CW consumer warps
 // each score 4 blocks per stage (one 16-byte load per lane per block, packed
 // fp32x2 multiply-adds, transposed shuffle reduction), keep a running top-KP
-// list in registers (bitonic sort of each filled buffer of KP keys, then a
-// bitonic merge), and finally merge their lists in a tree.  Shared memory is
-// sized from the actual NBmax (the fused admission reuses the ring).  Two
-// variants: CW = 8 (16 KiB stages, ~41 KB, 4 CTAs per SM) and CW = 4 (8 KiB
-// stages, ~21 KB and 48 registers per thread, 8 CTAs per SM); the launcher
-// picks one by wave quantisation (see scan_warps).  Alone on the 128 x 16K
-// layer CW = 4 is faster (92 vs 98 us) but inside the step, beside the
-// host-link gather, CW = 8 is (120 vs 129 us).
+// list in registers (each filled buffer of KP keys bitonic-sorted, then
+// merged in; with CW = 8 every 32-key run of a buffer is sorted as soon as
+// it exists, while the stream runs), and finally merge their lists in a
+// tree.  Shared memory is sized from the actual NBmax (the fused admission
+// reuses the ring).  Two variants: CW = 8 (16 KiB stages, ~41 KB, 4 CTAs per
+// SM) and CW = 4 (8 KiB stages, ~21 KB and 48 registers per thread, 8 CTAs
+// per SM); the launcher picks one by wave quantisation (see scan_warps).
+// Alone on the 128 x 16K layer CW = 4 is faster (92.5 vs 95 us) but inside
+// the step, beside the host-link gather, CW = 8 is (118-120 vs 129 us).
 // Keys are 64-bit: order-preserving score bits above the complemented block
 // id, so ties break to the lower id and all keys are distinct.
 #include <cstdlib>
