@@ -1,6 +1,6 @@
 """Failure detection without a GPU fault: a host-side bounded wait that runs
-out (the side work is held up by a slow emulated network transfer, a host
-callback, not by a GPU spin) and then succeeds; argument and state errors
+out (the side work is held up by a slow emulated network transfer on the
+remote tier's host worker thread, not by a GPU spin) and then succeeds; argument and state errors
 reported as status codes with messages."""
 import dataclasses
 import time
@@ -25,7 +25,7 @@ def dev():
 
 def test_bounded_wait_times_out_then_completes(dev):
     # 0.001 GB/s: the step's first transfer of up to 2 x 2 x 4 units (64 KiB)
-    # is held ~65 ms in its host callback.
+    # takes the remote tier's worker thread ~65 ms; the gather waits for it.
     L = H.make_layer(TINY, seed=61, steps=2, fetch_ratio=0.25, remote_capacity=TINY.NBmax,
                      remote_gbps=0.001)
     eng = L.eng
