@@ -63,8 +63,8 @@ def test_remote_fused_steps_match_oracle(dev, groups, schedule):
 
 
 def test_remote_back_to_back_steps(dev):
-    # Host callbacks between the slot assignment and the gather of every step,
-    # steps issued without host synchronisation.
+    # The worker thread's transfer between the slot assignment and the
+    # gather of every step, steps issued without host synchronisation.
     sh = dataclasses.replace(TINY, R=5)
     L = H.make_layer(sh, seed=13, steps=8, fetch_ratio=0.25, out_fp32=True,
                      remote_capacity=sh.NBmax)
