@@ -435,31 +435,50 @@ def run_oasis(args, ws, rank, local):
     oh, odh = [pinned(), pinned()], [pinned(), pinned()]
     done = [torch.cuda.Event(), torch.cuda.Event()]
     e2e_steps = args.steps
-    checksum = 0.0
-    barrier(ws)
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(main)
-    for i in range(e2e_steps):
-        b = i & 1
-        if i >= 2:
-            done[b].synchronize()                   # step i - 2 finished: read its result
-            checksum += float(oh[b][0, 0, 0])
-        eng.oasis_step_host(0, step, qh[i % n_in], qdh[i % n_in], oh[b], odh[b], main)
-        done[b].record(main)
-        step += 1
-    for i in range(max(e2e_steps - 2, 0), e2e_steps):
-        done[i & 1].synchronize()
-        checksum += float(oh[i & 1][0, 0, 0])
-    eng.oasis_join(0, main)
-    f1.record(main)
-    torch.cuda.synchronize(dev)
-    e2e_wall = time.perf_counter() - t0
-    barrier(ws)
-    e2e_s = max_over_ranks(e2e_wall, ws)
+
+    def e2e_pass(async_outputs: bool) -> float:
+        """Wall seconds for e2e_steps host-buffer steps.  async_outputs: the
+        outputs come back on the library's output stream
+        (oasis_step_host_async + oasis_wait_outputs); else on `main`
+        (oasis_step_host + an event per step)."""
+        nonlocal step
+        checksum = 0.0
+        barrier(ws)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        first = step
+        for i in range(e2e_steps):
+            b = i & 1
+            if i >= 2:                              # step i - 2 finished: read its result
+                if async_outputs:
+                    if not eng.oasis_wait_outputs(0, step - 2, 60000.0):
+                        raise RuntimeError("outputs not back within 60 s")
+                else:
+                    done[b].synchronize()
+                checksum += float(oh[b][0, 0, 0])
+            if async_outputs:
+                eng.oasis_step_host_async(0, step, qh[i % n_in], qdh[i % n_in], oh[b], odh[b],
+                                          main)
+            else:
+                eng.oasis_step_host(0, step, qh[i % n_in], qdh[i % n_in], oh[b], odh[b], main)
+                done[b].record(main)
+            step += 1
+        for j in range(max(e2e_steps - 2, 0), e2e_steps):
+            if async_outputs:
+                eng.oasis_wait_outputs(0, first + j, 60000.0)
+            else:
+                done[j & 1].synchronize()
+            checksum += float(oh[j & 1][0, 0, 0])
+        eng.oasis_join(0, main)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        barrier(ws)
+        return wall
+
+    e2e_sync_s = max_over_ranks(e2e_pass(False), ws)
+    e2e_s = max_over_ranks(e2e_pass(True), ws)
     e2e_value = ws * e2e_steps / e2e_s
+    e2e_sync_value = ws * e2e_steps / e2e_sync_s
     eng.oasis_sync()
 
     # ---------------- roofline of the dominant kernel
@@ -525,10 +544,13 @@ def run_oasis(args, ws, rank, local):
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": 2 * R * Hq * 128 * 2,
                     "d2h_bytes_per_step": 2 * R * Hq * 128 * 2,
-                    "note": "oasis_step_host: each step copies its q/q_draft from pinned "
-                            "host memory (a ring of 8 steps' inputs) and its attention "
-                            "outputs back; the host reads every result once its step ends, "
-                            "two steps in flight"},
+                    "note": "oasis_step_host_async: each step copies its q/q_draft from "
+                            "pinned host memory (a ring of 8 steps' inputs) and its "
+                            "attention outputs back; the host reads every result once "
+                            "oasis_wait_outputs says it is back, two steps in flight",
+                    "stream_ordered_value": round(e2e_sync_value, 2),
+                    "stream_ordered_note": "the same loop through oasis_step_host (outputs "
+                                           "copied back on the step's stream)"},
             "gpu_launches": int(sum(counts)), "clocks": clk,
             "profiled_pass_ms_per_step": round(ms_prof / args.steps, 5)}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -129,10 +129,11 @@ typedef struct {
  * stream each for ranking, selection and transfer): a stand-alone scan + top-K, a
  * stand-alone admission and the gathers on three streams, the attention
  * starting at once.  AUTO: SCAN_FIRST for oasis_step (device buffers) and
- * CONCURRENT for oasis_step_host, whose output copy back to the host then
- * overlaps the next step's scan (measured on GB300: device path 3090
- * scan-first against 3053 concurrent layer-steps/s; host path 2814 against
- * 2912).  Results are identical. */
+ * oasis_step_host_async, CONCURRENT for oasis_step_host, whose output copy
+ * back to the host on `stream` then overlaps the next step's scan (measured
+ * on GB300: device path 3090 scan-first against 3053 concurrent
+ * layer-steps/s; host path 2814 against 2912; asynchronous host path 3072
+ * against 2910).  Results are identical. */
 #define OASIS_SCHEDULE_SCAN_FIRST 0
 #define OASIS_SCHEDULE_CONCURRENT 1
 #define OASIS_SCHEDULE_THREE_STREAMS 2
@@ -355,6 +356,27 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step,
                               const void* q_host, const void* q_draft_host,
                               void* out_host, void* out_draft_host,
                               void* stream);
+
+/* oasis_step_host whose outputs go back on the context's own output stream
+ * instead of `stream`: the copies of step t then overlap the following
+ * steps.  The inputs are read as in oasis_step_host; out/out_draft are
+ * complete once oasis_wait_outputs(layer, t) returns OASIS_OK (or the device
+ * is synchronised), and must stay valid until then.  Outputs are
+ * double-buffered by step parity: the attention of step t + 2 waits for the
+ * copies of step t.  Nothing of the pages corresponds to this call; it is the
+ * asynchronous form of the host-buffer step. */
+OASIS_API int oasis_step_host_async(oasis_ctx* ctx, int layer, int step,
+                                    const void* q_host, const void* q_draft_host,
+                                    void* out_host, void* out_draft_host,
+                                    void* stream);
+
+/* Bounded host wait for the outputs of the host-buffer step `step` of
+ * `layer` (oasis_step_host_async, or oasis_step_host) to be in host memory:
+ * OASIS_OK, OASIS_ETIMEOUT after timeout_ms (>= 0), OASIS_ESTATE if the
+ * layer's latest host steps do not include `step` (only the last two are
+ * tracked, by parity). */
+OASIS_API int oasis_wait_outputs(oasis_ctx* ctx, int layer, int step,
+                                 double timeout_ms);
 
 /* Pointers to the workspace lists that oasis_step(layer, step) writes
  * (topk_ids, topk_scores, admit_ids, admit_slots, evict_ids, n_admit; any

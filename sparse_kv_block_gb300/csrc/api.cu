@@ -298,8 +298,15 @@ struct LayerState {
   cudaEvent_t ev_in[2] = {nullptr, nullptr};          // inputs of the slot copied
   cudaEvent_t ev_stage_free[2] = {nullptr, nullptr};  // last reader of the slot done
   bool stage_used[2] = {false, false};
-  void* out_stage = nullptr;
-  void* outd_stage = nullptr;
+  // Attention outputs of host-buffer steps, by step parity; with
+  // oasis_step_host_async they are copied back on the context's output
+  // stream, so a slot is reused only after its copy (step - 2) is done.
+  void* out_stage[2] = {nullptr, nullptr};
+  void* outd_stage[2] = {nullptr, nullptr};
+  cudaEvent_t ev_attn_done = nullptr;                // the latest host step's attention
+  cudaEvent_t ev_out_done[2] = {nullptr, nullptr};   // a slot's outputs are in host memory
+  bool out_pending[2] = {false, false};
+  int out_step[2] = {-1, -1};
   void* qd_ring[2] = {nullptr, nullptr};  // staged draft queries, by step parity
   cudaEvent_t ev_start = nullptr;
   cudaEvent_t ev_side_done = nullptr;
@@ -331,6 +338,7 @@ struct WsLayout {
   size_t err, per_layer;
   size_t topk_ids, topk_scores, admit_ids, admit_slots, evict_ids, n_admit;
   size_t q_stage, qd_stage, q_stage1, qd_stage1, out_stage, outd_stage, qd_ring0, qd_ring1;
+  size_t out_stage1, outd_stage1;
   size_t total;
 };
 
@@ -363,6 +371,8 @@ WsLayout ws_layout(const oasis_config& c) {
   w.qd_stage1 = o;   o += align_up(D * qbytes);
   w.out_stage = o;   o += align_up(obytes);
   w.outd_stage = o;  o += align_up(D * obytes);
+  w.out_stage1 = o;  o += align_up(obytes);
+  w.outd_stage1 = o; o += align_up(D * obytes);
   w.qd_ring0 = o;    o += align_up(D * qbytes);
   w.qd_ring1 = o;    o += align_up(D * qbytes);
   w.per_layer = o - kAlign;
@@ -434,6 +444,7 @@ struct oasis_ctx {
   cudaEvent_t ev_ctx_mut = nullptr;  // the library's last write of ctx_len
   bool ctx_mut_pending = false;
   cudaStream_t io = nullptr;     // oasis_step_host input copies
+  cudaStream_t io_out = nullptr; // oasis_step_host_async output copies
   std::string last_error;
   bool prof = false;
   std::vector<ProfPair> prof_pool;
@@ -787,6 +798,7 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
       cudaStreamCreateWithPriority(&c->side2, cudaStreamNonBlocking, hi) != cudaSuccess ||
       cudaStreamCreateWithPriority(&c->side3, cudaStreamNonBlocking, hi) != cudaSuccess ||
       cudaStreamCreateWithPriority(&c->io, cudaStreamNonBlocking, hi) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&c->io_out, cudaStreamNonBlocking, hi) != cudaSuccess ||
       cudaEventCreateWithFlags(&c->ev_ctx_mut, cudaEventDisableTiming) != cudaSuccess)
     return bail(OASIS_ENOMEM);
   {
@@ -863,15 +875,20 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
         return bail(OASIS_ENOMEM);
     S.qd_ring[0] = w + (c->wl.qd_ring0 - b0);
     S.qd_ring[1] = w + (c->wl.qd_ring1 - b0);
-    S.out_stage = w + (c->wl.out_stage - b0);
-    S.outd_stage = w + (c->wl.outd_stage - b0);
+    S.out_stage[0] = w + (c->wl.out_stage - b0);
+    S.outd_stage[0] = w + (c->wl.outd_stage - b0);
+    S.out_stage[1] = w + (c->wl.out_stage1 - b0);
+    S.outd_stage[1] = w + (c->wl.outd_stage1 - b0);
     if (cudaEventCreateWithFlags(&S.ev_start, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_side_done, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_scan_done, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_qd_copied, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_admitted[0], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_admitted[1], cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&S.ev_mut, cudaEventDisableTiming) != cudaSuccess)
+        cudaEventCreateWithFlags(&S.ev_mut, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_attn_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_out_done[0], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_out_done[1], cudaEventDisableTiming) != cudaSuccess)
       return bail(OASIS_ENOMEM);
     S.ev_group.assign(c->groups, nullptr);
     S.ev_group2.assign(c->groups, nullptr);
@@ -896,6 +913,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side2) cudaStreamSynchronize(ctx->side2);
   if (ctx->side3) cudaStreamSynchronize(ctx->side3);
   if (ctx->io) cudaStreamSynchronize(ctx->io);
+  if (ctx->io_out) cudaStreamSynchronize(ctx->io_out);
   // A remote tier's transfers may sit on a caller's stream.
   for (auto& L : ctx->layers)
     if (L.remote) {
@@ -912,7 +930,9 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
     if (L.ev_scan_done) cudaEventDestroy(L.ev_scan_done);
     if (L.ev_qd_copied) cudaEventDestroy(L.ev_qd_copied);
     if (L.ev_mut) cudaEventDestroy(L.ev_mut);
+    if (L.ev_attn_done) cudaEventDestroy(L.ev_attn_done);
     for (int k = 0; k < 2; ++k) {
+      if (L.ev_out_done[k]) cudaEventDestroy(L.ev_out_done[k]);
       if (L.ev_admitted[k]) cudaEventDestroy(L.ev_admitted[k]);
       if (L.ev_in[k]) cudaEventDestroy(L.ev_in[k]);
       if (L.ev_stage_free[k]) cudaEventDestroy(L.ev_stage_free[k]);
@@ -928,6 +948,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
   if (ctx->side3) cudaStreamDestroy(ctx->side3);
   if (ctx->ev_ctx_mut) cudaEventDestroy(ctx->ev_ctx_mut);
   if (ctx->io) cudaStreamDestroy(ctx->io);
+  if (ctx->io_out) cudaStreamDestroy(ctx->io_out);
   ctx->layers.clear();  // remote tiers: worker and copy threads joined
   delete ctx;
   return OASIS_OK;
@@ -1366,9 +1387,16 @@ OASIS_API int oasis_join(oasis_ctx* ctx, int layer, void* stream) {
                    "join");
 }
 
-OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q_host,
-                              const void* q_draft_host, void* out_host, void* out_draft_host,
-                              void* stream) {
+namespace {
+// The schedule AUTO picks for oasis_step_host_async.
+constexpr int kAsyncHostAuto = OASIS_SCHEDULE_SCAN_FIRST;
+
+// Host-buffer step.  async = false: outputs copied back on `stream`
+// (complete when `stream` passes the call); true: on the output stream,
+// complete when oasis_wait_outputs(layer, step) says so.
+int step_host_impl(oasis_ctx* ctx, int layer, int step, const void* q_host,
+                   const void* q_draft_host, void* out_host, void* out_draft_host, void* stream,
+                   bool async) {
   if (int rc = check_layer(ctx, layer)) return rc;
   if (!q_host || !q_draft_host || !out_host || !out_draft_host)
     return ctx->fail(OASIS_EINVAL, "step_host: null pointer");
@@ -1395,23 +1423,84 @@ OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q
     return rc;
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_in[slot], ctx->io), "record inputs")) return rc;
   if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_in[slot], 0), "wait inputs")) return rc;
-  // AUTO: with host buffers the attention starts at once, so the output
-  // copy back to the host overlaps the next step's scan instead of delaying
-  // it (measured end to end: 2912 against 2814 layer-steps/s scan-first).
-  const int sched = ctx->cfg.schedule == OASIS_SCHEDULE_AUTO ? OASIS_SCHEDULE_CONCURRENT
-                                                              : ctx->cfg.schedule;
-  if (int rc = step_impl(ctx, layer, step, L.q_stage[slot], L.qd_stage[slot], L.out_stage,
-                         L.outd_stage, stream, sched, L.ev_in[slot]))
+  // The output slot's previous copy back (step - 2, on the output stream)
+  // must be done before this step's attention rewrites it.
+  if (L.out_pending[slot]) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_out_done[slot], 0), "wait output slot"))
+      return rc;
+  }
+  // AUTO: with outputs copied back on `stream`, the attention starts at once,
+  // so that copy overlaps the next step's scan instead of delaying it
+  // (measured end to end: 2912 against 2814 layer-steps/s scan-first).  With
+  // the copies on the output stream the scan goes first, as for oasis_step.
+  const int sched = ctx->cfg.schedule != OASIS_SCHEDULE_AUTO ? ctx->cfg.schedule
+                    : async                                 ? kAsyncHostAuto
+                                                            : OASIS_SCHEDULE_CONCURRENT;
+  if (int rc = step_impl(ctx, layer, step, L.q_stage[slot], L.qd_stage[slot], L.out_stage[slot],
+                         L.outd_stage[slot], stream, sched, L.ev_in[slot]))
     return rc;
   if (int rc = ctx->cuda(cudaEventRecord(L.ev_stage_free[slot], s), "record stage")) return rc;
   L.stage_used[slot] = true;
   // The outputs go back with copies: the attention writing the mapped host
   // buffers itself was slower end to end (2871 against 2935 layer-steps/s).
-  if (int rc = ctx->cuda(cudaMemcpyAsync(out_host, L.out_stage, ob, cudaMemcpyDeviceToHost, s), "d2h out"))
+  cudaStream_t so = s;
+  if (async) {
+    if (int rc = ctx->cuda(cudaEventRecord(L.ev_attn_done, s), "record attention")) return rc;
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->io_out, L.ev_attn_done, 0), "out wait"))
+      return rc;
+    so = ctx->io_out;
+  }
+  if (int rc = ctx->cuda(cudaMemcpyAsync(out_host, L.out_stage[slot], ob, cudaMemcpyDeviceToHost,
+                                         so), "d2h out"))
     return rc;
-  return ctx->cuda(cudaMemcpyAsync(out_draft_host, L.outd_stage, ctx->D * ob,
-                                   cudaMemcpyDeviceToHost, s),
-                   "d2h out_draft");
+  if (int rc = ctx->cuda(cudaMemcpyAsync(out_draft_host, L.outd_stage[slot], ctx->D * ob,
+                                         cudaMemcpyDeviceToHost, so), "d2h out_draft"))
+    return rc;
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_out_done[slot], so), "record outputs")) return rc;
+  L.out_step[slot] = step;
+  // Only copies on the output stream need a wait before the slot's next use;
+  // those on `stream` are ordered before it anyway.
+  L.out_pending[slot] = async;
+  return OASIS_OK;
+}
+}  // namespace
+
+OASIS_API int oasis_step_host(oasis_ctx* ctx, int layer, int step, const void* q_host,
+                              const void* q_draft_host, void* out_host, void* out_draft_host,
+                              void* stream) {
+  return step_host_impl(ctx, layer, step, q_host, q_draft_host, out_host, out_draft_host, stream,
+                        false);
+}
+
+OASIS_API int oasis_step_host_async(oasis_ctx* ctx, int layer, int step, const void* q_host,
+                                    const void* q_draft_host, void* out_host,
+                                    void* out_draft_host, void* stream) {
+  return step_host_impl(ctx, layer, step, q_host, q_draft_host, out_host, out_draft_host, stream,
+                        true);
+}
+
+OASIS_API int oasis_wait_outputs(oasis_ctx* ctx, int layer, int step, double timeout_ms) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !(timeout_ms >= 0.0))
+    return ctx->fail(OASIS_EINVAL, "wait_outputs: bad step or timeout");
+  if (int rc = ctx->set_device()) return rc;
+  LayerState& L = ctx->layers[layer];
+  const int slot = step & 1;
+  if (L.out_step[slot] != step)
+    return ctx->fail(OASIS_ESTATE, "wait_outputs: layer %d holds no outputs of step %d", layer,
+                     step);
+  const auto t0 = std::chrono::steady_clock::now();
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(L.ev_out_done[slot]);
+    if (e == cudaSuccess) return OASIS_OK;
+    if (e != cudaErrorNotReady) return ctx->cuda(e, "wait_outputs: event query");
+    const double ms =
+        std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    if (ms >= timeout_ms)
+      return ctx->fail(OASIS_ETIMEOUT, "wait_outputs: layer %d step %d not done after %.1f ms",
+                       layer, step, timeout_ms);
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
 }
 
 OASIS_API int oasis_step_lists(oasis_ctx* ctx, int layer, int step, int32_t** topk_ids,

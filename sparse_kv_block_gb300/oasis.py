@@ -91,6 +91,8 @@ EXPORTS = {
     "oasis_wait": (c_int, [_P, c_int, c_double]),
     "oasis_join": (c_int, [_P, c_int, _P]),
     "oasis_step_host": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
+    "oasis_step_host_async": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
+    "oasis_wait_outputs": (c_int, [_P, c_int, c_int, c_double]),
     "oasis_step_lists": (c_int, [_P, c_int, c_int, POINTER(c_void_p), POINTER(c_void_p),
                                  POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
                                  POINTER(c_void_p)]),
@@ -330,6 +332,22 @@ class Oasis:
         self._sized(q_host, qd_host, out_host, outd_host)
         self._check(lib().oasis_step_host(self.ctx, layer, step, _ptr(q_host), _ptr(qd_host),
                                           _ptr(out_host), _ptr(outd_host), _stream(stream)))
+
+    def oasis_step_host_async(self, layer, step, q_host, qd_host, out_host, outd_host,
+                              stream=None) -> None:
+        self._sized(q_host, qd_host, out_host, outd_host)
+        self._check(lib().oasis_step_host_async(self.ctx, layer, step, _ptr(q_host),
+                                                _ptr(qd_host), _ptr(out_host), _ptr(outd_host),
+                                                _stream(stream)))
+
+    def oasis_wait_outputs(self, layer: int, step: int, timeout_ms: float) -> bool:
+        """True when the outputs of host-buffer step `step` are in host
+        memory, False on timeout."""
+        rc = lib().oasis_wait_outputs(self.ctx, layer, step, float(timeout_ms))
+        if rc == OASIS_ETIMEOUT:
+            return False
+        self._check(rc)
+        return True
 
     def oasis_step_lists(self, layer: int, step: int) -> dict:
         ps = [c_void_p() for _ in range(6)]

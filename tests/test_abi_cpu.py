@@ -53,8 +53,8 @@ def test_workspace_grows_with_draft_planes():
                                              fetch_ratio=0.05, num_drafts=D)).workspace_bytes
          for D in (1, 2, 3)]
     assert ob.oasis_query_sizes(base).workspace_bytes == w[0]
-    # qd_stage x2, qd_ring x2 (plane each) and outd_stage (bf16 plane) per extra draft
-    assert w[1] - w[0] == 5 * plane and w[2] - w[1] == 5 * plane
+    # qd_stage x2, qd_ring x2 and outd_stage x2 (a bf16 plane each) per extra draft
+    assert w[1] - w[0] == 6 * plane and w[2] - w[1] == 6 * plane
     zero = ob.make_config(R=128, NBmax=1024, Hq=32, Hkv=8, K=128, fetch_ratio=0.05,
                           num_drafts=0)
     assert ob.oasis_query_sizes(zero).workspace_bytes == w[0]

@@ -172,6 +172,49 @@ def test_host_buffer_steps_back_to_back(dev, schedule):
     eng.close()
 
 
+@pytest.mark.parametrize("schedule,mixed", [(3, False), (0, False), (1, False), (3, True)])
+def test_host_buffer_async_outputs(dev, schedule, mixed):
+    # oasis_step_host_async: the outputs of step t come back on the library's
+    # output stream; the host waits for them with oasis_wait_outputs, two
+    # steps later, in a two-deep ring of output buffers.  `mixed` alternates
+    # with the stream-ordered oasis_step_host (slot reuse across both).
+    sh = dataclasses.replace(TINY, R=5)
+    L = H.make_layer(sh, seed=15, steps=8, fetch_ratio=0.25, out_fp32=False, schedule=schedule)
+    eng = L.eng
+
+    def pinned():
+        return torch.empty((sh.R, sh.Hq, 128), dtype=torch.bfloat16, pin_memory=True)
+    qh, qdh = [pinned() for _ in range(8)], [pinned() for _ in range(8)]
+    for t in range(8):
+        qh[t].copy_(L.q[t])
+        qdh[t].copy_(L.qd[t])
+    oh, odh = [pinned(), pinned()], [pinned(), pinned()]
+    got = {}
+    for t in range(8):
+        b = t & 1
+        if t >= 2:
+            assert eng.oasis_wait_outputs(0, t - 2, 30000.0)
+            got[t - 2] = (oh[b].float().numpy().copy(), odh[b].float().numpy().copy())
+        if mixed and t % 2:
+            eng.oasis_step_host(0, t, qh[t], qdh[t], oh[b], odh[b])
+        else:
+            eng.oasis_step_host_async(0, t, qh[t], qdh[t], oh[b], odh[b])
+    for t in (6, 7):
+        assert eng.oasis_wait_outputs(0, t, 30000.0)
+        got[t] = (oh[t & 1].float().numpy().copy(), odh[t & 1].float().numpy().copy())
+    with pytest.raises(Exception) as ei:       # step 5's slot now holds step 7
+        eng.oasis_wait_outputs(0, 5, 1.0)
+    assert "no outputs of step 5" in str(ei.value)
+    eng.oasis_join(0)
+    eng.oasis_sync()
+    for t in range(8):
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        H.check_attention([got[t][0], got[t][1]], ref, sh.G)
+    assert (eng.res_ids[0][8 & 1].cpu().numpy() == L.orc.res).all()
+    H.check_pool(L, 8 & 1)
+    eng.close()
+
+
 def test_device_error_word_on_bad_block_id(dev):
     # An id past the context is reported through oasis_sync, not a fault:
     # the kernels skip it and set a bit in the device error word.
