@@ -366,8 +366,6 @@ __global__ void __maxnreg__(kNT == 2 ? 144 : 96)
 
 }  // namespace
 
-size_t attention_smem_bytes() { return AttnLayout<4>::kSmemBytes; }
-
 namespace {
 
 template <int W, int NT>

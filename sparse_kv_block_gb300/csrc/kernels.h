@@ -158,14 +158,12 @@ cudaError_t launch_tail_blocks(const int32_t* ctx_len, int R, int Hkv, int32_t* 
 cudaError_t launch_advance(const int32_t* cur, int32_t* nxt, int R, int grow,
                            cudaStream_t s);
 
-size_t attention_smem_bytes();
 
 // Load every kernel's code now (the runtime loads modules lazily on first
 // launch, and a lazy load waits for work already queued on the device).
 cudaError_t preload_attention_kernels();
 cudaError_t preload_score_kernels();
 cudaError_t preload_support_kernels();
-size_t score_topk_smem_bytes(int K, int NBmax);
 
 // Largest NBmax the fused score + admit kernel can hold in shared memory.
 constexpr int kMaxBlocksPerHead = 131072;

@@ -434,13 +434,6 @@ cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-size_t score_topk_smem_bytes(int K, int NBmax) {
-  if (K <= 32) return Layout<1, 8>::total(NBmax);
-  if (K <= 64) return Layout<2, 8>::total(NBmax);
-  if (K <= 128) return Layout<4, 8>::total(NBmax);
-  return Layout<8, 8>::total(NBmax);
-}
-
 cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s) {
   if (a.K <= 32) return launch_kpl<1>(a, s);
   if (a.K <= 64) return launch_kpl<2>(a, s);
