@@ -342,6 +342,21 @@ struct WsLayout {
   size_t total;
 };
 
+// The device address of page-locked host memory (cudaHostAlloc'd or
+// registered), or null.  Pageable memory is refused even where the device
+// could reach it through the system's address translation: the gathers need
+// memory that stays resident.
+void* mapped_host(const void* p) {
+  cudaPointerAttributes at{};
+  void* d = nullptr;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess || at.type != cudaMemoryTypeHost ||
+      cudaHostGetDevicePointer(&d, const_cast<void*>(p), 0) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return d;
+}
+
 int fetch_cap(const oasis_config& c) {
   return static_cast<int>(std::floor(static_cast<double>(c.fetch_ratio) * c.topk + 1e-9));
 }
@@ -830,9 +845,8 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
     S.res = bufs->res_ids[l];
     S.stamps = bufs->stamps[l];
     S.phys = bufs->phys[l];
-    void* dptr = nullptr;
-    if (cudaHostGetDevicePointer(&dptr, S.host, 0) != cudaSuccess || !dptr) {
-      cudaGetLastError();
+    void* dptr = mapped_host(S.host);
+    if (!dptr) {
       c->last_error = "host_kv is not page-locked host memory mapped for the device";
       return bail(OASIS_EINVAL);
     }
@@ -1644,17 +1658,13 @@ OASIS_API int oasis_remote_attach(oasis_ctx* ctx, int layer, const oasis_remote_
   T->gbps = rcfg->gbps;
   T->local = static_cast<uint8_t*>(local_tier);
   T->lists = miss_lists;
-  void* d = nullptr;
-  if (cudaHostGetDevicePointer(&d, local_tier, 0) != cudaSuccess || !d) {
-    cudaGetLastError();
+  void* d = mapped_host(local_tier);
+  if (!d)
     return ctx->fail(OASIS_EINVAL, "remote_attach: local_tier is not mapped page-locked memory");
-  }
   T->local_dev = d;
-  d = nullptr;
-  if (cudaHostGetDevicePointer(&d, miss_lists, 0) != cudaSuccess || !d) {
-    cudaGetLastError();
+  d = mapped_host(miss_lists);
+  if (!d)
     return ctx->fail(OASIS_EINVAL, "remote_attach: miss_lists is not mapped page-locked memory");
-  }
   T->lists_dev = static_cast<int32_t*>(d);
   const size_t pairs = static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_kv_heads;
   T->map = local_map;

@@ -62,3 +62,39 @@ def test_step_before_load_is_refused(dev):
         eng.oasis_step(0, 0, q, q, q, q)
     assert e.value.status == ob.OASIS_ESTATE
     eng.close()
+
+
+def test_init_refuses_a_host_store_that_is_not_page_locked(dev):
+    # The library itself (not only the binding) refuses a pageable host store
+    # with OASIS_EINVAL and no context; the same buffers with a pinned store
+    # give a working context.
+    import ctypes
+    sh = TINY
+    cfg = ob.make_config(sh.R, sh.NBmax, sh.Hq, sh.Hkv, sh.K, sh.fetch_ratio)
+    sz = ob.oasis_query_sizes(cfg)
+    U = sz.units_per_head
+    pool = torch.zeros((sh.R, sh.Hkv, U, 2, 16, 128), dtype=torch.bfloat16, device=dev)
+    summ = torch.zeros((sh.R, sh.Hkv, sh.NBmax, 2, 128), dtype=torch.bfloat16, device=dev)
+    res = torch.full((2, sh.R, sh.Hkv, sh.K), -1, dtype=torch.int32, device=dev)
+    stamps = torch.full((sh.R, sh.Hkv, sh.K), -1, dtype=torch.int32, device=dev)
+    phys = torch.zeros((2, sh.R, sh.Hkv, U), dtype=torch.int32, device=dev)
+    ctx_len = torch.zeros((2, sh.R), dtype=torch.int32, device=dev)
+    ws = torch.zeros(sz.workspace_bytes, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def init_with(host):
+        arrs = [(ctypes.c_void_p * 1)(t.data_ptr()) for t in (pool, summ, host, res, stamps, phys)]
+        bufs = ob.oasis_buffers(*[ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p)) for a in arrs],
+                                ctx_len.data_ptr(), ws.data_ptr())
+        h = ctypes.c_void_p()
+        rc = ob.lib().oasis_init(ctypes.byref(cfg), ctypes.byref(bufs), ctypes.byref(h))
+        return rc, h.value
+
+    pageable = torch.zeros((sh.R, sh.Hkv, sh.NBmax, 2, 16, 128), dtype=torch.bfloat16)
+    assert not pageable.is_pinned()
+    rc, h = init_with(pageable)
+    assert rc == ob.OASIS_EINVAL and h is None
+    pinned = pageable.pin_memory()
+    rc, h = init_with(pinned)
+    assert rc == ob.OASIS_OK and h is not None
+    assert ob.lib().oasis_destroy(h) == ob.OASIS_OK
