@@ -6,8 +6,9 @@
  * section "What carries the argument"; [V] = the pith.science verdict record
  * of arXiv 2608.08097, field "key_machinery"):
  *   a1  one shared paged-attention pass serves the normal query q and the
- *       speculative draft query qd of every request over the head-wise
- *       resident set of K blocks (B = 16 tokens each, GQA);
+ *       speculative draft query qd (or D of them, oasis_config.num_drafts)
+ *       of every request over the head-wise resident set of K blocks
+ *       (B = 16 tokens each, GQA);
  *   a2  the draft query scores every logical block from per-block
  *       coordinate-wise min/max key summaries held in HBM with the upper bound
  *       sum_j sum_i max(qd_ji * min_i, qd_ji * max_i) (j over the KV head's
