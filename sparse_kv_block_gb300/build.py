@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import concurrent.futures
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -19,7 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liboasis.so")
 SOURCES = ["api.cu", "attn.cu", "score_topk.cu", "admit_gather.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "kernels.h"]
+INCLUDE_DIRS = [CSRC, os.path.join(ROOT, "include")]
+_INCLUDE_RE = re.compile(r'^\s*#\s*include\s*"([^"]+)"', re.M)
 
 
 def _nvcc() -> str:
@@ -39,6 +41,28 @@ def _flags(extra=()) -> list:
     ]
 
 
+def deps(src: str) -> list:
+    """``src`` and every header it reaches through ``#include "..."``,
+    followed recursively through ``csrc/`` and ``include/`` (system headers,
+    in angle brackets, are not followed)."""
+    seen, todo = [], [src]
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.append(f)
+        base = os.path.dirname(f)
+        with open(f) as fh:
+            names = _INCLUDE_RE.findall(fh.read())
+        for name in names:
+            for d in [base] + INCLUDE_DIRS:
+                cand = os.path.normpath(os.path.join(d, name))
+                if os.path.exists(cand):
+                    todo.append(cand)
+                    break
+    return seen
+
+
 def _stale(target: str, deps: list) -> bool:
     if not os.path.exists(target):
         return True
@@ -50,13 +74,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     """Compile (only what changed unless ``force``) and return the .so path."""
     nvcc = _nvcc()
     os.makedirs(OUT_DIR, exist_ok=True)
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "oasis.h")]
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
         o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
         objs.append(o)
-        if force or _stale(o, [s] + hdrs):
+        if force or _stale(o, deps(s)):
             jobs.append([nvcc, *_flags(extra_flags), "-c", s, "-o", o])
 
     def run(cmd):
