@@ -53,6 +53,9 @@ def _load():
             "orc_admit_evict_rh": [P, P, P, I, I, I, P, P, P, P],
             "orc_step_rh": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, D,
                             I, I, P, P, P, P, P, P, P],
+            "orc_demand_rh": [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, P, P, P, P, P],
+            "orc_stall_step_rh": [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, D,
+                                  I, I, P, P, P, P, P, P, P, P, P, P, P, P, P],
             "orc_append_token": [P, P, P, P, P, I, I, I, I, I, I],
             "orc_remote_fetch_rh": [P, I, P, P, I, I, P, P, P],
         }
@@ -155,6 +158,28 @@ def admit_evict_rh(res_row, stamp_row, topk, C, step):
     return a[:C], s[:C], e[:C], int(n[0])
 
 
+def demand_rh(summ, ctx_len, res, stamp, q, r, h, K, step, B):
+    """Miss-stall demand fetch of one (r, h): rank with the normal query
+    ``q`` ([R][Hq][d]), then admit every missing block of its top-K (no cap).
+    ``res``/``stamp`` are the whole ``[R][Hkv][K]`` tables, updated in place
+    for (r, h).  Returns a dict with scores [NBmax], topk [K], admit_ids,
+    admit_slots, evict_ids [K] (-1 padded) and n_admit."""
+    R, Hkv, NBmax, _, d = summ.shape
+    Hq = q.shape[1]
+    out = dict(scores=np.empty(NBmax, dtype=np.float32), topk=np.empty(K, dtype=np.int32),
+               admit_ids=np.empty(K, dtype=np.int32), admit_slots=np.empty(K, dtype=np.int32),
+               evict_ids=np.empty(K, dtype=np.int32))
+    n = np.zeros(1, dtype=np.int32)
+    _ok(_load().orc_demand_rh(
+        _p(summ, np.uint16), _p(ctx_len, np.int32), _p(res, np.int32), _p(stamp, np.int32),
+        _p(q, np.uint16), R, Hq, Hkv, NBmax, B, d, K, step, r, h,
+        _p(out["scores"], np.float32), _p(out["topk"], np.int32),
+        _p(out["admit_ids"], np.int32), _p(out["admit_slots"], np.int32),
+        _p(out["evict_ids"], np.int32), _p(n, np.int32)), "demand_rh")
+    out["n_admit"] = int(n[0])
+    return out
+
+
 def append_token(host_kv, summ, ctx_len, k_new, v_new, r):
     """Write one token (``[Hkv][d]`` keys and values) at position ctx_len[r]
     and fold its key into the tail summary; ctx_len is not changed."""
@@ -234,35 +259,85 @@ class LayerOracle:
         self.local_count[r, h] = cnt[0]
         return dict(miss_ids=mi, miss_slots=ms, n_miss=len(mi), full=full)
 
+    def _step_outputs(self, Hq, D):
+        C1 = max(self.C, 1)
+        return dict(attn=np.empty((1 + D, Hq // self.Hkv, self.d), dtype=np.float32),
+                    scores=np.empty(self.NBmax, dtype=np.float32),
+                    topk=np.empty(self.K, dtype=np.int32),
+                    admit_ids=np.empty(C1, dtype=np.int32),
+                    admit_slots=np.empty(C1, dtype=np.int32),
+                    evict_ids=np.empty(C1, dtype=np.int32))
+
+    def _finish(self, v, n, r, h):
+        for k in ("admit_ids", "admit_slots", "evict_ids"):
+            v[k] = v[k][:self.C]
+        v["n_admit"] = int(n[0])
+        if self.remote_capacity is not None:
+            v.update(self._fetch(r, h, v["admit_ids"][:v["n_admit"]]))
+        return v
+
     def step(self, q, qd, t):
-        """Run one layer-step for every tracked pair, on the oracle's own
-        state only.  ``qd`` holds one draft ``[R][Hq][d]`` or D of them
-        ``[D][R][Hq][d]``.  Returns a dict keyed by (r, h) with attn [1+D][G][d],
-        scores, topk, admit_ids, admit_slots, evict_ids, n_admit (and, with
-        a remote tier, the slot assignment's miss lists)."""
+        """Run one layer-step (``orc_step_rh``: attention on the table as it
+        stands, then scan, top-K and capped admission) for every tracked
+        pair, on the oracle's own state only.  ``qd`` holds one draft
+        ``[R][Hq][d]`` or D of them ``[D][R][Hq][d]``.  Returns a dict keyed
+        by (r, h) with attn [1+D][G][d], scores, topk, admit_ids,
+        admit_slots, evict_ids, n_admit (and, with a remote tier, the slot
+        assignment's miss lists)."""
         L = _load()
         Hq = q.shape[1]
         D = drafts(qd)
         out = {}
         for (r, h) in self.pairs:
-            attn = np.empty((1 + D, Hq // self.Hkv, self.d), dtype=np.float32)
-            scores = np.empty(self.NBmax, dtype=np.float32)
-            _ok(L.orc_attention_rh(_p(self.host_kv, np.uint16),
-                                   _p(self.ctx_len, np.int32), _p(self.res, np.int32),
-                                   _p(q, np.uint16), _p(qd, np.uint16), D, self.R, Hq,
-                                   self.Hkv, self.NBmax, self.B, self.d, self.K,
-                                   float(self.scale), r, h, _p(attn, np.float32)),
-                "attention_rh")
-            _ok(L.orc_score_rh(_p(self.summ, np.uint16), _p(self.ctx_len, np.int32),
-                               _p(qd, np.uint16), D, self.R, Hq, self.Hkv, self.NBmax,
-                               self.d, self.B, r, h, _p(scores, np.float32)),
-                "score_rh")
-            nb = min(num_blocks(int(self.ctx_len[r]), self.B), self.NBmax)
-            topk = topk_rh(scores, nb, self.K)
-            a, s, e, n = admit_evict_rh(self.res[r, h], self.stamp[r, h], topk,
-                                        self.C, t)
-            out[(r, h)] = dict(attn=attn, scores=scores, topk=topk, admit_ids=a,
-                               admit_slots=s, evict_ids=e, n_admit=n)
-            if self.remote_capacity is not None:
-                out[(r, h)].update(self._fetch(r, h, a[:n]))
+            v = self._step_outputs(Hq, D)
+            n = np.zeros(1, dtype=np.int32)
+            _ok(L.orc_step_rh(
+                _p(self.host_kv, np.uint16), _p(self.summ, np.uint16),
+                _p(self.ctx_len, np.int32), _p(self.res, np.int32), _p(self.stamp, np.int32),
+                _p(q, np.uint16), _p(qd, np.uint16), D, self.R, Hq, self.Hkv, self.NBmax,
+                self.B, self.d, self.K, self.C, t, float(self.scale), r, h,
+                _p(v["attn"], np.float32), _p(v["scores"], np.float32),
+                _p(v["topk"], np.int32), _p(v["admit_ids"], np.int32),
+                _p(v["admit_slots"], np.int32), _p(v["evict_ids"], np.int32),
+                _p(n, np.int32)), "step_rh")
+            out[(r, h)] = self._finish(v, n, r, h)
+        return out
+
+    def stall_step(self, q, qd, t):
+        """Run one miss-stall layer-step (``orc_stall_step_rh``: the demand
+        fetch of the normal query's whole top-K, then ``step`` on the
+        resulting table) for every tracked pair.  Returns the dict of
+        ``step`` with, per pair, the demand lists under dm_scores, dm_topk,
+        dm_admit_ids, dm_admit_slots, dm_evict_ids ([K] each) and
+        dm_n_admit.  Not available with a remote tier."""
+        if self.remote_capacity is not None:
+            raise ValueError("the miss-stall step has no remote tier")
+        L = _load()
+        Hq = q.shape[1]
+        D = drafts(qd)
+        out = {}
+        for (r, h) in self.pairs:
+            v = self._step_outputs(Hq, D)
+            dm = dict(dm_scores=np.empty(self.NBmax, dtype=np.float32),
+                      dm_topk=np.empty(self.K, dtype=np.int32),
+                      dm_admit_ids=np.empty(self.K, dtype=np.int32),
+                      dm_admit_slots=np.empty(self.K, dtype=np.int32),
+                      dm_evict_ids=np.empty(self.K, dtype=np.int32))
+            dn = np.zeros(1, dtype=np.int32)
+            n = np.zeros(1, dtype=np.int32)
+            _ok(L.orc_stall_step_rh(
+                _p(self.host_kv, np.uint16), _p(self.summ, np.uint16),
+                _p(self.ctx_len, np.int32), _p(self.res, np.int32), _p(self.stamp, np.int32),
+                _p(q, np.uint16), _p(qd, np.uint16), D, self.R, Hq, self.Hkv, self.NBmax,
+                self.B, self.d, self.K, self.C, t, float(self.scale), r, h,
+                _p(dm["dm_scores"], np.float32), _p(dm["dm_topk"], np.int32),
+                _p(dm["dm_admit_ids"], np.int32), _p(dm["dm_admit_slots"], np.int32),
+                _p(dm["dm_evict_ids"], np.int32), _p(dn, np.int32),
+                _p(v["attn"], np.float32), _p(v["scores"], np.float32),
+                _p(v["topk"], np.int32), _p(v["admit_ids"], np.int32),
+                _p(v["admit_slots"], np.int32), _p(v["evict_ids"], np.int32),
+                _p(n, np.int32)), "stall_step_rh")
+            dm["dm_n_admit"] = int(dn[0])
+            v.update(dm)
+            out[(r, h)] = self._finish(v, n, r, h)
         return out

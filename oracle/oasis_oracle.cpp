@@ -264,6 +264,44 @@ extern "C" int orc_step_rh(const uint16_t* host_kv, const uint16_t* summ,
                             admit_slots, evict_ids, n_admit);
 }
 
+extern "C" int orc_demand_rh(const uint16_t* summ, const int32_t* ctx_len,
+                             int32_t* res, int32_t* stamp, const uint16_t* q,
+                             int R, int Hq, int Hkv, int NBmax, int B, int d,
+                             int K, int step, int r, int h, float* scores,
+                             int32_t* topk, int32_t* admit_ids,
+                             int32_t* admit_slots, int32_t* evict_ids,
+                             int32_t* n_admit) {
+  if (!res || !stamp || r < 0 || r >= R || h < 0 || h >= Hkv) return -1;
+  // The normal query ranks the blocks as one plane of query vectors.
+  if (orc_score_rh(summ, ctx_len, q, 1, R, Hq, Hkv, NBmax, d, B, r, h, scores))
+    return -1;
+  const int nb = std::min(blocks_of(ctx_len[r], B), NBmax);
+  if (orc_topk_rh(scores, nb, K, topk)) return -1;
+  // Every missing block of that top-K is admitted: the cap is K.
+  const size_t off = (static_cast<size_t>(r) * Hkv + h) * K;
+  return orc_admit_evict_rh(res + off, stamp + off, topk, K, K, step, admit_ids,
+                            admit_slots, evict_ids, n_admit);
+}
+
+extern "C" int orc_stall_step_rh(
+    const uint16_t* host_kv, const uint16_t* summ, const int32_t* ctx_len,
+    int32_t* res, int32_t* stamp, const uint16_t* q, const uint16_t* qd, int D,
+    int R, int Hq, int Hkv, int NBmax, int B, int d, int K, int C, int step,
+    double scale, int r, int h, float* dm_scores, int32_t* dm_topk,
+    int32_t* dm_admit_ids, int32_t* dm_admit_slots, int32_t* dm_evict_ids,
+    int32_t* dm_n_admit, float* attn_out, float* scores_scratch, int32_t* topk,
+    int32_t* admit_ids, int32_t* admit_slots, int32_t* evict_ids,
+    int32_t* n_admit) {
+  if (orc_demand_rh(summ, ctx_len, res, stamp, q, R, Hq, Hkv, NBmax, B, d, K,
+                    step, r, h, dm_scores, dm_topk, dm_admit_ids, dm_admit_slots,
+                    dm_evict_ids, dm_n_admit))
+    return -1;
+  return orc_step_rh(host_kv, summ, ctx_len, res, stamp, q, qd, D, R, Hq, Hkv,
+                     NBmax, B, d, K, C, step, scale, r, h, attn_out,
+                     scores_scratch, topk, admit_ids, admit_slots, evict_ids,
+                     n_admit);
+}
+
 extern "C" int orc_remote_fetch_rh(const int32_t* ids, int n, int32_t* local_map,
                                    int32_t* count, int capacity, int NBmax,
                                    int32_t* miss_ids, int32_t* miss_slots,

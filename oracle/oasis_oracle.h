@@ -98,6 +98,40 @@ int orc_step_rh(const uint16_t* host_kv, const uint16_t* summ,
                 int32_t* topk, int32_t* admit_ids, int32_t* admit_slots,
                 int32_t* evict_ids, int32_t* n_admit);
 
+/* Miss stall, the demand half, for one (r, h) at step t ([R] *What would
+ * settle it*: a block the look-ahead did not bring is either dropped from
+ * attention or fetched on demand, stalling the step).  The step's own normal
+ * query q ([R][Hq][d], its G vectors of the group) scores every logical
+ * block like a draft (orc_score_rh with one query plane), its top-K is taken
+ * (orc_topk_rh) and every block of that top-K that is not resident is
+ * admitted at once, without the fetch cap (orc_admit_evict_rh with C = K):
+ * an on-demand fetch that stopped at the cap would still drop context.  The
+ * least-recently-selected pairing and the stamps are those of the look-ahead
+ * admission.  Afterwards every id of the top-K is resident.
+ * scores[NBmax], topk[K]; admit_ids/admit_slots/evict_ids[K] (-1 padded). */
+int orc_demand_rh(const uint16_t* summ, const int32_t* ctx_len, int32_t* res,
+                  int32_t* stamp, const uint16_t* q, int R, int Hq, int Hkv,
+                  int NBmax, int B, int d, int K, int step, int r, int h,
+                  float* scores, int32_t* topk, int32_t* admit_ids,
+                  int32_t* admit_slots, int32_t* evict_ids, int32_t* n_admit);
+
+/* One miss-stall layer-step for one (r, h): orc_demand_rh (the demand
+ * fetch, on the critical path), then orc_step_rh on the resulting table
+ * (attention over a resident set that now holds the normal query's whole
+ * top-K, then the look-ahead scan, top-K and capped admission of the draft
+ * queries).  Outputs: the demand lists (dm_*: [K] each, scores NBmax) and
+ * those of orc_step_rh. */
+int orc_stall_step_rh(const uint16_t* host_kv, const uint16_t* summ,
+                      const int32_t* ctx_len, int32_t* res, int32_t* stamp,
+                      const uint16_t* q, const uint16_t* qd, int D, int R, int Hq,
+                      int Hkv, int NBmax, int B, int d, int K, int C, int step,
+                      double scale, int r, int h, float* dm_scores,
+                      int32_t* dm_topk, int32_t* dm_admit_ids,
+                      int32_t* dm_admit_slots, int32_t* dm_evict_ids,
+                      int32_t* dm_n_admit, float* attn_out, float* scores_scratch,
+                      int32_t* topk, int32_t* admit_ids, int32_t* admit_slots,
+                      int32_t* evict_ids, int32_t* n_admit);
+
 /* Remote-tier partial fetch for one (r, h) (emulated prefill-decode
  * disaggregation; [R] abstract: a request reaches the decode node with only
  * part of its KV and the decode node's host memory holds only part of the
