@@ -863,68 +863,84 @@ def run_kernels_alone(args, ws, rank, local):
 
 
 def run_miss_stall(args, ws, rank, local):
-    """The "stall" branch of a miss, against the look-ahead step ("drop").
+    """The "stall" outcome of a look-ahead miss against the look-ahead step
+    ("drop"), both through the C ABI on the same workload.
 
-    Stall: every step ranks blocks with the step's own normal query, admits
-    up to C missing blocks, gathers them and only then runs the attention,
-    all on one stream (the fetch sits on the critical path).  Look-ahead:
-    oasis_step, where the draft query's selection is fetched beside the
-    attention for the next step.  Both through the C ABI, same workload."""
-    from sparse_kv_block_gb300.oasis import lib
+    Stall (oasis_step_stall): each step ranks every block with its own normal
+    query, fetches every block of that top-K the look-ahead did not bring
+    (uncapped, on the critical path), attends, then runs the look-ahead side
+    work.  Drop (oasis_step): the attention reads what the look-ahead
+    brought.  Reports each mode's rate, the kernels of the stall step, and
+    the demand units per step (the top-K blocks the look-ahead missed)."""
+    from sparse_kv_block_gb300.oasis import PROFILE_KINDS, lib
     lib()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     shape = get_shape(args)
-    R, Hq, Hkv, K, C = shape.R, shape.Hq, shape.Hkv, shape.K, shape.C
+    R, Hq, Hkv, K = shape.R, shape.Hq, shape.Hkv, shape.K
     nq = min(args.queries, 16)
     results = {}
+    clocks = ClockSampler(local)
+    clocks.start()
     for mode in ("stall", "lookahead"):
         eng, lens, host = build_layer(shape, args.seed, dev, args.side_groups, args.schedule)
         q, qd = workload.queries(shape, args.seed, 0, nq, device=dev)
         warm_start(eng, shape, q[0], dev)
         out = torch.empty((R, Hq, 128), dtype=torch.bfloat16, device=dev)
         outd = torch.empty_like(out)
-        topk = torch.empty((R, Hkv, K), dtype=torch.int32, device=dev)
-        aid = torch.empty((R, Hkv, max(C, 1)), dtype=torch.int32, device=dev)
-        asl, evi = torch.empty_like(aid), torch.empty_like(aid)
-        nad = torch.empty((R, Hkv), dtype=torch.int32, device=dev)
         st = torch.cuda.Stream(dev)
+        fn = eng.oasis_step_stall if mode == "stall" else eng.oasis_step
         step = 0
 
         def one():
             nonlocal step
             t = step % nq
-            if mode == "stall":
-                # admission of step s writes table s+1, which this attention reads
-                eng.oasis_score_topk(0, step, q[t], topk, None, st)
-                eng.oasis_admit_evict(0, step, topk, aid, asl, evi, nad, st)
-                eng.oasis_prefetch(0, step, aid, asl, nad, st)
-                eng.oasis_lookahead_attn(0, step + 1, q[t], qd[t], out, outd, st)
-            else:
-                eng.oasis_step(0, step, q[t], qd[t], out, outd, st)
+            fn(0, step, q[t], qd[t], out, outd, st)
             step += 1
+
+        def timed(profiled):
+            eng.oasis_profile_enable(profiled)
+            eng.oasis_join(0, st)
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(args.steps):
+                one()
+            eng.oasis_join(0, st)
+            e1.record(st)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1) / args.steps
 
         for _ in range(args.warmup):
             one()
-        eng.oasis_join(0, st)
-        torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for _ in range(args.steps):
-            one()
-        eng.oasis_join(0, st)
-        e1.record(st)
-        torch.cuda.synchronize(dev)
+        ms = timed(False)
+        timed(True)
+        ms_sum, counts, _ = eng.oasis_profile_read(len(PROFILE_KINDS))
+        eng.oasis_profile_enable(False)
+        res = {"ms_per_step": round(ms, 4), "layer_steps_per_s": round(1e3 / ms, 1),
+               "kernel_ms_per_step": {PROFILE_KINDS[i]: round(ms_sum[i] / args.steps, 4)
+                                      for i in range(len(PROFILE_KINDS)) if counts[i]}}
+        if mode == "stall":
+            demand = []
+            for _ in range(8):
+                with torch.cuda.stream(st):
+                    one()
+                eng.oasis_join(0, st)
+                torch.cuda.synchronize(dev)
+                demand.append(int(eng.stall_lists(0, step - 1)["n_admit"].sum().item()))
+            res["demand_units_per_step"] = sum(demand) / len(demand)
+            res["demand_share_of_topk"] = round(sum(demand) / len(demand) / (R * Hkv * K), 4)
         eng.oasis_sync()
-        ms = e0.elapsed_time(e1) / args.steps
-        results[mode] = {"ms_per_step": round(ms, 4), "layer_steps_per_s": round(1e3 / ms, 1)}
+        results[mode] = res
         eng.close()
         del eng, host
         torch.cuda.empty_cache()
+    clk = clocks.stop()
     if rank == 0:
         print(json.dumps({"mode": "miss-stall vs look-ahead", "workload": workload_desc(shape),
-                          "steps": args.steps, **results}), flush=True)
+                          "steps": args.steps, "warmup": args.warmup, "clocks": clk,
+                          **results}), flush=True)
 
 
 def run_drafts(args, ws, rank, local):

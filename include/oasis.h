@@ -319,6 +319,69 @@ OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step,
                              const int32_t* admit_slots,
                              const int32_t* n_admit, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Miss stall (the other outcome of a look-ahead miss; [R] *What would settle
+ * it*: a block the look-ahead did not bring is either dropped from attention
+ * or fetched on demand, which stalls the step).  The look-ahead path above
+ * drops; these calls stall.  Reading: a miss is a block of the step's own
+ * normal query's top-K that is not resident when the step starts.  The step
+ * ranks every block with the normal query (a2 + a3 with q as the one plane
+ * of query vectors), admits every missing block of that top-K at once (a4's
+ * rule, but uncapped and in place in table (step & 1): the admitted block is
+ * written into the evicted slot's own pool unit), copies those units on the
+ * critical path, and only then attends; the look-ahead part of the step
+ * follows unchanged on the updated table.  Uncapped because a demand fetch
+ * that stopped at C would still drop context.  Not available with a remote
+ * tier (OASIS_ESTATE).  Demand lists are [R][Hkv][K] int32 (-1 padded) and
+ * n_admit [R][Hkv].
+ * ------------------------------------------------------------------------ */
+
+/* a2 + a3 for the demand fetch: oasis_score_topk with the normal query q
+ * ([R][Hq][d] bf16, one plane whatever num_drafts is) in place of the draft
+ * queries.  topk_scores is nullable. */
+OASIS_API int oasis_demand_topk(oasis_ctx* ctx, int layer, int step, const void* q,
+                                int32_t* topk_ids, float* topk_scores, void* stream);
+
+/* a4 for the demand fetch, per (r, h), in place in table (step & 1) and the
+ * stamps: steps (i)-(v) of oasis_admit_evict with n = |M| (no cap); slot
+ * E[i] takes M[i] and keeps its pool unit phys[step & 1][E[i]], which
+ * oasis_fetch_demand then overwrites.  Every block of topk_ids is resident
+ * afterwards.  topk_ids must hold distinct ids.  Lists [R][Hkv][K]. */
+OASIS_API int oasis_admit_demand(oasis_ctx* ctx, int layer, int step, const int32_t* topk_ids,
+                                 int32_t* admit_ids, int32_t* admit_slots,
+                                 int32_t* evict_ids, int32_t* n_admit, void* stream);
+
+/* a5 for the demand fetch: for every (r, h) and i < n_admit, copy host unit
+ * (r, h, admit_ids[i]) into pool unit phys[step & 1][admit_slots[i]], one
+ * warp per (r, h).  That unit belongs to table (step & 1): nothing may read
+ * the table's pool concurrently (order the call before the step's
+ * attention and after the layer's previous gathers). */
+OASIS_API int oasis_fetch_demand(oasis_ctx* ctx, int layer, int step,
+                                 const int32_t* admit_ids, const int32_t* admit_slots,
+                                 const int32_t* n_admit, void* stream);
+
+/* One miss-stall layer-step.  On `stream`: wait for this layer's previous
+ * side work; the demand ranking and uncapped admission (fused, one kernel);
+ * the demand gather; the attention (a1) of q and the draft queries over the
+ * updated table (step & 1).  On the side streams, after the demand
+ * admission: the look-ahead scan + top-K + capped admission (table
+ * (step & 1) -> ((step + 1) & 1)) and its gathers, as in oasis_step.
+ * cfg.schedule is not used (the order is fixed).  Outputs as oasis_step;
+ * the demand lists are read with oasis_stall_lists, the look-ahead lists
+ * with oasis_step_lists.  Steps of one layer may mix oasis_step and
+ * oasis_step_stall (consecutive step numbers). */
+OASIS_API int oasis_step_stall(oasis_ctx* ctx, int layer, int step, const void* q,
+                               const void* q_draft, void* out, void* out_draft,
+                               void* stream);
+
+/* Pointers to the demand lists oasis_step_stall(layer, step) writes (any
+ * output may be NULL), double-buffered by step parity like
+ * oasis_step_lists: valid until the stall step step + 2 is issued. */
+OASIS_API int oasis_stall_lists(oasis_ctx* ctx, int layer, int step, int32_t** topk_ids,
+                                float** topk_scores, int32_t** admit_ids,
+                                int32_t** admit_slots, int32_t** evict_ids,
+                                int32_t** n_admit);
+
 /* a1..a5 as one layer-step (a6; [R] *What carries the argument*: the
  * background work synchronises per layer).
  * q_draft is first copied (on `stream`) into a per-layer staging buffer.
@@ -491,14 +554,24 @@ OASIS_API int oasis_remote_stats(oasis_ctx* ctx, int layer, int64_t* units,
                                  int64_t* transfers, double* seconds,
                                  int64_t* bad_entries);
 
-/* Kernel timing: when enabled, oasis_step records CUDA events around each of
- * its kernels on the stream that launches it. */
+/* Kernel timing: when enabled, the step calls (oasis_step, oasis_step_stall)
+ * and the stage calls record CUDA events around each of their kernels on the
+ * stream that launches it. */
 OASIS_API int oasis_profile_enable(oasis_ctx* ctx, int enable);
 
-/* Sum of kernel durations (ms) and launch counts since the last read, in the
- * order attention, score_topk, admit_evict, prefetch; start_ms_sum4
- * (nullable) receives the summed start offsets of those launches from the
- * start of their oasis_step.  Synchronises. */
+/* Kinds of timed launches, in this order: attention, score_topk (fused
+ * admission included), admit_evict, prefetch, demand score_topk (with its
+ * fused admission, or a stand-alone demand admission), demand gather. */
+#define OASIS_PROFILE_KINDS 6
+
+/* Sum of kernel durations (ms) and launch counts since the last read, for
+ * the first nkinds (1..OASIS_PROFILE_KINDS) kinds; start_ms_sum (nullable)
+ * receives the summed start offsets of those launches from the start of
+ * their step.  Launches of the other kinds are discarded.  Synchronises. */
+OASIS_API int oasis_profile_read_n(oasis_ctx* ctx, int nkinds, double* ms_sum,
+                                   int64_t* count, double* start_ms_sum);
+
+/* oasis_profile_read_n with nkinds = 4. */
 OASIS_API int oasis_profile_read(oasis_ctx* ctx, double* ms_sum4,
                                  int64_t* count4, double* start_ms_sum4);
 

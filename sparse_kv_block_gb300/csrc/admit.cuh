@@ -12,7 +12,10 @@
 // ascending; (iv) at most C admissions; (v) the i-th missing block replaces
 // the i-th candidate.  The admitted block takes spare pool unit K+i and the
 // evicted unit becomes that spare, so the gather never writes a unit that
-// the current table still references.
+// the current table still references.  The miss-stall demand fetch runs the
+// same steps in place (in_place, C = K): its gather completes on the
+// critical path before any reader of the table, so the admitted block is
+// written into the evicted slot's own unit.
 //
 // Membership is tested with two NBmax-bit bitmaps in shared memory; the
 // eviction order is a bitonic sort of 64-bit keys
@@ -132,11 +135,13 @@ __device__ void admit_warp(const AdmitArgs& a, int pair, AdmitWarpSmem& S, uint3
   __syncwarp();
   for (int i = lane; i < n; i += 32) {
     const int s = S.evslot[i];
-    const int unit_old = S.phys[s];
     S.res[s] = S.missing[i];
     S.stamp[s] = a.step;
-    S.phys[s] = S.phys[K + i];
-    S.phys[K + i] = unit_old;
+    if (!a.in_place) {
+      const int unit_old = S.phys[s];
+      S.phys[s] = S.phys[K + i];
+      S.phys[K + i] = unit_old;
+    }
   }
   __syncwarp();
   for (int s = lane; s < K; s += 32) {

@@ -58,44 +58,57 @@ cudaError_t launch_admit_kpl(const AdmitArgs& a, cudaStream_t s) {
 constexpr int kGatherThreads = 128;
 constexpr int kGatherCtas = 40;
 
+// Copy item i of `pair` (one warp; skipped items and bad entries return).
+__device__ __forceinline__ void gather_item(const GatherArgs& a, int pair, int i, int lane) {
+  const long long it = static_cast<long long>(pair) * a.items + i;
+  const int id = a.src_ids[it];
+  if (id < 0) return;
+  const int slot = a.dst_slots ? a.dst_slots[it] : i;
+  const int unit = (slot >= 0 && slot < a.U) ? a.phys[static_cast<size_t>(pair) * a.U + slot] : -1;
+  if (id >= a.NBmax) {
+    if (lane == 0) raise_error(a.err, kErrBadBlock);
+    return;
+  }
+  if (unit < 0 || unit >= a.U) {
+    if (lane == 0) raise_error(a.err, kErrBadUnit);
+    return;
+  }
+  const int src_slot = a.local_map ? a.local_map[static_cast<size_t>(pair) * a.NBmax + id] : id;
+  if (src_slot < 0 || src_slot >= a.src_units) {
+    if (lane == 0 && a.phase != 2) raise_error(a.err, kErrNotLocal);
+    return;
+  }
+  if (a.phase != 0 && (a.phase == 1) == (src_slot >= a.base[pair])) return;
+  const uint4* src = static_cast<const uint4*>(a.host) +
+                     (static_cast<size_t>(pair) * a.src_units + src_slot) * (kUnitBytes / 16);
+  uint4* dst = static_cast<uint4*>(a.pool) +
+               (static_cast<size_t>(pair) * a.U + unit) * (kUnitBytes / 16);
+  uint4 v[kUnitBytes / 16 / 32];
+#pragma unroll
+  for (int j = 0; j < kUnitBytes / 16 / 32; ++j) v[j] = __ldcs(src + j * 32 + lane);
+#pragma unroll
+  for (int j = 0; j < kUnitBytes / 16 / 32; ++j) dst[j * 32 + lane] = v[j];
+}
+
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const GatherArgs a) {
   const int lane = threadIdx.x & 31;
   const long long nwarps = static_cast<long long>(gridDim.x) * (kGatherThreads / 32);
+  const long long w0 = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5);
+  if (a.pair_major) {
+    for (long long lp = w0; lp < a.pairs; lp += nwarps) {
+      const int pair = a.pair0 + static_cast<int>(lp);
+      const int n = a.n_valid ? min(a.n_valid[pair], a.items) : a.items;
+      for (int i = 0; i < n; ++i) gather_item(a, pair, i, lane);
+    }
+    return;
+  }
   const long long total = static_cast<long long>(a.pairs) * a.items;
-  for (long long lt = blockIdx.x * (kGatherThreads / 32) + (threadIdx.x >> 5); lt < total;
-       lt += nwarps) {
+  for (long long lt = w0; lt < total; lt += nwarps) {
     const int local = static_cast<int>(lt / a.items);
     const int i = static_cast<int>(lt - static_cast<long long>(local) * a.items);
     const int pair = a.pair0 + local;
-    const long long it = static_cast<long long>(pair) * a.items + i;
     if (a.n_valid && i >= a.n_valid[pair]) continue;
-    const int id = a.src_ids[it];
-    if (id < 0) continue;
-    const int slot = a.dst_slots ? a.dst_slots[it] : i;
-    const int unit = (slot >= 0 && slot < a.U) ? a.phys[static_cast<size_t>(pair) * a.U + slot] : -1;
-    if (id >= a.NBmax) {
-      if (lane == 0) raise_error(a.err, kErrBadBlock);
-      continue;
-    }
-    if (unit < 0 || unit >= a.U) {
-      if (lane == 0) raise_error(a.err, kErrBadUnit);
-      continue;
-    }
-    const int src_slot = a.local_map ? a.local_map[static_cast<size_t>(pair) * a.NBmax + id] : id;
-    if (src_slot < 0 || src_slot >= a.src_units) {
-      if (lane == 0 && a.phase != 2) raise_error(a.err, kErrNotLocal);
-      continue;
-    }
-    if (a.phase != 0 && (a.phase == 1) == (src_slot >= a.base[pair])) continue;
-    const uint4* src = static_cast<const uint4*>(a.host) +
-                       (static_cast<size_t>(pair) * a.src_units + src_slot) * (kUnitBytes / 16);
-    uint4* dst = static_cast<uint4*>(a.pool) +
-                 (static_cast<size_t>(pair) * a.U + unit) * (kUnitBytes / 16);
-    uint4 v[kUnitBytes / 16 / 32];
-#pragma unroll
-    for (int j = 0; j < kUnitBytes / 16 / 32; ++j) v[j] = __ldcs(src + j * 32 + lane);
-#pragma unroll
-    for (int j = 0; j < kUnitBytes / 16 / 32; ++j) dst[j * 32 + lane] = v[j];
+    gather_item(a, pair, i, lane);
   }
 }
 
@@ -383,6 +396,14 @@ cudaError_t launch_admit(const AdmitArgs& a, cudaStream_t s) {
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
   const long long total = static_cast<long long>(a.pairs) * a.items;
   if (total == 0) return cudaSuccess;
+  if (a.pair_major) {
+    // One warp per pair, every pair in one pass (at most kPairMajorCtas CTAs).
+    constexpr long long kPairMajorCtas = 1024;
+    long long grid = (a.pairs + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
+    if (grid > kPairMajorCtas) grid = kPairMajorCtas;
+    gather_kernel<<<static_cast<int>(grid), kGatherThreads, 0, s>>>(a);
+    return cudaGetLastError();
+  }
   const long long warps_needed = total;
   long long grid = (warps_needed + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
   static const int cap = [] {

@@ -291,6 +291,9 @@ struct LayerState {
     int32_t* evict_ids = nullptr;
     int32_t* n_admit = nullptr;
   } lists[2];
+  // Miss-stall demand lists (oasis_step_stall), by step parity; the
+  // admission lists are [R][Hkv][K] (the demand fetch is not capped).
+  Lists dm[2];
   // oasis_step_host's input staging, by step parity: the copies of step
   // t + 1 run on the context's input stream while step t computes.
   void* q_stage[2] = {nullptr, nullptr};
@@ -309,6 +312,7 @@ struct LayerState {
   int out_step[2] = {-1, -1};
   void* qd_ring[2] = {nullptr, nullptr};  // staged draft queries, by step parity
   cudaEvent_t ev_start = nullptr;
+  cudaEvent_t ev_demand_done = nullptr;  // a stall step's demand admission written
   cudaEvent_t ev_side_done = nullptr;
   cudaEvent_t ev_scan_done = nullptr;
   // Early-scan schedule: the draft queries staged on the scan stream; the
@@ -339,6 +343,7 @@ struct WsLayout {
   size_t topk_ids, topk_scores, admit_ids, admit_slots, evict_ids, n_admit;
   size_t q_stage, qd_stage, q_stage1, qd_stage1, out_stage, outd_stage, qd_ring0, qd_ring1;
   size_t out_stage1, outd_stage1;
+  size_t dm_topk_ids, dm_topk_scores, dm_admit_ids, dm_admit_slots, dm_evict_ids, dm_n_admit;
   size_t total;
 };
 
@@ -390,6 +395,13 @@ WsLayout ws_layout(const oasis_config& c) {
   w.outd_stage1 = o; o += align_up(D * obytes);
   w.qd_ring0 = o;    o += align_up(D * qbytes);
   w.qd_ring1 = o;    o += align_up(D * qbytes);
+  // miss-stall demand lists, [R][Hkv][K] each, both step parities
+  w.dm_topk_ids = o;    o += 2 * align_up(pairs * c.topk * 4);
+  w.dm_topk_scores = o; o += 2 * align_up(pairs * c.topk * 4);
+  w.dm_admit_ids = o;   o += 2 * align_up(pairs * c.topk * 4);
+  w.dm_admit_slots = o; o += 2 * align_up(pairs * c.topk * 4);
+  w.dm_evict_ids = o;   o += 2 * align_up(pairs * c.topk * 4);
+  w.dm_n_admit = o;     o += 2 * align_up(pairs * 4);
   w.per_layer = o - kAlign;
   w.total = kAlign + w.per_layer * static_cast<size_t>(c.num_layers);
   return w;
@@ -593,15 +605,25 @@ AdmitArgs admit_args(oasis_ctx* ctx, int layer, int step, const int32_t* topk, i
   return a;
 }
 
-// Scan + top-K of pairs [pair0, pair0 + pairs); with `fused` also their
-// capped eviction into the layer's workspace lists.
-int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
-              float* scores, cudaStream_t s, int pair0 = 0, int pairs = -1,
-              bool fused = false) {
-  LayerState& L = ctx->layers[layer];
+// The miss-stall demand admission: the same rule, uncapped (C = K), in place
+// in table (step & 1).
+AdmitArgs demand_admit_args(oasis_ctx* ctx, int layer, int step, const int32_t* topk,
+                            int32_t* aid, int32_t* aslot, int32_t* evid, int32_t* nadm) {
+  AdmitArgs a = admit_args(ctx, layer, step, topk, aid, aslot, evid, nadm);
+  a.res_nxt = ctx->res_tab(layer, step);
+  a.phys_nxt = ctx->phys_tab(layer, step);
+  a.C = ctx->cfg.topk;
+  a.in_place = 1;
+  return a;
+}
+
+// Scan arguments of all pairs: `x` holds `planes` planes of [R][Hq][d]
+// query vectors (the D draft queries, or the one normal query).
+ScoreArgs score_args(oasis_ctx* ctx, int layer, int step, const void* x, int planes,
+                     int32_t* ids, float* scores) {
   ScoreArgs a{};
-  a.qd = qd;
-  a.summ = L.summ;
+  a.qd = x;
+  a.summ = ctx->layers[layer].summ;
   a.ctx_len = ctx->ctx_tab(step);
   a.topk_ids = ids;
   a.topk_scores = scores;
@@ -610,11 +632,42 @@ int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
   a.Hq = ctx->cfg.num_q_heads;
   a.Hkv = ctx->cfg.num_kv_heads;
   a.G = ctx->G;
-  a.D = ctx->D;
+  a.D = planes;
   a.K = ctx->cfg.topk;
   a.NBmax = ctx->cfg.max_blocks;
+  a.pair0 = 0;
+  a.pairs = a.R * a.Hkv;
+  return a;
+}
+
+// Miss stall: scan + top-K of every pair with the step's normal query; with
+// `fused` also the uncapped in-place admission into the layer's demand
+// lists of this step's parity.
+int run_demand_score(oasis_ctx* ctx, int layer, int step, const void* q, int32_t* ids,
+                     float* scores, cudaStream_t s, bool fused) {
+  LayerState& L = ctx->layers[layer];
+  ScoreArgs a = score_args(ctx, layer, step, q, 1, ids, scores);
+  a.fuse_admit = fused ? 1 : 0;
+  if (fused) {
+    const LayerState::Lists& Dm = L.dm[step & 1];
+    a.admit = demand_admit_args(ctx, layer, step, nullptr, Dm.admit_ids, Dm.admit_slots,
+                                Dm.evict_ids, Dm.n_admit);
+  }
+  cudaEvent_t* pe = ctx->prof_begin(4, s);
+  cudaError_t e = launch_score_topk(a, s);
+  ctx->prof_end(pe, s);
+  return ctx->cuda(e, "demand score_topk launch");
+}
+
+// Scan + top-K of pairs [pair0, pair0 + pairs); with `fused` also their
+// capped eviction into the layer's workspace lists.
+int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
+              float* scores, cudaStream_t s, int pair0 = 0, int pairs = -1,
+              bool fused = false) {
+  LayerState& L = ctx->layers[layer];
+  ScoreArgs a = score_args(ctx, layer, step, qd, ctx->D, ids, scores);
   a.pair0 = pair0;
-  a.pairs = pairs < 0 ? a.R * a.Hkv : pairs;
+  if (pairs >= 0) a.pairs = pairs;
   a.fuse_admit = fused ? 1 : 0;
   if (fused)
     a.admit = admit_args(ctx, layer, step, nullptr, L.lists[step & 1].admit_ids,
@@ -740,6 +793,31 @@ int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
   const int rc = launch_gather_split(ctx, L, g, s);
   ctx->prof_end(pe, s);
   return rc;
+}
+
+// Miss stall: copy the demand-admitted units into their slots' own pool
+// units of table (step & 1), one warp per pair.
+int run_demand_gather(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
+                      const int32_t* aslot, const int32_t* nadm, cudaStream_t s) {
+  LayerState& L = ctx->layers[layer];
+  GatherArgs g{};
+  gather_source(ctx, L, g);
+  g.pool = L.pool;
+  g.src_ids = aid;
+  g.dst_slots = aslot;
+  g.n_valid = nadm;
+  g.phys = ctx->phys_tab(layer, step);
+  g.err = ctx->err;
+  g.pair0 = 0;
+  g.pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
+  g.items = ctx->cfg.topk;
+  g.NBmax = ctx->cfg.max_blocks;
+  g.U = ctx->U;
+  g.pair_major = 1;
+  cudaEvent_t* pe = ctx->prof_begin(5, s);
+  cudaError_t e = launch_gather(g, s);
+  ctx->prof_end(pe, s);
+  return ctx->cuda(e, "demand gather launch");
 }
 
 }  // namespace
@@ -877,6 +955,13 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
         Lp.admit_slots = reinterpret_cast<int32_t*>(w + (c->wl.admit_slots - b0) + p * ad);
         Lp.evict_ids = reinterpret_cast<int32_t*>(w + (c->wl.evict_ids - b0) + p * ad);
         Lp.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.n_admit - b0) + p * na);
+        auto& Dp = S.dm[p];
+        Dp.topk_ids = reinterpret_cast<int32_t*>(w + (c->wl.dm_topk_ids - b0) + p * tk);
+        Dp.topk_scores = reinterpret_cast<float*>(w + (c->wl.dm_topk_scores - b0) + p * tk);
+        Dp.admit_ids = reinterpret_cast<int32_t*>(w + (c->wl.dm_admit_ids - b0) + p * tk);
+        Dp.admit_slots = reinterpret_cast<int32_t*>(w + (c->wl.dm_admit_slots - b0) + p * tk);
+        Dp.evict_ids = reinterpret_cast<int32_t*>(w + (c->wl.dm_evict_ids - b0) + p * tk);
+        Dp.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.dm_n_admit - b0) + p * na);
       }
     }
     S.q_stage[0] = w + (c->wl.q_stage - b0);
@@ -894,6 +979,7 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
     S.out_stage[1] = w + (c->wl.out_stage1 - b0);
     S.outd_stage[1] = w + (c->wl.outd_stage1 - b0);
     if (cudaEventCreateWithFlags(&S.ev_start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&S.ev_demand_done, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_side_done, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_scan_done, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&S.ev_qd_copied, cudaEventDisableTiming) != cudaSuccess ||
@@ -940,6 +1026,7 @@ OASIS_API int oasis_destroy(oasis_ctx* ctx) {
     for (auto& e : L.ev_group2)
       if (e) cudaEventDestroy(e);
     if (L.ev_start) cudaEventDestroy(L.ev_start);
+    if (L.ev_demand_done) cudaEventDestroy(L.ev_demand_done);
     if (L.ev_side_done) cudaEventDestroy(L.ev_side_done);
     if (L.ev_scan_done) cudaEventDestroy(L.ev_scan_done);
     if (L.ev_qd_copied) cudaEventDestroy(L.ev_qd_copied);
@@ -1193,6 +1280,129 @@ OASIS_API int oasis_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t*
   if (int rc = ctx->set_device()) return rc;
   return run_prefetch(ctx, layer, step, admit_ids, admit_slots, n_admit,
                       static_cast<cudaStream_t>(stream));
+}
+
+OASIS_API int oasis_demand_topk(oasis_ctx* ctx, int layer, int step, const void* q,
+                                int32_t* topk_ids, float* topk_scores, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !q || !topk_ids)
+    return ctx->fail(OASIS_EINVAL, "demand_topk: bad step or null pointer");
+  if (int rc = ctx->set_device()) return rc;
+  return run_demand_score(ctx, layer, step, q, topk_ids, topk_scores,
+                          static_cast<cudaStream_t>(stream), false);
+}
+
+OASIS_API int oasis_admit_demand(oasis_ctx* ctx, int layer, int step, const int32_t* topk_ids,
+                                 int32_t* admit_ids, int32_t* admit_slots, int32_t* evict_ids,
+                                 int32_t* n_admit, void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || step > (1 << 30) || !topk_ids || !admit_ids || !admit_slots || !evict_ids ||
+      !n_admit)
+    return ctx->fail(OASIS_EINVAL, "admit_demand: bad step or null pointer");
+  if (ctx->layers[layer].remote)
+    return ctx->fail(OASIS_ESTATE, "admit_demand: the miss stall has no remote tier");
+  if (int rc = ctx->set_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const AdmitArgs a = demand_admit_args(ctx, layer, step, topk_ids, admit_ids, admit_slots,
+                                        evict_ids, n_admit);
+  cudaEvent_t* pe = ctx->prof_begin(4, s);
+  cudaError_t e = launch_admit(a, s);
+  ctx->prof_end(pe, s);
+  return ctx->cuda(e, "demand admission launch");
+}
+
+OASIS_API int oasis_fetch_demand(oasis_ctx* ctx, int layer, int step, const int32_t* admit_ids,
+                                 const int32_t* admit_slots, const int32_t* n_admit,
+                                 void* stream) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || !admit_ids || !admit_slots || !n_admit)
+    return ctx->fail(OASIS_EINVAL, "fetch_demand: bad step or null pointer");
+  if (ctx->layers[layer].remote)
+    return ctx->fail(OASIS_ESTATE, "fetch_demand: the miss stall has no remote tier");
+  if (int rc = ctx->set_device()) return rc;
+  return run_demand_gather(ctx, layer, step, admit_ids, admit_slots, n_admit,
+                           static_cast<cudaStream_t>(stream));
+}
+
+OASIS_API int oasis_step_stall(oasis_ctx* ctx, int layer, int step, const void* q,
+                               const void* q_draft, void* out, void* out_draft, void* stream) {
+  NvtxRange nvtx("oasis_step_stall");
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0 || step > (1 << 30) || !q || !q_draft || !out || !out_draft)
+    return ctx->fail(OASIS_EINVAL, "step_stall: bad step or null pointer");
+  LayerState& L = ctx->layers[layer];
+  if (!L.loaded) return ctx->fail(OASIS_ESTATE, "layer %d: oasis_load_resident first", layer);
+  if (L.remote) return ctx->fail(OASIS_ESTATE, "step_stall: the miss stall has no remote tier");
+  if (int rc = ctx->set_device()) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The look-ahead side work reads the draft queries from the layer's
+  // staging buffer, so the caller may reuse its buffer once `stream` passes.
+  void* qd_copy = L.qd_ring[step & 1];
+  const size_t qbytes = static_cast<size_t>(ctx->D) * ctx->cfg.num_requests *
+                        ctx->cfg.num_q_heads * kHeadDim * 2;
+  if (int rc = ctx->cuda(cudaMemcpyAsync(qd_copy, q_draft, qbytes, cudaMemcpyDeviceToDevice, s),
+                         "stage q_draft"))
+    return rc;
+  // The demand admission rewrites table (step & 1), which the layer's
+  // previous look-ahead admission wrote, and the demand gather may overwrite
+  // a unit that admission's gather filled: both wait for that side work.
+  if (L.side_pending) {
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_side_done, 0), "wait side")) return rc;
+  }
+  ctx->prof_step_start(s);
+  const LayerState::Lists& Dm = L.dm[step & 1];
+  if (int rc = run_demand_score(ctx, layer, step, q, Dm.topk_ids, Dm.topk_scores, s, true))
+    return rc;
+  // Look-ahead side work on the table the demand fetch left: the scan +
+  // top-K + capped admission per request group on `side`, each group's
+  // gather on `side2` (into spare units, which the attention does not read).
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_demand_done, s), "record demand")) return rc;
+  if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side, L.ev_demand_done, 0), "side wait"))
+    return rc;
+  if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_demand_done, 0), "side2 wait"))
+    return rc;
+  const int pairs = ctx->cfg.num_requests * ctx->cfg.num_kv_heads;
+  const LayerState::Lists& Ls = L.lists[step & 1];
+  for (int g = 0; g < ctx->groups; ++g) {
+    const int p0 = static_cast<int>(static_cast<long long>(pairs) * g / ctx->groups);
+    const int p1 = static_cast<int>(static_cast<long long>(pairs) * (g + 1) / ctx->groups);
+    if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side, p0,
+                           p1 - p0, true))
+      return rc;
+    if (int rc = ctx->cuda(cudaEventRecord(L.ev_group[g], ctx->side), "record group")) return rc;
+    if (int rc = ctx->cuda(cudaStreamWaitEvent(ctx->side2, L.ev_group[g], 0), "group wait"))
+      return rc;
+    if (ctx->C > 0) {
+      if (int rc = run_prefetch(ctx, layer, step, Ls.admit_ids, Ls.admit_slots, Ls.n_admit,
+                                ctx->side2, p0, p1 - p0))
+        return rc;
+    }
+  }
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_admitted[step & 1], ctx->side), "record admitted"))
+    return rc;
+  L.admitted_pending[step & 1] = true;
+  // The stall: the demand units land before the attention reads the table.
+  if (int rc = run_demand_gather(ctx, layer, step, Dm.admit_ids, Dm.admit_slots, Dm.n_admit, s))
+    return rc;
+  if (int rc = run_attention(ctx, layer, step, q, q_draft, out, out_draft, s)) return rc;
+  if (int rc = ctx->cuda(cudaEventRecord(L.ev_side_done, ctx->side2), "record side")) return rc;
+  L.side_pending = true;
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_stall_lists(oasis_ctx* ctx, int layer, int step, int32_t** topk_ids,
+                                float** topk_scores, int32_t** admit_ids, int32_t** admit_slots,
+                                int32_t** evict_ids, int32_t** n_admit) {
+  if (int rc = check_layer(ctx, layer)) return rc;
+  if (step < 0) return ctx->fail(OASIS_EINVAL, "stall_lists: bad step");
+  const LayerState::Lists& Dm = ctx->layers[layer].dm[step & 1];
+  if (topk_ids) *topk_ids = Dm.topk_ids;
+  if (topk_scores) *topk_scores = Dm.topk_scores;
+  if (admit_ids) *admit_ids = Dm.admit_ids;
+  if (admit_slots) *admit_slots = Dm.admit_slots;
+  if (evict_ids) *evict_ids = Dm.evict_ids;
+  if (n_admit) *n_admit = Dm.n_admit;
+  return OASIS_OK;
 }
 
 namespace {
@@ -1721,31 +1931,37 @@ OASIS_API int oasis_profile_enable(oasis_ctx* ctx, int enable) {
   return OASIS_OK;
 }
 
-OASIS_API int oasis_profile_read(oasis_ctx* ctx, double* ms_sum4, int64_t* count4,
-                                 double* start_ms_sum4) {
-  if (!ctx || !ms_sum4 || !count4) return OASIS_EINVAL;
+OASIS_API int oasis_profile_read_n(oasis_ctx* ctx, int nkinds, double* ms_sum, int64_t* count,
+                                   double* start_ms_sum) {
+  if (!ctx || !ms_sum || !count || nkinds < 1 || nkinds > OASIS_PROFILE_KINDS)
+    return OASIS_EINVAL;
   if (int rc = ctx->set_device()) return rc;
   if (int rc = ctx->cuda(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) return rc;
-  for (int k = 0; k < 4; ++k) {
-    ms_sum4[k] = 0.0;
-    count4[k] = 0;
-    if (start_ms_sum4) start_ms_sum4[k] = 0.0;
+  for (int k = 0; k < nkinds; ++k) {
+    ms_sum[k] = 0.0;
+    count[k] = 0;
+    if (start_ms_sum) start_ms_sum[k] = 0.0;
   }
   for (size_t i = 0; i < ctx->prof_used; ++i) {
     const ProfPair& p = ctx->prof_pool[i];
     float ms = 0.f;
-    if (cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
-      ms_sum4[p.kind] += ms;
-      count4[p.kind] += 1;
+    if (p.kind < nkinds && cudaEventElapsedTime(&ms, p.a, p.b) == cudaSuccess) {
+      ms_sum[p.kind] += ms;
+      count[p.kind] += 1;
       float off = 0.f;
-      if (start_ms_sum4 && p.start >= 0 &&
+      if (start_ms_sum && p.start >= 0 &&
           cudaEventElapsedTime(&off, ctx->prof_starts[p.start], p.a) == cudaSuccess)
-        start_ms_sum4[p.kind] += off;
+        start_ms_sum[p.kind] += off;
     }
   }
   ctx->prof_used = 0;
   ctx->prof_starts_used = 0;
   return OASIS_OK;
+}
+
+OASIS_API int oasis_profile_read(oasis_ctx* ctx, double* ms_sum4, int64_t* count4,
+                                 double* start_ms_sum4) {
+  return oasis_profile_read_n(ctx, 4, ms_sum4, count4, start_ms_sum4);
 }
 
 }  // extern "C"

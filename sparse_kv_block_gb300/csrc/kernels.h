@@ -41,6 +41,10 @@ struct AdmitArgs {
   int32_t* n_admit;          // [R][Hkv]
   int R, Hkv, K, C, U, NBmax, step;
   int pair0, pairs;
+  // in_place = 1 (the miss-stall demand fetch): res_nxt == res_cur and
+  // phys_nxt == phys_cur; an admitted block goes into its slot's own pool
+  // unit (no spare swap), so C may be up to K.
+  int in_place;
 };
 
 struct ScoreArgs {
@@ -77,6 +81,10 @@ struct GatherArgs {
   int phase;
   uint32_t* err;
   int pair0, pairs, items, NBmax, U, src_units;
+  // pair_major = 1: one warp per pair walks only that pair's n_valid items
+  // (lists padded far beyond their use, such as the miss-stall demand
+  // fetch); 0: one warp per (pair, item), the grid capped for the host link.
+  int pair_major;
 };
 
 // Remote tier slot assignment: item i of pair p names block

@@ -104,9 +104,21 @@ EXPORTS = {
     "oasis_remote_attach": (c_int, [_P, c_int, POINTER(oasis_remote_config), _P, _P, _P]),
     "oasis_remote_stats": (c_int, [_P, c_int, POINTER(c_int64), POINTER(c_int64),
                                    POINTER(c_double), POINTER(c_int64)]),
+    "oasis_demand_topk": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
+    "oasis_admit_demand": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P, _P]),
+    "oasis_fetch_demand": (c_int, [_P, c_int, c_int, _P, _P, _P, _P]),
+    "oasis_step_stall": (c_int, [_P, c_int, c_int, _P, _P, _P, _P, _P]),
+    "oasis_stall_lists": (c_int, [_P, c_int, c_int, POINTER(c_void_p), POINTER(c_void_p),
+                                  POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
+                                  POINTER(c_void_p)]),
     "oasis_profile_enable": (c_int, [_P, c_int]),
+    "oasis_profile_read_n": (c_int, [_P, c_int, POINTER(c_double), POINTER(c_int64),
+                                     POINTER(c_double)]),
     "oasis_profile_read": (c_int, [_P, POINTER(c_double), POINTER(c_int64), POINTER(c_double)]),
 }
+
+PROFILE_KINDS = ["attention", "score_topk", "admit_evict", "prefetch", "demand_score",
+                 "demand_gather"]
 
 _lib = None
 
@@ -316,6 +328,35 @@ class Oasis:
         self._check(lib().oasis_step(self.ctx, layer, step, _ptr(q), _ptr(qd), _ptr(out),
                                      _ptr(outd), _stream(stream)))
 
+    def oasis_demand_topk(self, layer, step, q, topk_ids, topk_scores=None, stream=None) -> None:
+        self._sized(q=q)
+        self._check(lib().oasis_demand_topk(self.ctx, layer, step, _ptr(q), _ptr(topk_ids),
+                                            _ptr(topk_scores), _stream(stream)))
+
+    def oasis_admit_demand(self, layer, step, topk_ids, admit_ids, admit_slots, evict_ids,
+                           n_admit, stream=None) -> None:
+        """Lists [R][Hkv][K] int32 and n_admit [R][Hkv] int32 (device)."""
+        self._check(lib().oasis_admit_demand(self.ctx, layer, step, _ptr(topk_ids),
+                                             _ptr(admit_ids), _ptr(admit_slots),
+                                             _ptr(evict_ids), _ptr(n_admit), _stream(stream)))
+
+    def oasis_fetch_demand(self, layer, step, admit_ids, admit_slots, n_admit,
+                           stream=None) -> None:
+        self._check(lib().oasis_fetch_demand(self.ctx, layer, step, _ptr(admit_ids),
+                                             _ptr(admit_slots), _ptr(n_admit), _stream(stream)))
+
+    def oasis_step_stall(self, layer, step, q, qd, out, outd, stream=None) -> None:
+        self._sized(q, qd, out, outd)
+        self._check(lib().oasis_step_stall(self.ctx, layer, step, _ptr(q), _ptr(qd), _ptr(out),
+                                           _ptr(outd), _stream(stream)))
+
+    def oasis_stall_lists(self, layer: int, step: int) -> dict:
+        ps = [c_void_p() for _ in range(6)]
+        self._check(lib().oasis_stall_lists(self.ctx, layer, step,
+                                            *[ctypes.byref(p) for p in ps]))
+        return dict(zip(["topk_ids", "topk_scores", "admit_ids", "admit_slots", "evict_ids",
+                         "n_admit"], [p.value for p in ps]))
+
     def oasis_wait(self, layer: int, timeout_ms: float) -> bool:
         """True when the layer's side work is done, False on timeout."""
         rc = lib().oasis_wait(self.ctx, layer, float(timeout_ms))
@@ -409,26 +450,34 @@ class Oasis:
     def oasis_profile_enable(self, enable: bool = True) -> None:
         self._check(lib().oasis_profile_enable(self.ctx, 1 if enable else 0))
 
-    def oasis_profile_read(self) -> tuple:
-        """(summed ms, launch counts, summed start offsets in ms) per kernel kind."""
-        ms = (c_double * 4)()
-        cnt = (c_int64 * 4)()
-        off = (c_double * 4)()
-        self._check(lib().oasis_profile_read(self.ctx, ms, cnt, off))
+    def oasis_profile_read(self, nkinds: int = 4) -> tuple:
+        """(summed ms, launch counts, summed start offsets in ms) per kernel
+        kind, for the first `nkinds` of PROFILE_KINDS."""
+        ms = (c_double * nkinds)()
+        cnt = (c_int64 * nkinds)()
+        off = (c_double * nkinds)()
+        self._check(lib().oasis_profile_read_n(self.ctx, nkinds, ms, cnt, off))
         return list(ms), list(cnt), list(off)
 
     # ------------------------------------------------------- tensor views
     def step_lists(self, layer: int, step: int) -> dict:
         """The workspace lists of oasis_step(layer, step) as torch tensors
         (views, no copy; valid until step + 2 is issued)."""
-        p = self.oasis_step_lists(layer, step)
-        R, Hkv, K, C = self.cfg.num_requests, self.cfg.num_kv_heads, self.cfg.topk, self.C
+        return self._list_views(self.oasis_step_lists(layer, step), max(self.C, 1))
+
+    def stall_lists(self, layer: int, step: int) -> dict:
+        """The demand lists of oasis_step_stall(layer, step) as torch tensors
+        (views, no copy; admission lists [R][Hkv][K])."""
+        return self._list_views(self.oasis_stall_lists(layer, step), self.cfg.topk)
+
+    def _list_views(self, p: dict, width: int) -> dict:
+        R, Hkv, K = self.cfg.num_requests, self.cfg.num_kv_heads, self.cfg.topk
         out = {}
         for name, shape, dt in [("topk_ids", (R, Hkv, K), torch.int32),
                                 ("topk_scores", (R, Hkv, K), torch.float32),
-                                ("admit_ids", (R, Hkv, max(C, 1)), torch.int32),
-                                ("admit_slots", (R, Hkv, max(C, 1)), torch.int32),
-                                ("evict_ids", (R, Hkv, max(C, 1)), torch.int32),
+                                ("admit_ids", (R, Hkv, width), torch.int32),
+                                ("admit_slots", (R, Hkv, width), torch.int32),
+                                ("evict_ids", (R, Hkv, width), torch.int32),
                                 ("n_admit", (R, Hkv), torch.int32)]:
             n = 1
             for s in shape:

@@ -221,3 +221,129 @@ def run_staged_step(L: Layer, t: int, dev, check_pool_every=True):
     if check_pool_every:
         check_pool(L, nxt)
     return ref
+
+
+def run_staged_stall_step(L: Layer, t: int, dev, check_pool_every=True):
+    """One miss-stall layer-step through the separate C-ABI stages: the
+    demand ranking with the normal query, the uncapped in-place demand
+    admission fed the oracle's list (lockstep) and the demand gather,
+    compared with the oracle's demand fetch (oracle.demand_rh, whose pairing
+    with LayerOracle.step is pinned equal to the oracle's stall step); then
+    the look-ahead stages of run_staged_step on the updated table."""
+    sh, eng = L.shape, L.eng
+    R, H, K = sh.R, sh.Hkv, sh.K
+    qg = L.q[t].to(dev)
+    dtk = torch.empty((R, H, K), dtype=torch.int32, device=dev)
+    dsc = torch.empty((R, H, K), dtype=torch.float32, device=dev)
+    eng.oasis_demand_topk(0, t, qg, dtk, dsc)
+    eng.oasis_sync()
+    gpu_dtk, gpu_dsc = dtk.cpu().numpy(), dsc.cpu().numpy()
+    qb = workload.bf16_bits(L.q[t])
+    dm = {(r, h): oracle.demand_rh(L.summ, L.lens, L.orc.res, L.orc.stamp, qb, r, h, K, t, 16)
+          for (r, h) in L.orc.pairs}
+    feed = gpu_dtk.copy()
+    for (r, h), v in dm.items():
+        assert topk_agrees(gpu_dtk[r, h], v["topk"], v["scores"], K), (t, r, h)
+        nv = (v["topk"] >= 0).sum()
+        np.testing.assert_allclose(gpu_dsc[r, h, :nv], v["scores"][v["topk"][:nv]],
+                                   rtol=2e-6, atol=1e-4)
+        feed[r, h] = v["topk"]
+    aid = torch.empty((R, H, K), dtype=torch.int32, device=dev)
+    asl, evi = torch.empty_like(aid), torch.empty_like(aid)
+    nad = torch.empty((R, H), dtype=torch.int32, device=dev)
+    eng.oasis_admit_demand(0, t, torch.from_numpy(feed).to(dev), aid, asl, evi, nad)
+    eng.oasis_fetch_demand(0, t, aid, asl, nad)
+    eng.oasis_sync()
+    aid, asl, evi, nad = (x.cpu().numpy() for x in (aid, asl, evi, nad))
+    cur = t & 1
+    res_c = eng.res_ids[0][cur].cpu().numpy()
+    st = eng.stamps[0].cpu().numpy()
+    for (r, h), v in dm.items():
+        n = v["n_admit"]
+        assert nad[r, h] == n, (t, r, h)
+        assert (aid[r, h] == v["admit_ids"]).all()
+        assert (asl[r, h] == v["admit_slots"]).all()
+        assert (evi[r, h] == v["evict_ids"]).all()
+        assert (res_c[r, h] == L.orc.res[r, h]).all()
+        assert (st[r, h] == L.orc.stamp[r, h]).all()
+    if check_pool_every:
+        check_pool(L, cur)
+    ref = run_staged_step(L, t, dev, check_pool_every)
+    return dm, ref
+
+
+def check_stall_step(L: Layer, t: int, ref: dict, pairs=None, exact=True):
+    """Lists of oasis_step_stall(t) and the tables after it against the
+    oracle's stall step.  exact: every pair's two top-K lists must equal the
+    oracle's; otherwise a pair whose list differs inside the tie window is
+    dropped from the returned set of pairs still in lockstep."""
+    sh, eng = L.shape, L.eng
+    dm = {k: v.cpu().numpy() for k, v in eng.stall_lists(0, t).items()}
+    la = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
+    res_n = eng.res_ids[0][(t + 1) & 1].cpu().numpy()
+    st = eng.stamps[0].cpu().numpy()
+    keep = []
+    for (r, h), v in ref.items():
+        if pairs is not None and (r, h) not in pairs:
+            continue
+        assert topk_agrees(dm["topk_ids"][r, h], v["dm_topk"], v["dm_scores"], sh.K)
+        assert topk_agrees(la["topk_ids"][r, h], v["topk"], v["scores"], sh.K)
+        same = (np.array_equal(dm["topk_ids"][r, h], v["dm_topk"]) and
+                np.array_equal(la["topk_ids"][r, h], v["topk"]))
+        if not same:
+            assert not exact, f"tie window hit at step {t}, pair {(r, h)}"
+            continue
+        assert dm["n_admit"][r, h] == v["dm_n_admit"]
+        assert (dm["admit_ids"][r, h] == v["dm_admit_ids"]).all()
+        assert (dm["admit_slots"][r, h] == v["dm_admit_slots"]).all()
+        assert (dm["evict_ids"][r, h] == v["dm_evict_ids"]).all()
+        assert la["n_admit"][r, h] == v["n_admit"]
+        assert (la["admit_ids"][r, h, :sh.C] == v["admit_ids"]).all()
+        assert (la["admit_slots"][r, h, :sh.C] == v["admit_slots"]).all()
+        assert (la["evict_ids"][r, h, :sh.C] == v["evict_ids"]).all()
+        assert (res_n[r, h] == L.orc.res[r, h]).all()
+        assert (st[r, h] == L.orc.stamp[r, h]).all()
+        keep.append((r, h))
+    return keep
+
+
+def oracle_scan_all_pairs(L: Layer, qd_bits: np.ndarray, threads: int = 0):
+    """The oracle's summary scores and top-K of every (request, KV head) pair
+    of the layer for draft queries qd_bits, on a pool of host threads (the
+    oracle's C functions release the interpreter lock).  Returns
+    (scores [R][Hkv][NBmax] float32, topk [R][Hkv][K] int32)."""
+    import concurrent.futures
+    import os
+    sh = L.shape
+    scores = np.empty((sh.R, sh.Hkv, sh.NBmax), dtype=np.float32)
+    topk = np.empty((sh.R, sh.Hkv, sh.K), dtype=np.int32)
+
+    def one(p):
+        r, h = divmod(p, sh.Hkv)
+        s = oracle.score_rh(L.summ, L.lens, qd_bits, r, h, 16)
+        scores[r, h] = s
+        topk[r, h] = oracle.topk_rh(s, oracle.num_blocks(int(L.lens[r]), 16), sh.K)
+
+    n = threads or min(32, os.cpu_count() or 1)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(one, range(sh.R * sh.Hkv)))
+    return scores, topk
+
+
+def check_scan_all_pairs(L: Layer, gpu_topk: np.ndarray, gpu_scores: np.ndarray,
+                         ref_scores: np.ndarray, ref_topk: np.ndarray):
+    """Every pair's GPU top-K against the oracle's (tie-window rule) and its
+    scores in rank order (rtol 2e-6); returns the pairs whose lists differ
+    inside the tie window."""
+    sh = L.shape
+    differ = []
+    for r in range(sh.R):
+        for h in range(sh.Hkv):
+            assert topk_agrees(gpu_topk[r, h], ref_topk[r, h], ref_scores[r, h], sh.K), (r, h)
+            if not np.array_equal(gpu_topk[r, h], ref_topk[r, h]):
+                differ.append((r, h))
+            nv = int((ref_topk[r, h] >= 0).sum())
+            np.testing.assert_allclose(gpu_scores[r, h, :nv],
+                                       ref_scores[r, h][ref_topk[r, h, :nv]],
+                                       rtol=2e-6, atol=1e-4)
+    return differ

@@ -64,6 +64,14 @@ def test_36_layer_workload_layer(dev):
     sample = [(0, 0), (13, 5), (44, 2), (61, 3), (89, 7)]
     L = H.make_layer(sh, seed=91, steps=4, gen_device="cuda", pairs=sample)
     H.check_summaries(L, sample)
+    # the scan + top-K of all 720 pairs (the 4-warp variant) against the oracle
+    topk = torch.empty((sh.R, sh.Hkv, sh.K), dtype=torch.int32, device=dev)
+    scores = torch.empty((sh.R, sh.Hkv, sh.K), dtype=torch.float32, device=dev)
+    L.eng.oasis_score_topk(0, 0, L.qd[0].to(dev), topk, scores)
+    L.eng.oasis_sync()
+    ref_s, ref_t = H.oracle_scan_all_pairs(L, workload.bf16_bits(L.qd[0]))
+    differ = H.check_scan_all_pairs(L, topk.cpu().numpy(), scores.cpu().numpy(), ref_s, ref_t)
+    assert len(differ) <= 8, differ
     for t in range(2):
         H.run_staged_step(L, t, dev, check_pool_every=False)
         H.check_pool(L, (t + 1) & 1, sample)

@@ -12,7 +12,10 @@ from tests import _harness as H
 pytestmark = pytest.mark.gpu
 
 SHAPE = workload.SHAPES["qwen3_8b_16k"]
-SAMPLE = [(0, 0), (0, 7), (5, 2), (31, 4), (64, 1), (77, 6), (100, 3), (127, 0), (127, 7)]
+# 71 pairs: every KV head, requests from the first to the last (so CTAs of
+# the first and the last wave of the one-CTA-per-pair grids).
+SAMPLE = sorted({(r, (3 * r + k) % 8) for r in range(0, 128, 4) for k in (0, 5)} |
+                {(0, 0), (0, 7), (64, 1), (127, 0), (127, 3), (127, 7), (77, 6), (101, 2)})
 
 
 @pytest.fixture(scope="module")
@@ -57,6 +60,27 @@ def test_staged_lockstep_and_properties(layer):
             got = pool[torch.arange(16, device=dev)[:, None, None],
                        torch.arange(SHAPE.Hkv, device=dev)[None, :, None], units]
             assert torch.equal(got.view(torch.int16).cpu(), want.view(torch.int16))
+
+
+def test_scan_topk_every_pair(layer):
+    # The draft scan + top-K of all 1024 pairs of one step against the
+    # oracle (every CTA position of the launch the step uses), and the
+    # normal-query demand scan of the miss stall the same way.
+    dev = torch.device("cuda", 0)
+    L = layer
+    R, Hkv, K = SHAPE.R, SHAPE.Hkv, SHAPE.K
+    t = 5
+    for which, x in (("draft", L.qd[t]), ("query", L.q[t])):
+        topk = torch.empty((R, Hkv, K), dtype=torch.int32, device=dev)
+        scores = torch.empty((R, Hkv, K), dtype=torch.float32, device=dev)
+        if which == "draft":
+            L.eng.oasis_score_topk(0, t, x.to(dev), topk, scores)
+        else:
+            L.eng.oasis_demand_topk(0, t, x.to(dev), topk, scores)
+        L.eng.oasis_sync()
+        ref_s, ref_t = H.oracle_scan_all_pairs(L, workload.bf16_bits(x))
+        differ = H.check_scan_all_pairs(L, topk.cpu().numpy(), scores.cpu().numpy(), ref_s, ref_t)
+        assert len(differ) <= 8, (which, differ)
 
 
 def test_fused_steps_sampled(layer):
