@@ -291,6 +291,14 @@ struct LayerState {
     int32_t* evict_ids = nullptr;
     int32_t* n_admit = nullptr;
   } lists[2];
+  // Scratch of the persistent scan by step parity: every scan of step t
+  // (look-ahead, demand, stage call) uses set t & 1.  Scans of one step are
+  // ordered one after the other; step t + 2's scans follow step t's.
+  struct Scan {
+    float* scores = nullptr;
+    int32_t* done = nullptr;
+    uint32_t* queue = nullptr;
+  } scan[2];
   // Miss-stall demand lists (oasis_step_stall), by step parity; the
   // admission lists are [R][Hkv][K] (the demand fetch is not capped).
   Lists dm[2];
@@ -344,6 +352,7 @@ struct WsLayout {
   size_t q_stage, qd_stage, q_stage1, qd_stage1, out_stage, outd_stage, qd_ring0, qd_ring1;
   size_t out_stage1, outd_stage1;
   size_t dm_topk_ids, dm_topk_scores, dm_admit_ids, dm_admit_slots, dm_evict_ids, dm_n_admit;
+  size_t scan_scores, scan_ctl;
   size_t total;
 };
 
@@ -402,6 +411,10 @@ WsLayout ws_layout(const oasis_config& c) {
   w.dm_admit_slots = o; o += 2 * align_up(pairs * c.topk * 4);
   w.dm_evict_ids = o;   o += 2 * align_up(pairs * c.topk * 4);
   w.dm_n_admit = o;     o += 2 * align_up(pairs * 4);
+  // persistent scan scratch, both step parities: block scores, then the
+  // per-pair item counters and the queue words (zeroed at init)
+  w.scan_scores = o;    o += 2 * align_up(pairs * static_cast<size_t>(c.max_blocks) * 4);
+  w.scan_ctl = o;       o += 2 * align_up(pairs * 4 + 16);
   w.per_layer = o - kAlign;
   w.total = kAlign + w.per_layer * static_cast<size_t>(c.num_layers);
   return w;
@@ -637,6 +650,10 @@ ScoreArgs score_args(oasis_ctx* ctx, int layer, int step, const void* x, int pla
   a.NBmax = ctx->cfg.max_blocks;
   a.pair0 = 0;
   a.pairs = a.R * a.Hkv;
+  const LayerState::Scan& sc = ctx->layers[layer].scan[step & 1];
+  a.scores_ws = sc.scores;
+  a.done = sc.done;
+  a.queue = sc.queue;
   return a;
 }
 
@@ -911,7 +928,7 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
   // transfer was pending blocked the calling thread for the transfer's
   // 130 ms).
   if (preload_attention_kernels() != cudaSuccess || preload_score_kernels() != cudaSuccess ||
-      preload_support_kernels() != cudaSuccess)
+      preload_stream_kernels() != cudaSuccess || preload_support_kernels() != cudaSuccess)
     return bail(OASIS_ECUDA);
 
   const size_t R = cfg->num_requests, H = cfg->num_kv_heads;
@@ -962,6 +979,14 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
         Dp.admit_slots = reinterpret_cast<int32_t*>(w + (c->wl.dm_admit_slots - b0) + p * tk);
         Dp.evict_ids = reinterpret_cast<int32_t*>(w + (c->wl.dm_evict_ids - b0) + p * tk);
         Dp.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.dm_n_admit - b0) + p * na);
+        const size_t sb = align_up(pairs * static_cast<size_t>(cfg->max_blocks) * 4);
+        const size_t cb = align_up(pairs * 4 + 16);
+        auto& Sc = S.scan[p];
+        Sc.scores = reinterpret_cast<float*>(w + (c->wl.scan_scores - b0) + p * sb);
+        Sc.done = reinterpret_cast<int32_t*>(w + (c->wl.scan_ctl - b0) + p * cb);
+        Sc.queue = reinterpret_cast<uint32_t*>(w + (c->wl.scan_ctl - b0) + p * cb + pairs * 4);
+        if (cudaMemsetAsync(Sc.done, 0, pairs * 4 + 16, c->side) != cudaSuccess)
+          return bail(OASIS_ECUDA);
       }
     }
     S.q_stage[0] = w + (c->wl.q_stage - b0);

@@ -34,6 +34,7 @@
 // Keys are 64-bit: order-preserving score bits above the complemented block
 // id, so ties break to the lower id and all keys are distinct.
 #include <cstdlib>
+#include <string>
 
 #include "admit.cuh"
 #include "common.cuh"
@@ -435,6 +436,13 @@ cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s) {
+  // The persistent scan (scan.cu) whenever its scratch is given, unless
+  // OASIS_SCAN=pair asks for this kernel.
+  static const bool per_pair = [] {
+    const char* e = std::getenv("OASIS_SCAN");
+    return e && std::string(e) == "pair";
+  }();
+  if (a.scores_ws && !per_pair) return launch_scan_stream(a, s);
   if (a.K <= 32) return launch_kpl<1>(a, s);
   if (a.K <= 64) return launch_kpl<2>(a, s);
   if (a.K <= 128) return launch_kpl<4>(a, s);
