@@ -340,8 +340,87 @@ def h2d_bandwidth(dev) -> float:
     return n / (best * 1e-3) / 1e9
 
 
+# Nominal HBM3e bandwidth of one GB300, for a second fraction beside the
+# measured copy peak.
+HBM_SPEC_GBS = 7900.0
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, one ncu
+# capture) by workload and reported kernel, with the SHA-256 (first 16 hex
+# digits) of the kernel's source file when the counters were taken: a
+# kernel whose source has changed since reports traffic null.  Captured on a
+# reduced case and scaled by (request, KV head) pairs where marked.
+PROFILED_TRAFFIC = {}
+
+
+def source_digest(name: str) -> str:
+    import hashlib
+    path = os.path.join(ROOT, "sparse_kv_block_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+KERNEL_SOURCES = {"attention": "attn.cu", "summary_scan": "score_topk.cu",
+                  "topk_select": "score_topk.cu", "prefetch": "admit_gather.cu"}
+
+
+def profiled_traffic(workload_name: str, kernel: str):
+    entry = PROFILED_TRAFFIC.get(workload_name, {}).get(kernel)
+    if entry is None:
+        return None
+    nbytes, digest = entry
+    return nbytes if source_digest(KERNEL_SOURCES[kernel]) == digest else None
+
+
+def kernel_rooflines(shape, ms_sum, counts, off_sum, steps, link_bytes, h2d_gbs, peaks):
+    """Per-kernel rooflines of one timed pass: summed CUDA-event durations of
+    each kind's launches per step (several request groups per step for the
+    side work), against the algorithmic bytes of one step.  Returns
+    (per-kernel dict, name of the longest kernel)."""
+    from sparse_kv_block_gb300.oasis import PROFILE_KINDS
+    show = {"score_topk": "summary_scan"}
+    names = [show.get(n, n) for n in PROFILE_KINDS]
+    avg_ms = {n: (ms_sum[i] / steps if counts[i] else None) for i, n in enumerate(names)}
+    avg_start = {n: (off_sum[i] / counts[i] if counts[i] else None) for i, n in enumerate(names)}
+    launches = {n: counts[i] / steps for i, n in enumerate(names)}
+    R, Hq, Hkv, K, NB = shape.R, shape.Hq, shape.Hkv, shape.K, shape.NBmax
+    qo_bytes = 4 * R * Hq * 128 * 2
+    attn_bytes = R * Hkv * K * UNIT_BYTES + qo_bytes
+    # The scan reads every summary row and the draft queries and writes one
+    # fp32 score per block.
+    scan_bytes = R * Hkv * NB * SUMM_BYTES + R * Hq * 128 * 2 + R * Hkv * NB * 4
+    hbm_src = ("measured hbm_gbs (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+               else "fallback 6.8 TB/s")
+    per_kernel = {}
+    for n, b, bound, peak in [("attention", attn_bytes, "hbm", peaks["hbm_gbs"]),
+                              ("summary_scan", scan_bytes, "hbm", peaks["hbm_gbs"]),
+                              ("prefetch", link_bytes, "host-link", h2d_gbs)]:
+        if avg_ms[n]:
+            a = b / (avg_ms[n] * 1e-3) / 1e9
+            k = {"bound": bound, "achieved": round(a, 1), "peak": round(peak, 1),
+                 "unit": "GB/s", "frac": round(a / peak, 4),
+                 "bytes_per_step": int(b), "ms_per_step": round(avg_ms[n], 5),
+                 "launches_per_step": launches[n], "avg_start_ms": round(avg_start[n], 5),
+                 "peak_source": (hbm_src if bound == "hbm" else
+                                 "pinned cudaMemcpyAsync H2D, 256 MiB, measured in this run"),
+                 "traffic": profiled_traffic(shape.name, n)}
+            if bound == "hbm":
+                k["frac_of_spec"] = round(a / HBM_SPEC_GBS, 4)
+                k["spec_gbs"] = HBM_SPEC_GBS
+            per_kernel[n] = k
+    if avg_ms["topk_select"]:
+        per_kernel["topk_select"] = {
+            "bound": "latency", "ms_per_step": round(avg_ms["topk_select"], 5),
+            "launches_per_step": launches["topk_select"],
+            "avg_start_ms": round(avg_start["topk_select"], 5),
+            "note": "head-wise top-K of the scan's fp32 scores (L2-resident) and the fused "
+                    "capped eviction; overlaps the attention"}
+    timed = [n for n in ("attention", "summary_scan", "prefetch") if avg_ms[n]]
+    dominant = max(timed, key=lambda n: avg_ms[n])
+    return per_kernel, dominant
+
+
 def run_oasis(args, ws, rank, local):
-    from sparse_kv_block_gb300.oasis import lib
+    from sparse_kv_block_gb300.oasis import PROFILE_KINDS, lib
     lib()  # fail loudly if the CUDA library is missing
     if not torch.cuda.is_available():
         raise RuntimeError("the CUDA path needs a GPU")
@@ -399,7 +478,7 @@ def run_oasis(args, ws, rank, local):
     # cost some time themselves) for the kernel rooflines.
     ms = timed_pass(False)
     ms_prof = timed_pass(True)
-    ms_sum, counts, off_sum = eng.oasis_profile_read()
+    ms_sum, counts, off_sum = eng.oasis_profile_read(len(PROFILE_KINDS))
     eng.oasis_profile_enable(False)
     clk = clocks.stop()
     eng.oasis_sync()
@@ -483,44 +562,8 @@ def run_oasis(args, ws, rank, local):
 
     # ---------------- roofline of the dominant kernel
     peaks = measured_peaks()
-    names = ["attention", "score_topk", "admit_evict", "prefetch"]
-    # Per step: summed durations of each kind's launches (several request
-    # groups per step for the side work), and the mean start offset.
-    avg_ms = {n: (ms_sum[i] / args.steps if counts[i] else None) for i, n in enumerate(names)}
-    avg_start = {n: (off_sum[i] / counts[i] if counts[i] else None) for i, n in enumerate(names)}
-    launches = {n: counts[i] / args.steps for i, n in enumerate(names)}
-    R, Hq, Hkv, K, NB = shape.R, shape.Hq, shape.Hkv, shape.K, shape.NBmax
-    qo_bytes = 4 * R * Hq * 128 * 2
-    attn_bytes = R * Hkv * K * UNIT_BYTES + qo_bytes
-    scan_bytes = R * Hkv * NB * SUMM_BYTES + R * Hq * 128 * 2 + R * Hkv * K * 8
-    dominant = max((n for n in names if avg_ms[n]), key=lambda n: avg_ms[n])
-    per_kernel = {}
-    for n, b, bound, peak in [("attention", attn_bytes, "hbm", peaks["hbm_gbs"]),
-                              ("score_topk", scan_bytes, "hbm", peaks["hbm_gbs"]),
-                              ("prefetch", link_bytes, "host-link", h2d_gbs)]:
-        if avg_ms[n]:
-            a = b / (avg_ms[n] * 1e-3) / 1e9
-            per_kernel[n] = {"bound": bound, "achieved": round(a, 1), "peak": round(peak, 1),
-                             "unit": "GB/s", "frac": round(a / peak, 4),
-                             "bytes_per_step": int(b), "ms_per_step": round(avg_ms[n], 5),
-                             "launches_per_step": launches[n],
-                             "avg_start_ms": round(avg_start[n], 5)}
-    hbm_src = ("measured hbm_gbs (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
-               else "fallback 6.8 TB/s")
-    for n, k in per_kernel.items():
-        k["peak_source"] = (hbm_src if k["bound"] == "hbm" else
-                            "pinned cudaMemcpyAsync H2D, 256 MiB, measured in this run")
-    # DRAM bytes per launch from ncu dram__bytes_read.sum + dram__bytes_write.sum
-    # at full size, mean of two launches (profiles/dram_traffic_qwen3_8b_16k.md);
-    # the gather's 50 MB of HBM writes are still in L2 when it ends, so its
-    # DRAM count is small.
-    if shape.name == "qwen3_8b_16k":
-        measured = {"attention": (1076981248 + 1761280 + 1076978688 + 1692672) // 2,
-                    "score_topk": (539682560 + 4603392 + 539652096 + 2043904) // 2,
-                    "prefetch": (434944 + 3588352 + 397568 + 3309312) // 2}
-        for n, v in measured.items():
-            if n in per_kernel:
-                per_kernel[n]["traffic"] = v
+    per_kernel, dominant = kernel_rooflines(shape, ms_sum, counts, off_sum, args.steps,
+                                            link_bytes, h2d_gbs, peaks)
     # The dominant kernel is the longest per step; the attention (the largest
     # HBM reader) is also reported on its own below.
     dk = per_kernel.get(dominant, per_kernel["attention"])
@@ -724,7 +767,7 @@ def run_oasis_layers(args, ws, rank, local):
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1)
     barrier(ws)
-    ms_sum, counts, off_sum = eng.oasis_profile_read()
+    ms_sum, counts, off_sum = eng.oasis_profile_read(len(PROFILE_KINDS))
     eng.oasis_profile_enable(False)
     clk = clocks.stop()
     eng.oasis_sync()
@@ -736,7 +779,7 @@ def run_oasis_layers(args, ws, rank, local):
     link_bytes = adm / L * UNIT_BYTES
     peaks = measured_peaks()
     R, Hq, Hkv, K, NB = shape.R, shape.Hq, shape.Hkv, shape.K, shape.NBmax
-    names = ["attention", "score_topk", "admit_evict", "prefetch"]
+    names = [{"score_topk": "summary_scan"}.get(n, n) for n in PROFILE_KINDS]
     per = {}
     for i, n in enumerate(names):
         if counts[i]:
@@ -744,6 +787,11 @@ def run_oasis_layers(args, ws, rank, local):
                       "launches_per_layer_step": counts[i] / (args.steps * L)}
     attn_bytes = R * Hkv * K * UNIT_BYTES + 4 * R * Hq * 128 * 2
     scan_bytes = R * Hkv * NB * SUMM_BYTES
+    if counts[1]:
+        sb = scan_bytes + R * Hq * 128 * 2 + R * Hkv * NB * 4
+        s_gbs = sb / (ms_sum[1] / counts[1] * 1e-3) / 1e9
+        per["summary_scan"].update({"achieved_gbs": round(s_gbs, 1),
+                                    "frac": round(s_gbs / peaks["hbm_gbs"], 4)})
     a_ms = ms_sum[0] / counts[0]
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
@@ -788,7 +836,7 @@ def run_kernels_alone(args, ws, rank, local):
     """Each stage of the step timed alone (CUDA events on its stream, after
     warm-up) on the single-layer workload, through the stage-level C ABI
     calls; reports achieved GB/s against the HBM / host-link peaks."""
-    from sparse_kv_block_gb300.oasis import lib
+    from sparse_kv_block_gb300.oasis import PROFILE_KINDS, lib
     lib()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -823,6 +871,14 @@ def run_kernels_alone(args, ws, rank, local):
     res = {}
     res["attention_ms"] = timed(lambda: eng.oasis_lookahead_attn(0, 0, q[1], qd[1], out, outd, st))
     res["score_topk_ms"] = timed(lambda: eng.oasis_score_topk(0, 0, qd[1], topk, sc, st))
+    # The same call with per-kernel events: the scan and the ranking apart.
+    eng.oasis_profile_enable(True)
+    for _ in range(n):
+        eng.oasis_score_topk(0, 0, qd[1], topk, sc, st)
+    kms, kcnt, _ = eng.oasis_profile_read(len(PROFILE_KINDS))
+    eng.oasis_profile_enable(False)
+    res["scan_ms"] = kms[1] / max(1, kcnt[1])
+    res["select_ms"] = kms[6] / max(1, kcnt[6]) if kcnt[6] else None
     eng.oasis_score_topk(0, 0, qd[1], topk, sc, st)
     torch.cuda.synchronize(dev)
     res["admit_evict_ms"] = timed(lambda: eng.oasis_admit_evict(0, 0, topk, aid, asl, evi, nad, st))
@@ -840,6 +896,7 @@ def run_kernels_alone(args, ws, rank, local):
     dense_b = R * Hkv * NB * UNIT_BYTES + 4 * R * Hq * 128 * 2
     attn_b = R * Hkv * K * UNIT_BYTES + 4 * R * Hq * 128 * 2
     scan_b = R * Hkv * NB * SUMM_BYTES + R * Hq * 128 * 2
+    scan_only_b = scan_b + R * Hkv * NB * 4
     gb = lambda b, ms: b / (ms * 1e-3) / 1e9
     line = {"mode": "kernels-alone", "workload": workload_desc(shape), "iters": n,
             "attention": {"ms": round(res["attention_ms"], 5), "bytes": attn_b,
@@ -847,7 +904,13 @@ def run_kernels_alone(args, ws, rank, local):
                           "frac_hbm": round(gb(attn_b, res["attention_ms"]) / peaks["hbm_gbs"], 4)},
             "score_topk": {"ms": round(res["score_topk_ms"], 5), "bytes": scan_b,
                            "GBs": round(gb(scan_b, res["score_topk_ms"]), 1),
-                           "frac_hbm": round(gb(scan_b, res["score_topk_ms"]) / peaks["hbm_gbs"], 4)},
+                           "frac_hbm": round(gb(scan_b, res["score_topk_ms"]) / peaks["hbm_gbs"], 4),
+                           "note": "oasis_score_topk as a whole (scan, then ranking)"},
+            "summary_scan": {"ms": round(res["scan_ms"], 5), "bytes": scan_only_b,
+                             "GBs": round(gb(scan_only_b, res["scan_ms"]), 1),
+                             "frac_hbm": round(gb(scan_only_b, res["scan_ms"]) / peaks["hbm_gbs"], 4),
+                             "frac_of_spec": round(gb(scan_only_b, res["scan_ms"]) / HBM_SPEC_GBS, 4)},
+            "topk_select": {"ms": None if res["select_ms"] is None else round(res["select_ms"], 5)},
             "admit_evict": {"ms": round(res["admit_evict_ms"], 5)},
             "prefetch": {"ms": round(res["prefetch_ms"], 5), "units": units,
                          "GBs": round(gb(units * UNIT_BYTES, res["prefetch_ms"]), 1),
@@ -989,9 +1052,9 @@ def run_drafts(args, ws, rank, local):
             eng.oasis_step(0, i, q[i % nq], qd[i % nq], out, outd, st)
         eng.oasis_join(0, st)
         torch.cuda.synchronize(dev)
-        ms_sum, counts, off_sum = eng.oasis_profile_read()
+        ms_sum, counts, off_sum = eng.oasis_profile_read(len(PROFILE_KINDS))
         eng.oasis_profile_enable(False)
-        names = ("attention", "score_topk", "admit_evict", "prefetch")
+        names = [{"score_topk": "summary_scan"}.get(n, n) for n in PROFILE_KINDS]
         kern = {n: {"ms": round(ms_sum[k] / max(counts[k], 1), 4),
                     "start_ms": round(off_sum[k] / max(counts[k], 1), 4)}
                 for k, n in enumerate(names) if counts[k]}

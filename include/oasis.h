@@ -559,10 +559,12 @@ OASIS_API int oasis_remote_stats(oasis_ctx* ctx, int layer, int64_t* units,
  * stream that launches it. */
 OASIS_API int oasis_profile_enable(oasis_ctx* ctx, int enable);
 
-/* Kinds of timed launches, in this order: attention, score_topk (fused
- * admission included), admit_evict, prefetch, demand score_topk (with its
- * fused admission, or a stand-alone demand admission), demand gather. */
-#define OASIS_PROFILE_KINDS 6
+/* Kinds of timed launches, in this order: attention, summary scan (a2;
+ * with OASIS_SCAN=fused in the environment the one-kernel scan + top-K +
+ * admission), admit_evict, prefetch, demand scan (or a stand-alone demand
+ * admission), demand gather, top-K ranking (a3, with the admission fused
+ * into it in the step calls). */
+#define OASIS_PROFILE_KINDS 7
 
 /* Sum of kernel durations (ms) and launch counts since the last read, for
  * the first nkinds (1..OASIS_PROFILE_KINDS) kinds; start_ms_sum (nullable)

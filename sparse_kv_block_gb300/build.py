@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liboasis.so")
-SOURCES = ["api.cu", "attn.cu", "score_topk.cu", "scan.cu", "admit_gather.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "attn.cu", "score_topk.cu", "admit_gather.cu", "noalloc.cu"]
 INCLUDE_DIRS = [CSRC, os.path.join(ROOT, "include")]
 _INCLUDE_RE = re.compile(r'^\s*#\s*include\s*"([^"]+)"', re.M)
 

@@ -291,14 +291,10 @@ struct LayerState {
     int32_t* evict_ids = nullptr;
     int32_t* n_admit = nullptr;
   } lists[2];
-  // Scratch of the persistent scan by step parity: every scan of step t
-  // (look-ahead, demand, stage call) uses set t & 1.  Scans of one step are
-  // ordered one after the other; step t + 2's scans follow step t's.
-  struct Scan {
-    float* scores = nullptr;
-    int32_t* done = nullptr;
-    uint32_t* queue = nullptr;
-  } scan[2];
+  // Block scores of the split scan by step parity: every scan of step t
+  // (look-ahead, demand, stage call) uses scores[t & 1].  The scans of one
+  // step run one after the other; step t + 2's scans follow step t's.
+  float* scan_scores[2] = {nullptr, nullptr};
   // Miss-stall demand lists (oasis_step_stall), by step parity; the
   // admission lists are [R][Hkv][K] (the demand fetch is not capped).
   Lists dm[2];
@@ -352,7 +348,7 @@ struct WsLayout {
   size_t q_stage, qd_stage, q_stage1, qd_stage1, out_stage, outd_stage, qd_ring0, qd_ring1;
   size_t out_stage1, outd_stage1;
   size_t dm_topk_ids, dm_topk_scores, dm_admit_ids, dm_admit_slots, dm_evict_ids, dm_n_admit;
-  size_t scan_scores, scan_ctl;
+  size_t scan_scores;
   size_t total;
 };
 
@@ -411,10 +407,8 @@ WsLayout ws_layout(const oasis_config& c) {
   w.dm_admit_slots = o; o += 2 * align_up(pairs * c.topk * 4);
   w.dm_evict_ids = o;   o += 2 * align_up(pairs * c.topk * 4);
   w.dm_n_admit = o;     o += 2 * align_up(pairs * 4);
-  // persistent scan scratch, both step parities: block scores, then the
-  // per-pair item counters and the queue words (zeroed at init)
+  // block scores of the split scan, both step parities
   w.scan_scores = o;    o += 2 * align_up(pairs * static_cast<size_t>(c.max_blocks) * 4);
-  w.scan_ctl = o;       o += 2 * align_up(pairs * 4 + 16);
   w.per_layer = o - kAlign;
   w.total = kAlign + w.per_layer * static_cast<size_t>(c.num_layers);
   return w;
@@ -650,11 +644,36 @@ ScoreArgs score_args(oasis_ctx* ctx, int layer, int step, const void* x, int pla
   a.NBmax = ctx->cfg.max_blocks;
   a.pair0 = 0;
   a.pairs = a.R * a.Hkv;
-  const LayerState::Scan& sc = ctx->layers[layer].scan[step & 1];
-  a.scores_ws = sc.scores;
-  a.done = sc.done;
-  a.queue = sc.queue;
+  a.scores_ws = ctx->layers[layer].scan_scores[step & 1];
   return a;
+}
+
+// Launch a scan + ranking: split (scan, then ranking and fused admission,
+// timed as profile kinds scan_kind and 6) or as one kernel (OASIS_SCAN=fused,
+// timed as scan_kind).  `scanned`, when given, is recorded on `s` once the
+// scan is done: work that needs only that (it reads HBM beside the scan)
+// may start while the ranking runs.
+int launch_scan_timed(oasis_ctx* ctx, const ScoreArgs& a, cudaStream_t s, int scan_kind,
+                      cudaEvent_t scanned) {
+  if (scan_is_split()) {
+    cudaEvent_t* pe = ctx->prof_begin(scan_kind, s);
+    cudaError_t e = launch_scan_scores(a, s);
+    ctx->prof_end(pe, s);
+    if (int rc = ctx->cuda(e, "scan launch")) return rc;
+    if (scanned) {
+      if (int rc = ctx->cuda(cudaEventRecord(scanned, s), "record scan")) return rc;
+    }
+    pe = ctx->prof_begin(6, s);
+    e = launch_topk_select(a, s);
+    ctx->prof_end(pe, s);
+    return ctx->cuda(e, "top-k launch");
+  }
+  cudaEvent_t* pe = ctx->prof_begin(scan_kind, s);
+  cudaError_t e = launch_score_topk(a, s);
+  ctx->prof_end(pe, s);
+  if (int rc = ctx->cuda(e, "score_topk launch")) return rc;
+  if (scanned) return ctx->cuda(cudaEventRecord(scanned, s), "record scan");
+  return OASIS_OK;
 }
 
 // Miss stall: scan + top-K of every pair with the step's normal query; with
@@ -670,17 +689,14 @@ int run_demand_score(oasis_ctx* ctx, int layer, int step, const void* q, int32_t
     a.admit = demand_admit_args(ctx, layer, step, nullptr, Dm.admit_ids, Dm.admit_slots,
                                 Dm.evict_ids, Dm.n_admit);
   }
-  cudaEvent_t* pe = ctx->prof_begin(4, s);
-  cudaError_t e = launch_score_topk(a, s);
-  ctx->prof_end(pe, s);
-  return ctx->cuda(e, "demand score_topk launch");
+  return launch_scan_timed(ctx, a, s, 4, nullptr);
 }
 
 // Scan + top-K of pairs [pair0, pair0 + pairs); with `fused` also their
 // capped eviction into the layer's workspace lists.
 int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
               float* scores, cudaStream_t s, int pair0 = 0, int pairs = -1,
-              bool fused = false) {
+              bool fused = false, cudaEvent_t scanned = nullptr) {
   LayerState& L = ctx->layers[layer];
   ScoreArgs a = score_args(ctx, layer, step, qd, ctx->D, ids, scores);
   a.pair0 = pair0;
@@ -690,10 +706,7 @@ int run_score(oasis_ctx* ctx, int layer, int step, const void* qd, int32_t* ids,
     a.admit = admit_args(ctx, layer, step, nullptr, L.lists[step & 1].admit_ids,
                          L.lists[step & 1].admit_slots, L.lists[step & 1].evict_ids,
                          L.lists[step & 1].n_admit);
-  cudaEvent_t* pe = ctx->prof_begin(1, s);
-  cudaError_t e = launch_score_topk(a, s);
-  ctx->prof_end(pe, s);
-  return ctx->cuda(e, "score_topk launch");
+  return launch_scan_timed(ctx, a, s, 1, scanned);
 }
 
 int run_admit(oasis_ctx* ctx, int layer, int step, const int32_t* topk, int32_t* aid,
@@ -928,7 +941,7 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
   // transfer was pending blocked the calling thread for the transfer's
   // 130 ms).
   if (preload_attention_kernels() != cudaSuccess || preload_score_kernels() != cudaSuccess ||
-      preload_stream_kernels() != cudaSuccess || preload_support_kernels() != cudaSuccess)
+      preload_support_kernels() != cudaSuccess)
     return bail(OASIS_ECUDA);
 
   const size_t R = cfg->num_requests, H = cfg->num_kv_heads;
@@ -980,13 +993,7 @@ OASIS_API int oasis_init(const oasis_config* cfg, const oasis_buffers* bufs,
         Dp.evict_ids = reinterpret_cast<int32_t*>(w + (c->wl.dm_evict_ids - b0) + p * tk);
         Dp.n_admit = reinterpret_cast<int32_t*>(w + (c->wl.dm_n_admit - b0) + p * na);
         const size_t sb = align_up(pairs * static_cast<size_t>(cfg->max_blocks) * 4);
-        const size_t cb = align_up(pairs * 4 + 16);
-        auto& Sc = S.scan[p];
-        Sc.scores = reinterpret_cast<float*>(w + (c->wl.scan_scores - b0) + p * sb);
-        Sc.done = reinterpret_cast<int32_t*>(w + (c->wl.scan_ctl - b0) + p * cb);
-        Sc.queue = reinterpret_cast<uint32_t*>(w + (c->wl.scan_ctl - b0) + p * cb + pairs * 4);
-        if (cudaMemsetAsync(Sc.done, 0, pairs * 4 + 16, c->side) != cudaSuccess)
-          return bail(OASIS_ECUDA);
+        S.scan_scores[p] = reinterpret_cast<float*>(w + (c->wl.scan_scores - b0) + p * sb);
       }
     }
     S.q_stage[0] = w + (c->wl.q_stage - b0);
@@ -1565,8 +1572,12 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
       }
       continue;
     }
+    // Scan-first: the attention waits for the last group's scan (the
+    // ranking and admission after it overlap the attention).
+    cudaEvent_t scanned =
+        schedule == OASIS_SCHEDULE_SCAN_FIRST && g == ctx->groups - 1 ? L.ev_scan_done : nullptr;
     if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side, p0,
-                           p1 - p0, true))
+                           p1 - p0, true, scanned))
       return rc;
     if (ctx->C > 0) {
       if (int rc = ctx->cuda(cudaEventRecord(L.ev_group[g], ctx->side), "record group"))
@@ -1594,8 +1605,9 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
   if (schedule == OASIS_SCHEDULE_SCAN_FIRST) {
     // The scan gets the whole HBM bandwidth and the SMs first, so the
     // gathers (host-link bound) start as early as possible; the attention
-    // then overlaps the gathers, which write only spare units.
-    if (int rc = ctx->cuda(cudaEventRecord(L.ev_scan_done, ctx->side), "record scan")) return rc;
+    // then overlaps the ranking, the admission and the gathers, which write
+    // only spare units.  (ev_scan_done was recorded after the last group's
+    // scan above.)
     if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_scan_done, 0), "wait scan")) return rc;
   }
   if (int rc = run_attention(ctx, layer, step, q, q_draft, out, out_draft, s)) return rc;

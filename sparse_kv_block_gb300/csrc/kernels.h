@@ -59,12 +59,10 @@ struct ScoreArgs {
   int pair0, pairs;
   int fuse_admit;        // run the capped eviction of each pair in the tail
   AdmitArgs admit;       // used when fuse_admit (its topk field is ignored)
-  // Scratch of the persistent scan (scan.cu); with scores_ws null the
-  // one-CTA-per-pair kernel (score_topk.cu) runs instead.  done and queue
-  // must be zero before a launch and are zero again after it.
-  float* scores_ws;      // [R][Hkv][NBmax] fp32 block scores
-  int32_t* done;         // [R][Hkv] items finished per pair
-  uint32_t* queue;       // [2]: next item, CTAs finished
+  // scores_ws set: the scan writes every block's fp32 score to
+  // scores_ws[pair][b] and a separate kernel ranks them (and admits, when
+  // fused); null: one kernel ranks while it scans (no scratch).
+  float* scores_ws;      // [R][Hkv][NBmax]
 };
 
 // Copies 8 KiB units host -> pool.  Item i of pair p = (r, h) reads block
@@ -156,8 +154,14 @@ struct AppendArgs {
 
 cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
                              cudaStream_t s);
+// Scan + top-K (+ admission) in one kernel, no scratch used.
 cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s);
-cudaError_t launch_scan_stream(const ScoreArgs& a, cudaStream_t s);
+// The same as two kernels: the scan writes every block's score to
+// a.scores_ws, then the ranking (and admission) reads them back.  Used
+// unless scan_is_split() is false (OASIS_SCAN=fused).
+bool scan_is_split();
+cudaError_t launch_scan_scores(const ScoreArgs& a, cudaStream_t s);
+cudaError_t launch_topk_select(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_admit(const AdmitArgs& a, cudaStream_t s);
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s);
 cudaError_t launch_remote_assign(const RemoteArgs& a, cudaStream_t s);
@@ -178,7 +182,6 @@ cudaError_t launch_advance(const int32_t* cur, int32_t* nxt, int R, int grow,
 // launch, and a lazy load waits for work already queued on the device).
 cudaError_t preload_attention_kernels();
 cudaError_t preload_score_kernels();
-cudaError_t preload_stream_kernels();
 cudaError_t preload_support_kernels();
 
 // Largest NBmax the fused score + admit kernel can hold in shared memory.

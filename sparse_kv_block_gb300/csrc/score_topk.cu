@@ -46,6 +46,102 @@ namespace {
 
 constexpr int kStages = 2;                   // ring depth
 
+// The pair's scan weights, 8 dims per lane: lanes 0-15 hold W- (min row),
+// 16-31 W+ (max row); every draft plane adds its group's vectors to them.
+// As fp32 pairs for the packed fp32x2 multiply-add.
+__device__ __forceinline__ void pair_weights(const ScoreArgs& a, int r, int h, int lane,
+                                             uint64_t (&w2)[4]) {
+  const int row = lane >> 4;
+  const int d0 = (lane & 15) * 8;
+  float w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = 0.f;
+  const size_t plane = static_cast<size_t>(a.R) * a.Hq * kHeadDim;
+  for (int e = 0; e < a.D; ++e) {
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.qd) + e * plane +
+                              (static_cast<size_t>(r) * a.Hq + h * a.G) * kHeadDim + d0;
+    for (int gi = 0; gi < a.G; ++gi) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(qg + gi * kHeadDim));
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = bf16lo(wd[i]), hi = bf16hi(wd[i]);
+        w[2 * i] += row ? fmaxf(lo, 0.f) : fminf(lo, 0.f);
+        w[2 * i + 1] += row ? fmaxf(hi, 0.f) : fminf(hi, 0.f);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w2[i] = f2pack(w[2 * i], w[2 * i + 1]);
+}
+
+// Partial scores (per lane) of this warp's 4 blocks of a staged chunk: one
+// 16-byte load per lane per block; blocks j >= nblk give 0.
+__device__ __forceinline__ void stage_partials(const uint8_t* stage, int warp, int lane,
+                                               int nblk, const uint64_t (&w2)[4],
+                                               float (&v)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = warp * 4 + q;
+    float acc = 0.f;
+    if (j < nblk) {
+      const uint4 u = *reinterpret_cast<const uint4*>(stage + j * kSummBytes + lane * 16);
+      uint64_t acc2 = 0ull;
+      acc2 = ffma2(w2[0], f2pack(bf16lo(u.x), bf16hi(u.x)), acc2);
+      acc2 = ffma2(w2[1], f2pack(bf16lo(u.y), bf16hi(u.y)), acc2);
+      acc2 = ffma2(w2[2], f2pack(bf16lo(u.z), bf16hi(u.z)), acc2);
+      acc2 = ffma2(w2[3], f2pack(bf16lo(u.w), bf16hi(u.w)), acc2);
+      acc = f2sum(acc2);
+    }
+    v[q] = acc;
+  }
+}
+
+// Transposed reduction of the 4 partials over 32 lanes (6 shuffles): lane
+// 8q' returns the score of block warp*4 + q' with
+// q' = (lane>>4)*2 + ((lane>>3)&1).
+__device__ __forceinline__ float reduce4(const float (&v)[4], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8;
+  float k0 = b4 ? v[2] : v[0], k1 = b4 ? v[3] : v[1];
+  const float s0 = b4 ? v[0] : v[2], s1 = b4 ? v[1] : v[3];
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  float x = b3 ? k1 : k0;
+  x += __shfl_xor_sync(0xffffffffu, b3 ? k0 : k1, 8);
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x;
+}
+
+// Producer of one pair's summary rows: chunk c of kChunk blocks into stage
+// c % kStages of the ring, after the stage's previous chunk was consumed
+// (kCW arrivals on empty).  Returns false if a wait ran out; drains its own
+// copies before returning either way.
+template <int kChunk>
+__device__ bool produce_pair(const uint8_t* src, int nb, uint8_t* ring, uint64_t* full,
+                             uint64_t* empty) {
+  constexpr int kChunkBytes = kChunk * kSummBytes;
+  const int nchunks = (nb + kChunk - 1) / kChunk;
+  int c = 0;
+  bool ok = true;
+  for (; c < nchunks && ok; ++c) {
+    const int st = c % kStages;
+    if (c >= kStages) ok = mbar_wait(&empty[st], ((c / kStages) - 1) & 1);
+    if (!ok) break;
+    const int nblk = min(kChunk, nb - c * kChunk);
+    const uint32_t bytes = static_cast<uint32_t>(nblk) * kSummBytes;
+    mbar_arrive_expect_tx(&full[st], bytes);
+    bulk_g2s(ring + st * kChunkBytes, src + static_cast<size_t>(c) * kChunkBytes, bytes,
+             &full[st]);
+  }
+  // Drain: the latest phase issued on each stage must have landed before
+  // the CTA may exit (a no-op on the normal path).
+  for (int cc = max(0, c - kStages); cc < c; ++cc)
+    (void)mbar_wait(&full[cc % kStages], (cc / kStages) & 1);
+  return ok;
+}
+
 // Shared memory: the ring of kStages stages (reused by the fused admission
 // once every stage has been consumed, so at least the admission's scratch
 // for this NBmax), the stage barriers, and the per-warp key buffers.  The
@@ -351,6 +447,163 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : (KPL <= 4 ? 4 : 3
   }
 }
 
+// ------------------------------------------------------------ split scan
+// Step a2 alone: one CTA per (request, KV head) streams the pair's summary
+// rows through the same producer and ring as the fused kernel and writes
+// every block's fp32 score to scores_ws[pair][b] (4 bytes per 512 read).
+// Nothing is ranked here, so each CTA ends with its stream: no sort or merge
+// tail holds its slot while HBM idles.
+template <int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
+    scan_kernel(const ScoreArgs a) {
+  constexpr int kChunk = 4 * CW;
+  constexpr int kChunkBytes = kChunk * kSummBytes;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kChunkBytes);
+  uint64_t* empty = full + kStages;
+
+  const int pair = a.pair0 + blockIdx.x;
+  const int r = pair / a.Hkv;
+  const int h = pair - r * a.Hkv;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ctx = a.ctx_len[r];
+  int nb = ctx > 0 ? (ctx + kBlock - 1) / kBlock : 0;
+  if (nb > a.NBmax) {
+    if (threadIdx.x == 0) raise_error(a.err, kErrBadBlock);
+    nb = a.NBmax;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], CW);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == CW) {
+    const uint8_t* src = static_cast<const uint8_t*>(a.summ) +
+                         static_cast<size_t>(pair) * a.NBmax * kSummBytes;
+    if (lane == 0 && !produce_pair<kChunk>(src, nb, ring, full, empty))
+      raise_error(a.err, kErrTimeout);
+    return;  // no block barrier follows
+  }
+  uint64_t w2[4];
+  pair_weights(a, r, h, lane, w2);
+  float* out = a.scores_ws + static_cast<size_t>(pair) * a.NBmax;
+  const int nchunks = (nb + kChunk - 1) / kChunk;
+  const int q = ((lane >> 4) << 1) | ((lane >> 3) & 1);
+  for (int c = 0; c < nchunks; ++c) {
+    const int st = c % kStages;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / kStages) & 1))) {
+      if (lane == 0) raise_error(a.err, kErrTimeout);
+      break;
+    }
+    const int nblk = min(kChunk, nb - c * kChunk);
+    float v[4];
+    stage_partials(ring + st * kChunkBytes, warp, lane, nblk, w2, v);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    const float x = reduce4(v, lane);
+    if ((lane & 7) == 0 && warp * 4 + q < nblk) out[c * kChunk + warp * 4 + q] = x;
+  }
+}
+
+// Steps a3 (and a4 when fused) of the split scan: one CTA of kSelWarps warps
+// per pair ranks the pair's block scores (written by scan_kernel just
+// before, so L2-resident): each warp folds KP = 32*KPL scores at a time into
+// a running top-KP of 64-bit keys (order-preserving score bits above the
+// complemented block id, so ties break to the lower id), a tree merges the
+// warps' lists, and warp 0 writes the top-K and runs the pair's capped
+// eviction.
+constexpr int kSelWarps = 8;
+
+template <int KPL>
+__host__ __device__ inline size_t select_smem_bytes(int NBmax) {
+  const size_t keys = static_cast<size_t>(kSelWarps) * 32 * KPL * 8;
+  const size_t adm = admit_warp_smem_bytes(NBmax);
+  return (keys > adm ? keys : adm) + 128;
+}
+
+template <int KPL>
+__global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs a) {
+  constexpr int KP = 32 * KPL;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* keybuf = reinterpret_cast<uint64_t*>(smem);
+  const int pair = a.pair0 + blockIdx.x;
+  const int r = pair / a.Hkv;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ctx = a.ctx_len[r];
+  int nb = ctx > 0 ? (ctx + kBlock - 1) / kBlock : 0;
+  if (nb > a.NBmax) nb = a.NBmax;  // reported by the scan
+  const float* sp = a.scores_ws + static_cast<size_t>(pair) * a.NBmax;
+
+  uint64_t top[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) top[i] = 0ull;
+  bool have_top = false;
+  for (int base = warp * KP; base < nb; base += kSelWarps * KP) {
+    uint64_t nk[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int e = base + i * 32 + lane;
+      nk[i] = e < nb ? (static_cast<uint64_t>(float_key(sp[e])) << 32) |
+                           static_cast<uint32_t>(~static_cast<uint32_t>(e))
+                     : 0ull;
+    }
+    if (have_top) {
+      bitonic_sort<KPL>(nk, false);
+      merge_top<KPL>(top, nk);
+    } else {
+      bitonic_sort<KPL>(nk, true);
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) top[i] = nk[i];
+      have_top = true;
+    }
+  }
+#pragma unroll 1
+  for (int sz = 1; sz < kSelWarps; sz <<= 1) {
+    __syncthreads();
+    if ((warp % (2 * sz)) == sz) {
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) keybuf[warp * KP + i * 32 + lane] = top[i];
+    }
+    __syncthreads();
+    if ((warp % (2 * sz)) == 0) {
+      const uint64_t* p = keybuf + (warp + sz) * KP;
+      uint64_t nk[KPL];
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) nk[i] = p[KP - 1 - (i * 32 + lane)];
+      merge_top<KPL>(top, nk);
+    }
+  }
+  if (warp == 0) {
+    // Only warp 0 is left using shared memory: the key lists make room for
+    // the admission's scratch.
+    AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(smem);
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int e = i * 32 + lane;
+      if (e < a.K) {
+        const uint64_t key = top[i];
+        const int id = key == 0ull ? -1 : static_cast<int>(~static_cast<uint32_t>(key));
+        a.topk_ids[static_cast<size_t>(pair) * a.K + e] = id;
+        if (a.topk_scores)
+          a.topk_scores[static_cast<size_t>(pair) * a.K + e] =
+              key == 0ull ? -INFINITY : key_float(static_cast<uint32_t>(key >> 32));
+        S.topk[e] = id;
+      }
+    }
+    if (a.fuse_admit) {
+      __syncwarp();
+      admit_warp<KPL>(a.admit, pair, S, reinterpret_cast<uint32_t*>(smem + sizeof(AdmitWarpSmem)));
+    }
+  }
+}
+
 // Raise the kernel's dynamic shared memory limit to `smem` (once per device
 // and size).
 template <int KPL, int CW>
@@ -433,16 +686,100 @@ cudaError_t launch_kpl(const ScoreArgs& a, cudaStream_t s) {
                                                 : launch_kpl_cw<KPL, 8>(a, s);
 }
 
+template <int CW>
+constexpr int scan_smem_bytes() {
+  return kStages * 4 * CW * kSummBytes + 64;
+}
+
+// CTAs of scan_kernel<CW> resident on the whole GPU at once (0 if unknown).
+template <int CW>
+int scan_slots() {
+  int dev = 0, sms = 0, per = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, scan_kernel<CW>, (CW + 1) * 32,
+                                                    scan_smem_bytes<CW>()) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return per * sms;
+}
+
+// Consumer warps of the split scan, by wave quantisation as for the fused
+// kernel: 8 unless its one-CTA-per-pair grid needs a second wave less than
+// half full while the 4-warp grid fits in one.  OASIS_SCAN_WARPS forces one.
+int split_scan_warps(int pairs) {
+  static const int forced = [] {
+    const char* e = std::getenv("OASIS_SCAN_WARPS");
+    const int v = e ? std::atoi(e) : 0;
+    return (v == 4 || v == 8) ? v : 0;
+  }();
+  if (forced) return forced;
+  static int cached_dev = -1, s8 = 0, s4 = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 8;
+  if (dev != cached_dev) {
+    s8 = scan_slots<8>();
+    s4 = scan_slots<4>();
+    cached_dev = dev;
+  }
+  if (s8 > 0 && s4 > 0 && pairs > s8 && pairs <= s4) {
+    const int last = pairs % s8;
+    if (last != 0 && 2 * last < s8) return 4;
+  }
+  return 8;
+}
+
+template <int KPL>
+cudaError_t launch_select_kpl(const ScoreArgs& a, cudaStream_t s) {
+  const size_t smem = select_smem_bytes<KPL>(a.NBmax);
+  if (smem > 48 * 1024) {
+    static int configured_device = -1;
+    static size_t configured_smem = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev != configured_device || smem > configured_smem) {
+      e = cudaFuncSetAttribute(select_kernel<KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      configured_device = dev;
+      configured_smem = smem;
+    }
+  }
+  select_kernel<KPL><<<a.pairs, kSelWarps * 32, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s) {
-  // The persistent scan (scan.cu) whenever its scratch is given, unless
-  // OASIS_SCAN=pair asks for this kernel.
-  static const bool per_pair = [] {
+bool scan_is_split() {
+  static const bool fused = [] {
     const char* e = std::getenv("OASIS_SCAN");
-    return e && std::string(e) == "pair";
+    return e && std::string(e) == "fused";
   }();
-  if (a.scores_ws && !per_pair) return launch_scan_stream(a, s);
+  return !fused;
+}
+
+cudaError_t launch_scan_scores(const ScoreArgs& a, cudaStream_t s) {
+  if (a.pairs <= 0) return cudaSuccess;
+  if (split_scan_warps(a.pairs) == 4) {
+    scan_kernel<4><<<a.pairs, 5 * 32, scan_smem_bytes<4>(), s>>>(a);
+  } else {
+    scan_kernel<8><<<a.pairs, 9 * 32, scan_smem_bytes<8>(), s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_select(const ScoreArgs& a, cudaStream_t s) {
+  if (a.pairs <= 0) return cudaSuccess;
+  if (a.K <= 32) return launch_select_kpl<1>(a, s);
+  if (a.K <= 64) return launch_select_kpl<2>(a, s);
+  if (a.K <= 128) return launch_select_kpl<4>(a, s);
+  return launch_select_kpl<8>(a, s);
+}
+
+cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s) {
   if (a.K <= 32) return launch_kpl<1>(a, s);
   if (a.K <= 64) return launch_kpl<2>(a, s);
   if (a.K <= 128) return launch_kpl<4>(a, s);
@@ -459,7 +796,13 @@ cudaError_t preload_score_kernels() {
       reinterpret_cast<const void*>(score_topk_kernel<1, 4>),
       reinterpret_cast<const void*>(score_topk_kernel<2, 4>),
       reinterpret_cast<const void*>(score_topk_kernel<4, 4>),
-      reinterpret_cast<const void*>(score_topk_kernel<8, 4>)};
+      reinterpret_cast<const void*>(score_topk_kernel<8, 4>),
+      reinterpret_cast<const void*>(scan_kernel<8>),
+      reinterpret_cast<const void*>(scan_kernel<4>),
+      reinterpret_cast<const void*>(select_kernel<1>),
+      reinterpret_cast<const void*>(select_kernel<2>),
+      reinterpret_cast<const void*>(select_kernel<4>),
+      reinterpret_cast<const void*>(select_kernel<8>)};
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncGetAttributes(&at, f);
     if (e != cudaSuccess) return e;

@@ -118,7 +118,7 @@ EXPORTS = {
 }
 
 PROFILE_KINDS = ["attention", "score_topk", "admit_evict", "prefetch", "demand_score",
-                 "demand_gather"]
+                 "demand_gather", "topk_select"]
 
 _lib = None
 
