@@ -623,7 +623,7 @@ def run_oasis_layers(args, ws, rank, local):
     host stores rewritten, and each layer's summaries and resident copies of
     the moved blocks refreshed (oasis_refresh_blocks); each step is then
     timed on its own and the steps' times are summed."""
-    from sparse_kv_block_gb300.oasis import Oasis, lib, make_config
+    from sparse_kv_block_gb300.oasis import PROFILE_KINDS, Oasis, lib, make_config
     lib()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -1012,7 +1012,7 @@ def run_drafts(args, ws, rank, local):
     workload, each draft attending over the one resident set and the drafts'
     summary bounds summed for the ranking.  Reports the step rate and the
     attention kernel alone (same resident bytes, 1 + D query kinds)."""
-    from sparse_kv_block_gb300.oasis import lib
+    from sparse_kv_block_gb300.oasis import PROFILE_KINDS, lib
     lib()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
