@@ -564,6 +564,7 @@ def run_oasis(args, ws, rank, local):
     peaks = measured_peaks()
     per_kernel, dominant = kernel_rooflines(shape, ms_sum, counts, off_sum, args.steps,
                                             link_bytes, h2d_gbs, peaks)
+    R, Hq = shape.R, shape.Hq
     # The dominant kernel is the longest per step; the attention (the largest
     # HBM reader) is also reported on its own below.
     dk = per_kernel.get(dominant, per_kernel["attention"])

@@ -18,9 +18,10 @@
 // written into the evicted slot's own unit.
 //
 // Membership is tested with two NBmax-bit bitmaps in shared memory; the
-// eviction order is a bitonic sort of 64-bit keys
+// eviction order is that of 64-bit keys
 //   [63] occupied | [62:32] stamp+1 | [31:8] block id+1 | [7:0] slot
-// (selected slots get the all-ones key and sort last).
+// (selected slots get the all-ones key and come last), the n first found by
+// repeated warp minima when n is small, else by a bitonic sort.
 #pragma once
 
 #include "common.cuh"
@@ -28,6 +29,10 @@
 #include "sortnet.cuh"
 
 namespace oasis {
+
+// Up to this many admissions the eviction order is found by repeated warp
+// minima instead of a full sort of the K slot keys.
+constexpr int kArgminRounds = 8;
 
 struct AdmitWarpSmem {
   int topk[kMaxTopK];
@@ -109,11 +114,30 @@ __device__ void admit_warp(const AdmitArgs& a, int pair, AdmitWarpSmem& S, uint3
       key[i] = ~0ull;
     }
   }
-  bitonic_sort<KPL>(key, false);
+  if (n <= kArgminRounds) {
+    // Few admissions: the n smallest keys by repeated warp minima (keys are
+    // distinct: the slot sits in the low byte).
+    for (int e = 0; e < n; ++e) {
+      uint64_t m = key[0];
 #pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const int e = i * 32 + lane;
-    if (e < n) S.evslot[e] = static_cast<int>(key[i] & 0xffu);
+      for (int i = 1; i < KPL; ++i) m = key[i] < m ? key[i] : m;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xffffffffu, m, off);
+        m = o < m ? o : m;
+      }
+      if (lane == 0) S.evslot[e] = static_cast<int>(m & 0xffu);
+#pragma unroll
+      for (int i = 0; i < KPL; ++i)
+        if (key[i] == m) key[i] = ~0ull;
+    }
+  } else {
+    bitonic_sort<KPL>(key, false);
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int e = i * 32 + lane;
+      if (e < n) S.evslot[e] = static_cast<int>(key[i] & 0xffu);
+    }
   }
   __syncwarp();
 

@@ -511,96 +511,157 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
   }
 }
 
-// Steps a3 (and a4 when fused) of the split scan: one CTA of kSelWarps warps
-// per pair ranks the pair's block scores (written by scan_kernel just
-// before, so L2-resident): each warp folds KP = 32*KPL scores at a time into
-// a running top-KP of 64-bit keys (order-preserving score bits above the
-// complemented block id, so ties break to the lower id), a tree merges the
-// warps' lists, and warp 0 writes the top-K and runs the pair's capped
-// eviction.
-constexpr int kSelWarps = 8;
+// Steps a3 (and a4 when fused) of the split scan: one CTA of kSelThreads
+// threads per pair ranks the pair's block scores (written by scan_kernel
+// just before, so L2-resident).  Each block's key is its order-preserving
+// score bits above its complemented block id: keys are distinct, larger is
+// better and equal scores rank the lower id first.  A most-significant-
+// byte-first radix selection finds the K-th largest key: each pass builds a
+// 256-bin histogram of the next byte over the keys that still match the
+// prefix chosen so far and picks the bin that holds the K-th key, until that
+// bin holds exactly the keys still wanted (with random scores, after about
+// three passes).  Every key at or above the final prefix is in the top-K:
+// the K of them are compacted, one warp sorts them with a bitonic network
+// and writes the list, and warp 0 then runs the pair's capped eviction.
+// Keys stay in registers (kSelKeys per thread) up to kSelKeys * kSelThreads
+// blocks; longer contexts re-read the scores for every pass.
+constexpr int kSelThreads = 256;   // = the histogram's bins
+constexpr int kSelKeys = 16;
 
 template <int KPL>
 __host__ __device__ inline size_t select_smem_bytes(int NBmax) {
-  const size_t keys = static_cast<size_t>(kSelWarps) * 32 * KPL * 8;
+  const size_t rank = 1024 + 64 + static_cast<size_t>(32) * KPL * 8;  // hist, ctl, list
   const size_t adm = admit_warp_smem_bytes(NBmax);
-  return (keys > adm ? keys : adm) + 128;
+  return (rank > adm ? rank : adm) + 128;
 }
 
 template <int KPL>
-__global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs a) {
   constexpr int KP = 32 * KPL;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* keybuf = reinterpret_cast<uint64_t*>(smem);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);           // [256]
+  int* ctl = reinterpret_cast<int*>(smem + 1024);               // bin, need, in bin, count
+  uint64_t* list = reinterpret_cast<uint64_t*>(smem + 1024 + 64);  // [KP]
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
   const int pair = a.pair0 + blockIdx.x;
   const int r = pair / a.Hkv;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
   const int ctx = a.ctx_len[r];
   int nb = ctx > 0 ? (ctx + kBlock - 1) / kBlock : 0;
   if (nb > a.NBmax) nb = a.NBmax;  // reported by the scan
   const float* sp = a.scores_ws + static_cast<size_t>(pair) * a.NBmax;
 
+  // Key of block e from its score-key bits u.
+  auto key64 = [](uint32_t u, int e) {
+    return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
+  };
+  const bool in_regs = nb <= kSelKeys * kSelThreads;
+  uint32_t ureg[kSelKeys];
+#pragma unroll
+  for (int j = 0; j < kSelKeys; ++j) {
+    const int e = j * kSelThreads + tid;
+    ureg[j] = (in_regs && e < nb) ? float_key(sp[e]) : 0u;
+  }
+  // f(key) for every key of this thread (block e = j * kSelThreads + tid).
+  auto for_each_key = [&](auto&& f) {
+    if (in_regs) {
+#pragma unroll
+      for (int j = 0; j < kSelKeys; ++j) {
+        const int e = j * kSelThreads + tid;
+        if (e < nb) f(key64(ureg[j], e));
+      }
+    } else {
+      for (int e = tid; e < nb; e += kSelThreads) f(key64(float_key(sp[e]), e));
+    }
+  };
+
+  // ---- radix selection of the prefix that holds exactly the top min(K, nb)
+  uint64_t prefix = 0ull, mask = 0ull;
+  int need = min(a.K, nb);
+  if (need > 0 && need < nb) {
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      hist[tid] = 0u;
+      __syncthreads();
+      for_each_key([&](uint64_t k) {
+        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+      });
+      __syncthreads();
+      if (warp == 0) {
+        // Lane l owns bins 8l .. 8l+7; the keys in higher bins than a lane's
+        // are the suffix sum of the lanes above it.
+        uint32_t c[8];
+        uint32_t total = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          c[i] = hist[lane * 8 + i];
+          total += c[i];
+        }
+        uint32_t incl = total;   // keys in bins of lanes >= this lane
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t v = __shfl_down_sync(0xffffffffu, incl, off);
+          if (lane + off < 32) incl += v;
+        }
+        uint32_t cum = incl - total;   // keys in bins above this lane's
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+          if (static_cast<int>(cum) < need && need <= static_cast<int>(cum + c[i])) {
+            ctl[0] = lane * 8 + i;
+            ctl[1] = need - static_cast<int>(cum);
+            ctl[2] = static_cast<int>(c[i]);
+          }
+          cum += c[i];
+        }
+      }
+      __syncthreads();
+      const int b = ctl[0];
+      need = ctl[1];
+      const int in_bin = ctl[2];
+      prefix |= static_cast<uint64_t>(b) << shift;
+      mask |= 0xffull << shift;
+      if (in_bin == need) break;   // the whole bin is wanted: done
+    }
+  }
+  // ---- compaction: the keys at or above the prefix (min(K, nb) of them)
+  if (tid == 0) ctl[3] = 0;
+  __syncthreads();
+  for_each_key([&](uint64_t k) {
+    if ((k & mask) >= prefix) {
+      const int pos = atomicAdd(&ctl[3], 1);
+      if (pos < KP) list[pos] = k;
+    }
+  });
+  __syncthreads();
+  if (warp != 0) return;
+  const int n = min(ctl[3], KP);
   uint64_t top[KPL];
 #pragma unroll
-  for (int i = 0; i < KPL; ++i) top[i] = 0ull;
-  bool have_top = false;
-  for (int base = warp * KP; base < nb; base += kSelWarps * KP) {
-    uint64_t nk[KPL];
+  for (int i = 0; i < KPL; ++i) {
+    const int e = i * 32 + lane;
+    top[i] = e < n ? list[e] : 0ull;
+  }
+  bitonic_sort<KPL>(top, true);
+  __syncwarp();
+  // The histogram and list are no longer read: the region takes the
+  // admission's scratch.
+  AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(smem);
 #pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      const int e = base + i * 32 + lane;
-      nk[i] = e < nb ? (static_cast<uint64_t>(float_key(sp[e])) << 32) |
-                           static_cast<uint32_t>(~static_cast<uint32_t>(e))
-                     : 0ull;
-    }
-    if (have_top) {
-      bitonic_sort<KPL>(nk, false);
-      merge_top<KPL>(top, nk);
-    } else {
-      bitonic_sort<KPL>(nk, true);
-#pragma unroll
-      for (int i = 0; i < KPL; ++i) top[i] = nk[i];
-      have_top = true;
+  for (int i = 0; i < KPL; ++i) {
+    const int e = i * 32 + lane;
+    if (e < a.K) {
+      const uint64_t key = top[i];
+      const int id = key == 0ull ? -1 : static_cast<int>(~static_cast<uint32_t>(key));
+      a.topk_ids[static_cast<size_t>(pair) * a.K + e] = id;
+      if (a.topk_scores)
+        a.topk_scores[static_cast<size_t>(pair) * a.K + e] =
+            key == 0ull ? -INFINITY : key_float(static_cast<uint32_t>(key >> 32));
+      S.topk[e] = id;
     }
   }
-#pragma unroll 1
-  for (int sz = 1; sz < kSelWarps; sz <<= 1) {
-    __syncthreads();
-    if ((warp % (2 * sz)) == sz) {
-#pragma unroll
-      for (int i = 0; i < KPL; ++i) keybuf[warp * KP + i * 32 + lane] = top[i];
-    }
-    __syncthreads();
-    if ((warp % (2 * sz)) == 0) {
-      const uint64_t* p = keybuf + (warp + sz) * KP;
-      uint64_t nk[KPL];
-#pragma unroll
-      for (int i = 0; i < KPL; ++i) nk[i] = p[KP - 1 - (i * 32 + lane)];
-      merge_top<KPL>(top, nk);
-    }
-  }
-  if (warp == 0) {
-    // Only warp 0 is left using shared memory: the key lists make room for
-    // the admission's scratch.
-    AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(smem);
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      const int e = i * 32 + lane;
-      if (e < a.K) {
-        const uint64_t key = top[i];
-        const int id = key == 0ull ? -1 : static_cast<int>(~static_cast<uint32_t>(key));
-        a.topk_ids[static_cast<size_t>(pair) * a.K + e] = id;
-        if (a.topk_scores)
-          a.topk_scores[static_cast<size_t>(pair) * a.K + e] =
-              key == 0ull ? -INFINITY : key_float(static_cast<uint32_t>(key >> 32));
-        S.topk[e] = id;
-      }
-    }
-    if (a.fuse_admit) {
-      __syncwarp();
-      admit_warp<KPL>(a.admit, pair, S, reinterpret_cast<uint32_t*>(smem + sizeof(AdmitWarpSmem)));
-    }
+  if (a.fuse_admit) {
+    __syncwarp();
+    admit_warp<KPL>(a.admit, pair, S, reinterpret_cast<uint32_t*>(smem + sizeof(AdmitWarpSmem)));
   }
 }
 
@@ -747,7 +808,7 @@ cudaError_t launch_select_kpl(const ScoreArgs& a, cudaStream_t s) {
       configured_smem = smem;
     }
   }
-  select_kernel<KPL><<<a.pairs, kSelWarps * 32, smem, s>>>(a);
+  select_kernel<KPL><<<a.pairs, kSelThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
