@@ -513,35 +513,38 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
 
 // Steps a3 (and a4 when fused) of the split scan: one CTA of kSelThreads
 // threads per pair ranks the pair's block scores (written by scan_kernel
-// just before, so L2-resident).  Each block's key is its order-preserving
-// score bits above its complemented block id: keys are distinct, larger is
-// better and equal scores rank the lower id first.  A most-significant-
-// byte-first radix selection finds the K-th largest key: each pass builds a
-// 256-bin histogram of the next byte over the keys that still match the
-// prefix chosen so far and picks the bin that holds the K-th key, until that
-// bin holds exactly the keys still wanted (with random scores, after about
-// three passes).  Every key at or above the final prefix is in the top-K:
-// the K of them are compacted, one warp sorts them with a bitonic network
-// and writes the list, and warp 0 then runs the pair's capped eviction.
-// Keys stay in registers (kSelKeys per thread) up to kSelKeys * kSelThreads
-// blocks; longer contexts re-read the scores for every pass.
+// just before).  A block's rank key is its order-preserving score bits
+// (larger is better); equal scores rank the lower block id first.  A
+// most-significant-byte-first radix selection finds the K-th largest score
+// key: each pass builds a 256-bin histogram of the next byte over the keys
+// that still match the prefix chosen so far and picks the bin that holds the
+// K-th key, until that bin holds exactly the keys still wanted (about three
+// passes with continuous scores).  Every key above the final prefix, and
+// every key in its bin, is in the top-K; if after all four bytes more keys
+// than wanted share the K-th score, the lowest block ids among them are
+// taken.  The K winners are compacted, one warp sorts them (score key above
+// the complemented block id) with a bitonic network and writes the list, and
+// warp 0 then runs the pair's capped eviction.  NPT keys per thread stay in
+// registers (NPT * kSelThreads >= NBmax); with NPT = 0 every pass re-reads
+// the scores (contexts beyond kSelThreads * 16 blocks).
 constexpr int kSelThreads = 256;   // = the histogram's bins
-constexpr int kSelKeys = 16;
 
 template <int KPL>
 __host__ __device__ inline size_t select_smem_bytes(int NBmax) {
-  const size_t rank = 1024 + 64 + static_cast<size_t>(32) * KPL * 8;  // hist, ctl, list
+  const size_t rank = 1024 + 64 + 64 + static_cast<size_t>(32) * KPL * 8;  // hist, ctl, tie, list
   const size_t adm = admit_warp_smem_bytes(NBmax);
   return (rank > adm ? rank : adm) + 128;
 }
 
-template <int KPL>
+template <int KPL, int NPT>
 __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs a) {
   constexpr int KP = 32 * KPL;
+  constexpr int kRegs = NPT > 0 ? NPT : 1;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);           // [256]
-  int* ctl = reinterpret_cast<int*>(smem + 1024);               // bin, need, in bin, count
-  uint64_t* list = reinterpret_cast<uint64_t*>(smem + 1024 + 64);  // [KP]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);            // [256]
+  int* ctl = reinterpret_cast<int*>(smem + 1024);                // bin, need, in bin, count
+  int* tie = reinterpret_cast<int*>(smem + 1024 + 64);           // per-warp tie counts [8]
+  uint64_t* list = reinterpret_cast<uint64_t*>(smem + 1024 + 128);  // [KP]
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -552,44 +555,43 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs 
   if (nb > a.NBmax) nb = a.NBmax;  // reported by the scan
   const float* sp = a.scores_ws + static_cast<size_t>(pair) * a.NBmax;
 
-  // Key of block e from its score-key bits u.
-  auto key64 = [](uint32_t u, int e) {
-    return (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
-  };
-  const bool in_regs = nb <= kSelKeys * kSelThreads;
-  uint32_t ureg[kSelKeys];
+  uint32_t ureg[kRegs];
+  if constexpr (NPT > 0) {
 #pragma unroll
-  for (int j = 0; j < kSelKeys; ++j) {
-    const int e = j * kSelThreads + tid;
-    ureg[j] = (in_regs && e < nb) ? float_key(sp[e]) : 0u;
+    for (int j = 0; j < NPT; ++j) {
+      const int e = j * kSelThreads + tid;
+      ureg[j] = e < nb ? float_key(sp[e]) : 0u;
+    }
   }
-  // f(key) for every key of this thread (block e = j * kSelThreads + tid).
+  // f(score key, block id) for every block of this thread (e = j * T + tid),
+  // in increasing block id.
   auto for_each_key = [&](auto&& f) {
-    if (in_regs) {
+    if constexpr (NPT > 0) {
 #pragma unroll
-      for (int j = 0; j < kSelKeys; ++j) {
+      for (int j = 0; j < NPT; ++j) {
         const int e = j * kSelThreads + tid;
-        if (e < nb) f(key64(ureg[j], e));
+        if (e < nb) f(ureg[j], e);
       }
     } else {
-      for (int e = tid; e < nb; e += kSelThreads) f(key64(float_key(sp[e]), e));
+      for (int e = tid; e < nb; e += kSelThreads) f(float_key(sp[e]), e);
     }
   };
 
-  // ---- radix selection of the prefix that holds exactly the top min(K, nb)
-  uint64_t prefix = 0ull, mask = 0ull;
+  // ---- radix selection over the score keys
+  uint32_t prefix = 0u, mask = 0u;
   int need = min(a.K, nb);
+  int in_bin = need;
   if (need > 0 && need < nb) {
-    for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
       hist[tid] = 0u;
       __syncthreads();
-      for_each_key([&](uint64_t k) {
-        if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+      for_each_key([&](uint32_t u, int) {
+        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
       });
       __syncthreads();
       if (warp == 0) {
         // Lane l owns bins 8l .. 8l+7; the keys in higher bins than a lane's
-        // are the suffix sum of the lanes above it.
+        // are the suffix sum over the lanes above it.
         uint32_t c[8];
         uint32_t total = 0;
 #pragma unroll
@@ -597,13 +599,13 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs 
           c[i] = hist[lane * 8 + i];
           total += c[i];
         }
-        uint32_t incl = total;   // keys in bins of lanes >= this lane
+        uint32_t incl = total;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           const uint32_t v = __shfl_down_sync(0xffffffffu, incl, off);
           if (lane + off < 32) incl += v;
         }
-        uint32_t cum = incl - total;   // keys in bins above this lane's
+        uint32_t cum = incl - total;
 #pragma unroll
         for (int i = 7; i >= 0; --i) {
           if (static_cast<int>(cum) < need && need <= static_cast<int>(cum + c[i])) {
@@ -615,23 +617,46 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs 
         }
       }
       __syncthreads();
-      const int b = ctl[0];
+      prefix |= static_cast<uint32_t>(ctl[0]) << shift;
+      mask |= 0xffu << shift;
       need = ctl[1];
-      const int in_bin = ctl[2];
-      prefix |= static_cast<uint64_t>(b) << shift;
-      mask |= 0xffull << shift;
-      if (in_bin == need) break;   // the whole bin is wanted: done
+      in_bin = ctl[2];
+      if (in_bin == need) break;   // the whole bin is wanted
     }
   }
-  // ---- compaction: the keys at or above the prefix (min(K, nb) of them)
+  // ---- compaction of the winners: keys above the prefix, then those in its
+  // bin (all of them, or when more share the K-th score than are wanted, the
+  // lowest block ids: ranked in block-id order, one slice of kSelThreads
+  // blocks at a time)
+  const bool ties = in_bin > need;
   if (tid == 0) ctl[3] = 0;
   __syncthreads();
-  for_each_key([&](uint64_t k) {
-    if ((k & mask) >= prefix) {
-      const int pos = atomicAdd(&ctl[3], 1);
-      if (pos < KP) list[pos] = k;
-    }
+  auto put = [&](uint32_t u, int e) {
+    const int pos = atomicAdd(&ctl[3], 1);
+    if (pos < KP)
+      list[pos] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
+  };
+  for_each_key([&](uint32_t u, int e) {
+    if ((u & mask) > prefix || (!ties && (u & mask) == prefix)) put(u, e);
   });
+  if (ties) {
+    // Only reached when the K-th score is shared (mask covers every bit).
+    int taken = 0;
+    const int slices = (nb + kSelThreads - 1) / kSelThreads;
+    for (int j = 0; j < slices; ++j) {
+      const int e = j * kSelThreads + tid;
+      const bool eq = e < nb && float_key(sp[e]) == prefix;
+      const unsigned bal = __ballot_sync(0xffffffffu, eq);
+      __syncthreads();
+      if (lane == 0) tie[warp] = __popc(bal);
+      __syncthreads();
+      int before = taken;
+      for (int w = 0; w < warp; ++w) before += tie[w];
+      before += __popc(bal & ((1u << lane) - 1u));
+      if (eq && before < need) put(prefix, e);
+      for (int w = 0; w < kSelThreads / 32; ++w) taken += tie[w];
+    }
+  }
   __syncthreads();
   if (warp != 0) return;
   const int n = min(ctl[3], KP);
@@ -791,8 +816,8 @@ int split_scan_warps(int pairs) {
   return 8;
 }
 
-template <int KPL>
-cudaError_t launch_select_kpl(const ScoreArgs& a, cudaStream_t s) {
+template <int KPL, int NPT>
+cudaError_t launch_select_npt(const ScoreArgs& a, cudaStream_t s) {
   const size_t smem = select_smem_bytes<KPL>(a.NBmax);
   if (smem > 48 * 1024) {
     static int configured_device = -1;
@@ -801,15 +826,28 @@ cudaError_t launch_select_kpl(const ScoreArgs& a, cudaStream_t s) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev != configured_device || smem > configured_smem) {
-      e = cudaFuncSetAttribute(select_kernel<KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem));
+      e = cudaFuncSetAttribute(select_kernel<KPL, NPT>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
       configured_device = dev;
       configured_smem = smem;
     }
   }
-  select_kernel<KPL><<<a.pairs, kSelThreads, smem, s>>>(a);
+  select_kernel<KPL, NPT><<<a.pairs, kSelThreads, smem, s>>>(a);
   return cudaGetLastError();
+}
+
+// Keys per thread: the smallest of 1, 2, 4, 8, 16 that holds NBmax blocks,
+// else 0 (scores re-read per pass).
+template <int KPL>
+cudaError_t launch_select_kpl(const ScoreArgs& a, cudaStream_t s) {
+  const int per = (a.NBmax + kSelThreads - 1) / kSelThreads;
+  if (per <= 1) return launch_select_npt<KPL, 1>(a, s);
+  if (per <= 2) return launch_select_npt<KPL, 2>(a, s);
+  if (per <= 4) return launch_select_npt<KPL, 4>(a, s);
+  if (per <= 8) return launch_select_npt<KPL, 8>(a, s);
+  if (per <= 16) return launch_select_npt<KPL, 16>(a, s);
+  return launch_select_npt<KPL, 0>(a, s);
 }
 
 }  // namespace
@@ -860,10 +898,10 @@ cudaError_t preload_score_kernels() {
       reinterpret_cast<const void*>(score_topk_kernel<8, 4>),
       reinterpret_cast<const void*>(scan_kernel<8>),
       reinterpret_cast<const void*>(scan_kernel<4>),
-      reinterpret_cast<const void*>(select_kernel<1>),
-      reinterpret_cast<const void*>(select_kernel<2>),
-      reinterpret_cast<const void*>(select_kernel<4>),
-      reinterpret_cast<const void*>(select_kernel<8>)};
+      reinterpret_cast<const void*>(select_kernel<1, 1>),
+      reinterpret_cast<const void*>(select_kernel<4, 4>),
+      reinterpret_cast<const void*>(select_kernel<4, 16>),
+      reinterpret_cast<const void*>(select_kernel<8, 4>)};
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncGetAttributes(&at, f);
     if (e != cudaSuccess) return e;

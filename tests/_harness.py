@@ -44,7 +44,8 @@ class Layer:
 
 def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_fp32=False,
                gen_device="cpu", pairs=None, res0=None, side_groups=0,
-               schedule=0, remote_capacity=None, remote_gbps=0.0, num_drafts=1) -> Layer:
+               schedule=0, remote_capacity=None, remote_gbps=0.0, num_drafts=1,
+               mutate_host=None) -> Layer:
     if K is not None or fetch_ratio is not None:
         shape = dataclasses.replace(shape, K=K if K is not None else shape.K,
                                     fetch_ratio=shape.fetch_ratio if fetch_ratio is None else fetch_ratio)
@@ -52,6 +53,8 @@ def make_layer(shape, seed=0, lens=None, steps=4, K=None, fetch_ratio=None, out_
     host = torch.empty((shape.R, shape.Hkv, shape.NBmax, 2, 16, 128), dtype=torch.bfloat16,
                        pin_memory=True)
     workload.host_kv(shape, seed, 0, lens, device=gen_device, out=host)
+    if mutate_host is not None:   # a test's own structure on top of the draw
+        mutate_host(host)
     if num_drafts == 1:
         q, qd = workload.queries(shape, seed, 0, steps, device=gen_device)
     else:
