@@ -511,44 +511,47 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
   }
 }
 
-// Steps a3 (and a4 when fused) of the split scan: one CTA of kSelThreads
-// threads per pair ranks the pair's block scores (written by scan_kernel
-// just before).  A block's rank key is its order-preserving score bits
-// (larger is better); equal scores rank the lower block id first.  A
-// most-significant-byte-first radix selection finds the K-th largest score
-// key: each pass builds a 256-bin histogram of the next byte over the keys
-// that still match the prefix chosen so far and picks the bin that holds the
-// K-th key, until that bin holds exactly the keys still wanted (about three
-// passes with continuous scores).  Every key above the final prefix, and
-// every key in its bin, is in the top-K; if after all four bytes more keys
-// than wanted share the K-th score, the lowest block ids among them are
-// taken.  The K winners are compacted, one warp sorts them (score key above
-// the complemented block id) with a bitonic network and writes the list, and
-// warp 0 then runs the pair's capped eviction.  NPT keys per thread stay in
-// registers (NPT * kSelThreads >= NBmax); with NPT = 0 every pass re-reads
-// the scores (contexts beyond kSelThreads * 16 blocks).
-constexpr int kSelThreads = 256;   // = the histogram's bins
+// Steps a3 (and a4 when fused) of the split scan: one warp per pair ranks
+// the pair's block scores (written by scan_kernel just before), kSelWarps
+// pairs per CTA, so every pair of a launch is ranked at once and no block
+// barrier is needed.  A block's rank key is its order-preserving score bits
+// (larger is better); equal scores rank the lower block id first.  A radix
+// selection finds the K-th largest score key, most significant digit first:
+// the first digit starts at the highest bit on which the pair's keys differ
+// (the bits above it are shared by all of them), and each pass builds a
+// 256-bin histogram of the next (up to) 8 bits over the keys that still
+// match the prefix chosen so far and picks the bin that holds the K-th key,
+// until that bin holds exactly the keys still wanted.  Every key above the
+// final prefix, and every key in its bin, is in the top-K; if after the last
+// bit more keys share the K-th score than are wanted, the lowest block ids
+// among them are taken.  The winners are compacted in block-id order by
+// ballots, sorted by a warp bitonic network (score key above the
+// complemented block id) and written, and the same warp then runs the pair's
+// capped eviction.  Each lane holds NPT keys in registers (32 * NPT >=
+// NBmax); with NPT = 0 every pass re-reads the scores.
+constexpr int kSelWarps = 8;
 
 template <int KPL>
-__host__ __device__ inline size_t select_smem_bytes(int NBmax) {
-  const size_t rank = 1024 + 64 + 64 + static_cast<size_t>(32) * KPL * 8;  // hist, ctl, tie, list
+__host__ __device__ inline size_t select_warp_smem_bytes(int NBmax) {
+  const size_t rank = 1024 + static_cast<size_t>(32) * KPL * 8;  // histogram, winners
   const size_t adm = admit_warp_smem_bytes(NBmax);
-  return (rank > adm ? rank : adm) + 128;
+  return ((rank > adm ? rank : adm) + 15) & ~static_cast<size_t>(15);
 }
 
 template <int KPL, int NPT>
-__global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs a) {
+__global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs a) {
   constexpr int KP = 32 * KPL;
   constexpr int kRegs = NPT > 0 ? NPT : 1;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);            // [256]
-  int* ctl = reinterpret_cast<int*>(smem + 1024);                // bin, need, in bin, count
-  int* tie = reinterpret_cast<int*>(smem + 1024 + 64);           // per-warp tie counts [8]
-  uint64_t* list = reinterpret_cast<uint64_t*>(smem + 1024 + 128);  // [KP]
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int pair = a.pair0 + blockIdx.x;
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int local = blockIdx.x * kSelWarps + warp;
+  if (local >= a.pairs) return;  // warp-uniform; no block barrier follows
+  const int pair = a.pair0 + local;
+  uint8_t* mine = smem + warp * select_warp_smem_bytes<KPL>(a.NBmax);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(mine);           // [256]
+  uint64_t* list = reinterpret_cast<uint64_t*>(mine + 1024);    // [KP]
+  const unsigned lt = (1u << lane) - 1u;
   const int r = pair / a.Hkv;
   const int ctx = a.ctx_len[r];
   int nb = ctx > 0 ? (ctx + kBlock - 1) / kBlock : 0;
@@ -559,107 +562,115 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs 
   if constexpr (NPT > 0) {
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
-      const int e = j * kSelThreads + tid;
+      const int e = j * 32 + lane;
       ureg[j] = e < nb ? float_key(sp[e]) : 0u;
     }
   }
-  // f(score key, block id) for every block of this thread (e = j * T + tid),
-  // in increasing block id.
-  auto for_each_key = [&](auto&& f) {
+  // f(score key, block id, valid) for slot j of every lane, j ascending:
+  // together, the pair's blocks in increasing id (warp-uniform trip count).
+  auto for_each_slot = [&](auto&& f) {
     if constexpr (NPT > 0) {
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
-        const int e = j * kSelThreads + tid;
-        if (e < nb) f(ureg[j], e);
+        const int e = j * 32 + lane;
+        f(ureg[j], e, e < nb);
       }
     } else {
-      for (int e = tid; e < nb; e += kSelThreads) f(float_key(sp[e]), e);
+      for (int j = 0; j * 32 < nb; ++j) {
+        const int e = j * 32 + lane;
+        f(e < nb ? float_key(sp[e]) : 0u, e, e < nb);
+      }
     }
   };
 
-  // ---- radix selection over the score keys
-  uint32_t prefix = 0u, mask = 0u;
-  int need = min(a.K, nb);
-  int in_bin = need;
-  if (need > 0 && need < nb) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      hist[tid] = 0u;
-      __syncthreads();
-      for_each_key([&](uint32_t u, int) {
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
-      });
-      __syncthreads();
-      if (warp == 0) {
-        // Lane l owns bins 8l .. 8l+7; the keys in higher bins than a lane's
-        // are the suffix sum over the lanes above it.
-        uint32_t c[8];
-        uint32_t total = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          c[i] = hist[lane * 8 + i];
-          total += c[i];
-        }
-        uint32_t incl = total;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const uint32_t v = __shfl_down_sync(0xffffffffu, incl, off);
-          if (lane + off < 32) incl += v;
-        }
-        uint32_t cum = incl - total;
-#pragma unroll
-        for (int i = 7; i >= 0; --i) {
-          if (static_cast<int>(cum) < need && need <= static_cast<int>(cum + c[i])) {
-            ctl[0] = lane * 8 + i;
-            ctl[1] = need - static_cast<int>(cum);
-            ctl[2] = static_cast<int>(c[i]);
-          }
-          cum += c[i];
-        }
-      }
-      __syncthreads();
-      prefix |= static_cast<uint32_t>(ctl[0]) << shift;
-      mask |= 0xffu << shift;
-      need = ctl[1];
-      in_bin = ctl[2];
-      if (in_bin == need) break;   // the whole bin is wanted
+  // ---- the bits shared by every key, then radix passes below them
+  uint32_t any = 0u, all = ~0u;
+  for_each_slot([&](uint32_t u, int, bool v) {
+    if (v) {
+      any |= u;
+      all &= u;
     }
-  }
-  // ---- compaction of the winners: keys above the prefix, then those in its
-  // bin (all of them, or when more share the K-th score than are wanted, the
-  // lowest block ids: ranked in block-id order, one slice of kSelThreads
-  // blocks at a time)
-  const bool ties = in_bin > need;
-  if (tid == 0) ctl[3] = 0;
-  __syncthreads();
-  auto put = [&](uint32_t u, int e) {
-    const int pos = atomicAdd(&ctl[3], 1);
-    if (pos < KP)
-      list[pos] = (static_cast<uint64_t>(u) << 32) | static_cast<uint32_t>(~static_cast<uint32_t>(e));
-  };
-  for_each_key([&](uint32_t u, int e) {
-    if ((u & mask) > prefix || (!ties && (u & mask) == prefix)) put(u, e);
   });
-  if (ties) {
-    // Only reached when the K-th score is shared (mask covers every bit).
-    int taken = 0;
-    const int slices = (nb + kSelThreads - 1) / kSelThreads;
-    for (int j = 0; j < slices; ++j) {
-      const int e = j * kSelThreads + tid;
-      const bool eq = e < nb && float_key(sp[e]) == prefix;
-      const unsigned bal = __ballot_sync(0xffffffffu, eq);
-      __syncthreads();
-      if (lane == 0) tie[warp] = __popc(bal);
-      __syncthreads();
-      int before = taken;
-      for (int w = 0; w < warp; ++w) before += tie[w];
-      before += __popc(bal & ((1u << lane) - 1u));
-      if (eq && before < need) put(prefix, e);
-      for (int w = 0; w < kSelThreads / 32; ++w) taken += tie[w];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    any |= __shfl_xor_sync(0xffffffffu, any, off);
+    all &= __shfl_xor_sync(0xffffffffu, all, off);
+  }
+  const uint32_t diff = any ^ all;   // bits on which some keys differ
+  const int hb = diff ? 31 - __clz(diff) : -1;   // -1: every key equal
+  const uint32_t mask0 = hb < 0 ? ~0u : (hb >= 31 ? 0u : ~((2u << hb) - 1u));
+  uint32_t mask = mask0;   // bits above hb
+  uint32_t prefix = all & mask;
+  int need = min(a.K, nb);
+  int in_bin = nb;   // keys matching the prefix
+  if (need > 0 && need < nb) {
+    for (int hi = hb; hi >= 0 && in_bin != need; ) {
+      const int lo = hi >= 7 ? hi - 7 : 0;
+      const uint32_t dmask = (hi - lo == 31) ? ~0u : ((2u << (hi - lo)) - 1u);
+      for (int i = lane; i < 256; i += 32) hist[i] = 0u;
+      __syncwarp();
+      for_each_slot([&](uint32_t u, int, bool v) {
+        if (v && (u & mask) == prefix) atomicAdd(&hist[(u >> lo) & dmask], 1u);
+      });
+      __syncwarp();
+      // Lane l owns bins 8l .. 8l+7: keys in higher bins than a lane's are
+      // the suffix sum over the lanes above it.
+      uint32_t c[8];
+      uint32_t total = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        c[k] = hist[lane * 8 + k];
+        total += c[k];
+      }
+      uint32_t incl = total;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t x = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32) incl += x;
+      }
+      uint32_t cum = incl - total;
+      int bin = -1, left = 0, held = 0;
+#pragma unroll
+      for (int k = 7; k >= 0; --k) {
+        if (static_cast<int>(cum) < need && need <= static_cast<int>(cum + c[k])) {
+          bin = lane * 8 + k;
+          left = need - static_cast<int>(cum);
+          held = static_cast<int>(c[k]);
+        }
+        cum += c[k];
+      }
+      const int src = __ffs(__ballot_sync(0xffffffffu, bin >= 0)) - 1;
+      bin = __shfl_sync(0xffffffffu, bin, src);
+      need = __shfl_sync(0xffffffffu, left, src);
+      in_bin = __shfl_sync(0xffffffffu, held, src);
+      prefix |= static_cast<uint32_t>(bin) << lo;
+      mask |= dmask << lo;
+      __syncwarp();   // the histogram is read before the next pass clears it
+      hi = lo - 1;
     }
   }
-  __syncthreads();
-  if (warp != 0) return;
-  const int n = min(ctl[3], KP);
+  // ---- compaction in block-id order: keys above the prefix, and those in
+  // its bin (all of them, or the `need` lowest ids when more share the K-th
+  // score than are wanted)
+  const bool ties = in_bin > need;
+  int cnt = 0, tcnt = 0;
+  for_each_slot([&](uint32_t u, int e, bool v) {
+    const bool eq = v && (u & mask) == prefix;
+    const unsigned beq = __ballot_sync(0xffffffffu, eq);
+    const bool take = (v && (u & mask) > prefix) ||
+                      (eq && (!ties || tcnt + __popc(beq & lt) < need));
+    const unsigned bt = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int pos = cnt + __popc(bt & lt);
+      if (pos < KP)
+        list[pos] = (static_cast<uint64_t>(u) << 32) |
+                    static_cast<uint32_t>(~static_cast<uint32_t>(e));
+    }
+    cnt += __popc(bt);
+    tcnt += __popc(beq);
+  });
+  __syncwarp();
+  const int n = min(cnt, KP);
   uint64_t top[KPL];
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
@@ -668,9 +679,9 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs 
   }
   bitonic_sort<KPL>(top, true);
   __syncwarp();
-  // The histogram and list are no longer read: the region takes the
-  // admission's scratch.
-  AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(smem);
+  // The histogram and winners are in registers now: the warp's region takes
+  // the admission's scratch.
+  AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(mine);
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int e = i * 32 + lane;
@@ -686,7 +697,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(const ScoreArgs 
   }
   if (a.fuse_admit) {
     __syncwarp();
-    admit_warp<KPL>(a.admit, pair, S, reinterpret_cast<uint32_t*>(smem + sizeof(AdmitWarpSmem)));
+    admit_warp<KPL>(a.admit, pair, S, reinterpret_cast<uint32_t*>(mine + sizeof(AdmitWarpSmem)));
   }
 }
 
@@ -818,7 +829,7 @@ int split_scan_warps(int pairs) {
 
 template <int KPL, int NPT>
 cudaError_t launch_select_npt(const ScoreArgs& a, cudaStream_t s) {
-  const size_t smem = select_smem_bytes<KPL>(a.NBmax);
+  const size_t smem = kSelWarps * select_warp_smem_bytes<KPL>(a.NBmax);
   if (smem > 48 * 1024) {
     static int configured_device = -1;
     static size_t configured_smem = 0;
@@ -833,20 +844,21 @@ cudaError_t launch_select_npt(const ScoreArgs& a, cudaStream_t s) {
       configured_smem = smem;
     }
   }
-  select_kernel<KPL, NPT><<<a.pairs, kSelThreads, smem, s>>>(a);
+  select_kernel<KPL, NPT><<<(a.pairs + kSelWarps - 1) / kSelWarps, kSelWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-// Keys per thread: the smallest of 1, 2, 4, 8, 16 that holds NBmax blocks,
-// else 0 (scores re-read per pass).
+// Keys per lane: the smallest of 1, 2, 4, 8, 16, 32 that holds NBmax blocks,
+// else 0 (scores re-read for every pass).
 template <int KPL>
 cudaError_t launch_select_kpl(const ScoreArgs& a, cudaStream_t s) {
-  const int per = (a.NBmax + kSelThreads - 1) / kSelThreads;
+  const int per = (a.NBmax + 31) / 32;
   if (per <= 1) return launch_select_npt<KPL, 1>(a, s);
   if (per <= 2) return launch_select_npt<KPL, 2>(a, s);
   if (per <= 4) return launch_select_npt<KPL, 4>(a, s);
   if (per <= 8) return launch_select_npt<KPL, 8>(a, s);
   if (per <= 16) return launch_select_npt<KPL, 16>(a, s);
+  if (per <= 32) return launch_select_npt<KPL, 32>(a, s);
   return launch_select_npt<KPL, 0>(a, s);
 }
 
@@ -898,10 +910,10 @@ cudaError_t preload_score_kernels() {
       reinterpret_cast<const void*>(score_topk_kernel<8, 4>),
       reinterpret_cast<const void*>(scan_kernel<8>),
       reinterpret_cast<const void*>(scan_kernel<4>),
-      reinterpret_cast<const void*>(select_kernel<1, 1>),
-      reinterpret_cast<const void*>(select_kernel<4, 4>),
-      reinterpret_cast<const void*>(select_kernel<4, 16>),
-      reinterpret_cast<const void*>(select_kernel<8, 4>)};
+      reinterpret_cast<const void*>(select_kernel<1, 2>),
+      reinterpret_cast<const void*>(select_kernel<4, 32>),
+      reinterpret_cast<const void*>(select_kernel<4, 0>),
+      reinterpret_cast<const void*>(select_kernel<8, 32>)};
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncGetAttributes(&at, f);
     if (e != cudaSuccess) return e;
