@@ -529,7 +529,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
 // complemented block id) and written, and the same warp then runs the pair's
 // capped eviction.  Each lane holds NPT keys in registers (32 * NPT >=
 // NBmax); with NPT = 0 every pass re-reads the scores.
-constexpr int kSelWarps = 8;
+constexpr int kSelWarps = 4;   // pairs per CTA, fewer when a warp's scratch is large
 
 template <int KPL>
 __host__ __device__ inline size_t select_warp_smem_bytes(int NBmax) {
@@ -545,7 +545,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs 
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int local = blockIdx.x * kSelWarps + warp;
+  const int local = blockIdx.x * (blockDim.x >> 5) + warp;
   if (local >= a.pairs) return;  // warp-uniform; no block barrier follows
   const int pair = a.pair0 + local;
   uint8_t* mine = smem + warp * select_warp_smem_bytes<KPL>(a.NBmax);
@@ -829,7 +829,12 @@ int split_scan_warps(int pairs) {
 
 template <int KPL, int NPT>
 cudaError_t launch_select_npt(const ScoreArgs& a, cudaStream_t s) {
-  const size_t smem = kSelWarps * select_warp_smem_bytes<KPL>(a.NBmax);
+  // Warps per CTA: kSelWarps unless their scratch (which grows with NBmax
+  // through the admission's bitmaps) exceeds a CTA's shared memory.
+  const size_t per_warp = select_warp_smem_bytes<KPL>(a.NBmax);
+  int wpc = kSelWarps;
+  while (wpc > 1 && wpc * per_warp > 200 * 1024) --wpc;
+  const size_t smem = wpc * per_warp;
   if (smem > 48 * 1024) {
     static int configured_device = -1;
     static size_t configured_smem = 0;
@@ -844,7 +849,7 @@ cudaError_t launch_select_npt(const ScoreArgs& a, cudaStream_t s) {
       configured_smem = smem;
     }
   }
-  select_kernel<KPL, NPT><<<(a.pairs + kSelWarps - 1) / kSelWarps, kSelWarps * 32, smem, s>>>(a);
+  select_kernel<KPL, NPT><<<(a.pairs + wpc - 1) / wpc, wpc * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
