@@ -554,6 +554,16 @@ OASIS_API int oasis_remote_stats(oasis_ctx* ctx, int layer, int64_t* units,
                                  int64_t* transfers, double* seconds,
                                  int64_t* bad_entries);
 
+/* Time limit of the kernels' bounded barrier waits, in GPU clock cycles,
+ * for the launches that follow (attention, scan).  cycles <= 0 restores the
+ * default (2e9 cycles, about a second).  A wait that runs out sets
+ * OASIS_DEVERR_TIMEOUT (reported by oasis_sync) and its kernel ends early
+ * with undefined outputs; copies the kernel has already issued are still
+ * waited for with the default limit before it exits.  Nothing of the pages
+ * corresponds to this call: it lets a test take the timeout path on purpose
+ * (a limit of a few cycles runs out before any copy lands). */
+OASIS_API int oasis_set_wait_limit(oasis_ctx* ctx, long long cycles);
+
 /* Kernel timing: when enabled, the step calls (oasis_step, oasis_step_stall)
  * and the stage calls record CUDA events around each of their kernels on the
  * stream that launches it. */

@@ -467,6 +467,7 @@ struct oasis_ctx {
   int D = 1;  // draft queries per step
   int groups = 1;  // request groups the side work is pipelined in
   float scale_log2 = 0.f;
+  long long wait_limit = kWaitLimitCycles;  // oasis_set_wait_limit
   std::vector<LayerState> layers;
   int32_t* ctx_len = nullptr;
   uint8_t* ws = nullptr;
@@ -581,6 +582,7 @@ int run_attention(oasis_ctx* ctx, int layer, int step, const void* q, const void
   a.NBmax = ctx->cfg.max_blocks;
   a.scale_log2 = ctx->scale_log2;
   a.out_fp32 = ctx->cfg.out_fp32;
+  a.wait_limit = ctx->wait_limit;
   cudaEvent_t* pe = ctx->prof_begin(0, s);
   cudaError_t e = launch_attention(a, &L.pool_map, s);
   ctx->prof_end(pe, s);
@@ -645,6 +647,7 @@ ScoreArgs score_args(oasis_ctx* ctx, int layer, int step, const void* x, int pla
   a.pair0 = 0;
   a.pairs = a.R * a.Hkv;
   a.scores_ws = ctx->layers[layer].scan_scores[step & 1];
+  a.wait_limit = ctx->wait_limit;
   return a;
 }
 
@@ -1253,6 +1256,7 @@ OASIS_API int oasis_dense_attn(oasis_ctx* ctx, const void* kv_dense, int table, 
   a.scale_log2 = ctx->scale_log2;
   a.out_fp32 = ctx->cfg.out_fp32;
   a.dense = 1;
+  a.wait_limit = ctx->wait_limit;
   return ctx->cuda(launch_attention(a, &map, static_cast<cudaStream_t>(stream)),
                    "dense attention launch");
 }
@@ -1957,6 +1961,12 @@ OASIS_API int oasis_remote_stats(oasis_ctx* ctx, int layer, int64_t* units, int6
   if (transfers) *transfers = S.transfers.load();
   if (seconds) *seconds = static_cast<double>(S.nanos.load()) * 1e-9;
   if (bad_entries) *bad_entries = S.bad.load();
+  return OASIS_OK;
+}
+
+OASIS_API int oasis_set_wait_limit(oasis_ctx* ctx, long long cycles) {
+  if (!ctx) return OASIS_EINVAL;
+  ctx->wait_limit = cycles > 0 ? cycles : kWaitLimitCycles;
   return OASIS_OK;
 }
 

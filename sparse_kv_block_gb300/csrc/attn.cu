@@ -212,7 +212,8 @@ __global__ void __maxnreg__(kNT == 2 ? 144 : 96)
   bool failed = false;
   for (; k < my_count; ++k) {
     const int st = k % kStages;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(&my_bars[st], (k / kStages) & 1));
+    const bool ok =
+        __all_sync(0xffffffffu, mbar_wait(&my_bars[st], (k / kStages) & 1, a.wait_limit));
     if (!ok) {
       failed = true;
       break;

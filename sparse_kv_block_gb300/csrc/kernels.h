@@ -24,6 +24,7 @@ struct AttnArgs {
   // dense = 1: no resident table; every block b < ceil(ctx_len / B) of a pair
   // is read from unit pair * NBmax + b of a dense [R][Hkv][NBmax] cache.
   int dense;
+  long long wait_limit;  // clock cycles a barrier wait may take (drains excepted)
 };
 
 // Pairs (request, KV head) are flattened as pair = r * Hkv + h; a launch
@@ -63,6 +64,7 @@ struct ScoreArgs {
   // scores_ws[pair][b] and a separate kernel ranks them (and admits, when
   // fused); null: one kernel ranks while it scans (no scratch).
   float* scores_ws;      // [R][Hkv][NBmax]
+  long long wait_limit;  // clock cycles a barrier wait may take (drains excepted)
 };
 
 // Copies 8 KiB units host -> pool.  Item i of pair p = (r, h) reads block

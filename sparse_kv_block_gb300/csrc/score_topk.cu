@@ -120,14 +120,14 @@ __device__ __forceinline__ float reduce4(const float (&v)[4], int lane) {
 // copies before returning either way.
 template <int kChunk>
 __device__ bool produce_pair(const uint8_t* src, int nb, uint8_t* ring, uint64_t* full,
-                             uint64_t* empty) {
+                             uint64_t* empty, long long limit) {
   constexpr int kChunkBytes = kChunk * kSummBytes;
   const int nchunks = (nb + kChunk - 1) / kChunk;
   int c = 0;
   bool ok = true;
   for (; c < nchunks && ok; ++c) {
     const int st = c % kStages;
-    if (c >= kStages) ok = mbar_wait(&empty[st], ((c / kStages) - 1) & 1);
+    if (c >= kStages) ok = mbar_wait(&empty[st], ((c / kStages) - 1) & 1, limit);
     if (!ok) break;
     const int nblk = min(kChunk, nb - c * kChunk);
     const uint32_t bytes = static_cast<uint32_t>(nblk) * kSummBytes;
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : (KPL <= 4 ? 4 : 3
       bool ok = true;
       for (; c < nchunks && ok; ++c) {
         const int st = c % kStages;
-        if (c >= kStages) ok = mbar_wait(&empty[st], ((c / kStages) - 1) & 1);
+        if (c >= kStages) ok = mbar_wait(&empty[st], ((c / kStages) - 1) & 1, a.wait_limit);
         if (!ok) break;
         const int nblk = min(kChunk, nb - c * kChunk);
         const uint32_t bytes = static_cast<uint32_t>(nblk) * kSummBytes;
@@ -304,7 +304,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : (KPL <= 4 ? 4 : 3
     bool ok = true;
     for (int c = 0; c < nchunks; ++c) {
       const int st = c % kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (c / kStages) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (c / kStages) & 1, a.wait_limit));
       if (!ok) break;
       const int nblk = min(kChunk, nb - c * kChunk);
       const uint8_t* stage = ring + st * kChunkBytes;
@@ -486,7 +486,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
   if (warp == CW) {
     const uint8_t* src = static_cast<const uint8_t*>(a.summ) +
                          static_cast<size_t>(pair) * a.NBmax * kSummBytes;
-    if (lane == 0 && !produce_pair<kChunk>(src, nb, ring, full, empty))
+    if (lane == 0 && !produce_pair<kChunk>(src, nb, ring, full, empty, a.wait_limit))
       raise_error(a.err, kErrTimeout);
     return;  // no block barrier follows
   }
@@ -497,7 +497,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
   const int q = ((lane >> 4) << 1) | ((lane >> 3) & 1);
   for (int c = 0; c < nchunks; ++c) {
     const int st = c % kStages;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / kStages) & 1))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (c / kStages) & 1, a.wait_limit))) {
       if (lane == 0) raise_error(a.err, kErrTimeout);
       break;
     }

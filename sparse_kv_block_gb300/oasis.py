@@ -111,6 +111,7 @@ EXPORTS = {
     "oasis_stall_lists": (c_int, [_P, c_int, c_int, POINTER(c_void_p), POINTER(c_void_p),
                                   POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
                                   POINTER(c_void_p)]),
+    "oasis_set_wait_limit": (c_int, [_P, ctypes.c_longlong]),
     "oasis_profile_enable": (c_int, [_P, c_int]),
     "oasis_profile_read_n": (c_int, [_P, c_int, POINTER(c_double), POINTER(c_int64),
                                      POINTER(c_double)]),
@@ -446,6 +447,11 @@ class Oasis:
         self._check(lib().oasis_remote_stats(self.ctx, layer, ctypes.byref(u), ctypes.byref(n),
                                              ctypes.byref(sec), ctypes.byref(b)))
         return dict(units=u.value, transfers=n.value, seconds=sec.value, bad_entries=b.value)
+
+    def oasis_set_wait_limit(self, cycles: int) -> None:
+        """Barrier-wait limit of the following launches in clock cycles
+        (<= 0: the default, about a second)."""
+        self._check(lib().oasis_set_wait_limit(self.ctx, int(cycles)))
 
     def oasis_profile_enable(self, enable: bool = True) -> None:
         self._check(lib().oasis_profile_enable(self.ctx, 1 if enable else 0))
