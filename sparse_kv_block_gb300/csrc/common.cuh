@@ -74,12 +74,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of phase `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are polled with test_wait: try_wait may itself suspend
+// the thread for a while, long enough for a copy in flight to land.
+constexpr long long kShortWaitCycles = 1LL << 20;
+
 // Wait for phase `parity` of `bar`; false if it did not complete within
 // `limit` clock cycles.  Waits for copies already issued (drains) keep the
 // default; a kernel's other waits take the launch's limit, which a caller
 // may shorten to make them run out (the timeout path's test).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           long long limit = kWaitLimitCycles) {
+  if (limit < kShortWaitCycles) {
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity)) {
+      if (clock64() - t0 > limit) return false;
+    }
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
