@@ -419,6 +419,13 @@ def kernel_rooflines(shape, ms_sum, counts, off_sum, steps, link_bytes, h2d_gbs,
     return per_kernel, dominant
 
 
+def spread(per_step_ms) -> dict:
+    """min / median / max of per-step times (ms)."""
+    v = sorted(per_step_ms)
+    return {"min": round(v[0], 4), "median": round(v[len(v) // 2], 4), "max": round(v[-1], 4),
+            "steps": len(v)}
+
+
 def run_oasis(args, ws, rank, local):
     from sparse_kv_block_gb300.oasis import PROFILE_KINDS, lib
     lib()  # fail loudly if the CUDA library is missing
@@ -753,20 +760,23 @@ def run_oasis_layers(args, ws, rank, local):
         torch.cuda.synchronize(dev)
         per_step = sorted(a.elapsed_time(b) for a, b in ev)
         ms = sum(per_step)
-        step_spread = {"min": round(per_step[0], 3),
-                       "median": round(per_step[len(per_step) // 2], 3),
-                       "max": round(per_step[-1], 3)}
+        step_spread = spread(per_step)
     else:
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         e0.record(main)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             one_step()
+            marks[i].record(main)   # after the step's last attention (steps overlap)
         for l in range(L):
             eng.oasis_join(l, main)
         e1.record(main)
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1)
+        gaps = [e0.elapsed_time(marks[0])] + [marks[i - 1].elapsed_time(marks[i])
+                                               for i in range(1, args.steps)]
+        step_spread = spread(gaps)
     barrier(ws)
     ms_sum, counts, off_sum = eng.oasis_profile_read(len(PROFILE_KINDS))
     eng.oasis_profile_enable(False)
@@ -1192,6 +1202,8 @@ def run_cap_sweep(args, ws, rank, local):
         return sc.topk(min(base.K, base.NBmax), dim=-1).indices
 
     results = []
+    clocks = ClockSampler(local)
+    clocks.start()
     for cap in (0.01, 0.05, 0.25, 1.0):
         shape = dataclasses.replace(base, fetch_ratio=cap)
         cfg = make_config(shape.R, shape.NBmax, shape.Hq, shape.Hkv, shape.K, cap,
@@ -1237,18 +1249,23 @@ def run_cap_sweep(args, ws, rank, local):
         torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         e0.record(main)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             eng.oasis_step(0, step, q[step % nq], qd[step % nq], out, outd, main)
+            marks[i].record(main)
             step += 1
         eng.oasis_join(0, main)
         e1.record(main)
         torch.cuda.synchronize(dev)
         eng.oasis_sync()
         ms = e0.elapsed_time(e1) / args.steps
+        gaps = [e0.elapsed_time(marks[0])] + [marks[i - 1].elapsed_time(marks[i])
+                                               for i in range(1, args.steps)]
         results.append({"fetch_ratio": cap, "C": shape.C,
                         "layer_steps_per_s": round(1e3 / ms, 1),
                         "ms_per_step": round(ms, 4),
+                        "step_ms_spread": spread(gaps),
                         "h2d_GB_per_layer_step": round(sum(adm) / len(adm) * UNIT_BYTES / 1e9, 5),
                         "admitted_units_per_step": sum(adm) / len(adm),
                         "topk_agreement_draft_vs_next": round(sum(agree) / len(agree), 5),
@@ -1259,9 +1276,12 @@ def run_cap_sweep(args, ws, rank, local):
         eng.close()
         del eng
         torch.cuda.empty_cache()
+    clk = clocks.stop()
     if rank == 0:
-        print(json.dumps({"cap_sweep": results, "workload": workload_desc(base),
-                          "steps": args.steps}), flush=True)
+        print(json.dumps({"mode": "cap-sweep", "metric": METRIC, "unit": UNIT,
+                          "cap_sweep": results, "workload": workload_desc(base),
+                          "steps": args.steps, "warmup": args.warmup, "clocks": clk,
+                          "data": "synthetic"}), flush=True)
 
 
 def main():
