@@ -183,6 +183,18 @@ def pinned_device_alias(t: torch.Tensor, dev) -> torch.Tensor:
     return flat.view(torch.bfloat16).view(t.shape)
 
 
+def pretouch_host(host: torch.Tensor, dev) -> None:
+    """Read the whole pinned host store once through its device mapping (a
+    sequential GPU read, untimed), as a store in long use would have been."""
+    alias = pinned_device_alias(host, dev)
+    flat = alias.view(-1)
+    step = 1 << 28
+    acc = torch.zeros((), dtype=torch.float32, device=dev)
+    for i in range(0, flat.numel(), step):
+        acc += flat[i:i + step].float().sum()
+    torch.cuda.synchronize(dev)
+
+
 def warm_start(eng, shape, q0, dev):
     """Resident set = the summary-ranked top-K of the first query (warm cache)."""
     topk = torch.empty((shape.R, shape.Hkv, shape.K), dtype=torch.int32, device=dev)
@@ -438,6 +450,8 @@ def run_oasis(args, ws, rank, local):
     eng, lens, host = build_layer(shape, args.seed + rank, dev, args.side_groups, args.schedule)
     q, qd = workload.queries(shape, args.seed + rank, 0, nq, device=dev)
     warm_start(eng, shape, q[0], dev)
+    if args.host_pretouch:
+        pretouch_host(host, dev)
     odt = torch.bfloat16
     out = torch.empty((shape.R, shape.Hq, 128), dtype=odt, device=dev)
     outd = torch.empty_like(out)
@@ -1306,6 +1320,8 @@ def main():
     ap.add_argument("--queries", type=int, default=64, help="distinct query steps, cycled")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-pretouch", action="store_true",
+                    help="read the host store once through its device mapping before timing")
     ap.add_argument("--side-groups", type=int, default=0,
                     help="request groups of the side work (0 = library default)")
     ap.add_argument("--schedule", type=int, default=3,

@@ -10,6 +10,7 @@ the timeout, that the context stays usable, and that steps issued with the
 default limit afterwards (for the fused step: after resuming from the
 caller's saved state) match the oracle again."""
 import ctypes
+import dataclasses
 
 import numpy as np
 import pytest
@@ -41,7 +42,11 @@ def sync_bits(eng):
 
 
 def test_stage_calls_time_out_then_recover(dev):
-    L = H.make_layer(TINY, seed=50, steps=3, out_fp32=True)
+    # 512 blocks per request: the scan streams 16 chunks through its 2-stage
+    # ring, so its producer must wait for consumed stages (with two chunks
+    # both copies are issued at once and land before any wait).
+    sh = dataclasses.replace(TINY, ctx=512 * 16)
+    L = H.make_layer(sh, seed=50, steps=3, out_fp32=True)
     eng, sh = L.eng, L.shape
     out = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
     outd = torch.empty_like(out)
