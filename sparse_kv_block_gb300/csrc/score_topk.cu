@@ -528,12 +528,24 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
 // ballots, sorted by a warp bitonic network (score key above the
 // complemented block id) and written, and the same warp then runs the pair's
 // capped eviction.  Each lane holds NPT keys in registers (32 * NPT >=
-// NBmax); with NPT = 0 every pass re-reads the scores.
+// NBmax); with NPT = 0 every pass reads the scores again, from a copy in the
+// warp's shared memory up to kSelStageMax blocks, else from global memory.
 constexpr int kSelWarps = 4;   // pairs per CTA, fewer when a warp's scratch is large
+
+// Contexts longer than 32 keys per lane stage the pair's scores in the
+// warp's shared memory up to this many blocks (32 KiB), else re-read them.
+constexpr int kSelStageMax = 8192;
+
+template <int KPL>
+__host__ __device__ inline bool select_stages(int NBmax) {
+  return NBmax > 32 * 32 && NBmax <= kSelStageMax;
+}
 
 template <int KPL>
 __host__ __device__ inline size_t select_warp_smem_bytes(int NBmax) {
-  const size_t rank = 1024 + static_cast<size_t>(32) * KPL * 8;  // histogram, winners
+  // histogram, winners, staged scores
+  const size_t rank = 1024 + static_cast<size_t>(32) * KPL * 8 +
+                      (select_stages<KPL>(NBmax) ? static_cast<size_t>(NBmax) * 4 : 0);
   const size_t adm = admit_warp_smem_bytes(NBmax);
   return ((rank > adm ? rank : adm) + 15) & ~static_cast<size_t>(15);
 }
@@ -565,6 +577,13 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs 
       const int e = j * 32 + lane;
       ureg[j] = e < nb ? float_key(sp[e]) : 0u;
     }
+  } else if (select_stages<KPL>(a.NBmax)) {
+    // The pair's scores into this warp's shared memory once; every pass then
+    // reads them there.
+    float* staged = reinterpret_cast<float*>(mine + 1024 + KP * 8);
+    for (int e = lane; e < nb; e += 32) staged[e] = sp[e];
+    __syncwarp();
+    sp = staged;
   }
   // f(score key, block id, valid) for slot j of every lane, j ascending:
   // together, the pair's blocks in increasing id (warp-uniform trip count).
