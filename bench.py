@@ -252,70 +252,70 @@ def oracle_rate(shape, host, lens, q, qd, budget_s: float, threads: int = 1):
 
 
 def run_reference(args, ws, rank):
+    """The reference arm: the CPU oracle as it stands (fp64, sequential per
+    (request, KV head) pair) on this machine's host cores, on the same workload,
+    metric and config as the CUDA arm.  Every step is a whole layer-step:
+    all of the layer's pairs, split over one host thread per core (the
+    oracle's C functions release the interpreter lock), timed from the first
+    pair's start to the last pair's end.  Nothing is extrapolated."""
     if rank != 0:
         return
+    import concurrent.futures
+    import oracle
     shape = get_shape(args)
-    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    cuda = torch.cuda.is_available()
     lens = workload.ctx_lens(shape)
     host = torch.empty((shape.R, shape.Hkv, shape.NBmax, 2, 16, 128), dtype=torch.bfloat16,
-                       pin_memory=torch.cuda.is_available())
-    workload.host_kv(shape, args.seed, 0, lens, device=dev if dev.type == "cuda" else "cpu",
-                     out=host)
-    q, qd = workload.queries(shape, args.seed, 0, 2, device=dev if dev.type == "cuda" else "cpu")
-    import oracle
-    # A pool of sampled requests prepared once (untimed: their summaries and
-    # oracle state); each step then times whole-request oracle steps, one
-    # request at a time, until the step's share of a ~90 s budget is spent.
+                       pin_memory=cuda)
+    gen = torch.device("cuda", 0) if cuda else "cpu"
+    workload.host_kv(shape, args.seed, 0, lens, device=gen, out=host)
+    nq = min(args.queries, 8)
+    q, qd = workload.queries(shape, args.seed, 0, nq, device=gen)
+    qb = [np.ascontiguousarray(workload.bf16_bits(q[i].cpu().contiguous())) for i in range(nq)]
+    qdb = [np.ascontiguousarray(workload.bf16_bits(qd[i].cpu().contiguous())) for i in range(nq)]
     hb = workload.bf16_bits(host)
+    summ = oracle.summary_build(hb, lens)
     res0 = workload.initial_resident(shape, args.seed, 0, lens)
-    pool = []
-    for r in range(min(4, shape.R)):
-        sub = np.ascontiguousarray(hb[r:r + 1])
-        sl = np.ascontiguousarray(lens[r:r + 1])
-        orc = oracle.LayerOracle(sub, oracle.summary_build(sub, sl), sl, res0[r:r + 1], shape.K,
-                                 shape.C, [(0, h) for h in range(shape.Hkv)])
-        qb = [np.ascontiguousarray(workload.bf16_bits(x[r:r + 1].cpu().contiguous()))
-              for x in (q[0], qd[0], q[1], qd[1])]
-        pool.append((orc, qb))
-    per_step_budget = max(0.02, min(2.0, 90.0 / max(1, args.steps + args.warmup)))
-    state = {"i": 0, "t": 0}
+    cores = os.cpu_count() or 1
+    pairs = [(r, h) for r in range(shape.R) for h in range(shape.Hkv)]
+    parts = [pairs[k::cores] for k in range(cores)]
+    orcs = [oracle.LayerOracle(hb, summ, lens, res0, shape.K, shape.C, p) for p in parts if p]
+    state = {"t": 0}
 
-    def one_step():
-        pairs, sec = 0, 0.0
-        while sec < per_step_budget:
-            orc, qb = pool[state["i"] % len(pool)]
-            k = state["t"] & 1
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(orcs)) as ex:
+        def one_step():
+            t = state["t"]
             t0 = time.perf_counter()
-            orc.step(qb[2 * k], qb[2 * k + 1], state["t"])
-            sec += time.perf_counter() - t0
-            pairs += shape.Hkv
-            state["i"] += 1
-            if state["i"] % len(pool) == 0:
-                state["t"] += 1
-        return pairs, sec
+            list(ex.map(lambda o: o.step(qb[t % nq], qdb[t % nq], t), orcs))
+            state["t"] += 1
+            return time.perf_counter() - t0
 
-    for _ in range(args.warmup):
-        one_step()
-    total_pairs, total_s = 0, 0.0
-    for _ in range(args.steps):
-        p, sec = one_step()
-        total_pairs += p
-        total_s += sec
-    value = (total_pairs / total_s) / (shape.R * shape.Hkv)
-    sample = (f"per step: oracle_step (fp64, single-threaded) on whole requests (all "
-              f"{shape.Hkv} KV heads) of the {shape.name} layer until >= {per_step_budget:.3f} s; "
-              f"{total_pairs} pair-steps in {total_s:.1f} s over {args.steps} steps, "
-              f"extrapolated to {shape.R * shape.Hkv} pairs per layer-step")
+        for _ in range(args.warmup):
+            one_step()
+        secs = [one_step() for _ in range(args.steps)]
+    total = sum(secs)
+    value = args.steps / total
+    sample = (f"whole layer-steps: oracle_step (attention + summary score + top-K + capped "
+              f"eviction, fp64) on all {len(pairs)} (request, KV head) pairs of the "
+              f"{shape.name} layer per step, split over {len(orcs)} host threads; "
+              f"{args.steps} steps timed in {total:.1f} s")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(shape)},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(shape, ws), "tokens_per_s": round(value * shape.R, 3),
+            "step_ms_spread": spread([1000.0 * x for x in secs]),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(orcs), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def config_dict(shape, ws) -> dict:
+    """The `config` of both arms' lines: what was run, no results."""
+    return {"workload": workload_desc(shape), "parallelism": f"replicas{ws}",
+            "l2": "inputs larger than L2: 1.5 GiB of pool + summaries read per step"}
 
 
 def get_shape(args):
@@ -598,9 +598,7 @@ def run_oasis(args, ws, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": workload_desc(shape), "parallelism": f"replicas{ws}",
-                       "l2": "inputs larger than L2: 1.5 GiB of pool + summaries read per step",
-                       "tokens_per_s": round(value * shape.R, 1)},
+            "config": config_dict(shape, ws), "tokens_per_s": round(value * shape.R, 1),
             "roofline": roofline, "roofline_hbm": per_kernel.get("attention"),
             "kernels": per_kernel,
             "host_link": {"h2d_memcpy_gbs": round(h2d_gbs, 1),
