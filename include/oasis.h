@@ -299,7 +299,10 @@ OASIS_API int oasis_admit_evict(oasis_ctx* ctx, int layer, int step,
  * driving the decode loop).  Outputs and table updates are those of the two
  * calls.  The scratch's device address is looked up once per device, with
  * that device current, on the first call: make that first call before any
- * stream capture.  Nothing in the scratch needs to start at zero.  The
+ * stream capture.  The address is kept for the life of the process: after
+ * cudaDeviceReset (or anything else that destroys the device's primary
+ * context) it is stale, so do not call this entry point again in that
+ * process.  Nothing in the scratch needs to start at zero.  The
  * scratch is shared by every context and layer in the process: two calls
  * whose work may overlap on the device (other streams, layers or contexts
  * without ordering between them) race on it, so order them (one stream, or
