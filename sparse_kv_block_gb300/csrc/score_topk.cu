@@ -511,10 +511,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
   }
 }
 
-// Steps a3 (and a4 when fused) of the split scan: one warp per pair ranks
-// the pair's block scores (written by scan_kernel just before), kSelWarps
-// pairs per CTA, so every pair of a launch is ranked at once and no block
-// barrier is needed.  A block's rank key is its order-preserving score bits
+// Steps a3 (and a4 when fused) of the split scan: one CTA of kSelThreads
+// threads per pair ranks the pair's block scores (written by scan_kernel
+// just before).  A block's rank key is its order-preserving score bits
 // (larger is better); equal scores rank the lower block id first.  A radix
 // selection finds the K-th largest score key, most significant digit first:
 // the first digit starts at the highest bit on which the pair's keys differ
@@ -524,46 +523,45 @@ __global__ void __launch_bounds__((CW + 1) * 32, CW == 4 ? 0 : 4)
 // until that bin holds exactly the keys still wanted.  Every key above the
 // final prefix, and every key in its bin, is in the top-K; if after the last
 // bit more keys share the K-th score than are wanted, the lowest block ids
-// among them are taken.  The winners are compacted in block-id order by
-// ballots, sorted by a warp bitonic network (score key above the
-// complemented block id) and written, and the same warp then runs the pair's
-// capped eviction.  Each lane holds NPT keys in registers (32 * NPT >=
-// NBmax); with NPT = 0 every pass reads the scores again, from a copy in the
-// warp's shared memory up to kSelStageMax blocks, else from global memory.
-constexpr int kSelWarps = 4;   // pairs per CTA, fewer when a warp's scratch is large
-
-// Contexts longer than 32 keys per lane stage the pair's scores in the
-// warp's shared memory up to this many blocks (32 KiB), else re-read them.
+// among them are taken (ranked in block-id order).  The winners (score key
+// above the complemented block id) are sorted by a bitonic network spread
+// over the CTA's warps (shuffles within a warp, shared memory across warps)
+// and written, and warp 0 then runs the pair's capped eviction.  Each thread
+// holds NPT keys in registers (kSelThreads * NPT >= NBmax); with NPT = 0
+// every pass reads the scores again, from a copy in shared memory up to
+// kSelStageMax blocks, else from global memory.
+constexpr int kSelThreads = 128;
+constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelStageMax = 8192;
 
-template <int KPL>
 __host__ __device__ inline bool select_stages(int NBmax) {
-  return NBmax > 32 * 32 && NBmax <= kSelStageMax;
+  return NBmax > kSelThreads * 8 && NBmax <= kSelStageMax;
 }
 
 template <int KPL>
-__host__ __device__ inline size_t select_warp_smem_bytes(int NBmax) {
-  // histogram, winners, staged scores
-  const size_t rank = 1024 + static_cast<size_t>(32) * KPL * 8 +
-                      (select_stages<KPL>(NBmax) ? static_cast<size_t>(NBmax) * 4 : 0);
+__host__ __device__ inline size_t select_smem_bytes(int NBmax) {
+  // histogram, control words, winners, staged scores; the admission's
+  // scratch reuses the region once the winners are sorted
+  const size_t rank = 1024 + 64 + static_cast<size_t>(32) * KPL * 8 +
+                      (select_stages(NBmax) ? static_cast<size_t>(NBmax) * 4 : 0);
   const size_t adm = admit_warp_smem_bytes(NBmax);
   return ((rank > adm ? rank : adm) + 15) & ~static_cast<size_t>(15);
 }
 
 template <int KPL, int NPT>
-__global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs a) {
-  constexpr int KP = 32 * KPL;
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const ScoreArgs a) {
+  constexpr int P = 32 * KPL;                        // sorted list length (>= K)
+  constexpr int kHeld = P > kSelThreads ? P / kSelThreads : 1;
   constexpr int kRegs = NPT > 0 ? NPT : 1;
   extern __shared__ __align__(16) uint8_t smem[];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int local = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (local >= a.pairs) return;  // warp-uniform; no block barrier follows
-  const int pair = a.pair0 + local;
-  uint8_t* mine = smem + warp * select_warp_smem_bytes<KPL>(a.NBmax);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(mine);           // [256]
-  uint64_t* list = reinterpret_cast<uint64_t*>(mine + 1024);    // [KP]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem);           // [256]
+  int* ctl = reinterpret_cast<int*>(smem + 1024);               // [16]
+  uint64_t* buf = reinterpret_cast<uint64_t*>(smem + 1024 + 64);  // [P]
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
   const unsigned lt = (1u << lane) - 1u;
+  const int pair = a.pair0 + blockIdx.x;
   const int r = pair / a.Hkv;
   const int ctx = a.ctx_len[r];
   int nb = ctx > 0 ? (ctx + kBlock - 1) / kBlock : 0;
@@ -574,35 +572,34 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs 
   if constexpr (NPT > 0) {
 #pragma unroll
     for (int j = 0; j < NPT; ++j) {
-      const int e = j * 32 + lane;
+      const int e = j * kSelThreads + tid;
       ureg[j] = e < nb ? float_key(sp[e]) : 0u;
     }
-  } else if (select_stages<KPL>(a.NBmax)) {
-    // The pair's scores into this warp's shared memory once; every pass then
-    // reads them there.
-    float* staged = reinterpret_cast<float*>(mine + 1024 + KP * 8);
-    for (int e = lane; e < nb; e += 32) staged[e] = sp[e];
-    __syncwarp();
+  } else if (select_stages(a.NBmax)) {
+    float* staged = reinterpret_cast<float*>(smem + 1024 + 64 + P * 8);
+    for (int e = tid; e < nb; e += kSelThreads) staged[e] = sp[e];
+    __syncthreads();
     sp = staged;
   }
-  // f(score key, block id, valid) for slot j of every lane, j ascending:
-  // together, the pair's blocks in increasing id (warp-uniform trip count).
+  // f(score key, block id, valid) for slot j of every thread, j ascending:
+  // the same trip count in every thread (barriers may sit inside f).
+  const int nslots = (nb + kSelThreads - 1) / kSelThreads;
   auto for_each_slot = [&](auto&& f) {
     if constexpr (NPT > 0) {
 #pragma unroll
       for (int j = 0; j < NPT; ++j) {
-        const int e = j * 32 + lane;
+        const int e = j * kSelThreads + tid;
         f(ureg[j], e, e < nb);
       }
     } else {
-      for (int j = 0; j * 32 < nb; ++j) {
-        const int e = j * 32 + lane;
+      for (int j = 0; j < nslots; ++j) {
+        const int e = j * kSelThreads + tid;
         f(e < nb ? float_key(sp[e]) : 0u, e, e < nb);
       }
     }
   };
 
-  // ---- the bits shared by every key, then radix passes below them
+  // ---- the bits every key shares, then radix passes below them
   uint32_t any = 0u, all = ~0u;
   for_each_slot([&](uint32_t u, int, bool v) {
     if (v) {
@@ -615,97 +612,158 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs 
     any |= __shfl_xor_sync(0xffffffffu, any, off);
     all &= __shfl_xor_sync(0xffffffffu, all, off);
   }
-  const uint32_t diff = any ^ all;   // bits on which some keys differ
+  if (lane == 0) {
+    ctl[8 + warp] = static_cast<int>(any);
+    ctl[12 + warp] = static_cast<int>(all);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < kSelWarps; ++w) {
+    any |= static_cast<uint32_t>(ctl[8 + w]);
+    all &= static_cast<uint32_t>(ctl[12 + w]);
+  }
+  const uint32_t diff = any ^ all;
   const int hb = diff ? 31 - __clz(diff) : -1;   // -1: every key equal
-  const uint32_t mask0 = hb < 0 ? ~0u : (hb >= 31 ? 0u : ~((2u << hb) - 1u));
-  uint32_t mask = mask0;   // bits above hb
+  uint32_t mask = hb < 0 ? ~0u : (hb >= 31 ? 0u : ~((2u << hb) - 1u));
   uint32_t prefix = all & mask;
   int need = min(a.K, nb);
   int in_bin = nb;   // keys matching the prefix
   if (need > 0 && need < nb) {
-    for (int hi = hb; hi >= 0 && in_bin != need; ) {
+    for (int hi = hb; hi >= 0 && in_bin != need;) {
       const int lo = hi >= 7 ? hi - 7 : 0;
-      const uint32_t dmask = (hi - lo == 31) ? ~0u : ((2u << (hi - lo)) - 1u);
-      for (int i = lane; i < 256; i += 32) hist[i] = 0u;
-      __syncwarp();
+      const uint32_t dmask = (2u << (hi - lo)) - 1u;
+      hist[tid] = 0u;
+      hist[tid + kSelThreads] = 0u;
+      __syncthreads();
       for_each_slot([&](uint32_t u, int, bool v) {
         if (v && (u & mask) == prefix) atomicAdd(&hist[(u >> lo) & dmask], 1u);
       });
-      __syncwarp();
-      // Lane l owns bins 8l .. 8l+7: keys in higher bins than a lane's are
-      // the suffix sum over the lanes above it.
-      uint32_t c[8];
-      uint32_t total = 0;
+      __syncthreads();
+      if (warp == 0) {
+        // Lane l owns bins 8l .. 8l+7: keys in higher bins than a lane's are
+        // the suffix sum over the lanes above it.
+        uint32_t c[8];
+        uint32_t total = 0;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        c[k] = hist[lane * 8 + k];
-        total += c[k];
-      }
-      uint32_t incl = total;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t x = __shfl_down_sync(0xffffffffu, incl, off);
-        if (lane + off < 32) incl += x;
-      }
-      uint32_t cum = incl - total;
-      int bin = -1, left = 0, held = 0;
-#pragma unroll
-      for (int k = 7; k >= 0; --k) {
-        if (static_cast<int>(cum) < need && need <= static_cast<int>(cum + c[k])) {
-          bin = lane * 8 + k;
-          left = need - static_cast<int>(cum);
-          held = static_cast<int>(c[k]);
+        for (int k = 0; k < 8; ++k) {
+          c[k] = hist[lane * 8 + k];
+          total += c[k];
         }
-        cum += c[k];
+        uint32_t incl = total;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t x = __shfl_down_sync(0xffffffffu, incl, off);
+          if (lane + off < 32) incl += x;
+        }
+        uint32_t cum = incl - total;
+#pragma unroll
+        for (int k = 7; k >= 0; --k) {
+          if (static_cast<int>(cum) < need && need <= static_cast<int>(cum + c[k])) {
+            ctl[0] = lane * 8 + k;
+            ctl[1] = need - static_cast<int>(cum);
+            ctl[2] = static_cast<int>(c[k]);
+          }
+          cum += c[k];
+        }
       }
-      const int src = __ffs(__ballot_sync(0xffffffffu, bin >= 0)) - 1;
-      bin = __shfl_sync(0xffffffffu, bin, src);
-      need = __shfl_sync(0xffffffffu, left, src);
-      in_bin = __shfl_sync(0xffffffffu, held, src);
-      prefix |= static_cast<uint32_t>(bin) << lo;
+      __syncthreads();
+      prefix |= static_cast<uint32_t>(ctl[0]) << lo;
       mask |= dmask << lo;
-      __syncwarp();   // the histogram is read before the next pass clears it
+      need = ctl[1];
+      in_bin = ctl[2];
       hi = lo - 1;
     }
   }
-  // ---- compaction in block-id order: keys above the prefix, and those in
-  // its bin (all of them, or the `need` lowest ids when more share the K-th
+  // ---- compaction of the winners: keys above the prefix, and those in its
+  // bin (all of them, or the `need` lowest ids when more share the K-th
   // score than are wanted)
   const bool ties = in_bin > need;
-  int cnt = 0, tcnt = 0;
-  for_each_slot([&](uint32_t u, int e, bool v) {
-    const bool eq = v && (u & mask) == prefix;
-    const unsigned beq = __ballot_sync(0xffffffffu, eq);
-    const bool take = (v && (u & mask) > prefix) ||
-                      (eq && (!ties || tcnt + __popc(beq & lt) < need));
-    const unsigned bt = __ballot_sync(0xffffffffu, take);
-    if (take) {
-      const int pos = cnt + __popc(bt & lt);
-      if (pos < KP)
-        list[pos] = (static_cast<uint64_t>(u) << 32) |
-                    static_cast<uint32_t>(~static_cast<uint32_t>(e));
-    }
-    cnt += __popc(bt);
-    tcnt += __popc(beq);
-  });
-  __syncwarp();
-  const int n = min(cnt, KP);
-  uint64_t top[KPL];
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const int e = i * 32 + lane;
-    top[i] = e < n ? list[e] : 0ull;
+  if (tid == 0) ctl[3] = 0;
+  __syncthreads();
+  auto put = [&](uint32_t u, int e) {
+    const int pos = atomicAdd(&ctl[3], 1);
+    if (pos < P)
+      buf[pos] = (static_cast<uint64_t>(u) << 32) |
+                 static_cast<uint32_t>(~static_cast<uint32_t>(e));
+  };
+  if (!ties) {
+    for_each_slot([&](uint32_t u, int e, bool v) {
+      if (v && (u & mask) >= prefix) put(u, e);
+    });
+  } else {
+    // Only when the K-th score is shared (the mask covers every bit):
+    // equal keys are ranked in block-id order, one slot of every thread at
+    // a time.
+    int taken = 0;
+    for_each_slot([&](uint32_t u, int e, bool v) {
+      if (v && (u & mask) > prefix) put(u, e);
+      const bool eq = v && (u & mask) == prefix;
+      const unsigned b = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) ctl[4 + warp] = __popc(b);
+      __syncthreads();
+      int before = taken + __popc(b & lt);
+      for (int w = 0; w < warp; ++w) before += ctl[4 + w];
+      if (eq && before < need) put(u, e);
+      for (int w = 0; w < kSelWarps; ++w) taken += ctl[4 + w];
+      __syncthreads();
+    });
   }
-  bitonic_sort<KPL>(top, true);
-  __syncwarp();
-  // The histogram and winners are in registers now: the warp's region takes
-  // the admission's scratch.
-  AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(mine);
+  __syncthreads();
+  const int n = min(ctl[3], P);
+
+  // ---- bitonic sort of the P winner slots, descending: element
+  // e = i * kSelThreads + tid sits in x[i]; partners closer than 32 are
+  // swapped by shuffles, farther ones through shared memory, and within a
+  // thread when they are kSelThreads apart.
+  uint64_t x[kHeld];
 #pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const int e = i * 32 + lane;
+  for (int i = 0; i < kHeld; ++i) {
+    const int e = i * kSelThreads + tid;
+    x[i] = (e < P && e < n) ? buf[e] : 0ull;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int size = 2; size <= P; size <<= 1) {
+#pragma unroll
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      uint64_t y[kHeld];
+      if (j < 32) {
+#pragma unroll
+        for (int i = 0; i < kHeld; ++i) y[i] = __shfl_xor_sync(0xffffffffu, x[i], j);
+      } else if (j < kSelThreads) {
+#pragma unroll
+        for (int i = 0; i < kHeld; ++i) {
+          const int e = i * kSelThreads + tid;
+          if (e < P) buf[e] = x[i];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kHeld; ++i) {
+          const int e = i * kSelThreads + tid;
+          y[i] = e < P ? buf[e ^ j] : 0ull;
+        }
+        __syncthreads();
+      } else {
+#pragma unroll
+        for (int i = 0; i < kHeld; ++i) y[i] = x[i ^ (j / kSelThreads)];
+      }
+#pragma unroll
+      for (int i = 0; i < kHeld; ++i) {
+        const int e = i * kSelThreads + tid;
+        const bool d = (e & size) == 0;          // this block sorted descending
+        const bool lower = (e & j) == 0;
+        const bool take_max = lower == d;
+        x[i] = take_max ? (x[i] > y[i] ? x[i] : y[i]) : (x[i] < y[i] ? x[i] : y[i]);
+      }
+    }
+  }
+  // ---- outputs; the region takes the admission's scratch
+  AdmitWarpSmem& S = *reinterpret_cast<AdmitWarpSmem*>(smem);
+#pragma unroll
+  for (int i = 0; i < kHeld; ++i) {
+    const int e = i * kSelThreads + tid;
     if (e < a.K) {
-      const uint64_t key = top[i];
+      const uint64_t key = x[i];
       const int id = key == 0ull ? -1 : static_cast<int>(~static_cast<uint32_t>(key));
       a.topk_ids[static_cast<size_t>(pair) * a.K + e] = id;
       if (a.topk_scores)
@@ -714,10 +772,10 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(const ScoreArgs 
       S.topk[e] = id;
     }
   }
-  if (a.fuse_admit) {
-    __syncwarp();
-    admit_warp<KPL>(a.admit, pair, S, reinterpret_cast<uint32_t*>(mine + sizeof(AdmitWarpSmem)));
-  }
+  if (!a.fuse_admit) return;
+  __syncthreads();
+  if (warp == 0)
+    admit_warp<KPL>(a.admit, pair, S, reinterpret_cast<uint32_t*>(smem + sizeof(AdmitWarpSmem)));
 }
 
 // Raise the kernel's dynamic shared memory limit to `smem` (once per device
@@ -848,12 +906,7 @@ int split_scan_warps(int pairs) {
 
 template <int KPL, int NPT>
 cudaError_t launch_select_npt(const ScoreArgs& a, cudaStream_t s) {
-  // Warps per CTA: kSelWarps unless their scratch (which grows with NBmax
-  // through the admission's bitmaps) exceeds a CTA's shared memory.
-  const size_t per_warp = select_warp_smem_bytes<KPL>(a.NBmax);
-  int wpc = kSelWarps;
-  while (wpc > 1 && wpc * per_warp > 200 * 1024) --wpc;
-  const size_t smem = wpc * per_warp;
+  const size_t smem = select_smem_bytes<KPL>(a.NBmax);
   if (smem > 48 * 1024) {
     static int configured_device = -1;
     static size_t configured_smem = 0;
@@ -868,21 +921,19 @@ cudaError_t launch_select_npt(const ScoreArgs& a, cudaStream_t s) {
       configured_smem = smem;
     }
   }
-  select_kernel<KPL, NPT><<<(a.pairs + wpc - 1) / wpc, wpc * 32, smem, s>>>(a);
+  select_kernel<KPL, NPT><<<a.pairs, kSelThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-// Keys per lane: the smallest of 1, 2, 4, 8, 16, 32 that holds NBmax blocks,
-// else 0 (scores re-read for every pass).
+// Keys per thread: the smallest of 1, 2, 4, 8 that holds NBmax blocks, else
+// 0 (scores read again per pass).
 template <int KPL>
 cudaError_t launch_select_kpl(const ScoreArgs& a, cudaStream_t s) {
-  const int per = (a.NBmax + 31) / 32;
+  const int per = (a.NBmax + kSelThreads - 1) / kSelThreads;
   if (per <= 1) return launch_select_npt<KPL, 1>(a, s);
   if (per <= 2) return launch_select_npt<KPL, 2>(a, s);
   if (per <= 4) return launch_select_npt<KPL, 4>(a, s);
   if (per <= 8) return launch_select_npt<KPL, 8>(a, s);
-  if (per <= 16) return launch_select_npt<KPL, 16>(a, s);
-  if (per <= 32) return launch_select_npt<KPL, 32>(a, s);
   return launch_select_npt<KPL, 0>(a, s);
 }
 
@@ -934,10 +985,10 @@ cudaError_t preload_score_kernels() {
       reinterpret_cast<const void*>(score_topk_kernel<8, 4>),
       reinterpret_cast<const void*>(scan_kernel<8>),
       reinterpret_cast<const void*>(scan_kernel<4>),
-      reinterpret_cast<const void*>(select_kernel<1, 2>),
-      reinterpret_cast<const void*>(select_kernel<4, 32>),
+      reinterpret_cast<const void*>(select_kernel<1, 1>),
+      reinterpret_cast<const void*>(select_kernel<4, 8>),
       reinterpret_cast<const void*>(select_kernel<4, 0>),
-      reinterpret_cast<const void*>(select_kernel<8, 32>)};
+      reinterpret_cast<const void*>(select_kernel<8, 8>)};
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncGetAttributes(&at, f);
     if (e != cudaSuccess) return e;
