@@ -185,7 +185,11 @@ def pinned_device_alias(t: torch.Tensor, dev) -> torch.Tensor:
 
 def pretouch_host(host: torch.Tensor, dev) -> None:
     """Read the whole pinned host store once through its device mapping (a
-    sequential GPU read, untimed), as a store in long use would have been."""
+    sequential GPU read, untimed), as a store in long use would have been:
+    the gather's random 8 KiB reads run several times slower while the
+    store's pages are still cold on the device side (measured: a first timed
+    pass of 1192 against 2416 layer-steps/s in the next pass of one process;
+    under a profiler that replays each launch cold, 12x slower)."""
     alias = pinned_device_alias(host, dev)
     flat = alias.view(-1)
     step = 1 << 28
@@ -450,7 +454,7 @@ def run_oasis(args, ws, rank, local):
     eng, lens, host = build_layer(shape, args.seed + rank, dev, args.side_groups, args.schedule)
     q, qd = workload.queries(shape, args.seed + rank, 0, nq, device=dev)
     warm_start(eng, shape, q[0], dev)
-    if args.host_pretouch:
+    if not args.no_host_pretouch:
         pretouch_host(host, dev)
     odt = torch.bfloat16
     out = torch.empty((shape.R, shape.Hq, 128), dtype=odt, device=dev)
@@ -662,6 +666,9 @@ def run_oasis_layers(args, ws, rank, local):
                       schedule=args.schedule)
     eng = Oasis(cfg, host_kv=[stores[l % M] for l in range(L)])
     eng.set_context(lens)
+    if not args.no_host_pretouch:
+        for h in stores:
+            pretouch_host(h, dev)
     qs, qds = [], []
     for l in range(L):
         q, qd = workload.queries(shape, args.seed + rank, l, nq, device=dev,
@@ -972,6 +979,8 @@ def run_miss_stall(args, ws, rank, local):
         eng, lens, host = build_layer(shape, args.seed, dev, args.side_groups, args.schedule)
         q, qd = workload.queries(shape, args.seed, 0, nq, device=dev)
         warm_start(eng, shape, q[0], dev)
+        if not args.no_host_pretouch:
+            pretouch_host(host, dev)
         out = torch.empty((R, Hq, 128), dtype=torch.bfloat16, device=dev)
         outd = torch.empty_like(out)
         st = torch.cuda.Stream(dev)
@@ -1198,6 +1207,8 @@ def run_cap_sweep(args, ws, rank, local):
     host = torch.empty((base.R, base.Hkv, base.NBmax, 2, 16, 128), dtype=torch.bfloat16,
                        pin_memory=True)
     workload.host_kv(base, args.seed, 0, lens, device=dev, out=host)
+    if not args.no_host_pretouch:
+        pretouch_host(host, dev)
     nq = args.queries
     q, qd = workload.queries(base, args.seed, 0, nq + 1, device=dev)
     main = torch.cuda.Stream(dev)
@@ -1318,8 +1329,9 @@ def main():
     ap.add_argument("--queries", type=int, default=64, help="distinct query steps, cycled")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--host-pretouch", action="store_true",
-                    help="read the host store once through its device mapping before timing")
+    ap.add_argument("--no-host-pretouch", action="store_true",
+                    help="skip the one untimed read of every host store through its device "
+                         "mapping before timing")
     ap.add_argument("--side-groups", type=int, default=0,
                     help="request groups of the side work (0 = library default)")
     ap.add_argument("--schedule", type=int, default=3,
