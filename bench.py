@@ -469,17 +469,17 @@ def run_oasis(args, ws, rank, local):
         eng.oasis_step(0, step, q[step % nq], qd[step % nq], out, outd, main)
         step += 1
 
-    with torch.cuda.stream(main):
-        for _ in range(args.warmup):
-            one_step()
-    eng.oasis_join(0, main)
-    torch.cuda.synchronize(dev)
-    eng.oasis_sync()
-
-    # ---------------- timed region: K layer-steps, inputs resident in HBM
+    # The clock sampler starts first: the GPU must not idle between the
+    # warm-up steps and the timed region (it lowers its clocks when idle).
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
+    with torch.cuda.stream(main):
+        for _ in range(args.warmup):
+            one_step()
+    eng.oasis_sync()
+
+    # ---------------- timed region: K layer-steps, inputs resident in HBM
 
     def timed_pass(profiled: bool):
         """K steps between CUDA events on the main stream (barrier + sync on
@@ -750,6 +750,11 @@ def run_oasis_layers(args, ws, rank, local):
             eng.oasis_advance_context(step, 1, main)
         step += 1
 
+    # The clock sampler starts before the warm-up: no idle gap between the
+    # warm-up steps and the timed region.
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         one_step()
         if drift:
@@ -759,9 +764,6 @@ def run_oasis_layers(args, ws, rank, local):
     torch.cuda.synchronize(dev)
     eng.oasis_sync()
     moved[0] = 0
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
     eng.oasis_profile_enable(True)
     barrier(ws)
     torch.cuda.synchronize(dev)
