@@ -449,6 +449,10 @@ def run_oasis(args, ws, rank, local):
         raise RuntimeError("the CUDA path needs a GPU")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    # The clock sampler starts now, seconds before the timed region, so that
+    # its start-up is over by then.
+    clocks = ClockSampler(local)
+    clocks.start()
     shape = get_shape(args)
     nq = args.queries
     eng, lens, host = build_layer(shape, args.seed + rank, dev, args.side_groups, args.schedule)
@@ -469,11 +473,7 @@ def run_oasis(args, ws, rank, local):
         eng.oasis_step(0, step, q[step % nq], qd[step % nq], out, outd, main)
         step += 1
 
-    # The clock sampler starts first: the GPU must not idle between the
-    # warm-up steps and the timed region (it lowers its clocks when idle).
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
+    # No idle gap between the warm-up steps and the timed region.
     with torch.cuda.stream(main):
         for _ in range(args.warmup):
             one_step()

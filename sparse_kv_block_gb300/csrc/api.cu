@@ -652,13 +652,13 @@ ScoreArgs score_args(oasis_ctx* ctx, int layer, int step, const void* x, int pla
 }
 
 // Launch a scan + ranking: split (scan, then ranking and fused admission,
-// timed as profile kinds scan_kind and 6) or as one kernel (OASIS_SCAN=fused,
-// timed as scan_kind).  `scanned`, when given, is recorded on `s` once the
+// timed as profile kinds scan_kind and 6) or as one kernel (longer contexts,
+// or OASIS_SCAN=fused; timed as scan_kind).  `scanned`, when given, is recorded on `s` once the
 // scan is done: work that needs only that (it reads HBM beside the scan)
 // may start while the ranking runs.
 int launch_scan_timed(oasis_ctx* ctx, const ScoreArgs& a, cudaStream_t s, int scan_kind,
                       cudaEvent_t scanned) {
-  if (scan_is_split()) {
+  if (scan_is_split(a.NBmax)) {
     cudaEvent_t* pe = ctx->prof_begin(scan_kind, s);
     cudaError_t e = launch_scan_scores(a, s);
     ctx->prof_end(pe, s);

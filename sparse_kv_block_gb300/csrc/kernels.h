@@ -159,9 +159,9 @@ cudaError_t launch_attention(const AttnArgs& a, const CUtensorMap* pool_map,
 // Scan + top-K (+ admission) in one kernel, no scratch used.
 cudaError_t launch_score_topk(const ScoreArgs& a, cudaStream_t s);
 // The same as two kernels: the scan writes every block's score to
-// a.scores_ws, then the ranking (and admission) reads them back.  Used
-// unless scan_is_split() is false (OASIS_SCAN=fused).
-bool scan_is_split();
+// a.scores_ws, then the ranking (and admission) reads them back.  Used when
+// scan_is_split(NBmax).
+bool scan_is_split(int NBmax);
 cudaError_t launch_scan_scores(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_topk_select(const ScoreArgs& a, cudaStream_t s);
 cudaError_t launch_admit(const AdmitArgs& a, cudaStream_t s);

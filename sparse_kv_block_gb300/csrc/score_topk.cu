@@ -939,12 +939,25 @@ cudaError_t launch_select_kpl(const ScoreArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-bool scan_is_split() {
-  static const bool fused = [] {
+// Split (scan, then ranking) while the ranking keeps a pair's keys in
+// registers (NBmax <= kSelThreads * 8 = 1024 blocks); one kernel for longer
+// contexts, whose stream amortises the in-kernel ranking and whose separate
+// ranking would compete longer with the attention beside it.  Measured on
+// GB300, alternating on one box: 128 x 16K layer split 2935 / 3003 against
+// fused 2862 / 2876 layer-steps/s (profiled passes; end to end 3137 / 3092
+// against 3063 / 3078); 32-layer loop of 64 x 32K contexts (2064 blocks)
+// split 3670 / 3595 against fused 3897 / 3879.  OASIS_SCAN=split or
+// OASIS_SCAN=fused forces one form.
+bool scan_is_split(int NBmax) {
+  static const int forced = [] {
     const char* e = std::getenv("OASIS_SCAN");
-    return e && std::string(e) == "fused";
+    if (!e) return 0;
+    if (std::string(e) == "fused") return 1;
+    if (std::string(e) == "split") return 2;
+    return 0;
   }();
-  return !fused;
+  if (forced) return forced == 2;
+  return NBmax <= kSelThreads * 8;
 }
 
 cudaError_t launch_scan_scores(const ScoreArgs& a, cudaStream_t s) {
