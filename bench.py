@@ -365,7 +365,14 @@ HBM_SPEC_GBS = 7900.0
 # digits) of the kernel's source file when the counters were taken: a
 # kernel whose source has changed since reports traffic null.  Captured on a
 # reduced case and scaled by (request, KV head) pairs where marked.
-PROFILED_TRAFFIC = {}
+PROFILED_TRAFFIC = {
+    "qwen3_8b_16k": {
+        "attention": (1083310592, "f53ce477022af819"),
+        "summary_scan": (547601920, "41a81604dd3ab5ff"),
+        "topk_select": (4326400, "41a81604dd3ab5ff"),
+        "prefetch": (662016, "ce5db5adf09fa456"),
+    },
+}
 
 
 def source_digest(name: str) -> str:
@@ -428,8 +435,9 @@ def kernel_rooflines(shape, ms_sum, counts, off_sum, steps, link_bytes, h2d_gbs,
             "bound": "latency", "ms_per_step": round(avg_ms["topk_select"], 5),
             "launches_per_step": launches["topk_select"],
             "avg_start_ms": round(avg_start["topk_select"], 5),
-            "note": "head-wise top-K of the scan's fp32 scores (L2-resident) and the fused "
-                    "capped eviction; overlaps the attention"}
+            "note": "head-wise top-K of the scan's fp32 scores and the fused capped "
+                    "eviction; overlaps the attention",
+            "traffic": profiled_traffic(shape.name, "topk_select")}
     timed = [n for n in ("attention", "summary_scan", "prefetch") if avg_ms[n]]
     dominant = max(timed, key=lambda n: avg_ms[n])
     return per_kernel, dominant
