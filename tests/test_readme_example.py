@@ -17,4 +17,6 @@ def test_readme_python_example_runs():
     scope = {}
     exec(compile(m.group(1), "README.md", "exec"), scope)
     assert scope["out"].abs().sum().item() > 0
+    n = scope["lists"]["n_admit"]
+    assert int(n.min()) >= 0 and int(n.max()) <= scope["shape"].K
     scope["eng"].close()
