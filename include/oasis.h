@@ -387,8 +387,9 @@ OASIS_API int oasis_stall_lists(oasis_ctx* ctx, int layer, int step, int32_t** t
 
 /* a1..a5 as one layer-step (a6; [R] *What carries the argument*: the
  * background work synchronises per layer).
- * q_draft is first copied (on `stream`) into a per-layer staging buffer.
- * Side work, on the context's two high-priority side streams, ordered after
+ * Except in the scan-first schedule (the default), q_draft is first copied
+ * (on `stream`) into a per-layer staging buffer; scan-first scans read it in
+ * place, since `stream` waits for them before the attention.  Side work, on the context's two high-priority side streams, ordered after
  * everything already on `stream` (so after this layer's previous attention):
  * a2+a3 fused with a4 per request group, each group's a5 gather as soon as
  * its admissions exist; results go to the context's workspace lists.  On

@@ -1470,7 +1470,12 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
   const bool early = schedule == OASIS_SCHEDULE_EARLY_SCAN;
   // The side work reads the draft query from a per-layer double buffer, so
   // the caller may reuse its buffer as soon as `stream` passes this call.
+  // Scan-first needs no copy: `stream` passes the call only after the
+  // attention, which waits for the last scan, the only reader of q_draft on
+  // the side streams.
+  const bool stage_qd = schedule != OASIS_SCHEDULE_SCAN_FIRST;
   void* qd_copy = L.qd_ring[step & 1];
+  const void* qd_scan = stage_qd ? qd_copy : q_draft;
   const size_t qbytes = static_cast<size_t>(ctx->D) * ctx->cfg.num_requests *
                         ctx->cfg.num_q_heads * kHeadDim * 2;
   if (early) {
@@ -1502,10 +1507,10 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
       return rc;
     if (int rc = ctx->cuda(cudaEventRecord(L.ev_qd_copied, sc), "record q_draft staged"))
       return rc;
-  } else if (int rc = ctx->cuda(cudaMemcpyAsync(qd_copy, q_draft, qbytes,
-                                                cudaMemcpyDeviceToDevice, s),
-                                "stage q_draft")) {
-    return rc;
+  } else if (stage_qd) {
+    if (int rc = ctx->cuda(cudaMemcpyAsync(qd_copy, q_draft, qbytes, cudaMemcpyDeviceToDevice, s),
+                           "stage q_draft"))
+      return rc;
   }
   // Start of this step's side work: everything earlier on `stream`, which
   // includes the previous step's attention of this layer.  That is all the
@@ -1531,7 +1536,7 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
       // Scan + top-K on side3 (already running ahead); the group's
       // admission on `side` after the step start and the group's scan; its
       // gather on side2.
-      if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side3,
+      if (int rc = run_score(ctx, layer, step, qd_scan, Ls.topk_ids, Ls.topk_scores, ctx->side3,
                              p0, p1 - p0, false))
         return rc;
       if (int rc = ctx->cuda(cudaEventRecord(L.ev_group2[g], ctx->side3), "record top-k"))
@@ -1555,7 +1560,7 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
     if (schedule == OASIS_SCHEDULE_THREE_STREAMS) {
       // The pages' pipeline: top-K prediction, KV selection and KV transfer
       // on three streams, each stage of a group ordered by an event.
-      if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side,
+      if (int rc = run_score(ctx, layer, step, qd_scan, Ls.topk_ids, Ls.topk_scores, ctx->side,
                              p0, p1 - p0, false))
         return rc;
       if (int rc = ctx->cuda(cudaEventRecord(L.ev_group2[g], ctx->side), "record top-k"))
@@ -1580,7 +1585,7 @@ int step_impl(oasis_ctx* ctx, int layer, int step, const void* q, const void* q_
     // ranking and admission after it overlap the attention).
     cudaEvent_t scanned =
         schedule == OASIS_SCHEDULE_SCAN_FIRST && g == ctx->groups - 1 ? L.ev_scan_done : nullptr;
-    if (int rc = run_score(ctx, layer, step, qd_copy, Ls.topk_ids, Ls.topk_scores, ctx->side, p0,
+    if (int rc = run_score(ctx, layer, step, qd_scan, Ls.topk_ids, Ls.topk_scores, ctx->side, p0,
                            p1 - p0, true, scanned))
       return rc;
     if (ctx->C > 0) {
