@@ -1675,8 +1675,9 @@ int step_host_impl(oasis_ctx* ctx, int layer, int step, const void* q_host,
   if (int rc = ctx->set_device()) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Inputs go to the staging slot of this step's parity on the input stream,
-  // as soon as the slot's last reader (step - 2's attention and q_draft copy
-  // on `stream`) is done, so they usually land while the previous step still
+  // as soon as the slot's last readers are done (step - 2's attention, and
+  // its q_draft copy or scan-first scans, which `stream` passed before that
+  // attention), so they usually land while the previous step still
   // computes; `stream` waits for them before the step.
   const int slot = step & 1;
   const size_t qb = static_cast<size_t>(ctx->cfg.num_requests) * ctx->cfg.num_q_heads * kHeadDim * 2;
