@@ -394,6 +394,19 @@ def profiled_traffic(workload_name: str, kernel: str):
     return nbytes if source_digest(KERNEL_SOURCES[kernel]) == digest else None
 
 
+def traffic_fields(workload_name: str, kernel: str) -> dict:
+    """`traffic` (DRAM bytes per launch from the recorded capture, or None)
+    and where it comes from: never from this run."""
+    t = profiled_traffic(workload_name, kernel)
+    if t is None:
+        src = "none: no ncu capture of this kernel's current source for this workload"
+    else:
+        src = ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, recorded "
+               f"capture of {KERNEL_SOURCES[kernel]} sha256 "
+               f"{PROFILED_TRAFFIC[workload_name][kernel][1]} (not measured in this run)")
+    return {"traffic": t, "traffic_source": src}
+
+
 def kernel_rooflines(shape, ms_sum, counts, off_sum, steps, link_bytes, h2d_gbs, peaks):
     """Per-kernel rooflines of one timed pass: summed CUDA-event durations of
     each kind's launches per step (several request groups per step for the
@@ -425,7 +438,7 @@ def kernel_rooflines(shape, ms_sum, counts, off_sum, steps, link_bytes, h2d_gbs,
                  "launches_per_step": launches[n], "avg_start_ms": round(avg_start[n], 5),
                  "peak_source": (hbm_src if bound == "hbm" else
                                  "pinned cudaMemcpyAsync H2D, 256 MiB, measured in this run"),
-                 "traffic": profiled_traffic(shape.name, n)}
+                 **traffic_fields(shape.name, n)}
             if bound == "hbm":
                 k["frac_of_spec"] = round(a / HBM_SPEC_GBS, 4)
                 k["spec_gbs"] = HBM_SPEC_GBS
@@ -437,7 +450,7 @@ def kernel_rooflines(shape, ms_sum, counts, off_sum, steps, link_bytes, h2d_gbs,
             "avg_start_ms": round(avg_start["topk_select"], 5),
             "note": "head-wise top-K of the scan's fp32 scores and the fused capped "
                     "eviction; overlaps the attention",
-            "traffic": profiled_traffic(shape.name, "topk_select")}
+            **traffic_fields(shape.name, "topk_select")}
     timed = [n for n in ("attention", "summary_scan", "prefetch") if avg_ms[n]]
     dominant = max(timed, key=lambda n: avg_ms[n])
     return per_kernel, dominant
@@ -604,7 +617,7 @@ def run_oasis(args, ws, rank, local):
     roofline = {"bound": dk["bound"], "kernel": dominant,
                 "achieved": dk["achieved"], "peak": dk["peak"], "unit": "GB/s",
                 "frac": dk["frac"], "traffic": dk.get("traffic"),
-                "peak_source": dk["peak_source"]}
+                "traffic_source": dk.get("traffic_source"), "peak_source": dk["peak_source"]}
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
@@ -850,7 +863,7 @@ def run_oasis_layers(args, ws, rank, local):
                          "achieved": round(attn_bytes / (a_ms * 1e-3) / 1e9, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(attn_bytes / (a_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-                         "traffic": None},
+                         **traffic_fields(shape.name, "attention")},
             "hbm_bytes_per_layer_step": attn_bytes + scan_bytes,
             "hbm_achieved_gbs_whole_step": round((attn_bytes + scan_bytes) * value / 1e9, 1),
             "host_link": {"h2d_memcpy_gbs": round(h2d_gbs, 1),
