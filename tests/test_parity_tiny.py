@@ -43,7 +43,7 @@ def test_dense_when_k_covers_every_block(dev):
     L.eng.close()
 
 
-@pytest.mark.parametrize("lens", [[1000, 37], [16, 1024], [0, 5], [1024, 1]])
+@pytest.mark.parametrize("lens", [[1000, 37], [16, 1024], [0, 5], [1024, 1], [0, 0]])
 def test_ragged_contexts(dev, lens):
     L = H.make_layer(TINY, seed=2, lens=lens, steps=3, out_fp32=True)
     H.check_summaries(L)
@@ -99,6 +99,33 @@ def test_fused_step_matches_oracle(dev, groups, R, schedule):
             assert (lists["admit_ids"][r, h, :sh.C] == v["admit_ids"]).all()
             assert (lists["admit_slots"][r, h, :sh.C] == v["admit_slots"]).all()
             assert (lists["evict_ids"][r, h, :sh.C] == v["evict_ids"]).all()
+        assert (eng.res_ids[0][(t + 1) & 1].cpu().numpy() == L.orc.res).all()
+        assert (eng.stamps[0].cpu().numpy() == L.orc.stamp).all()
+        H.check_pool(L, (t + 1) & 1)
+    eng.close()
+
+
+@pytest.mark.parametrize("lens", [None, [0]])
+def test_single_pair_fused_steps(dev, lens):
+    # One request with one KV head (G = 4): one-CTA grids everywhere; also
+    # with an empty context (nothing to rank, admit or attend: zero outputs).
+    sh = dataclasses.replace(TINY, R=1, Hq=4, Hkv=1)
+    L = H.make_layer(sh, seed=8, steps=4, lens=lens, out_fp32=True)
+    eng = L.eng
+    out = torch.empty((sh.R, sh.Hq, 128), dtype=torch.float32, device=dev)
+    outd = torch.empty_like(out)
+    for t in range(4):
+        eng.oasis_step(0, t, L.q[t].to(dev), L.qd[t].to(dev), out, outd)
+        eng.oasis_join(0)
+        eng.oasis_sync()
+        ref = L.orc.step(workload.bf16_bits(L.q[t]), workload.bf16_bits(L.qd[t]), t)
+        H.check_attention([out.cpu().numpy(), outd.cpu().numpy()], ref, sh.G)
+        if lens == [0]:
+            assert not out.any() and not outd.any()
+        lists = {k: v.cpu().numpy() for k, v in eng.step_lists(0, t).items()}
+        v = ref[(0, 0)]
+        assert np.array_equal(lists["topk_ids"][0, 0], v["topk"])
+        assert lists["n_admit"][0, 0] == v["n_admit"]
         assert (eng.res_ids[0][(t + 1) & 1].cpu().numpy() == L.orc.res).all()
         assert (eng.stamps[0].cpu().numpy() == L.orc.stamp).all()
         H.check_pool(L, (t + 1) & 1)
