@@ -129,12 +129,11 @@ typedef struct {
  * describe it ([R] *What carries the argument*: per layer, one background
  * stream each for ranking, selection and transfer): a stand-alone scan + top-K, a
  * stand-alone admission and the gathers on three streams, the attention
- * starting at once.  AUTO: SCAN_FIRST for oasis_step (device buffers) and
- * oasis_step_host_async, CONCURRENT for oasis_step_host, whose output copy
- * back to the host on `stream` then overlaps the next step's scan (measured
- * on GB300: device path 3090 scan-first against 3053 concurrent
- * layer-steps/s; host path 2814 against 2912; asynchronous host path 3072
- * against 2910).  Results are identical. */
+ * starting at once.  AUTO: SCAN_FIRST for every step call (measured on
+ * GB300, 128 x 16K layer, scan-first against concurrent: oasis_step 3343-3346
+ * against 2254-2866 layer-steps/s, oasis_step_host_async 3268-3279 against
+ * 2784-2804, oasis_step_host 3070-3073 against 2546-2673).  Results are
+ * identical. */
 #define OASIS_SCHEDULE_SCAN_FIRST 0
 #define OASIS_SCHEDULE_CONCURRENT 1
 #define OASIS_SCHEDULE_THREE_STREAMS 2
@@ -148,9 +147,10 @@ typedef struct {
  * between steps only through this library's calls (build_summaries,
  * append_token, refresh_blocks, advance_context), which the early scan
  * follows, or with the device idle.  Results are identical.  Measured on
- * GB300 (128 x 16K layer, oasis_step): 3177 against 3079 layer-steps/s
- * scan-first at cap 0.05, 3497-4129 against 3467 at cap 0.01; through
- * oasis_step_host 2864-2875 against 2904 for AUTO, so AUTO never picks it. */
+ * GB300 (128 x 16K layer): oasis_step 3456-3482 against 3336-3340
+ * layer-steps/s scan-first, oasis_step_host 3267-3281 against 3070-3073,
+ * oasis_step_host_async 3093-3100 against 3262-3269.  AUTO never picks it:
+ * its contract is the caller's to keep. */
 #define OASIS_SCHEDULE_EARLY_SCAN 4
 
 typedef struct {

@@ -1658,8 +1658,8 @@ OASIS_API int oasis_join(oasis_ctx* ctx, int layer, void* stream) {
 }
 
 namespace {
-// The schedule AUTO picks for oasis_step_host_async.
-constexpr int kAsyncHostAuto = OASIS_SCHEDULE_SCAN_FIRST;
+// The schedule AUTO picks for the host-buffer steps.
+constexpr int kHostAuto = OASIS_SCHEDULE_SCAN_FIRST;
 
 // Host-buffer step.  async = false: outputs copied back on `stream`
 // (complete when `stream` passes the call); true: on the output stream,
@@ -1700,13 +1700,12 @@ int step_host_impl(oasis_ctx* ctx, int layer, int step, const void* q_host,
     if (int rc = ctx->cuda(cudaStreamWaitEvent(s, L.ev_out_done[slot], 0), "wait output slot"))
       return rc;
   }
-  // AUTO: with outputs copied back on `stream`, the attention starts at once,
-  // so that copy overlaps the next step's scan instead of delaying it
-  // (measured end to end: 2912 against 2814 layer-steps/s scan-first).  With
-  // the copies on the output stream the scan goes first, as for oasis_step.
+  // AUTO: scan-first, as for oasis_step, with the outputs copied back on
+  // `stream` too (measured end to end since the scan-first scans read the
+  // draft queries in place: 3070-3073 against 2683-2703 layer-steps/s with
+  // the attention starting at once).
   const int sched = ctx->cfg.schedule != OASIS_SCHEDULE_AUTO ? ctx->cfg.schedule
-                    : async                                 ? kAsyncHostAuto
-                                                            : OASIS_SCHEDULE_CONCURRENT;
+                                                             : kHostAuto;
   if (int rc = step_impl(ctx, layer, step, L.q_stage[slot], L.qd_stage[slot], L.out_stage[slot],
                          L.outd_stage[slot], stream, sched, L.ev_in[slot]))
     return rc;
