@@ -172,7 +172,7 @@ def test_host_buffer_step_pageable_outputs(dev):
     eng.close()
 
 
-@pytest.mark.parametrize("schedule", [0, 3, 4])
+@pytest.mark.parametrize("schedule", [0, 1, 3, 4])
 def test_host_buffer_steps_back_to_back(dev, schedule):
     # oasis_step_host issued for consecutive steps with no host wait between
     # them: step t + 1's input copies may overlap step t's side work.  The
