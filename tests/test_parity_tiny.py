@@ -175,8 +175,8 @@ def test_host_buffer_step_pageable_outputs(dev):
 @pytest.mark.parametrize("schedule", [0, 1, 3, 4])
 def test_host_buffer_steps_back_to_back(dev, schedule):
     # oasis_step_host issued for consecutive steps with no host wait between
-    # them: step t + 1's input copies may overlap step t's side work.  The
-    # automatic schedule runs host-buffer steps concurrently.
+    # them: step t + 1's input copies may overlap step t's side work; every
+    # schedule but the pages' three streams (the automatic one is scan-first).
     sh = dataclasses.replace(TINY, R=5)
     L = H.make_layer(sh, seed=9, steps=6, fetch_ratio=0.25, out_fp32=False, schedule=schedule)
     eng = L.eng
