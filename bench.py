@@ -370,7 +370,7 @@ PROFILED_TRAFFIC = {
         "attention": (1083310592, "f53ce477022af819"),
         "summary_scan": (547601920, "41a81604dd3ab5ff"),
         "topk_select": (4326400, "41a81604dd3ab5ff"),
-        "prefetch": (662016, "ce5db5adf09fa456"),
+        "prefetch": (653312, "06148c34713b870d"),
     },
 }
 

@@ -54,7 +54,8 @@ cudaError_t launch_admit_kpl(const AdmitArgs& a, cudaStream_t s) {
 // in flight compete with HBM traffic in the memory system.  In the 128 x 16K
 // layer-step 24 / 32 / 40 / 48 / 64 CTAs give 3040 / 3036 / 3066 / 2980 /
 // 2787 layer-steps/s: 40 moves the units in time (266 us of a 326 us step)
-// while slowing the attention least.
+// while slowing the attention least.  The caller may ask for another cap
+// (GatherArgs::max_ctas), as the step does for a one-layer context.
 constexpr int kGatherThreads = 128;
 constexpr int kGatherCtas = 40;
 
@@ -406,12 +407,13 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t s) {
   }
   const long long warps_needed = total;
   long long grid = (warps_needed + (kGatherThreads / 32) - 1) / (kGatherThreads / 32);
-  static const int cap = [] {
+  static const int forced = [] {
     // Tuning override of the gather's CTA count (units in flight / 4).
     const char* e = std::getenv("OASIS_GATHER_CTAS");
     const int v = e ? std::atoi(e) : 0;
-    return v > 0 ? v : kGatherCtas;
+    return v > 0 ? v : 0;
   }();
+  const int cap = forced > 0 ? forced : a.max_ctas > 0 ? a.max_ctas : kGatherCtas;
   if (grid > cap) grid = cap;
   gather_kernel<<<static_cast<int>(grid), kGatherThreads, 0, s>>>(a);
   return cudaGetLastError();

@@ -822,6 +822,14 @@ int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
   g.items = ctx->C;
   g.NBmax = ctx->cfg.max_blocks;
   g.U = ctx->U;
+  // A one-layer context's gathers must land within one step (the next
+  // attention of the layer follows at once), so they get a few more units
+  // in flight; with several layers they have the other layers' time and
+  // slow the HBM kernels beside them less with the default.  Measured on
+  // GB300 (2000-step runs): 128 x 16K layer 44 CTAs 3342 / end to end 3286-
+  // 3289 layer-steps/s against 40: 3337-3338 / 3260-3261; 32-layer 64 x 32K
+  // loop 44: 3716 against 40: 3918-3935.
+  g.max_ctas = ctx->cfg.num_layers == 1 ? 44 : 0;
   cudaEvent_t* pe = ctx->prof_begin(3, s);
   const int rc = launch_gather_split(ctx, L, g, s);
   ctx->prof_end(pe, s);

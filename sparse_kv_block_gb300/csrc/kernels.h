@@ -91,6 +91,8 @@ struct GatherArgs {
   // (lists padded far beyond their use, such as the miss-stall demand
   // fetch); 0: one warp per (pair, item), the grid capped for the host link.
   int pair_major;
+  // Item-major mode: CTAs at most (0: the launcher's default).
+  int max_ctas;
 };
 
 // Remote tier slot assignment: item i of pair p names block
