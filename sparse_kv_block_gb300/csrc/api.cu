@@ -824,12 +824,16 @@ int run_prefetch(oasis_ctx* ctx, int layer, int step, const int32_t* aid,
   g.U = ctx->U;
   // A one-layer context's gathers must land within one step (the next
   // attention of the layer follows at once), so they get a few more units
-  // in flight; with several layers they have the other layers' time and
-  // slow the HBM kernels beside them less with the default.  Measured on
-  // GB300 (2000-step runs): 128 x 16K layer 44 CTAs 3342 / end to end 3286-
-  // 3289 layer-steps/s against 40: 3337-3338 / 3260-3261; 32-layer 64 x 32K
-  // loop 44: 3716 against 40: 3918-3935.
-  g.max_ctas = ctx->cfg.num_layers == 1 ? 44 : 0;
+  // in flight; with several layers they have the other layers' time, and
+  // fewer in flight slow the HBM kernels beside them less, the fewer the
+  // more a step's admissions leave the link idle.  Measured on GB300: 128 x
+  // 16K layer (6144 units a step) 44 CTAs 3342 / end to end 3286-3289
+  // layer-steps/s against 40: 3337-3338 / 3260-3261; 32-layer 64 x 32K loop
+  // (3072 units a layer-step) 20 / 24 / 40 / 44 CTAs: 3837-3932 / 4105-4149
+  // / 3981-4006 / 3716; 36-layer 90 x 16K loop (4320 units) 32 / 40 / 48:
+  // 3548 / 3736 / 3636.
+  const long long units = static_cast<long long>(pairs) * ctx->C;
+  g.max_ctas = ctx->cfg.num_layers == 1 ? 44 : units <= 3072 ? 24 : 0;
   cudaEvent_t* pe = ctx->prof_begin(3, s);
   const int rc = launch_gather_split(ctx, L, g, s);
   ctx->prof_end(pe, s);
