@@ -316,10 +316,22 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+L2_BYTES = 129 * 10 ** 6   # GB300 L2
+
+
+def l2_note(shape) -> str:
+    """Whether one layer-step's resident units + summaries exceed L2 (the
+    timing rule's alternative to flushing it between steps)."""
+    nbytes = shape.R * shape.Hkv * (shape.K * UNIT_BYTES + shape.NBmax * SUMM_BYTES)
+    rel = "larger" if nbytes > L2_BYTES else "smaller"
+    size = f"{nbytes / 2 ** 30:.2f} GiB" if nbytes >= 2 ** 28 else f"{nbytes / 2 ** 20:.1f} MiB"
+    return f"inputs {rel} than L2: {size} of pool + summaries read per layer-step"
+
+
 def config_dict(shape, ws) -> dict:
     """The `config` of both arms' lines: what was run, no results."""
     return {"workload": workload_desc(shape), "parallelism": f"replicas{ws}",
-            "l2": "inputs larger than L2: 1.5 GiB of pool + summaries read per step"}
+            "l2": l2_note(shape)}
 
 
 def get_shape(args):
@@ -858,7 +870,7 @@ def run_oasis_layers(args, ws, rank, local):
                                   f"{moved[0] / args.steps:.0f} moves per step over "
                                   f"{M} stores), each step timed alone" if drift else ""),
                        "tokens_per_s": round(value * R / L, 1),
-                       "l2": "inputs larger than L2"},
+                       "l2": l2_note(shape)},
             "roofline": {"bound": "hbm", "kernel": "attention",
                          "achieved": round(attn_bytes / (a_ms * 1e-3) / 1e9, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
