@@ -468,6 +468,18 @@ def kernel_rooflines(shape, ms_sum, counts, off_sum, steps, link_bytes, h2d_gbs,
     return per_kernel, dominant
 
 
+def whole_step_rates(per_kernel, link_bytes, steps_per_s, peaks, h2d_gbs) -> dict:
+    """HBM and host-link rates of the whole step at `steps_per_s` (one GPU),
+    and their fractions of the measured peaks."""
+    hbm = per_kernel["attention"]["bytes_per_step"] + per_kernel["summary_scan"]["bytes_per_step"]
+    hbm_gbs = hbm * steps_per_s / 1e9
+    link_gbs = link_bytes * steps_per_s / 1e9
+    return {"hbm_bytes_per_step": int(hbm), "hbm_gbs": round(hbm_gbs, 1),
+            "hbm_frac": round(hbm_gbs / peaks["hbm_gbs"], 4),
+            "link_bytes_per_step": int(link_bytes), "link_gbs": round(link_gbs, 1),
+            "link_frac": round(link_gbs / h2d_gbs, 4)}
+
+
 def spread(per_step_ms) -> dict:
     """min / median / max of per-step times (ms)."""
     v = sorted(per_step_ms)
@@ -638,6 +650,10 @@ def run_oasis(args, ws, rank, local):
             "config": config_dict(shape, ws), "tokens_per_s": round(value * shape.R, 1),
             "roofline": roofline, "roofline_hbm": per_kernel.get("attention"),
             "kernels": per_kernel,
+            # one GPU's whole step against the two peaks it shares: every
+            # HBM byte of its kernels (attention + scan) and every link byte,
+            # at the per-GPU step rate
+            "whole_step": whole_step_rates(per_kernel, link_bytes, value / ws, peaks, h2d_gbs),
             "host_link": {"h2d_memcpy_gbs": round(h2d_gbs, 1),
                           "admitted_units_per_step": adm_units,
                           "bytes_per_step": int(link_bytes)},

@@ -1,6 +1,7 @@
-"""The reference arm of bench.py (the oracle stepping whole layer-steps on
-the host cores) prints one JSON line with every key the benchmark contract
-asks for, on the tiny workload, without a GPU."""
+"""bench.py's host-side logic without a GPU: the reference arm (the oracle
+stepping whole layer-steps on the host cores) prints one JSON line with
+every key the benchmark contract asks for, on the tiny workload; the
+whole-step rates of the GPU arm's line are its bytes times its step rate."""
 import json
 import os
 import subprocess
@@ -29,3 +30,12 @@ def test_reference_arm_line_has_the_contract_keys():
     e = line["e2e"]
     assert e["value"] == line["value"] and e["unit"] == line["unit"]
     assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_whole_step_rates():
+    import bench
+    pk = {"attention": {"bytes_per_step": 1_000_000}, "summary_scan": {"bytes_per_step": 500_000}}
+    r = bench.whole_step_rates(pk, 50_000, 2000.0, {"hbm_gbs": 6.0}, 0.2)
+    assert r["hbm_bytes_per_step"] == 1_500_000 and r["link_bytes_per_step"] == 50_000
+    assert r["hbm_gbs"] == 3.0 and r["hbm_frac"] == 0.5        # 1.5 MB x 2000 / s
+    assert r["link_gbs"] == 0.1 and r["link_frac"] == 0.5       # 50 kB x 2000 / s
